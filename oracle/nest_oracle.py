@@ -1,0 +1,304 @@
+"""CPU oracle for the nested-bit quantized linear layer.  TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module.  The product path (the CUDA library and
+its Python binding) never imports or calls it, and the oracle imports nothing
+from the product package except the seeded input generators.
+
+Everything is numpy float64 and written as the pages state it, one step at a
+time, with no blocking or fusion beyond what the definitions themselves say:
+
+* rotation -- randomized Hadamard transform, Sylvester construction,
+  block-diagonal, two-sided:  W~ = H_o S_o W S_i H_i,  x' = H_i S_i x,
+  y = S_o H_o z.  Source: feedman.me/posts/wZBTJ ("2-bit base in VRAM,
+  residual in RAM" post), POC recipe, step 1 "Rotation".  The block-diagonal
+  H is applied as an explicit dense H_b per block (a matrix product is the
+  library step).
+* 2-bit base -- per (output row, 128-column group) scale = RMS of the block
+  rounded to fp16; code = nearest of the 4 Lloyd-Max levels.  Same post, POC
+  recipe step 2 (RTN variant: the GPTQ/LDLQ error feedback needs calibration
+  data and is not part of this path).
+* residual -- R~ = W~ - Q_base in the rotated basis; uniform symmetric b-bit,
+  levels -qm..qm with qm = 2^(b-1) - 1 (printed garbled as "2b-1 - 1"),
+  scale = max|block| / qm per (row, 128-group) in fp16.  POC recipe step 3
+  (RTN variant).
+* forward -- x' = H_i S_i x; draft z = Q_base x'; verify z = (Q_base +
+  Q_resid) x'; y = S_o H_o z.  POC recipe step 4 ("the draft forward is the
+  same but without y_r").  The split between GPU and CPU in that step is
+  prior art; the oracle computes the plain sum.
+
+Readings where the pages are silent (each also listed in the design doc):
+* nearest-level ties: |u| exactly at the midpoint of the inner and outer
+  level goes to the inner level; u == 0 takes the positive inner level.
+* zero groups: scale 0 gives code 2 (+inner level) and a zero base; a zero
+  residual scale gives residual code 0.
+* residual rounding is round-half-to-even (numpy ``rint``).
+* levels are exactly +-0.4528 and +-1.5104 (the workload definition), the
+  Gaussian 4-level Lloyd-Max quantizer; the post's own fitted sets
+  (+-0.4535/+-1.5066, +-0.4511/+-1.5021) are reproduced by ``lloyd_max_fit``
+  as a check, not used.
+
+Parity status: every function here is pinned by tests under ``tests/``
+(closed forms, printed values, invariants and brute force); the GEMM output
+values themselves have no worked example on the pages and are pinned only
+through those invariants.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Tuple
+
+import numpy as np
+
+GROUP = 128
+HAD_CAP = 4096
+LEVELS = np.array([-1.5104, -0.4528, 0.4528, 1.5104], dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------
+# 1. Randomized Hadamard rotation
+# ----------------------------------------------------------------------------
+
+def hadamard_block_size(n: int) -> int:
+    """Largest power of two dividing n, capped at 4096 (POC recipe step 1)."""
+    if n <= 0:
+        raise ValueError("n must be positive")
+    b = 1
+    while n % (2 * b) == 0 and 2 * b <= HAD_CAP:
+        b *= 2
+    return b
+
+
+def sylvester_unnormalised(b: int) -> np.ndarray:
+    """Sylvester +-1 matrix: start from [1], repeat H <- [[H, H], [H, -H]]."""
+    if b < 1 or (b & (b - 1)) != 0:
+        raise ValueError("block size must be a power of two")
+    H = np.ones((1, 1), dtype=np.float64)
+    while H.shape[0] < b:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+def sylvester(b: int) -> np.ndarray:
+    """Normalised Sylvester Hadamard H_b = (+-1 matrix) / sqrt(b)."""
+    return sylvester_unnormalised(b) / math.sqrt(b)
+
+
+def block_hadamard_left(A: np.ndarray) -> np.ndarray:
+    """H_n @ A for the block-diagonal H_n = diag(H_b, ..., H_b), b = block size of n.
+
+    A has n rows.  Each band of b rows is multiplied by the dense H_b."""
+    n = A.shape[0]
+    b = hadamard_block_size(n)
+    H = sylvester(b)
+    out = np.empty_like(A, dtype=np.float64)
+    for j in range(n // b):
+        out[j * b:(j + 1) * b] = H @ A[j * b:(j + 1) * b]
+    return out
+
+
+def rotate_weights(W: np.ndarray, s_o: np.ndarray, s_i: np.ndarray) -> np.ndarray:
+    """W~ = H_o . S_o . W . S_i . H_i   (S = diag of the sign vector)."""
+    W = np.asarray(W, dtype=np.float64)
+    WS = W * s_i.astype(np.float64)[None, :]              # W . S_i
+    WSH = block_hadamard_left(WS.T).T                      # (H_i (W S_i)^T)^T = W S_i H_i, H_i symmetric
+    SWSH = s_o.astype(np.float64)[:, None] * WSH           # S_o . (...)
+    return block_hadamard_left(SWSH)                       # H_o . (...)
+
+
+def unrotate_weights(Wr: np.ndarray, s_o: np.ndarray, s_i: np.ndarray) -> np.ndarray:
+    """W = S_o . H_o . W~ . H_i . S_i  (the exact inverse)."""
+    A = s_o.astype(np.float64)[:, None] * block_hadamard_left(np.asarray(Wr, np.float64))
+    AH = block_hadamard_left(A.T).T
+    return AH * s_i.astype(np.float64)[None, :]
+
+
+def rotate_activations(x: np.ndarray, s_i: np.ndarray) -> np.ndarray:
+    """x' = H_i . S_i . x for every token.  x is [T][K] (one row per token)."""
+    x = np.asarray(x, dtype=np.float64)
+    Sx = s_i.astype(np.float64)[:, None] * x.T             # [K][T]: S_i x_t as columns
+    return block_hadamard_left(Sx).T
+
+
+def unrotate_outputs(z: np.ndarray, s_o: np.ndarray) -> np.ndarray:
+    """y = S_o . H_o . z for every token.  z is [T][M]."""
+    Hz = block_hadamard_left(np.asarray(z, np.float64).T)  # [M][T]
+    return (s_o.astype(np.float64)[:, None] * Hz).T
+
+
+# ----------------------------------------------------------------------------
+# 2. 2-bit base (RTN, 4 Lloyd-Max levels, fp16 RMS group scale)
+# ----------------------------------------------------------------------------
+
+def to_fp16(a) -> np.ndarray:
+    """Round float64 values to fp16 (round to nearest even, numpy's conversion)."""
+    return np.asarray(a, dtype=np.float64).astype(np.float16)
+
+
+def base_threshold(levels: np.ndarray = LEVELS) -> float:
+    """Decision point between the inner and the outer positive level."""
+    return float((levels[2] + levels[3]) / 2.0)
+
+
+def quantize_base(Wr: np.ndarray, levels: np.ndarray = LEVELS) -> Tuple[np.ndarray, np.ndarray]:
+    """Per (row, 128-group): s = fp16(RMS of the block); code = nearest level of W~/s.
+
+    Returns (codes uint8 [M][K] in 0..3 indexing ``levels`` ascending,
+             scales float16 [M][K/128])."""
+    Wr = np.asarray(Wr, dtype=np.float64)
+    M, K = Wr.shape
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 128")
+    G = K // GROUP
+    blocks = Wr.reshape(M, G, GROUP)
+    rms = np.sqrt(np.mean(blocks * blocks, axis=2))
+    s16 = to_fp16(rms)
+    s = s16.astype(np.float64)
+    t = base_threshold(levels)
+    codes = np.full((M, G, GROUP), 2, dtype=np.uint8)
+    nz = s > 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = blocks / s[:, :, None]
+    outer = np.abs(u) > t
+    neg = u < 0
+    c = np.where(neg, np.where(outer, 0, 1), np.where(outer, 3, 2)).astype(np.uint8)
+    codes[nz] = c[nz]
+    return codes.reshape(M, K), s16
+
+
+def dequant_base(codes: np.ndarray, scales16: np.ndarray, levels: np.ndarray = LEVELS) -> np.ndarray:
+    """Q_base = L[code] * s  (float64 [M][K])."""
+    M, K = codes.shape
+    G = K // GROUP
+    L = levels[codes.reshape(M, G, GROUP)]
+    return (L * scales16.astype(np.float64)[:, :, None]).reshape(M, K)
+
+
+# ----------------------------------------------------------------------------
+# 3. b-bit uniform residual
+# ----------------------------------------------------------------------------
+
+def qmax(bits: int) -> int:
+    """Largest residual level: 2^(bits-1) - 1."""
+    return (1 << (bits - 1)) - 1
+
+
+def quantize_residual(R: np.ndarray, bits: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Per (row, 128-group): s = fp16(max|R| / qm); q = clip(rint(R/s), -qm, qm).
+
+    Returns (codes int8 [M][K], scales float16 [M][K/128])."""
+    R = np.asarray(R, dtype=np.float64)
+    M, K = R.shape
+    G = K // GROUP
+    qm = qmax(bits)
+    blocks = R.reshape(M, G, GROUP)
+    amax = np.max(np.abs(blocks), axis=2)
+    s16 = to_fp16(amax / qm)
+    s = s16.astype(np.float64)
+    q = np.zeros((M, G, GROUP), dtype=np.int64)
+    nz = s > 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.rint(blocks / s[:, :, None])
+    r = np.clip(r, -qm, qm)
+    q[nz] = r[nz].astype(np.int64)
+    return q.reshape(M, K).astype(np.int8), s16
+
+
+def dequant_residual(codes: np.ndarray, scales16: np.ndarray) -> np.ndarray:
+    """Q_resid = q * s (float64 [M][K])."""
+    M, K = codes.shape
+    G = K // GROUP
+    q = codes.reshape(M, G, GROUP).astype(np.float64)
+    return (q * scales16.astype(np.float64)[:, :, None]).reshape(M, K)
+
+
+# ----------------------------------------------------------------------------
+# offline pipeline and forward passes
+# ----------------------------------------------------------------------------
+
+def quantize_layer(W: np.ndarray, s_o: np.ndarray, s_i: np.ndarray, bits: int) -> Dict[str, np.ndarray]:
+    """Rotate, fit the base, quantize the residual.  Returns codes, scales and W~."""
+    Wr = rotate_weights(W, s_o, s_i)
+    bc, bs = quantize_base(Wr)
+    R = Wr - dequant_base(bc, bs)
+    rc, rs = quantize_residual(R, bits)
+    return {"Wr": Wr, "base_codes": bc, "base_scales": bs,
+            "resid_codes": rc, "resid_scales": rs}
+
+
+def dense_rotated(layer: Dict[str, np.ndarray], verify: bool) -> np.ndarray:
+    """W_v = Q_base (+ Q_resid) in the rotated basis (float64 [M][K])."""
+    Wv = dequant_base(layer["base_codes"], layer["base_scales"])
+    if verify:
+        Wv = Wv + dequant_residual(layer["resid_codes"], layer["resid_scales"])
+    return Wv
+
+
+def forward(layer: Dict[str, np.ndarray], s_o: np.ndarray, s_i: np.ndarray,
+            x: np.ndarray, verify: bool) -> Dict[str, np.ndarray]:
+    """x' = H_i S_i x; z = W_v x' (rotated basis); y = S_o H_o z.
+
+    x is [T][K] (float values of the bf16 activations); returns x', z, y as
+    float64 [T][K], [T][M], [T][M]."""
+    xr = rotate_activations(x, s_i)
+    Wv = dense_rotated(layer, verify)
+    z = xr @ Wv.T
+    y = unrotate_outputs(z, s_o)
+    return {"x_rot": xr, "z": z, "y": y}
+
+
+def forward_rows(layer_rows: Dict[str, np.ndarray], xr: np.ndarray, verify: bool) -> np.ndarray:
+    """z for a subset of output rows, given x' (used for sampled checks at full size)."""
+    Wv = dequant_base(layer_rows["base_codes"], layer_rows["base_scales"])
+    if verify:
+        Wv = Wv + dequant_residual(layer_rows["resid_codes"], layer_rows["resid_scales"])
+    return np.asarray(xr, np.float64) @ Wv.T
+
+
+# ----------------------------------------------------------------------------
+# level fitting (checks on the level constants)
+# ----------------------------------------------------------------------------
+
+def lloyd_max_fit(samples: np.ndarray, iters: int = 60) -> np.ndarray:
+    """4-level scalar Lloyd-Max fit as the post describes it: start from the
+    0.125/0.375/0.625/0.875 quantiles, alternate nearest-level assignment and
+    centroid update for ``iters`` iterations, then make the set symmetric."""
+    v = np.sort(np.asarray(samples, dtype=np.float64).ravel())
+    L = np.quantile(v, [0.125, 0.375, 0.625, 0.875])
+    for _ in range(iters):
+        edges = (L[:-1] + L[1:]) / 2.0
+        cut = np.searchsorted(v, edges)
+        parts = np.split(v, cut)
+        L = np.array([p.mean() if p.size else L[i] for i, p in enumerate(parts)])
+    inner = (L[2] - L[1]) / 2.0
+    outer = (L[3] - L[0]) / 2.0
+    return np.array([-outer, -inner, inner, outer])
+
+
+def gaussian_lloyd_max_4(iters: int = 200) -> Tuple[float, float, float]:
+    """Fixed point of the centroid conditions of the 4-level quantizer for a
+    standard normal: inner = E[X | 0 < X < t], outer = E[X | X > t],
+    t = (inner + outer) / 2.  Returns (inner, outer, t)."""
+    phi = lambda a: math.exp(-a * a / 2.0) / math.sqrt(2.0 * math.pi)
+    Phi = lambda a: 0.5 * (1.0 + math.erf(a / math.sqrt(2.0)))
+    inner, outer = 0.5, 1.5
+    for _ in range(iters):
+        t = (inner + outer) / 2.0
+        inner = (phi(0.0) - phi(t)) / (Phi(t) - 0.5)
+        outer = phi(t) / (1.0 - Phi(t))
+    return inner, outer, (inner + outer) / 2.0
+
+
+# ----------------------------------------------------------------------------
+# storage accounting
+# ----------------------------------------------------------------------------
+
+def bits_per_weight(base: bool, resid_bits: int | None) -> float:
+    """Storage bits per weight: 2 code bits (+ b residual bits) and one fp16
+    scale per 128 weights for each part."""
+    bpw = 0.0
+    if base:
+        bpw += 2 + 16 / GROUP
+    if resid_bits:
+        bpw += resid_bits + 16 / GROUP
+    return bpw

@@ -1,0 +1,396 @@
+"""Pins for the CPU oracle: printed values, closed forms, invariants, brute force.
+
+Each test pins the oracle to something other than itself, chosen so that a
+plausible slip (a dropped term, a wrong sign or index, a transposed operand,
+a wrong rounding) fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+from oracle import nest_oracle as O
+from oracle import pack as P
+from nested_bit_quantized_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    out = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                out.append(line.split())
+    return out
+
+
+# ----------------------------------------------------------------------------
+# rotation
+# ----------------------------------------------------------------------------
+
+def test_block_size_printed_examples():
+    for n, b, nb in _rows("block_sizes.txt"):
+        n, b, nb = int(n), int(b), int(nb)
+        assert O.hadamard_block_size(n) == b
+        assert n // O.hadamard_block_size(n) == nb
+
+
+def test_block_size_rule_small():
+    # largest power of two dividing n, capped at 4096: odd n -> 1, 2^20 -> 4096
+    assert O.hadamard_block_size(1) == 1
+    assert O.hadamard_block_size(6) == 2
+    assert O.hadamard_block_size(96) == 32
+    assert O.hadamard_block_size(1 << 20) == 4096
+    assert O.hadamard_block_size(3 * 8192) == 4096
+
+
+@pytest.mark.parametrize("b", [1, 2, 4, 8, 16, 64, 256, 1024, 4096])
+def test_sylvester_is_textbook_walsh_hadamard(b):
+    # scipy.linalg.hadamard is the Sylvester construction (natural order)
+    assert np.array_equal(O.sylvester_unnormalised(b), scipy.linalg.hadamard(b).astype(np.float64))
+
+
+@pytest.mark.parametrize("b", [2, 8, 128, 512, 2048])
+def test_hadamard_orthonormal_symmetric_self_inverse(b):
+    Hu = O.sylvester_unnormalised(b)
+    assert np.array_equal(Hu @ Hu.T, b * np.eye(b))
+    H = O.sylvester(b)
+    assert np.array_equal(H, H.T)
+    assert np.allclose(H @ H, np.eye(b), atol=1e-12)
+
+
+def _dense_blockdiag(n):
+    b = O.hadamard_block_size(n)
+    Hb = scipy.linalg.hadamard(b) / math.sqrt(b)
+    return scipy.linalg.block_diag(*([Hb] * (n // b)))
+
+
+@pytest.mark.parametrize("M,K", [(64, 128), (48, 96), (24, 40), (16, 384)])
+def test_rotate_weights_matches_dense_formula(M, K):
+    rng = np.random.default_rng(1)
+    W = rng.normal(size=(M, K))
+    s_o = rng.choice([-1, 1], size=M).astype(np.int8)
+    s_i = rng.choice([-1, 1], size=K).astype(np.int8)
+    Ho, Hi = _dense_blockdiag(M), _dense_blockdiag(K)
+    ref = Ho @ np.diag(s_o.astype(float)) @ W @ np.diag(s_i.astype(float)) @ Hi
+    assert np.allclose(O.rotate_weights(W, s_o, s_i), ref, atol=1e-12)
+
+
+def test_rotation_exact_inverse_and_norm():
+    rng = np.random.default_rng(2)
+    M, K = 96, 256
+    W = rng.normal(size=(M, K))
+    s_o, s_i = synth.sign_pair(M, K, 11)
+    Wr = O.rotate_weights(W, s_o, s_i)
+    assert np.allclose(O.unrotate_weights(Wr, s_o, s_i), W, atol=1e-12)
+    assert math.isclose(np.linalg.norm(Wr), np.linalg.norm(W), rel_tol=1e-12)
+    # the rotation does change the matrix (signs and mixing are applied)
+    assert not np.allclose(Wr, W)
+
+
+def test_activation_rotation_dense_and_norm():
+    rng = np.random.default_rng(3)
+    T, K = 5, 384
+    x = rng.normal(size=(T, K))
+    s_i = synth.signs(K, 9)
+    Hi = _dense_blockdiag(K)
+    ref = (Hi @ np.diag(s_i.astype(float)) @ x.T).T
+    xr = O.rotate_activations(x, s_i)
+    assert np.allclose(xr, ref, atol=1e-12)
+    assert np.allclose(np.linalg.norm(xr, axis=1), np.linalg.norm(x, axis=1), rtol=1e-12)
+    # outputs: y = S_o H_o z is the inverse of z = H_o S_o y
+    z = rng.normal(size=(T, 96))
+    s_o = synth.signs(96, 4)
+    Ho = _dense_blockdiag(96)
+    assert np.allclose(O.unrotate_outputs(z, s_o), (np.diag(s_o.astype(float)) @ Ho @ z.T).T, atol=1e-12)
+
+
+def test_rotated_product_equals_plain_product():
+    # unquantized: S_o H_o (W~ x') == W x, which ties the activation rotation to the weight rotation
+    rng = np.random.default_rng(4)
+    M, K, T = 128, 512, 3
+    W = rng.normal(size=(M, K))
+    x = rng.normal(size=(T, K))
+    s_o, s_i = synth.sign_pair(M, K, 21)
+    Wr = O.rotate_weights(W, s_o, s_i)
+    y = O.unrotate_outputs(O.rotate_activations(x, s_i) @ Wr.T, s_o)
+    assert np.allclose(y, x @ W.T, atol=1e-10)
+
+
+# ----------------------------------------------------------------------------
+# levels
+# ----------------------------------------------------------------------------
+
+def test_gaussian_lloyd_max_closed_form_gives_levels():
+    inner, outer, t = O.gaussian_lloyd_max_4()
+    gold = {r[0]: (float(r[1]), float(r[2])) for r in _rows("levels.txt")}
+    assert round(inner, 4) == gold["gaussian"][0] == O.LEVELS[2]
+    assert round(outer, 4) == gold["gaussian"][1] == O.LEVELS[3]
+    assert O.LEVELS[0] == -O.LEVELS[3] and O.LEVELS[1] == -O.LEVELS[2]
+    assert abs(t - 0.9816) < 1e-3
+
+
+def test_lloyd_fit_on_rotated_weights_near_printed_fits():
+    # ~2M rotated weights normalised by their group RMS, quantile init, 60 iterations, symmetrised
+    M, K = 1024, 2048
+    W = synth.weights(M, K, 5, "entries").astype(np.float64)
+    s_o, s_i = synth.sign_pair(M, K, 5)
+    Wr = O.rotate_weights(W, s_o, s_i).reshape(M, K // 128, 128)
+    u = Wr / np.sqrt(np.mean(Wr * Wr, axis=2, keepdims=True))
+    L = O.lloyd_max_fit(u.ravel(), iters=60)
+    gold = {r[0]: (float(r[1]), float(r[2])) for r in _rows("levels.txt")}
+    for key in ("fitted_12b", "fitted_31b"):
+        gi, go = gold[key]
+        assert abs(L[2] - gi) / gi < 0.01
+        assert abs(L[3] - go) / go < 0.01
+    assert np.allclose(L, -L[::-1])
+
+
+# ----------------------------------------------------------------------------
+# 2-bit base
+# ----------------------------------------------------------------------------
+
+def _layer(M, K, bits, seed=7, outliers="entries"):
+    W = synth.weights(M, K, seed, outliers)
+    s_o, s_i = synth.sign_pair(M, K, seed + 100)
+    return W, s_o, s_i, O.quantize_layer(W, s_o, s_i, bits)
+
+
+def test_base_codes_bruteforce_nearest_level():
+    M, K = 32, 256
+    _, _, _, q = _layer(M, K, 8)
+    Wr, codes, s = q["Wr"], q["base_codes"], q["base_scales"].astype(np.float64)
+    for m in range(M):
+        for g in range(K // 128):
+            sc = s[m, g]
+            # scale: the fp16 value nearest the RMS (no fp16 value is closer)
+            blk = Wr[m, g * 128:(g + 1) * 128]
+            rms = math.sqrt(sum(v * v for v in blk) / 128.0)
+            s16 = np.float16(sc)
+            up = float(np.nextafter(s16, np.float16(np.inf)))
+            dn = float(np.nextafter(s16, np.float16(-np.inf)))
+            assert abs(sc - rms) <= abs(up - rms) and abs(sc - rms) <= abs(dn - rms)
+            for j in range(128):
+                w = blk[j]
+                dist = [abs(w - lv * sc) for lv in O.LEVELS]
+                assert codes[m, g * 128 + j] == int(np.argmin(dist))
+
+
+def test_base_relative_mse_is_gaussian_lloyd_max_distortion():
+    # textbook: the 4-level Lloyd-Max quantizer of a unit Gaussian has MSE 0.1175
+    M, K = 512, 4096
+    W = synth.weights(M, K, 8, None).astype(np.float64)
+    s_o, s_i = synth.sign_pair(M, K, 8)
+    Wr = O.rotate_weights(W, s_o, s_i)
+    c, s = O.quantize_base(Wr)
+    err = Wr - O.dequant_base(c, s)
+    rel = np.sum(err ** 2) / np.sum(Wr ** 2)
+    assert abs(rel - 0.1175) < 0.003
+
+
+def test_base_ties_and_zero_groups():
+    t = O.base_threshold()
+    Wr = np.zeros((2, 128))
+    Wr[1, :] = 1.0                      # RMS 1 -> scale 1.0 exactly
+    Wr[1, 0] = 0.0                      # u == 0 -> positive inner
+    Wr[1, 1] = -t                       # |u| == threshold -> inner level
+    Wr[1, 2] = np.nextafter(t, 2.0)     # just past it -> outer level
+    Wr[1, 3] = -5.0
+    # RMS is no longer 1 once entries change; compute what the scale must be
+    c, s = O.quantize_base(Wr)
+    assert s[0, 0] == 0 and np.all(c[0] == 2)            # zero group: code 2, zero base
+    assert np.all(O.dequant_base(c, s)[0] == 0.0)
+    sc = float(s[1, 0])
+    u = Wr[1] / sc
+    assert c[1, 0] == 2
+    assert c[1, 3] == 0
+    exp = np.where(u < 0, np.where(np.abs(u) > t, 0, 1), np.where(np.abs(u) > t, 3, 2))
+    assert np.array_equal(c[1], exp)
+
+
+# ----------------------------------------------------------------------------
+# residual
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [6, 7, 8])
+def test_residual_bruteforce_and_bound(bits):
+    M, K = 16, 256
+    _, _, _, q = _layer(M, K, bits, seed=9)
+    R = q["Wr"] - O.dequant_base(q["base_codes"], q["base_scales"])
+    rc, rs = q["resid_codes"], q["resid_scales"].astype(np.float64)
+    qm = (1 << (bits - 1)) - 1
+    levels = np.arange(-qm, qm + 1)
+    for m in range(M):
+        for g in range(K // 128):
+            sc = rs[m, g]
+            blk = R[m, g * 128:(g + 1) * 128]
+            assert np.max(np.abs(rc[m, g * 128:(g + 1) * 128])) == qm   # the block max maps to +-qm
+            for j in range(128):
+                d = np.abs(blk[j] - levels * sc)
+                assert abs(int(rc[m, g * 128 + j]) - levels[np.argmin(d)]) == 0 or \
+                    math.isclose(d.min(), d[int(rc[m, g * 128 + j]) + qm], rel_tol=1e-12)
+    E = R - O.dequant_residual(rc, q["resid_scales"])
+    half = np.repeat(rs, 128, axis=1) / 2.0
+    assert np.all(np.abs(E) <= half * (1 + 1e-12))
+
+
+def test_residual_zero_scale_gives_zero_codes():
+    R = np.zeros((1, 128))
+    q, s = O.quantize_residual(R, 7)
+    assert np.all(q == 0) and s[0, 0] == 0
+
+
+def test_residual_scale_is_fp16_of_absmax_over_qm():
+    rng = np.random.default_rng(5)
+    R = rng.normal(size=(3, 256)) * 1e-3
+    for bits in (6, 7, 8):
+        q, s = O.quantize_residual(R, bits)
+        qm = (1 << (bits - 1)) - 1
+        for m in range(3):
+            for g in range(2):
+                amax = max(abs(v) for v in R[m, g * 128:(g + 1) * 128])
+                assert s[m, g] == np.float16(amax / qm)
+
+
+# ----------------------------------------------------------------------------
+# forward passes
+# ----------------------------------------------------------------------------
+
+def test_draft_is_exact_subset_of_verify():
+    M, K, T = 64, 256, 4
+    W, s_o, s_i, q = _layer(M, K, 8)
+    _, x = synth.activations(T, K, 3)
+    q0 = dict(q)
+    q0["resid_codes"] = np.zeros_like(q["resid_codes"])
+    a = O.forward(q0, s_o, s_i, x, verify=True)
+    b = O.forward(q, s_o, s_i, x, verify=False)
+    assert np.array_equal(a["z"], b["z"]) and np.array_equal(a["y"], b["y"])
+
+
+@pytest.mark.parametrize("bits", [6, 8])
+def test_verify_matches_plain_product_within_residual_error(bits):
+    M, K, T = 256, 1024, 8
+    W, s_o, s_i, q = _layer(M, K, bits)
+    _, x = synth.activations(T, K, 4)
+    yv = O.forward(q, s_o, s_i, x, verify=True)["y"]
+    yd = O.forward(q, s_o, s_i, x, verify=False)["y"]
+    y = x.astype(np.float64) @ W.astype(np.float64).T
+    E = q["Wr"] - O.dense_rotated(q, verify=True)
+    bound = np.linalg.norm(E, 2) * np.linalg.norm(x, axis=1)
+    assert np.all(np.linalg.norm(yv - y, axis=1) <= bound * (1 + 1e-9))
+    # errors of the expected size: verify ~ residual rounding, draft ~ base distortion
+    ev = np.linalg.norm(yv - y) / np.linalg.norm(y)
+    ed = np.linalg.norm(yd - y) / np.linalg.norm(y)
+    qm = (1 << (bits - 1)) - 1
+    assert ev < 0.05 * 127 / qm / 10
+    assert 0.25 < ed < 0.45                     # sqrt(0.1175) = 0.343 for Gaussianised weights
+    assert ev < ed / 10
+
+
+def test_token_columns_are_independent():
+    M, K, T = 128, 512, 6
+    W, s_o, s_i, q = _layer(M, K, 7)
+    _, x = synth.activations(T, K, 6)
+    full = O.forward(q, s_o, s_i, x, verify=True)
+    for t in range(T):
+        one = O.forward(q, s_o, s_i, x[t:t + 1], verify=True)
+        assert np.allclose(one["y"][0], full["y"][t], rtol=1e-12, atol=1e-14)
+
+
+def test_bruteforce_tiny_forward():
+    # y[t][m] by explicit loops over the dense dequantised matrix and dense H.D
+    M, K, T = 16, 128, 2
+    W, s_o, s_i, q = _layer(M, K, 8, seed=12, outliers=None)
+    _, x = synth.activations(T, K, 13)
+    Wv = O.dense_rotated(q, verify=True)
+    Ho, Hi = _dense_blockdiag(M), _dense_blockdiag(K)
+    y = np.zeros((T, M))
+    for t in range(T):
+        xr = [sum(Hi[k, kk] * s_i[kk] * float(x[t, kk]) for kk in range(K)) for k in range(K)]
+        z = [sum(Wv[m, k] * xr[k] for k in range(K)) for m in range(M)]
+        for m in range(M):
+            y[t, m] = s_o[m] * sum(Ho[m, mm] * z[mm] for mm in range(M))
+    assert np.allclose(O.forward(q, s_o, s_i, x, verify=True)["y"], y, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# storage accounting and packing
+# ----------------------------------------------------------------------------
+
+def test_bits_per_weight_printed():
+    for label, bits, group, bpw in _rows("bits_per_weight.txt"):
+        bits, group, bpw = int(bits), int(group), float(bpw)
+        assert bits + 16 / group == bpw
+    assert O.bits_per_weight(True, None) == 2.125
+    for b, v in ((6, 6.125), (7, 7.125), (8, 8.125)):
+        assert O.bits_per_weight(False, b) == v
+    assert O.bits_per_weight(True, 8) == 10.25
+
+
+@pytest.mark.parametrize("bits", [6, 7, 8])
+def test_packed_sizes_match_accounting(bits):
+    M, K = 256, 512
+    assert P.base_bytes(M, K) * 8 / (M * K) == O.bits_per_weight(True, None)
+    assert P.resid_bytes(M, K, bits) * 8 / (M * K) == O.bits_per_weight(False, bits)
+
+
+def test_storage_printed_approximately():
+    for name, layers, gb in _rows("storage_gb.txt"):
+        wl = synth.WORKLOADS[name]
+        n = sum(l.M * l.K for l in wl.linears) * int(layers)
+        est = n * O.bits_per_weight(True, None) / 8 / 1e9
+        assert abs(est - float(gb)) / float(gb) < 0.03
+
+
+@pytest.mark.parametrize("M,K,bits", [(128, 128, 8), (200, 256, 7), (77, 384, 6), (1, 128, 8)])
+def test_pack_roundtrip(M, K, bits):
+    bc, bs, rc, rs = synth.uniform_codes(M, K, bits, 17)
+    pb = P.pack_base(bc, bs)
+    pr = P.pack_resid(rc, rs, bits)
+    c2, s2 = P.unpack_base(pb, M, K)
+    r2, t2 = P.unpack_resid(pr, M, K, bits)
+    assert np.array_equal(c2, bc) and np.array_equal(s2, bs)
+    assert np.array_equal(r2, rc) and np.array_equal(t2, rs)
+
+
+def _word(buf, unit_off, r, w):
+    off = unit_off + ((w // 4) * 128 + r) * 16 + (w % 4) * 4
+    return int.from_bytes(bytes(buf[off:off + 4]), "little")
+
+
+def test_pack_hand_worked_examples():
+    # base: column j holds code j % 4.  Column 16w + 4p + q sits at bits 8q + 2p, so byte q of
+    # every word holds the code q four times: bytes 00 55 AA FF, word 0xFFAA5500.
+    M, K = 1, 128
+    bc = (np.arange(K) % 4).astype(np.uint8)[None, :]
+    bs = np.array([[0x3C00]], dtype=np.uint16)               # fp16 1.0
+    pb = P.pack_base(bc, bs)
+    assert pb.size == 4352
+    for w in range(8):
+        assert _word(pb, 0, 0, w) == 0xFFAA5500
+    assert pb[4096] == 0x00 and pb[4097] == 0x3C
+    assert not pb[16:2048].any()                              # rows 1..127 of chunk 0 are padding
+    # residual b = 8: q_j = j - 64 stored as u = j + 64, column 4w + q in byte q of word w
+    rc = (np.arange(K) - 64).astype(np.int8)[None, :]
+    pr = P.pack_resid(rc, np.array([[0x1234]], np.uint16), 8)
+    for w in range(32):
+        assert _word(pr, 0, 0, w) == sum((4 * w + q + 64) << (8 * q) for q in range(4))
+    assert pr[16384] == 0x34 and pr[16385] == 0x12
+    # rows past M store q = 0 (u = 128) and scale 0
+    assert _word(pr, 0, 1, 0) == 0x80808080
+    # residual b = 7: all q = 0 (u = 64 = 0b1000000) except column 5 with q = 63 (u = 127)
+    rc = np.zeros((1, K), np.int8)
+    rc[0, 5] = 63
+    pr = P.pack_resid(rc, np.array([[0]], np.uint16), 7)
+    # column 5 = 8*0 + 4*1 + 1: low nibble 15 at bits 8*1 + 4 = 12..15 of word 0
+    assert _word(pr, 0, 0, 0) == 0x0000F000
+    assert all(_word(pr, 0, 0, w) == 0 for w in range(1, 16))
+    # column 5 = 16*0 + 4*1 + 1: middle pair 3 at bits 8*1 + 2*1 = 10..11 of word 16
+    assert _word(pr, 0, 0, 16) == 0x00000C00
+    assert all(_word(pr, 0, 0, w) == 0 for w in range(17, 24))
+    # bit 6 of u is 1 for every column (u = 64 and u = 127): words 24..27 all ones
+    assert all(_word(pr, 0, 0, w) == 0xFFFFFFFF for w in range(24, 28))
