@@ -1,0 +1,385 @@
+"""Benchmark of the nested-bit quantized linear layer on one GB300 (or N replicas).
+
+Workload: the Qwen-4B-like MLP triplet (gate and up 9728x2560, down 2560x9728),
+2-bit base + 7-bit residual with 128-column fp16 scales, synthetic
+N(0, 0.02^2) weights with 0.5% Student-t(4) outliers, bf16 N(0,1)
+activations.  Weights are quantised and packed on the device by the library
+itself.  `--copies` distinct quantised copies of the triplet (a stack of
+layers) are resident in HBM so each pass streams far more than the 129 MB L2.
+
+One step = one speculative check over the stack: a draft pass at T = 1
+(rotate in, base-only GEMV, rotate out for every linear), then a verify pass
+at T = 16 (rotate in, base + residual GEMM, rotate out).  `value` is the
+effective HBM bandwidth of the step: the algorithmic bytes of every linear
+(M*K*(2.125 [+ b + 0.125])/8 weight bytes + 2*T*K input + 4*T*M output bytes)
+divided by the step time.  The verify GEMM alone is timed as well (at T = 16
+and T = 1) and carries the roofline figure.
+
+`--impl reference` times the CPU oracle (numpy fp64) on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify GEMM effective HBM GB/s and µs/layer at T=16 (vs T=1), % of 8 TB/s roofline"
+WORKLOAD = "mlp_triplet_4b"
+BITS = 7
+T_VERIFY, T_DRAFT = 16, 1
+
+
+def lin_bytes(M, K, T, bits):
+    w = M * K * (2.125 + ((bits + 0.125) if bits else 0.0)) / 8.0
+    return w + 2.0 * T * K + 4.0 * T * M
+
+
+def weight_bytes(M, K, bits):
+    return M * K * (2.125 + ((bits + 0.125) if bits else 0.0)) / 8.0
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and --impl reference)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(n_linears=3, seconds_cap=25.0):
+    """Times the oracle's draft (T=1) and verify (T=16) forward passes on the
+    workload's linears (offline quantisation excluded).  Returns bytes, seconds, what."""
+    import numpy as np
+    from nested_bit_quantized_gb300 import synth
+    from oracle import nest_oracle as O
+    wl = synth.WORKLOADS[WORKLOAD]
+    tot_b, tot_s, done = 0.0, 0.0, []
+    for lin in wl.linears[:n_linears]:
+        W = synth.weights(lin.M, lin.K, lin.w_seed, lin.outliers)
+        s_o, s_i = synth.sign_pair(lin.M, lin.K, lin.sign_seed)
+        q = O.quantize_layer(W, s_o, s_i, BITS)
+        for T, verify in ((T_DRAFT, False), (T_VERIFY, True)):
+            _, x = synth.activations(T, lin.K, wl.x_seed)
+            t0 = time.perf_counter()
+            O.forward(q, s_o, s_i, x, verify)
+            tot_s += time.perf_counter() - t0
+            tot_b += lin_bytes(lin.M, lin.K, T, BITS if verify else 0)
+        done.append(lin.name)
+        if tot_s > seconds_cap:
+            break
+    what = (f"oracle draft T={T_DRAFT} + verify T={T_VERIFY} forward of {'/'.join(done)} "
+            f"(one copy, quantisation untimed)")
+    return tot_b, tot_s, what
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    tot_b = tot_s = 0.0
+    what = ""
+    for i in range(args.warmup + args.steps):
+        b, s, what = oracle_sample(n_linears=1)
+        if i >= args.warmup:
+            tot_b += b
+            tot_s += s
+    value = tot_b / tot_s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "bits": BITS, "T_verify": T_VERIFY, "T_draft": T_DRAFT,
+                       "sample": what},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle", "sample": what},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args, rank, world):
+    import numpy as np
+    import torch
+    from nested_bit_quantized_gb300 import build as nb
+    from nested_bit_quantized_gb300 import nest, synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    nb.build()
+    nest.load()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    C = args.copies
+    # quantise and pack C copies of the triplet on the device
+    layers = []
+    work = None
+    for c in range(C):
+        trip = []
+        for lin in wl.linears:
+            seed = lin.w_seed + 1000 * c + 100_000 * rank
+            W = synth.weights_device(lin.M, lin.K, seed, lin.outliers, dev)
+            s_o, s_i = synth.sign_pair(lin.M, lin.K, lin.sign_seed + 2 * c)
+            if work is None or work.numel() < lin.M * lin.K:
+                work = torch.empty(lin.M * lin.K, dtype=torch.float64, device=dev)
+            q = nest.quantize(W, torch.from_numpy(s_o).to(dev), torch.from_numpy(s_i).to(dev), BITS,
+                              work=work[:lin.M * lin.K].view(lin.M, lin.K))
+            trip.append(nest.pack(q["base_codes"], q["base_scales"], q["resid_codes"], q["resid_scales"], BITS,
+                                  torch.from_numpy(s_o).to(dev), torch.from_numpy(s_i).to(dev)))
+            del W, q
+        layers.append(trip)
+    del work
+    torch.cuda.synchronize()
+
+    # activations (bf16), one per (input width, T)
+    xs = {}
+    for T in (T_DRAFT, T_VERIFY):
+        for K in sorted({l.K for l in wl.linears}):
+            b, _ = synth.activations(T, K, wl.x_seed + K + T)
+            xs[(K, T)] = torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+    maxM = max(l.M for l in wl.linears)
+    maxK = max(l.K for l in wl.linears)
+    scratch = torch.zeros(max(nest.linear_scratch_bytes(l.M, l.K, T) for l in wl.linears
+                              for T in (T_DRAFT, T_VERIFY)), dtype=torch.uint8, device=dev)
+    ys = {(l.M, T): torch.empty((T, l.M), dtype=torch.float32, device=dev) for l in wl.linears
+          for T in (T_DRAFT, T_VERIFY)}
+    xops = {(l.K, T): nest.new_xop(l.K, T, dev) for l in wl.linears for T in (T_DRAFT, T_VERIFY)}
+    zbuf = torch.empty((64, maxM), dtype=torch.float32, device=dev)
+    ws = nest.new_workspace(maxM, maxK, 64, dev)
+    for l in wl.linears:
+        assert ws.numel() >= nest.workspace_bytes(l.M, l.K, T_VERIFY)
+
+    def step():
+        for trip in layers:                      # draft pass through the stack
+            for L in trip:
+                nest.linear(L, xs[(L.K, T_DRAFT)], False, y=ys[(L.M, T_DRAFT)], scratch=scratch)
+        for trip in layers:                      # verify pass through the stack
+            for L in trip:
+                nest.linear(L, xs[(L.K, T_VERIFY)], True, y=ys[(L.M, T_VERIFY)], scratch=scratch)
+
+    def gemm_only(T, verify):
+        for trip in layers:
+            for L in trip:
+                nest.gemm(L, xops[(L.K, T)], T, verify, z=zbuf[:T, :L.M], workspace=ws)
+
+    # operands for the GEMM-only regions
+    for l in layers[0]:
+        for T in (T_DRAFT, T_VERIFY):
+            nest.rotate(xs[(l.K, T)], l.sign_in, 0, x_op=xops[(l.K, T)])
+
+    stream = torch.cuda.Stream(device=dev)
+    graphs = {}
+    with torch.cuda.stream(stream):
+        for name, fn in (("step", step), ("v16", lambda: gemm_only(T_VERIFY, True)),
+                         ("v1", lambda: gemm_only(T_DRAFT, True)), ("d1", lambda: gemm_only(T_DRAFT, False))):
+            fn()                                  # first launches configure the kernels
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            graphs[name] = g
+    torch.cuda.synchronize()
+    nest.error_check()
+
+    def timed(g, reps, warm):
+        for _ in range(warm):
+            g.replay()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            s.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e.record(stream)
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e)
+        if dist is not None:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    n_lin = 3 * C
+    step_bytes = sum(lin_bytes(L.M, L.K, T_DRAFT, 0) + lin_bytes(L.M, L.K, T_VERIFY, BITS)
+                     for trip in layers for L in trip)
+    with ClockSampler(local) as clk:
+        ms = timed(graphs["step"], args.steps, args.warmup)
+    clocks = clk.summary()
+    ms_step = ms / args.steps
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+
+    sub = {}
+    for name, T, bits in (("v16", T_VERIFY, BITS), ("v1", T_DRAFT, BITS), ("d1", T_DRAFT, 0)):
+        reps = max(3, args.steps)
+        tms = timed(graphs[name], reps, max(3, args.warmup)) / reps
+        per = tms * 1e3 / n_lin                   # us per launch (all three linears move equal bytes)
+        by = sum(lin_bytes(L.M, L.K, T, bits) for L in layers[0]) / 3
+        sub[name] = {"us_per_gemm": per, "GBps": by / (per * 1e-6) / 1e9, "bytes_per_gemm": by}
+    hbm, src = peaks()
+
+    # end to end through the public API: pinned host inputs in, the last verify output back
+    host_x = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in xs.items()}
+    for k in xs:
+        host_x[k].copy_(xs[k].cpu())
+    last = layers[-1][-1]
+    host_y = torch.empty(ys[(last.M, T_VERIFY)].shape, dtype=torch.float32, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host_x.values())
+    d2h = host_y.numel() * 4
+
+    def e2e_once():
+        with torch.cuda.stream(stream):
+            for k in xs:
+                xs[k].copy_(host_x[k], non_blocking=True)
+            graphs["step"].replay()
+            host_y.copy_(ys[(last.M, T_VERIFY)], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_once()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(args.steps):
+        e2e_once()
+    e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s.elapsed_time(e) / args.steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    nest.error_check()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        b, sec, what = oracle_sample()
+        cpu = {"value": b / sec / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle", "sample": what}
+
+    if rank == 0:
+        v16, v1, d1 = sub["v16"], sub["v1"], sub["d1"]
+        ach = v16["GBps"]
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": "mlp_triplet_4b: gate/up 9728x2560, down 2560x9728, 2-bit base + 7-bit "
+                                   "residual, g128 fp16 scales; draft T=1 then verify T=16 per step",
+                       "copies": C, "resident_weight_GB": C * sum(weight_bytes(l.M, l.K, BITS) for l in wl.linears) / 1e9,
+                       "l2": f"inputs larger than L2: {C} distinct quantised triplet copies per pass",
+                       "accumulate": "f32", "parallelism": f"replicas x{world}"},
+            "verify_T16": {"us_per_gemm": v16["us_per_gemm"], "GBps": v16["GBps"],
+                           "frac_of_8TBps": v16["GBps"] / 8000.0},
+            "verify_T1": {"us_per_gemm": v1["us_per_gemm"], "GBps": v1["GBps"]},
+            "t16_over_t1": v16["us_per_gemm"] / v1["us_per_gemm"],
+            "draft_T1": {"us_per_gemm": d1["us_per_gemm"], "GBps": d1["GBps"]},
+            "roofline": {"bound": "hbm", "kernel": "k_nest_gemm<7,16> (verify, T=16)", "achieved": ach,
+                         "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": src,
+                         "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 18 * C * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="nest", choices=["nest", "reference"])
+    ap.add_argument("--copies", type=int, default=12)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world if "RANK" in os.environ else 1)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+/*
+ * libnest -- nested-bit quantized linear layer for GB300 (sm_103a).
+ *
+ * One weight matrix W (M = d_out rows, K = d_in columns) is stored once, in
+ * a randomized-Hadamard-rotated basis W~ = H_o S_o W S_i H_i, as
+ *   - a 2-bit base: 4 Lloyd-Max levels (+-0.4528, +-1.5104) times an fp16
+ *     scale per (row, 128-column group), the scale being the RMS of the block;
+ *   - a b-bit residual (b = 6, 7, 8): the error W~ - Q_base on a uniform
+ *     symmetric grid -qm..qm, qm = 2^(b-1) - 1, with an fp16 scale
+ *     max|block|/qm per (row, 128-group).
+ * Source: feedman.me/posts/wZBTJ (2-bit base in VRAM + residual in RAM
+ * post), POC recipe steps 1-4.  The draft pass reads the base alone
+ * (z = Q_base x'); the verify pass reads both parts in one weight-streaming
+ * pass over all T tokens of a draft tree (z = (Q_base + Q_resid) x').  Base
+ * and residual are separate buffers so the draft never fetches residual
+ * bytes (BitNest, arXiv 2610.02800, section 3.3 "Dual-Plane Weight
+ * Storage").
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller, except
+ *     where an argument says "host".  The library allocates no memory.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream).  No entry point
+ *     synchronises, except nest_error_check.
+ *   - Arguments are validated on the host before any launch; a bad argument
+ *     returns an error status and launches nothing.
+ *   - Pointers must be 16-byte aligned unless stated otherwise
+ *     (NEST_ERR_MISALIGNED otherwise).
+ *   - Inputs and outputs must not overlap.
+ *   - Supported envelope of the GEMMs: K % 128 == 0, any M >= 1,
+ *     1 <= T <= 64.  Device: compute capability 10.3 (sm_103a).
+ *
+ * Storage format (packed buffers): arrays of UNITS, one unit per (tile of
+ * 128 output rows, 128-column group), tile-major.  A base unit is 4352 bytes
+ * (4096 bytes of 2-bit codes for 128 rows x 128 columns + 128 fp16 scales);
+ * a residual unit is 2048*b + 256 bytes.  The bit layout inside a unit is
+ * specified in nest_pack below.  Rows past M in the last tile are padding.
+ *
+ * Activation operand ("x_op"): the rotated activations x' = H_i S_i x in
+ * fp16, laid out as the GEMM reads them: per 128-column group g, a block of
+ * 256*Np bytes (Np = T rounded up to 16, 32 or 64); inside it, the fp16
+ * value of token t, column k = 128 g + 8 c + e sits at byte
+ * ((c * Np/8 + t/8) * 8 + t%8) * 16 + 2 e.  Rows t >= T are never read
+ * into an output.
+ */
+#ifndef NEST_H
+#define NEST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NEST_OK = 0,
+    NEST_ERR_INVALID_ARG = 1,   /* null pointer, negative or zero size, bad enum */
+    NEST_ERR_UNSUPPORTED = 2,   /* outside the supported envelope (K % 128, T > 64, bits, device) */
+    NEST_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    NEST_ERR_CUDA = 4,          /* a CUDA runtime call or a launch failed */
+    NEST_ERR_TIMEOUT = 5        /* a kernel gave up waiting on a pipeline barrier (nest_error_check) */
+} nest_status;
+
+/* A packed layer.  Plain descriptor; the pointers are device pointers owned by the caller. */
+typedef struct {
+    int32_t M;                  /* d_out, >= 1 */
+    int32_t K;                  /* d_in, multiple of 128 */
+    int32_t resid_bits;         /* 6, 7 or 8; 0 = base only (draft-only layer) */
+    const uint8_t* base;        /* nest_base_bytes(M, K) bytes */
+    const uint8_t* resid;       /* nest_resid_bytes(M, K, resid_bits) bytes, or NULL if resid_bits == 0 */
+    const int8_t* sign_out;     /* S_o, M entries of +-1 */
+    const int8_t* sign_in;      /* S_i, K entries of +-1 */
+} nest_layer;
+
+/* Human-readable name of a status. */
+const char* nest_status_string(nest_status s);
+
+/* ---- sizes (host-only, no device work) --------------------------------- */
+
+/* Hadamard block size of a dimension n: the largest power of two dividing n,
+ * capped at 4096 (feedman.me/posts/wZBTJ, POC recipe step 1).  0 if n < 1. */
+int32_t nest_hadamard_block(int32_t n);
+
+/* Bytes of the packed base buffer: ceil(M/128) * (K/128) * 4352.  0 if the shape is unsupported. */
+size_t nest_base_bytes(int32_t M, int32_t K);
+
+/* Bytes of the packed residual buffer: ceil(M/128) * (K/128) * (2048*bits + 256). */
+size_t nest_resid_bytes(int32_t M, int32_t K, int32_t bits);
+
+/* Bytes of the activation operand for K columns and T tokens: (K/128) * 256 * Np. */
+size_t nest_xop_bytes(int32_t K, int32_t T);
+
+/* Bytes of the GEMM workspace (partial sums of row tiles split across CTAs,
+ * and one counter per tile).  The workspace must be zero-filled once after
+ * allocation; every call that completes leaves its counters at zero again.
+ * Calls that share a workspace must not run concurrently. */
+size_t nest_workspace_bytes(int32_t M, int32_t K, int32_t T);
+
+/* ---- offline: quantize and pack --------------------------------------- */
+
+/* RTN quantizer of one layer (feedman.me/posts/wZBTJ, POC recipe steps 1-3,
+ * without the GPTQ/LDLQ error feedback), computed in fp64:
+ *   W~ = H_o S_o W S_i H_i (block-diagonal Sylvester Hadamard, 1/sqrt(b));
+ *   base: s_b = fp16(RMS of the (row, group) block), code = nearest level of
+ *         W~/s_b (index 0..3 into -1.5104, -0.4528, +0.4528, +1.5104; |u| at the
+ *         inner/outer midpoint goes inner, u == 0 goes to +0.4528; s_b == 0 gives code 2);
+ *   residual: R = W~ - L[code] s_b; s_r = fp16(max|R| / qm);
+ *             q = clip(rint(R / s_r), -qm, qm) (half to even; s_r == 0 gives 0).
+ * W          float32 [M][K] (device).
+ * sign_out   int8 [M] +-1; sign_in int8 [K] +-1.
+ * work       fp64 scratch of M*K doubles (device, 16-byte aligned), overwritten.
+ * base_codes uint8 [M][K] out (0..3); base_scales fp16 bits [M][K/128] out.
+ * resid_codes int8 [M][K] out; resid_scales fp16 bits [M][K/128] out
+ *            (both may be NULL when bits == 0).
+ * Pointers to uint8/int8/fp16 arrays need only natural alignment. */
+nest_status nest_quantize(const float* W, const int8_t* sign_out, const int8_t* sign_in,
+                          int32_t M, int32_t K, int32_t bits, double* work,
+                          uint8_t* base_codes, uint16_t* base_scales,
+                          int8_t* resid_codes, uint16_t* resid_scales, void* stream);
+
+/* Pack codes and scales into the unit format (storage of POC recipe steps 2-3).
+ * base_codes  uint8 [M][K], values 0..3 (level index, ascending).
+ * base_scales fp16 bits [M][K/128].
+ * resid_codes int8 [M][K] in [-qm, qm]; resid_scales fp16 bits [M][K/128]
+ *             (NULL with bits == 0 to pack the base alone).
+ * base_out    nest_base_bytes(M, K) bytes; resid_out nest_resid_bytes(M, K, bits).
+ * Unit bit layout (row r = 0..127 of the tile, a row's words are 32-bit little endian,
+ * word w of row r at unit byte ((w/4)*128 + r)*16 + (w%4)*4):
+ *   base: words 0..7; column 16w + 4p + q (p, q in 0..3) at bits 8q + 2p..8q + 2p + 1;
+ *         fp16 scale of row r at unit byte 4096 + 2r.
+ *   residual, stored u = q + 2^(b-1):
+ *     b = 8: words 0..31, column 4w + q in byte q of word w;
+ *     b = 6, 7: words 0..15 hold u & 15, column 8a + 4h + q of word a at bits 8q + 4h;
+ *               words 16..23 hold (u >> 4) & 3, column 16a + 4p + q of word 16 + a at bits 8q + 2p;
+ *               b = 7 only: words 24..27 hold (u >> 6) & 1, column 32a + 4p + q of word 24 + a at bit 8q + p;
+ *     fp16 scale of row r at unit byte 2048*b + 2r.
+ *   Rows past M: codes 0, residual q = 0, scales 0. */
+nest_status nest_pack(const uint8_t* base_codes, const uint16_t* base_scales,
+                      const int8_t* resid_codes, const uint16_t* resid_scales,
+                      int32_t M, int32_t K, int32_t bits,
+                      uint8_t* base_out, uint8_t* resid_out, void* stream);
+
+/* Inverse of nest_pack (used by tests).  resid_* may be NULL when layer->resid_bits == 0. */
+nest_status nest_unpack(const nest_layer* layer, uint8_t* base_codes, uint16_t* base_scales,
+                        int8_t* resid_codes, uint16_t* resid_scales, void* stream);
+
+/* ---- per-forward kernels ----------------------------------------------- */
+
+/* Randomized Hadamard rotation of T vectors of length n (POC recipe steps 1 and 4).
+ * mode 0 (input side):  out_t = H S x_t   (signs first, then the block FWHT);
+ * mode 1 (output side): out_t = S H x_t   (block FWHT first, then the signs).
+ * H is block-diagonal with Sylvester blocks of size nest_hadamard_block(n), each scaled by 1/sqrt(b).
+ * x        [T][n], fp32 (x_dtype 0) or bf16 bits (x_dtype 1).
+ * signs    int8 [n] +-1 (natural alignment).
+ * y        fp32 [T][n] out, or NULL.
+ * x_op     activation operand out (mode 0 only, n % 128 == 0, T <= 64), or NULL.
+ * At least one of y, x_op must be given.  n >= 1, T >= 1. */
+nest_status nest_rotate(const void* x, int32_t x_dtype, const int8_t* signs, int32_t n, int32_t T,
+                        int32_t mode, float* y, uint16_t* x_op, void* stream);
+
+/* Draft GEMV/GEMM: z[t][m] = sum_k Q_base[m][k] x'[t][k] for t < T, in the rotated
+ * output basis (POC recipe step 4, "the same but without y_r").  Reads the base buffer only.
+ * x_op      activation operand from nest_rotate (T tokens).
+ * z         fp32 [T][M] out.
+ * workspace nest_workspace_bytes(M, K, T) bytes (see there). */
+nest_status nest_draft_gemv(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T,
+                            void* workspace, void* stream);
+
+/* Verify GEMM: z[t][m] = sum_k (Q_base + Q_resid)[m][k] x'[t][k] for t < T, one pass over
+ * both buffers for all T tokens (POC recipe step 4: y_b + y_r before the output rotation).
+ * Needs layer->resid_bits in {6, 7, 8}.  Arguments as nest_draft_gemv. */
+nest_status nest_verify_gemm(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T,
+                             void* workspace, void* stream);
+
+/* Whole linear: y = S_o H_o (Q x'), x' = H_i S_i x (rotate in, GEMM, rotate out).
+ * verify  0 = draft (base only), 1 = verify (base + residual).
+ * x       [T][K] fp32 (x_dtype 0) or bf16 bits (x_dtype 1).
+ * y       fp32 [T][M] out.
+ * scratch nest_linear_scratch_bytes(M, K, T) bytes; its workspace part obeys the
+ *         rules of nest_workspace_bytes (zero-filled once). */
+size_t nest_linear_scratch_bytes(int32_t M, int32_t K, int32_t T);
+nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype,
+                        int32_t T, float* y, void* scratch, void* stream);
+
+/* Reads and clears the device-side error flag that kernels set when a pipeline
+ * wait runs past its limit.  Synchronises `stream`.  Returns NEST_ERR_TIMEOUT if
+ * the flag was set, NEST_ERR_CUDA on a CUDA error, NEST_OK otherwise. */
+nest_status nest_error_check(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NEST_H */

@@ -1,0 +1,235 @@
+// C-ABI entry points of libnest (declared in include/nest.h): host-side
+// argument validation, launch configuration, and status codes.  No entry
+// point allocates memory or synchronises (except nest_error_check).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/nest.h"
+#include "nest_internal.h"
+
+using namespace nest;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+nest_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NEST_OK : NEST_ERR_CUDA; }
+
+// number of SMs of the current device (queried once per device)
+int device_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
+// the tcgen05 kernels are built for sm_103a only
+bool device_supported() {
+    static int cached[64] = {0};   // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (cached[dev] == 0) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return cached[dev] == 1;
+}
+
+bool bits_ok(int bits) { return bits == 6 || bits == 7 || bits == 8; }
+
+nest_status check_layer(const nest_layer* L, bool need_resid) {
+    if (L == nullptr) return NEST_ERR_INVALID_ARG;
+    if (L->M < 1 || L->K < 1) return NEST_ERR_INVALID_ARG;
+    if (L->K % 128 != 0) return NEST_ERR_UNSUPPORTED;
+    if (L->base == nullptr) return NEST_ERR_INVALID_ARG;
+    if (!aligned16(L->base)) return NEST_ERR_MISALIGNED;
+    if (need_resid) {
+        if (!bits_ok(L->resid_bits)) return L->resid_bits == 0 ? NEST_ERR_INVALID_ARG : NEST_ERR_UNSUPPORTED;
+        if (L->resid == nullptr) return NEST_ERR_INVALID_ARG;
+        if (!aligned16(L->resid)) return NEST_ERR_MISALIGNED;
+    } else if (L->resid_bits != 0 && !bits_ok(L->resid_bits)) {
+        return NEST_ERR_UNSUPPORTED;
+    }
+    return NEST_OK;
+}
+
+nest_status run_gemm(const nest_layer* L, int bits, const uint16_t* xop, float* z, int T, void* ws, void* stream) {
+    nest_status st = check_layer(L, bits != 0);
+    if (st != NEST_OK) return st;
+    if (xop == nullptr || z == nullptr || ws == nullptr) return NEST_ERR_INVALID_ARG;
+    if (T < 1) return NEST_ERR_INVALID_ARG;
+    if (T > 64) return NEST_ERR_UNSUPPORTED;
+    if (!aligned16(xop) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(z) & 3u)) return NEST_ERR_MISALIGNED;
+    if (!device_supported()) return NEST_ERR_UNSUPPORTED;
+    const int sms = device_sms();
+    if (sms <= 0) return NEST_ERR_CUDA;
+    GemmArgs a;
+    a.base = L->base;
+    a.resid = bits ? L->resid : nullptr;
+    a.xop = xop;
+    a.z = z;
+    a.counters = reinterpret_cast<int*>(ws);
+    a.partial = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + ws_counter_bytes(L->M));
+    a.M = L->M;
+    a.K = L->K;
+    a.T = T;
+    a.G = L->K / 128;
+    a.units = (long long)n_tiles(L->M) * a.G;
+    long long grid = a.units < sms ? a.units : sms;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+    return from_cuda(launch_gemm(a, bits, (int)grid, as_stream(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nest_status_string(nest_status s) {
+    switch (s) {
+        case NEST_OK: return "ok";
+        case NEST_ERR_INVALID_ARG: return "invalid argument";
+        case NEST_ERR_UNSUPPORTED: return "unsupported shape, bit width or device";
+        case NEST_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case NEST_ERR_CUDA: return "CUDA error";
+        case NEST_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    }
+    return "unknown status";
+}
+
+int32_t nest_hadamard_block(int32_t n) { return hadamard_block(n); }
+
+size_t nest_base_bytes(int32_t M, int32_t K) {
+    if (M < 1 || K < 1 || K % 128) return 0;
+    return (size_t)n_tiles(M) * (K / 128) * 4352;
+}
+
+size_t nest_resid_bytes(int32_t M, int32_t K, int32_t bits) {
+    if (M < 1 || K < 1 || K % 128 || !bits_ok(bits)) return 0;
+    return (size_t)n_tiles(M) * (K / 128) * (2048 * (size_t)bits + 256);
+}
+
+size_t nest_xop_bytes(int32_t K, int32_t T) {
+    if (K < 1 || K % 128 || T < 1 || T > 64) return 0;
+    return (size_t)(K / 128) * 256 * n_pad(T);
+}
+
+size_t nest_workspace_bytes(int32_t M, int32_t K, int32_t T) {
+    if (M < 1 || K < 1 || K % 128 || T < 1 || T > 64) return 0;
+    return ws_counter_bytes(M) + ws_partial_bytes(M, K, T);
+}
+
+nest_status nest_quantize(const float* W, const int8_t* sign_out, const int8_t* sign_in, int32_t M, int32_t K,
+                          int32_t bits, double* work, uint8_t* base_codes, uint16_t* base_scales,
+                          int8_t* resid_codes, uint16_t* resid_scales, void* stream) {
+    if (!W || !sign_out || !sign_in || !work || !base_codes || !base_scales) return NEST_ERR_INVALID_ARG;
+    if (M < 1 || K < 1) return NEST_ERR_INVALID_ARG;
+    if (K % 128) return NEST_ERR_UNSUPPORTED;
+    if (bits != 0 && !bits_ok(bits)) return NEST_ERR_UNSUPPORTED;
+    if (bits != 0 && (!resid_codes || !resid_scales)) return NEST_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(work)) return NEST_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(base_scales) & 1u) || (bits && (reinterpret_cast<uintptr_t>(resid_scales) & 1u)))
+        return NEST_ERR_MISALIGNED;
+    if ((long long)M * (K / hadamard_block(K)) > 0x7fffffffLL) return NEST_ERR_UNSUPPORTED;
+    return from_cuda(launch_quantize(W, sign_out, sign_in, M, K, bits, work, base_codes, base_scales,
+                                     resid_codes, resid_scales, as_stream(stream)));
+}
+
+nest_status nest_pack(const uint8_t* base_codes, const uint16_t* base_scales, const int8_t* resid_codes,
+                      const uint16_t* resid_scales, int32_t M, int32_t K, int32_t bits, uint8_t* base_out,
+                      uint8_t* resid_out, void* stream) {
+    if (!base_codes || !base_scales || !base_out) return NEST_ERR_INVALID_ARG;
+    if (M < 1 || K < 1) return NEST_ERR_INVALID_ARG;
+    if (K % 128) return NEST_ERR_UNSUPPORTED;
+    if (bits != 0 && !bits_ok(bits)) return NEST_ERR_UNSUPPORTED;
+    if (bits != 0 && (!resid_codes || !resid_scales || !resid_out)) return NEST_ERR_INVALID_ARG;
+    if (!aligned16(base_out) || (bits && !aligned16(resid_out))) return NEST_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(base_scales) & 1u) || (bits && (reinterpret_cast<uintptr_t>(resid_scales) & 1u)))
+        return NEST_ERR_MISALIGNED;
+    return from_cuda(launch_pack(base_codes, base_scales, resid_codes, resid_scales, M, K, bits, base_out,
+                                 resid_out, as_stream(stream)));
+}
+
+nest_status nest_unpack(const nest_layer* layer, uint8_t* base_codes, uint16_t* base_scales, int8_t* resid_codes,
+                        uint16_t* resid_scales, void* stream) {
+    nest_status st = check_layer(layer, false);
+    if (st != NEST_OK) return st;
+    const int bits = layer->resid_bits;
+    if (!base_codes || !base_scales) return NEST_ERR_INVALID_ARG;
+    if (bits && (!layer->resid || !resid_codes || !resid_scales)) return NEST_ERR_INVALID_ARG;
+    if (bits && !aligned16(layer->resid)) return NEST_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(base_scales) & 1u) || (bits && (reinterpret_cast<uintptr_t>(resid_scales) & 1u)))
+        return NEST_ERR_MISALIGNED;
+    return from_cuda(launch_unpack(layer->base, bits ? layer->resid : nullptr, layer->M, layer->K, bits, base_codes,
+                                   base_scales, resid_codes, resid_scales, as_stream(stream)));
+}
+
+nest_status nest_rotate(const void* x, int32_t x_dtype, const int8_t* signs, int32_t n, int32_t T, int32_t mode,
+                        float* y, uint16_t* x_op, void* stream) {
+    if (!x || !signs || (!y && !x_op)) return NEST_ERR_INVALID_ARG;
+    if (n < 1 || T < 1) return NEST_ERR_INVALID_ARG;
+    if ((x_dtype != 0 && x_dtype != 1) || (mode != 0 && mode != 1)) return NEST_ERR_INVALID_ARG;
+    if (x_op != nullptr) {
+        if (mode != 0) return NEST_ERR_INVALID_ARG;
+        if (n % 128 || T > 64) return NEST_ERR_UNSUPPORTED;
+        if (!aligned16(x_op)) return NEST_ERR_MISALIGNED;
+    }
+    if ((reinterpret_cast<uintptr_t>(x) & (x_dtype == 1 ? 1u : 3u)) || (y && (reinterpret_cast<uintptr_t>(y) & 3u)))
+        return NEST_ERR_MISALIGNED;
+    return from_cuda(launch_rotate(x, x_dtype, signs, n, T, mode, y, x_op, as_stream(stream)));
+}
+
+nest_status nest_draft_gemv(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* workspace,
+                            void* stream) {
+    return run_gemm(layer, 0, x_op, z, T, workspace, stream);
+}
+
+nest_status nest_verify_gemm(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* workspace,
+                             void* stream) {
+    if (layer != nullptr && layer->resid_bits == 0) return NEST_ERR_INVALID_ARG;
+    return run_gemm(layer, layer ? layer->resid_bits : 0, x_op, z, T, workspace, stream);
+}
+
+// scratch of nest_linear: [x_op][z][workspace], each 256-byte aligned
+static size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+size_t nest_linear_scratch_bytes(int32_t M, int32_t K, int32_t T) {
+    if (M < 1 || K < 1 || K % 128 || T < 1 || T > 64) return 0;
+    return round256(nest_xop_bytes(K, T)) + round256((size_t)T * M * sizeof(float)) + nest_workspace_bytes(M, K, T);
+}
+
+nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype, int32_t T, float* y,
+                        void* scratch, void* stream) {
+    nest_status st = check_layer(layer, verify != 0);
+    if (st != NEST_OK) return st;
+    if (!x || !y || !scratch || !layer->sign_in || !layer->sign_out) return NEST_ERR_INVALID_ARG;
+    if (T < 1) return NEST_ERR_INVALID_ARG;
+    if (T > 64) return NEST_ERR_UNSUPPORTED;
+    if (!aligned16(scratch)) return NEST_ERR_MISALIGNED;
+    const int M = layer->M, K = layer->K;
+    uint8_t* s = reinterpret_cast<uint8_t*>(scratch);
+    uint16_t* xop = reinterpret_cast<uint16_t*>(s);
+    float* z = reinterpret_cast<float*>(s + round256(nest_xop_bytes(K, T)));
+    void* ws = s + round256(nest_xop_bytes(K, T)) + round256((size_t)T * M * sizeof(float));
+    st = nest_rotate(x, x_dtype, layer->sign_in, K, T, 0, nullptr, xop, stream);
+    if (st != NEST_OK) return st;
+    st = verify ? nest_verify_gemm(layer, xop, z, T, ws, stream) : nest_draft_gemv(layer, xop, z, T, ws, stream);
+    if (st != NEST_OK) return st;
+    return nest_rotate(z, 0, layer->sign_out, M, T, 1, y, nullptr, stream);
+}
+
+nest_status nest_error_check(void* stream) {
+    int flag = 0;
+    cudaError_t e = read_and_clear_error(&flag, as_stream(stream));
+    if (e != cudaSuccess) return NEST_ERR_CUDA;
+    return flag ? NEST_ERR_TIMEOUT : NEST_OK;
+}
+
+}  // extern "C"

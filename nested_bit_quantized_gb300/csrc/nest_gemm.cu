@@ -1,0 +1,451 @@
+// Draft and verify GEMMs of the nested-bit linear layer on tcgen05 tensor cores.
+//
+//   draft : z[t][m] = sum_k Q_base[m][k] x'[t][k]
+//   verify: z[t][m] = sum_k (Q_base + Q_resid)[m][k] x'[t][k]
+// (feedman.me/posts/wZBTJ, POC recipe step 4: y_b = Q_base x', y_r = Q_resid x';
+//  the draft is the same without y_r.)  All T tokens share one pass over the
+// packed weights, so the weight bytes are streamed from HBM once per call.
+//
+// Design (one CTA per SM, warp-specialised pipeline):
+//   producer warp  : 1-D bulk copies (TMA engine) of one unit per stage -- the
+//                    base unit, the residual unit and the fp16 activation block
+//                    of the unit's 128-column group -- into shared memory.
+//   dequant warps  : two warpgroups; thread r of a warpgroup owns row r of the
+//                    tile.  It decodes its row's 128 weights of the unit into
+//                    fp16 w = s_b*L[code] + s_r*q in registers (PRMT look-up of
+//                    the four scaled levels, fp16 magic-number decode of the
+//                    residual) and stores them to tensor memory with tcgen05.st.
+//   MMA thread     : tcgen05.mma kind::f16, A = the dequantised weights in tensor
+//                    memory (128 x 16 per instruction), B = the activation block
+//                    in shared memory (Np x 16), D = fp32 accumulators in tensor
+//                    memory (128 lanes x Np columns).
+//   epilogue       : warpgroup 0 reads D with tcgen05.ld and writes z.
+// Work split: the (tile, group) units, tile-major, are cut into equal
+// contiguous ranges, one per CTA ("stream-K").  A tile whose groups span
+// several CTAs is finished by whichever CTA arrives last: each contributor
+// writes its partial sums to the workspace and bumps a per-tile counter; the
+// last one adds the partials in CTA order (deterministic) and writes z.
+#include "nest_device.cuh"
+#include "nest_internal.h"
+
+namespace nest {
+
+__device__ int g_nest_error;
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for a single thread.  Gives up after kWaitLimitNs or when the
+// CTA's abort flag is raised; on a timeout it raises the flag and the device
+// error flag.  `honour_abort == false` is used while draining in-flight copies.
+__device__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int* abort, bool honour_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (honour_abort && *abort) return false;
+        if ((it & 31u) == 31u && globaltimer() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            atomicExch(&g_nest_error, 1);
+            return false;
+        }
+    }
+}
+
+// Bounded wait for a whole warp; the result is the same on every lane.
+__device__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        if (!ok) ok = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        const bool stop = (*abort != 0) || ((it & 31u) == 31u && globaltimer() - t0 > kWaitLimitNs);
+        if (__any_sync(0xffffffffu, stop)) {
+            if ((threadIdx.x & 31) == 0) {
+                *abort = 1;
+                atomicExch(&g_nest_error, 1);
+            }
+            return false;
+        }
+    }
+}
+
+template <int BITS, int NP>
+struct Cfg {
+    static constexpr int kResUnit = resid_unit_bytes(BITS);
+    static constexpr int kXBytes = 256 * NP;                // Np tokens x 128 columns of fp16
+    static constexpr int kStage = kBaseUnit + kResUnit + kXBytes;
+    static constexpr int kStagesRaw = (220 * 1024 - 1024) / kStage;
+    static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
+    static constexpr int kNumA = 6;                         // A buffers of 64 TMEM columns
+    static constexpr int kDeqWG = 2;                        // dequantising warpgroups
+    static constexpr int kProducerWarp = 4 * kDeqWG;
+    static constexpr int kMmaWarp = 4 * kDeqWG + 1;
+    static constexpr int kThreads = 32 * (4 * kDeqWG + 2);
+    static constexpr int kTmemCols = 512;
+    static constexpr int kColA = 128;                       // A buffers after the two D buffers
+    // barriers: full[S], empty[S], a_full[NA], a_empty[NA], d_full[2], d_empty[2], drain
+    static constexpr int kNumBars = 2 * kStages + 2 * kNumA + 5;
+    static constexpr int kSmemBytes = kStages * kStage + kNumBars * 8 + 16;
+    static_assert(kStages >= 2, "stage too large");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kStage % 128 == 0, "stage alignment");
+};
+
+// Decode 64 columns (half h of the 128-column group) of row r of one unit into
+// 32 fp16x2 registers: w = s_b * L[code] (+ s_r * q).
+template <int BITS>
+__device__ __forceinline__ void dequant_half(const uint8_t* sb, const uint8_t* sr, int r, int h,
+                                             uint32_t lut_lo, uint32_t lut_hi, __half2 sr2, __half2 off2,
+                                             uint32_t (&out)[32]) {
+    const uint4 bw4 = *reinterpret_cast<const uint4*>(sb + (h * kRows + r) * 16);
+    const uint32_t bw[4] = {bw4.x, bw4.y, bw4.z, bw4.w};
+    uint32_t rw[16];
+    uint32_t mid[4], hi[2];
+    if constexpr (BITS == 8) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sr + ((4 * h + c) * kRows + r) * 16);
+            rw[4 * c] = v.x; rw[4 * c + 1] = v.y; rw[4 * c + 2] = v.z; rw[4 * c + 3] = v.w;
+        }
+    } else if constexpr (BITS == 6 || BITS == 7) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sr + ((2 * h + c) * kRows + r) * 16);
+            rw[4 * c] = v.x; rw[4 * c + 1] = v.y; rw[4 * c + 2] = v.z; rw[4 * c + 3] = v.w;
+        }
+        const uint4 m = *reinterpret_cast<const uint4*>(sr + ((4 + h) * kRows + r) * 16);
+        mid[0] = m.x; mid[1] = m.y; mid[2] = m.z; mid[3] = m.w;
+        if constexpr (BITS == 7) {
+            const uint2 o = *reinterpret_cast<const uint2*>(sr + (6 * kRows + r) * 16 + 8 * h);
+            hi[0] = o.x; hi[1] = o.y;
+        }
+    }
+#pragma unroll
+    for (int qd = 0; qd < 16; ++qd) {
+        // base: bytes of v hold the codes of columns 4Q .. 4Q+3 (Q = 16h + qd)
+        const uint32_t v = (bw[qd >> 2] >> (2 * (qd & 3))) & 0x03030303u;
+        const uint32_t sel = v * 0x11u + 0x40404040u;
+        const uint32_t b01 = prmt(lut_lo, lut_hi, sel);
+        const uint32_t b23 = prmt(lut_lo, lut_hi, sel >> 16);
+        if constexpr (BITS == 0) {
+            out[2 * qd] = b01;
+            out[2 * qd + 1] = b23;
+        } else {
+            uint32_t u;
+            if constexpr (BITS == 8) {
+                u = rw[qd];
+            } else {
+                const uint32_t lo = (rw[qd >> 1] >> (4 * (qd & 1))) & 0x0F0F0F0Fu;
+                const int pm = qd & 3;
+                const uint32_t ms = pm < 2 ? (mid[qd >> 2] << (4 - 2 * pm)) : (mid[qd >> 2] >> (2 * pm - 4));
+                u = lo | (ms & 0x30303030u);
+                if constexpr (BITS == 7) {
+                    const int ph = qd & 7;
+                    const uint32_t hs = ph < 7 ? (hi[qd >> 3] << (6 - ph)) : (hi[qd >> 3] >> 1);
+                    u |= hs & 0x40404040u;
+                }
+            }
+            // 1024 + u as fp16 (exact), minus 1024 + 2^(b-1), gives q exactly
+            const __half2 q01 = __hsub2(u32_as_h2(prmt(u, 0x64646464u, 0x5140u)), off2);
+            const __half2 q23 = __hsub2(u32_as_h2(prmt(u, 0x64646464u, 0x7362u)), off2);
+            out[2 * qd] = h2_as_u32(__hfma2(q01, sr2, u32_as_h2(b01)));
+            out[2 * qd + 1] = h2_as_u32(__hfma2(q23, sr2, u32_as_h2(b23)));
+        }
+    }
+}
+
+__device__ __forceinline__ void tmem_st32_wait(uint32_t taddr, const uint32_t (&v)[32]) {
+    tmem_st32(taddr, v);
+    tc_wait_st();
+}
+
+// Load NP accumulator columns of this thread's lane and wait for them.
+template <int NP>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NP]) {
+#pragma unroll
+    for (int j = 0; j < NP / 16; ++j) {
+        float t[16];
+        uint32_t r[16];
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {"
+                     "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+                     "tcgen05.wait::ld.sync.aligned;"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                       "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                       "=r"(r[14]), "=r"(r[15])
+                     : "r"(taddr + 16 * j) : "memory");
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t[i] = __uint_as_float(r[i]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[16 * j + i] = t[i];
+    }
+}
+
+__device__ __forceinline__ long long unit_begin(int c, long long units, int grid) {
+    return (long long)c * units / grid;
+}
+__device__ __forceinline__ int unit_owner(long long u, long long units, int grid) {
+    return (int)(((u + 1) * grid - 1) / units);
+}
+
+template <int BITS, int NP>
+__global__ void __launch_bounds__(Cfg<BITS, NP>::kThreads, 1)
+k_nest_gemm(const GemmArgs p) {
+    using C = Cfg<BITS, NP>;
+    constexpr int S = C::kStages, NA = C::kNumA;
+    extern __shared__ __align__(1024) uint8_t smem[];
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStage);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+    auto a_full = [&](int a) { return bar0 + 8u * (2 * S + a); };
+    auto a_empty = [&](int a) { return bar0 + 8u * (2 * S + NA + a); };
+    auto d_full = [&](int d) { return bar0 + 8u * (2 * S + 2 * NA + d); };
+    auto d_empty = [&](int d) { return bar0 + 8u * (2 * S + 2 * NA + 2 + d); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 2 * NA + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    auto st_base = [&](int s) { return smem + s * C::kStage; };
+    auto st_res = [&](int s) { return smem + s * C::kStage + kBaseUnit; };
+    auto st_x = [&](int s) { return smem + s * C::kStage + kBaseUnit + C::kResUnit; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+        for (int a = 0; a < NA; ++a) { mbar_init(a_full(a), kRows); mbar_init(a_empty(a), 1); }
+        for (int d = 0; d < 2; ++d) { mbar_init(d_full(d), 1); mbar_init(d_empty(d), kRows); }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == C::kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const long long units = p.units;
+    const int grid = gridDim.x, cta = blockIdx.x, G = p.G;
+    const long long u0 = unit_begin(cta, units, grid);
+    const int n = (int)(unit_begin(cta + 1, units, grid) - u0);
+
+    if (warp == C::kProducerWarp) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < n; ++i) {
+                const int s = i % S;
+                if (i >= S && !thread_wait(empty(s), ((i / S) - 1) & 1, abort_flag)) break;
+                const long long u = u0 + i;
+                const int g = (int)(u % G);
+                mbar_arrive_expect_tx(full(s), C::kStage);
+                bulk_g2s(smem_u32(st_base(s)), p.base + u * kBaseUnit, kBaseUnit, full(s));
+                if constexpr (BITS != 0)
+                    bulk_g2s(smem_u32(st_res(s)), p.resid + u * C::kResUnit, C::kResUnit, full(s));
+                bulk_g2s(smem_u32(st_x(s)), p.xop + (size_t)g * (C::kXBytes / 2), C::kXBytes, full(s));
+                ++issued;
+            }
+            // every issued copy has landed before the CTA may leave
+            for (int j = issued > S ? issued - S : 0; j < issued; ++j)
+                thread_wait(full(j % S), (j / S) & 1, abort_flag, false);
+        }
+    } else if (warp == C::kMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(128, NP);
+            int seg = -1;
+            bool issued_any = false;
+            for (int i = 0; i < n; ++i) {
+                const long long u = u0 + i;
+                const int g = (int)(u % G);
+                const bool first = (i == 0) || g == 0;
+                const bool last = (i == n - 1) || g == G - 1;
+                if (first) {
+                    ++seg;
+                    if (seg >= 2 && !thread_wait(d_empty(seg & 1), ((seg >> 1) - 1) & 1, abort_flag)) break;
+                }
+                const int s = i % S, a = i % NA, d = seg & 1;
+                if (!thread_wait(full(s), (i / S) & 1, abort_flag)) break;
+                if (!thread_wait(a_full(a), (i / NA) & 1, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t xb = smem_u32(st_x(s));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    // B block: core matrix (token block nb, column chunk c) at ((c * NP/8) + nb) * 128 bytes
+                    const uint64_t bdesc = smem_desc_noswizzle(xb + (2 * kk) * (NP / 8) * 128, (NP / 8) * 128, 128);
+                    mma_f16_ts(tmem + d * NP, tmem + C::kColA + 64 * a + 8 * kk, bdesc, idesc,
+                               (first && kk == 0) ? 0u : 1u);
+                }
+                issued_any = true;
+                tc_commit(empty(s));
+                tc_commit(a_empty(a));
+                if (last) tc_commit(d_full(d));
+            }
+            if (issued_any) {          // all MMAs finished before tensor memory is released
+                tc_commit(drain_bar);
+                thread_wait(drain_bar, 0, abort_flag, false);
+            }
+        }
+    } else {
+        // dequantisation warpgroups; warpgroup 0 also runs the epilogues
+        const int wg = warp >> 2;
+        const int r = 32 * (warp & 3) + lane;               // row of the tile == TMEM lane
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const __half2 off2 = __float2half2_rn(1024.0f + (BITS ? (float)(1 << (BITS - 1)) : 0.0f));
+        int seg = -1;
+        bool ok = true;
+        for (int i = 0; i < n && ok; ++i) {
+            const long long u = u0 + i;
+            const int g = (int)(u % G);
+            const int tile = (int)(u / G);
+            if ((i == 0) || g == 0) ++seg;
+            if (i % C::kDeqWG == wg) {
+                const int s = i % S, a = i % NA;
+                ok = warp_wait(full(s), (i / S) & 1, abort_flag);
+                if (ok && i >= NA) ok = warp_wait(a_empty(a), ((i / NA) - 1) & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                const uint8_t* sb = st_base(s);
+                const uint8_t* sr = st_res(s);
+                const float s_b = __half2float(*reinterpret_cast<const __half*>(sb + 4096 + 2 * r));
+                // scaled levels as fp16, low bytes in lut_lo and high bytes in lut_hi
+                uint32_t h[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) h[c] = __half_as_ushort(__float2half_rn(s_b * level_f(c)));
+                const uint32_t lut_lo = (h[0] & 0xFFu) | ((h[1] & 0xFFu) << 8) | ((h[2] & 0xFFu) << 16) | ((h[3] & 0xFFu) << 24);
+                const uint32_t lut_hi = (h[0] >> 8) | ((h[1] >> 8) << 8) | ((h[2] >> 8) << 16) | ((h[3] >> 8) << 24);
+                __half2 sr2 = __float2half2_rn(0.0f);
+                if constexpr (BITS != 0)
+                    sr2 = __half2half2(*reinterpret_cast<const __half*>(sr + 2048 * BITS + 2 * r));
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t w[32];
+                    dequant_half<BITS>(sb, sr, r, hh, lut_lo, lut_hi, sr2, off2, w);
+                    tmem_st32_wait(tmem + lane_base + C::kColA + 64 * a + 32 * hh, w);
+                }
+                tc_fence_before();
+                mbar_arrive(a_full(a));
+            }
+            const bool last = (i == n - 1) || g == G - 1;
+            if (wg == 0 && last) {
+                const int d = seg & 1;
+                if (!warp_wait(d_full(d), (seg >> 1) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                float v[NP];
+                tmem_ld_cols<NP>(tmem + lane_base + d * NP, v);
+                tc_fence_before();
+                mbar_arrive(d_empty(d));
+                const int m = tile * kRows + r;
+                const int T = p.T, M = p.M;
+                const bool whole = (g == G - 1) && (u - (long long)tile * G + 1 == (long long)G) &&
+                                   (u0 <= (long long)tile * G);
+                if (whole) {
+                    if (m < M) {
+#pragma unroll
+                        for (int t = 0; t < NP; ++t)
+                            if (t < T) p.z[(size_t)t * M + m] = v[t];
+                    }
+                } else {
+                    // partial tile: slot 0 for this CTA's first segment, 1 for its last
+                    const int slot = ((long long)tile * G <= u0) ? 0 : 1;
+                    float* part = p.partial + ((size_t)(2 * cta + slot) * T) * kRows;
+#pragma unroll
+                    for (int t = 0; t < NP; ++t)
+                        if (t < T) part[(size_t)t * kRows + r] = v[t];
+                    __threadfence();
+                    __syncwarp();
+                    const int c_lo = unit_owner((long long)tile * G, units, grid);
+                    const int c_hi = unit_owner((long long)tile * G + G - 1, units, grid);
+                    int* ctr = p.counters + 4 * tile + (warp & 3);
+                    int old = 0;
+                    if (lane == 0) old = atomicAdd(ctr, 1);
+                    old = __shfl_sync(0xffffffffu, old, 0);
+                    if (old == c_hi - c_lo) {
+                        __threadfence();
+                        float acc[NP];
+#pragma unroll
+                        for (int t = 0; t < NP; ++t) acc[t] = 0.0f;
+                        for (int c = c_lo; c <= c_hi; ++c) {
+                            const int sl = ((long long)tile * G <= unit_begin(c, units, grid)) ? 0 : 1;
+                            const float* pp = p.partial + ((size_t)(2 * c + sl) * T) * kRows;
+#pragma unroll
+                            for (int t = 0; t < NP; ++t)
+                                if (t < T) acc[t] += __ldcg(pp + (size_t)t * kRows + r);
+                        }
+                        if (m < M) {
+#pragma unroll
+                            for (int t = 0; t < NP; ++t)
+                                if (t < T) p.z[(size_t)t * M + m] = acc[t];
+                        }
+                        if (lane == 0) atomicExch(ctr, 0);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int BITS, int NP>
+cudaError_t launch_t(const GemmArgs& a, int grid, cudaStream_t stream) {
+    using C = Cfg<BITS, NP>;
+    static bool configured = false;       // per instantiation; attribute is per device context
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k_nest_gemm<BITS, NP>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    k_nest_gemm<BITS, NP><<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t launch_bits(const GemmArgs& a, int grid, cudaStream_t stream) {
+    if (a.T <= 16) return launch_t<BITS, 16>(a, grid, stream);
+    if (a.T <= 32) return launch_t<BITS, 32>(a, grid, stream);
+    return launch_t<BITS, 64>(a, grid, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, int bits, int grid, cudaStream_t stream) {
+    switch (bits) {
+        case 0: return launch_bits<0>(a, grid, stream);
+        case 6: return launch_bits<6>(a, grid, stream);
+        case 7: return launch_bits<7>(a, grid, stream);
+        case 8: return launch_bits<8>(a, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t read_and_clear_error(int* flag, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_nest_error, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    if (*flag) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_nest_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    }
+    return e;
+}
+
+}  // namespace nest

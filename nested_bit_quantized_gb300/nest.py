@@ -1,0 +1,279 @@
+"""Python binding of libnest (include/nest.h): argument marshalling only.
+
+Every step runs in the CUDA library; this module only checks tensor
+properties, passes ``data_ptr()`` values and the current CUDA stream through
+ctypes, and turns status codes into exceptions.  PyTorch is used for device
+memory and streams.  There is no CPU path: if the library is not built, or
+the device is not sm_103a, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_P, _I32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "misaligned", 4: "CUDA error", 5: "timeout"}
+
+
+class NestError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [("M", _I32), ("K", _I32), ("resid_bits", _I32),
+                ("base", _P), ("resid", _P), ("sign_out", _P), ("sign_in", _P)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load the built library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"libnest is not built ({_build.LIB} missing); run nested_bit_quantized_gb300.build.build()")
+    lib = ctypes.CDLL(_build.LIB)
+    sig = {
+        "nest_status_string": ([_I32], ctypes.c_char_p),
+        "nest_hadamard_block": ([_I32], _I32),
+        "nest_base_bytes": ([_I32, _I32], _SZ),
+        "nest_resid_bytes": ([_I32, _I32, _I32], _SZ),
+        "nest_xop_bytes": ([_I32, _I32], _SZ),
+        "nest_workspace_bytes": ([_I32, _I32, _I32], _SZ),
+        "nest_linear_scratch_bytes": ([_I32, _I32, _I32], _SZ),
+        "nest_quantize": ([_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P], _I32),
+        "nest_pack": ([_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P], _I32),
+        "nest_unpack": ([ctypes.POINTER(_Layer), _P, _P, _P, _P, _P], _I32),
+        "nest_rotate": ([_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P], _I32),
+        "nest_draft_gemv": ([ctypes.POINTER(_Layer), _P, _P, _I32, _P, _P], _I32),
+        "nest_verify_gemm": ([ctypes.POINTER(_Layer), _P, _P, _I32, _P, _P], _I32),
+        "nest_linear": ([ctypes.POINTER(_Layer), _I32, _P, _I32, _I32, _P, _P, _P], _I32),
+        "nest_error_check": ([_P], _I32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes, fn.restype = args, res
+    _lib = lib
+    return lib
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise NestError(st, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+# ---------------------------------------------------------------------------
+# sizes
+# ---------------------------------------------------------------------------
+
+def hadamard_block(n: int) -> int:
+    return int(load().nest_hadamard_block(n))
+
+
+def base_bytes(M: int, K: int) -> int:
+    return int(load().nest_base_bytes(M, K))
+
+
+def resid_bytes(M: int, K: int, bits: int) -> int:
+    return int(load().nest_resid_bytes(M, K, bits))
+
+
+def xop_bytes(K: int, T: int) -> int:
+    return int(load().nest_xop_bytes(K, T))
+
+
+def workspace_bytes(M: int, K: int, T: int) -> int:
+    return int(load().nest_workspace_bytes(M, K, T))
+
+
+def linear_scratch_bytes(M: int, K: int, T: int) -> int:
+    return int(load().nest_linear_scratch_bytes(M, K, T))
+
+
+def _u8(n: int, device) -> torch.Tensor:
+    # 16-byte aligned byte buffer (the caching allocator returns 512-byte aligned blocks)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def new_workspace(M: int, K: int, T: int, device="cuda") -> torch.Tensor:
+    """A zero-filled GEMM workspace for shapes up to (M, K, T)."""
+    return torch.zeros(max(workspace_bytes(M, K, T), 16), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------
+# offline: quantize, pack, unpack
+# ---------------------------------------------------------------------------
+
+def quantize(W: torch.Tensor, sign_out: torch.Tensor, sign_in: torch.Tensor, bits: int,
+             work: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """RTN quantizer on the device (nest_quantize).  Returns codes and fp16 scale bits."""
+    _dev(W, torch.float32, "W")
+    _dev(sign_out, torch.int8, "sign_out")
+    _dev(sign_in, torch.int8, "sign_in")
+    M, K = W.shape
+    dev = W.device
+    if work is None:
+        work = torch.empty((M, K), dtype=torch.float64, device=dev)
+    out = {
+        "base_codes": torch.empty((M, K), dtype=torch.uint8, device=dev),
+        "base_scales": torch.empty((M, K // 128), dtype=torch.int16, device=dev),
+        "resid_codes": torch.empty((M, K), dtype=torch.int8, device=dev) if bits else None,
+        "resid_scales": torch.empty((M, K // 128), dtype=torch.int16, device=dev) if bits else None,
+    }
+    st = load().nest_quantize(_ptr(W), _ptr(sign_out), _ptr(sign_in), M, K, bits, _ptr(work),
+                              _ptr(out["base_codes"]), _ptr(out["base_scales"]),
+                              _ptr(out["resid_codes"]), _ptr(out["resid_scales"]), _stream(stream))
+    _check(st, "nest_quantize")
+    return out
+
+
+@dataclass
+class Layer:
+    """A packed layer resident on the device (owns its buffers)."""
+    M: int
+    K: int
+    bits: int
+    base: torch.Tensor
+    resid: Optional[torch.Tensor]
+    sign_out: torch.Tensor
+    sign_in: torch.Tensor
+
+    def c_struct(self) -> _Layer:
+        return _Layer(self.M, self.K, self.bits, self.base.data_ptr(),
+                      self.resid.data_ptr() if self.resid is not None else None,
+                      self.sign_out.data_ptr(), self.sign_in.data_ptr())
+
+    @property
+    def weight_bytes(self) -> int:
+        return self.base.numel() + (self.resid.numel() if self.resid is not None else 0)
+
+
+def pack(base_codes: torch.Tensor, base_scales: torch.Tensor, resid_codes: Optional[torch.Tensor],
+         resid_scales: Optional[torch.Tensor], bits: int, sign_out: torch.Tensor, sign_in: torch.Tensor,
+         stream=None) -> Layer:
+    """Pack device codes/scales into the unit format (nest_pack)."""
+    _dev(base_codes, torch.uint8, "base_codes")
+    M, K = base_codes.shape
+    dev = base_codes.device
+    base = _u8(base_bytes(M, K), dev)
+    resid = _u8(resid_bytes(M, K, bits), dev) if bits else None
+    st = load().nest_pack(_ptr(base_codes), _ptr(base_scales), _ptr(resid_codes), _ptr(resid_scales),
+                          M, K, bits, _ptr(base), _ptr(resid), _stream(stream))
+    _check(st, "nest_pack")
+    return Layer(M, K, bits, base, resid, sign_out, sign_in)
+
+
+def unpack(layer: Layer, stream=None) -> dict:
+    M, K, dev = layer.M, layer.K, layer.base.device
+    out = {
+        "base_codes": torch.empty((M, K), dtype=torch.uint8, device=dev),
+        "base_scales": torch.empty((M, K // 128), dtype=torch.int16, device=dev),
+        "resid_codes": torch.empty((M, K), dtype=torch.int8, device=dev) if layer.bits else None,
+        "resid_scales": torch.empty((M, K // 128), dtype=torch.int16, device=dev) if layer.bits else None,
+    }
+    L = layer.c_struct()
+    st = load().nest_unpack(ctypes.byref(L), _ptr(out["base_codes"]), _ptr(out["base_scales"]),
+                            _ptr(out["resid_codes"]), _ptr(out["resid_scales"]), _stream(stream))
+    _check(st, "nest_unpack")
+    return out
+
+
+def quantize_and_pack(W: torch.Tensor, sign_out: torch.Tensor, sign_in: torch.Tensor, bits: int,
+                      stream=None) -> Layer:
+    q = quantize(W, sign_out, sign_in, bits, stream=stream)
+    return pack(q["base_codes"], q["base_scales"], q["resid_codes"], q["resid_scales"], bits,
+                sign_out, sign_in, stream=stream)
+
+
+# ---------------------------------------------------------------------------
+# forward kernels
+# ---------------------------------------------------------------------------
+
+def rotate(x: torch.Tensor, signs: torch.Tensor, mode: int, y: Optional[torch.Tensor] = None,
+           x_op: Optional[torch.Tensor] = None, stream=None):
+    """nest_rotate: mode 0 -> H S x (optionally into the GEMM operand), mode 1 -> S H x."""
+    if x.dtype == torch.bfloat16:
+        dt = 1
+    elif x.dtype == torch.float32:
+        dt = 0
+    else:
+        raise ValueError("x must be float32 or bfloat16")
+    _dev(x, x.dtype, "x")
+    _dev(signs, torch.int8, "signs")
+    T, n = x.shape
+    st = load().nest_rotate(_ptr(x), dt, _ptr(signs), n, T, mode, _ptr(y), _ptr(x_op), _stream(stream))
+    _check(st, "nest_rotate")
+    return y, x_op
+
+
+def new_xop(K: int, T: int, device="cuda") -> torch.Tensor:
+    return torch.empty(xop_bytes(K, T) // 2, dtype=torch.int16, device=device)
+
+
+def gemm(layer: Layer, x_op: torch.Tensor, T: int, verify: bool, z: Optional[torch.Tensor] = None,
+         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """nest_verify_gemm (verify=True) or nest_draft_gemv: z [T][M] fp32 in the rotated basis."""
+    dev = layer.base.device
+    if z is None:
+        z = torch.empty((T, layer.M), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(layer.M, layer.K, T, dev)
+    L = layer.c_struct()
+    fn = load().nest_verify_gemm if verify else load().nest_draft_gemv
+    st = fn(ctypes.byref(L), _ptr(x_op), _ptr(z), T, _ptr(workspace), _stream(stream))
+    _check(st, "nest_verify_gemm" if verify else "nest_draft_gemv")
+    return z
+
+
+def linear(layer: Layer, x: torch.Tensor, verify: bool, y: Optional[torch.Tensor] = None,
+           scratch: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """nest_linear: y = S_o H_o (Q (H_i S_i x)) for x [T][K] (bf16 or fp32)."""
+    T = x.shape[0]
+    dev = layer.base.device
+    if y is None:
+        y = torch.empty((T, layer.M), dtype=torch.float32, device=dev)
+    if scratch is None:
+        scratch = torch.zeros(linear_scratch_bytes(layer.M, layer.K, T), dtype=torch.uint8, device=dev)
+    dt = 1 if x.dtype == torch.bfloat16 else 0
+    L = layer.c_struct()
+    st = load().nest_linear(ctypes.byref(L), int(verify), _ptr(x), dt, T, _ptr(y), _ptr(scratch), _stream(stream))
+    _check(st, "nest_linear")
+    return y
+
+
+def error_check(stream=None) -> None:
+    _check(load().nest_error_check(_stream(stream)), "nest_error_check")

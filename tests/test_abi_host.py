@@ -1,0 +1,112 @@
+"""Host-only checks of the C-ABI library: it loads, exports every declared
+symbol, computes sizes, and rejects bad arguments before any device work.
+No call here touches a GPU (all rejected cases fail validation first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from nested_bit_quantized_gb300 import build as nb
+from nested_bit_quantized_gb300 import nest
+from oracle import pack as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nb.build()
+    return nest.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "nest.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nest_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 14
+    so = ctypes.CDLL(nb.LIB)
+    for n in names:
+        assert hasattr(so, n), f"{n} declared in nest.h but not exported"
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.nest_status_string(s)
+
+
+def test_hadamard_block_sizes(lib):
+    for n, b in [(4096, 4096), (8192, 4096), (15360, 1024), (3840, 256), (5376, 256), (7, 1), (96, 32), (0, 0)]:
+        assert nest.hadamard_block(n) == b
+
+
+@pytest.mark.parametrize("M,K,bits", [(128, 128, 8), (200, 256, 7), (77, 384, 6), (9728, 2560, 7), (1, 128, 8)])
+def test_sizes_match_reference_packer(lib, M, K, bits):
+    assert nest.base_bytes(M, K) == P.base_bytes(M, K)
+    assert nest.resid_bytes(M, K, bits) == P.resid_bytes(M, K, bits)
+
+
+def test_sizes_reject_bad_shapes(lib):
+    assert nest.base_bytes(128, 100) == 0
+    assert nest.resid_bytes(128, 128, 5) == 0
+    assert nest.xop_bytes(128, 65) == 0
+    assert nest.xop_bytes(256, 1) == 2 * 256 * 16
+    assert nest.xop_bytes(256, 17) == 2 * 256 * 32
+    assert nest.workspace_bytes(128, 128, 0) == 0
+    assert nest.linear_scratch_bytes(4096, 4096, 16) > nest.workspace_bytes(4096, 4096, 16)
+
+
+def _layer(M=256, K=512, bits=8, base=0x10000, resid=0x20000):
+    return nest._Layer(M, K, bits, base, resid, 0x30000, 0x40000)
+
+
+def test_gemm_argument_validation(lib):
+    L = _layer()
+    ok = ctypes.c_void_p(0x50000)
+    f = lib.nest_verify_gemm
+    assert f(None, ok, ok, 16, ok, None) == 1                              # null layer
+    assert f(ctypes.byref(L), None, ok, 16, ok, None) == 1                 # null operand
+    assert f(ctypes.byref(L), ok, ok, 0, ok, None) == 1                    # T < 1
+    assert f(ctypes.byref(L), ok, ok, 65, ok, None) == 2                   # T > 64
+    assert f(ctypes.byref(_layer(K=200)), ok, ok, 4, ok, None) == 2         # K % 128
+    assert f(ctypes.byref(_layer(bits=5)), ok, ok, 4, ok, None) == 2        # bit width
+    assert f(ctypes.byref(_layer(bits=0)), ok, ok, 4, ok, None) == 1        # verify needs a residual
+    assert f(ctypes.byref(_layer(base=0x10001)), ok, ok, 4, ok, None) == 3  # misaligned base
+    assert f(ctypes.byref(L), ctypes.c_void_p(0x50008), ok, 4, ok, None) == 3
+    assert f(ctypes.byref(_layer(M=0)), ok, ok, 4, ok, None) == 1
+    d = lib.nest_draft_gemv
+    assert d(ctypes.byref(_layer(bits=0, resid=0)), ok, ok, 70, ok, None) == 2
+    assert d(ctypes.byref(_layer(bits=0, resid=0)), ok, None, 4, ok, None) == 1
+
+
+def test_rotate_pack_quantize_validation(lib):
+    ok = ctypes.c_void_p(0x50000)
+    r = lib.nest_rotate
+    assert r(None, 1, ok, 128, 4, 0, ok, None, None) == 1
+    assert r(ok, 2, ok, 128, 4, 0, ok, None, None) == 1          # dtype
+    assert r(ok, 1, ok, 128, 4, 2, ok, None, None) == 1          # mode
+    assert r(ok, 1, ok, 128, 4, 0, None, None, None) == 1        # no output
+    assert r(ok, 1, ok, 100, 4, 0, None, ok, None) == 2          # operand needs n % 128
+    assert r(ok, 1, ok, 128, 65, 0, None, ok, None) == 2         # operand needs T <= 64
+    assert r(ok, 1, ok, 128, 4, 1, None, ok, None) == 1          # operand only on the input side
+    assert r(ok, 1, ok, 128, 4, 0, None, ctypes.c_void_p(0x50002), None) == 3
+    p = lib.nest_pack
+    assert p(None, ok, None, None, 128, 128, 0, ok, None, None) == 1
+    assert p(ok, ok, None, None, 128, 100, 0, ok, None, None) == 2
+    assert p(ok, ok, None, None, 128, 128, 7, ok, None, None) == 1   # residual pointers missing
+    assert p(ok, ok, ok, ok, 128, 128, 9, ok, ok, None) == 2
+    q = lib.nest_quantize
+    assert q(ok, ok, ok, 128, 100, 8, ok, ok, ok, ok, ok, None) == 2
+    assert q(ok, ok, ok, 128, 128, 8, ok, ok, ok, None, ok, None) == 1
+    assert q(ctypes.c_void_p(0x50004), ok, ok, 128, 128, 8, ok, ok, ok, ok, ok, None) == 3
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(nest, "_lib", None)
+    monkeypatch.setattr(nest._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        nest.load()

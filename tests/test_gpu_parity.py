@@ -1,0 +1,251 @@
+"""GPU parity: the CUDA library (through its C-ABI binding) against the CPU oracle.
+
+Integer work (packing, codes, scales) must match bit for bit; floating-point
+outputs must pass the gate of the workload definition: relative L2 <= 1e-3
+and every element within 1e-2 * rms(reference).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from nested_bit_quantized_gb300 import nest, synth  # noqa: E402
+from oracle import nest_oracle as O  # noqa: E402
+from oracle import pack as P  # noqa: E402
+from tests.helpers import decode_xop, parity, to_dev  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+_CACHE = {}
+
+
+def ref_layer(M, K, bits, seed=1, outliers="entries"):
+    key = (M, K, bits, seed, outliers)
+    if key not in _CACHE:
+        W = synth.weights(M, K, seed, outliers)
+        s_o, s_i = synth.sign_pair(M, K, seed + 7)
+        _CACHE[key] = (W, s_o, s_i, O.quantize_layer(W, s_o, s_i, bits))
+    return _CACHE[key]
+
+
+def dev_layer(q, bits, s_o, s_i, dev):
+    return nest.pack(to_dev(q["base_codes"], torch, dev), to_dev(q["base_scales"], torch, dev),
+                     to_dev(q["resid_codes"], torch, dev) if bits else None,
+                     to_dev(q["resid_scales"], torch, dev) if bits else None, bits,
+                     to_dev(s_o, torch, dev), to_dev(s_i, torch, dev))
+
+
+def bf16_x(T, K, seed, dev):
+    bits, vals = synth.activations(T, K, seed)
+    return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16), vals
+
+
+def run_gemm(layer, x, verify, dev):
+    T = x.shape[0]
+    xop = nest.new_xop(layer.K, T, dev)
+    nest.rotate(x, layer.sign_in, 0, x_op=xop)
+    return nest.gemm(layer, xop, T, verify).cpu().numpy()
+
+
+# ----------------------------------------------------------------------------
+# packing and quantisation: bit-exact
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,bits", [(128, 128, 8), (200, 256, 7), (77, 384, 6), (1, 128, 8), (300, 1024, 7)])
+def test_pack_bit_exact(dev, M, K, bits):
+    bc, bs, rc, rs = synth.uniform_codes(M, K, bits, 23)
+    layer = nest.pack(to_dev(bc, torch, dev), to_dev(bs, torch, dev), to_dev(rc, torch, dev),
+                      to_dev(rs, torch, dev), bits, torch.ones(M, dtype=torch.int8, device=dev),
+                      torch.ones(K, dtype=torch.int8, device=dev))
+    assert np.array_equal(layer.base.cpu().numpy()[:P.base_bytes(M, K)], P.pack_base(bc, bs))
+    assert np.array_equal(layer.resid.cpu().numpy()[:P.resid_bytes(M, K, bits)], P.pack_resid(rc, rs, bits))
+    u = nest.unpack(layer)
+    assert np.array_equal(u["base_codes"].cpu().numpy(), bc)
+    assert np.array_equal(u["base_scales"].cpu().numpy().view(np.uint16), bs)
+    assert np.array_equal(u["resid_codes"].cpu().numpy(), rc)
+    assert np.array_equal(u["resid_scales"].cpu().numpy().view(np.uint16), rs)
+
+
+def _boundary_ok(q, mism_b, mism_r, bits):
+    """Code differences are allowed only where the oracle's value sits on a decision boundary."""
+    Wr = q["Wr"]
+    s = np.repeat(q["base_scales"].astype(np.float64), 128, axis=1)
+    t = O.base_threshold()
+    u = np.abs(Wr[mism_b] / s[mism_b])
+    assert np.all(np.abs(u - t) <= 1e-9 * t), "base code mismatch away from the decision point"
+    if bits:
+        R = Wr - O.dequant_base(q["base_codes"], q["base_scales"])
+        sr = np.repeat(q["resid_scales"].astype(np.float64), 128, axis=1)
+        v = R[mism_r] / sr[mism_r]
+        assert np.all(np.abs(np.abs(v - np.floor(v)) - 0.5) <= 1e-9 * np.maximum(1, np.abs(v))), \
+            "residual code mismatch away from a rounding tie"
+
+
+@pytest.mark.parametrize("M,K,bits,outl", [(256, 512, 8, "columns"), (200, 384, 7, "entries"), (96, 1024, 6, None),
+                                           (512, 2560, 7, "entries"), (33, 128, 0, None)])
+def test_quantize_matches_oracle(dev, M, K, bits, outl):
+    W, s_o, s_i, q = ref_layer(M, K, bits or 8, seed=5, outliers=outl)
+    g = nest.quantize(to_dev(W, torch, dev), to_dev(s_o, torch, dev), to_dev(s_i, torch, dev), bits)
+    assert np.array_equal(g["base_scales"].cpu().numpy().view(np.uint16), q["base_scales"].view(np.uint16))
+    mb = g["base_codes"].cpu().numpy() != q["base_codes"]
+    mr = np.zeros_like(mb)
+    if bits:
+        assert np.array_equal(g["resid_scales"].cpu().numpy().view(np.uint16), q["resid_scales"].view(np.uint16))
+        mr = g["resid_codes"].cpu().numpy() != q["resid_codes"]
+    _boundary_ok(q, mb, mr, bits)
+
+
+# ----------------------------------------------------------------------------
+# rotation
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,T", [(128, 1), (384, 3), (2560, 16), (4096, 17), (5376, 5), (8192, 2), (96, 4),
+                                 (200, 3), (7, 2), (15360, 1), (1024, 64)])
+def test_rotate_matches_oracle(dev, n, T):
+    s = synth.signs(n, 31)
+    xb, xv = synth.activations(T, n, 32)
+    x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((T, n), dtype=torch.float32, device=dev)
+    xop = nest.new_xop(n, T, dev) if n % 128 == 0 else None
+    nest.rotate(x, to_dev(s, torch, dev), 0, y=y, x_op=xop)
+    ref = O.rotate_activations(xv, s)
+    got = y.cpu().numpy()
+    assert np.max(np.abs(got - ref)) <= 1e-5 * max(1.0, np.max(np.abs(ref)))
+    if xop is not None:
+        h = decode_xop(xop.cpu().numpy(), n, T).astype(np.float64)
+        assert np.max(np.abs(h - ref) / np.maximum(np.abs(ref), 6.2e-5)) <= 2.0 ** -10
+    # output side from fp32 input
+    z = np.random.default_rng(n).normal(size=(T, n)).astype(np.float32)
+    yo = torch.empty((T, n), dtype=torch.float32, device=dev)
+    nest.rotate(torch.from_numpy(z).to(dev), to_dev(s, torch, dev), 1, y=yo)
+    refo = O.unrotate_outputs(z, s)
+    assert np.max(np.abs(yo.cpu().numpy() - refo)) <= 1e-5 * max(1.0, np.max(np.abs(refo)))
+
+
+# ----------------------------------------------------------------------------
+# draft / verify GEMMs
+# ----------------------------------------------------------------------------
+
+SHAPES = [(128, 128), (256, 512), (200, 384), (1280, 1024), (384, 9728), (1, 128), (129, 256)]
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+@pytest.mark.parametrize("bits", [6, 7, 8])
+def test_gemm_parity_small(dev, M, K, bits):
+    W, s_o, s_i, q = ref_layer(M, K, bits)
+    layer = dev_layer(q, bits, s_o, s_i, dev)
+    for T in (1, 2, 16, 17, 33, 64):
+        x, xv = bf16_x(T, K, 40 + T, dev)
+        for verify in (False, True):
+            z = run_gemm(layer, x, verify, dev)
+            ref = O.forward(q, s_o, s_i, xv, verify)["z"]
+            parity(z, ref)
+
+
+@pytest.mark.parametrize("bits", [6, 7, 8])
+def test_linear_parity(dev, bits):
+    M, K = 640, 1536
+    W, s_o, s_i, q = ref_layer(M, K, bits, seed=3)
+    layer = dev_layer(q, bits, s_o, s_i, dev)
+    for T in (1, 9, 16, 64):
+        x, xv = bf16_x(T, K, 50 + T, dev)
+        for verify in (False, True):
+            y = nest.linear(layer, x, verify).cpu().numpy()
+            parity(y, O.forward(q, s_o, s_i, xv, verify)["y"])
+
+
+def test_draft_is_bitexact_subset_of_verify(dev):
+    M, K, bits = 512, 1024, 7
+    W, s_o, s_i, q = ref_layer(M, K, bits)
+    q0 = dict(q)
+    q0["resid_codes"] = np.zeros_like(q["resid_codes"])
+    lv = dev_layer(q0, bits, s_o, s_i, dev)
+    x, _ = bf16_x(16, K, 7, dev)
+    assert np.array_equal(run_gemm(lv, x, True, dev), run_gemm(lv, x, False, dev))
+
+
+def test_deterministic_and_token_independent(dev):
+    M, K, bits = 1024, 2560, 7
+    W, s_o, s_i, q = ref_layer(M, K, bits)
+    layer = dev_layer(q, bits, s_o, s_i, dev)
+    x, xv = bf16_x(16, K, 8, dev)
+    a = run_gemm(layer, x, True, dev)
+    b = run_gemm(layer, x, True, dev)
+    assert np.array_equal(a, b)
+    for t in (0, 5, 15):
+        one = run_gemm(layer, x[t:t + 1].contiguous(), True, dev)
+        parity(one[0], a[t])
+    nest.error_check()
+
+
+# ----------------------------------------------------------------------------
+# full sizes of the workloads
+# ----------------------------------------------------------------------------
+
+def _full_layer(wl, lin, bits):
+    W = synth.weights(lin.M, lin.K, lin.w_seed, lin.outliers)
+    s_o, s_i = synth.sign_pair(lin.M, lin.K, lin.sign_seed)
+    return W, s_o, s_i, O.quantize_layer(W, s_o, s_i, bits)
+
+
+@pytest.mark.slow
+def test_full_single_4096(dev):
+    wl = synth.WORKLOADS["single_4096"]
+    lin = wl.linears[0]
+    W, s_o, s_i, q = _full_layer(wl, lin, 8)
+    layer = dev_layer(q, 8, s_o, s_i, dev)
+    for T in wl.T:
+        x, xv = bf16_x(T, lin.K, wl.x_seed, dev)
+        for verify in (False, True):
+            ref = O.forward(q, s_o, s_i, xv, verify)
+            parity(run_gemm(layer, x, verify, dev), ref["z"])
+            parity(nest.linear(layer, x, verify).cpu().numpy(), ref["y"])
+
+
+@pytest.mark.slow
+def test_full_mlp_triplet(dev):
+    wl = synth.WORKLOADS["mlp_triplet_4b"]
+    for lin in wl.linears:
+        W, s_o, s_i, q = _full_layer(wl, lin, 7)
+        layer = dev_layer(q, 7, s_o, s_i, dev)
+        for T in (1, 16, 32):
+            x, xv = bf16_x(T, lin.K, wl.x_seed, dev)
+            for verify in (False, True):
+                parity(nest.linear(layer, x, verify).cpu().numpy(), O.forward(q, s_o, s_i, xv, verify)["y"])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,idx,T", [("decoder_31b", 4, 64), ("decoder_31b", 6, 1), ("decoder_12b", 6, 16)])
+def test_full_size_sampled_rows(dev, name, idx, T):
+    """Full-size shapes of the 31B/12B workloads with uniformly drawn codes: every
+    output row of 3 sampled tiles and every token, against the oracle's dequantised rows."""
+    lin = synth.WORKLOADS[name].linears[idx]
+    M, K = lin.M, lin.K
+    bc, bs, rc, rs = synth.uniform_codes(M, K, 8, lin.w_seed)
+    s_o, s_i = synth.sign_pair(M, K, lin.sign_seed)
+    layer = nest.pack(to_dev(bc, torch, dev), to_dev(bs, torch, dev), to_dev(rc, torch, dev), to_dev(rs, torch, dev),
+                      8, to_dev(s_o, torch, dev), to_dev(s_i, torch, dev))
+    x, xv = bf16_x(T, K, 77, dev)
+    xr = O.rotate_activations(xv, s_i)
+    tiles = [0, (M // 128) // 2, (M - 1) // 128]
+    rows = np.concatenate([np.arange(t * 128, min(M, t * 128 + 128)) for t in tiles])
+    for verify in (False, True):
+        z = run_gemm(layer, x, verify, dev)
+        sub = {"base_codes": bc[rows], "base_scales": bs[rows].view(np.float16),
+               "resid_codes": rc[rows], "resid_scales": rs[rows].view(np.float16)}
+        parity(z[:, rows], O.forward_rows(sub, xr, verify))
+
+
+def test_error_flag_clear(dev):
+    nest.error_check()
