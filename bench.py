@@ -209,16 +209,12 @@ def run_gpu(args, rank, world):
             b, _ = synth.activations(T, K, wl.x_seed + K + T)
             xs[(K, T)] = torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
     maxM = max(l.M for l in wl.linears)
-    maxK = max(l.K for l in wl.linears)
     scratch = torch.zeros(max(nest.linear_scratch_bytes(l.M, l.K, T) for l in wl.linears
                               for T in (T_DRAFT, T_VERIFY)), dtype=torch.uint8, device=dev)
     ys = {(l.M, T): torch.empty((T, l.M), dtype=torch.float32, device=dev) for l in wl.linears
           for T in (T_DRAFT, T_VERIFY)}
     xops = {(l.K, T): nest.new_xop(l.K, T, dev) for l in wl.linears for T in (T_DRAFT, T_VERIFY)}
-    zbuf = torch.empty((64, maxM), dtype=torch.float32, device=dev)
-    ws = nest.new_workspace(maxM, maxK, 64, dev)
-    for l in wl.linears:
-        assert ws.numel() >= nest.workspace_bytes(l.M, l.K, T_VERIFY)
+    zbuf = torch.zeros((64, maxM), dtype=torch.float32, device=dev)   # accumulated into by the GEMM-only runs
 
     def step():
         for trip in layers:                      # draft pass through the stack
@@ -231,7 +227,7 @@ def run_gpu(args, rank, world):
     def gemm_only(T, verify):
         for trip in layers:
             for L in trip:
-                nest.gemm(L, xops[(L.K, T)], T, verify, z=zbuf[:T, :L.M], workspace=ws)
+                nest.gemm(L, xops[(L.K, T)], T, verify, z=zbuf.view(-1)[:T * L.M].view(T, L.M))
 
     # operands for the GEMM-only regions
     for l in layers[0]:

@@ -21,7 +21,9 @@
  *     where an argument says "host".  The library allocates no memory.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *     void*; NULL is the legacy default stream).  No entry point
- *     synchronises, except nest_error_check.
+ *     synchronises, except nest_error_check.  Kernels are launched with
+ *     programmatic dependent launch: each waits for the previous kernel in
+ *     the stream before it reads that kernel's results or writes its outputs.
  *   - Arguments are validated on the host before any launch; a bad argument
  *     returns an error status and launches nothing.
  *   - Pointers must be 16-byte aligned unless stated otherwise
@@ -91,12 +93,6 @@ size_t nest_resid_bytes(int32_t M, int32_t K, int32_t bits);
 /* Bytes of the activation operand for K columns and T tokens: (K/128) * 256 * Np. */
 size_t nest_xop_bytes(int32_t K, int32_t T);
 
-/* Bytes of the GEMM workspace (partial sums of row tiles split across CTAs,
- * and one counter per tile).  The workspace must be zero-filled once after
- * allocation; every call that completes leaves its counters at zero again.
- * Calls that share a workspace must not run concurrently. */
-size_t nest_workspace_bytes(int32_t M, int32_t K, int32_t T);
-
 /* ---- offline: quantize and pack --------------------------------------- */
 
 /* RTN quantizer of one layer (feedman.me/posts/wZBTJ, POC recipe steps 1-3,
@@ -151,7 +147,7 @@ nest_status nest_unpack(const nest_layer* layer, uint8_t* base_codes, uint16_t* 
  * mode 0 (input side):  out_t = H S x_t   (signs first, then the block FWHT);
  * mode 1 (output side): out_t = S H x_t   (block FWHT first, then the signs).
  * H is block-diagonal with Sylvester blocks of size nest_hadamard_block(n), each scaled by 1/sqrt(b).
- * x        [T][n], fp32 (x_dtype 0) or bf16 bits (x_dtype 1).
+ * x        [T][n], fp32 (x_dtype 0) or bf16 bits (x_dtype 1); T * n < 2^31.
  * signs    int8 [n] +-1 (natural alignment).
  * y        fp32 [T][n] out, or NULL.
  * x_op     activation operand out (mode 0 only, n % 128 == 0, T <= 64), or NULL.
@@ -159,26 +155,29 @@ nest_status nest_unpack(const nest_layer* layer, uint8_t* base_codes, uint16_t* 
 nest_status nest_rotate(const void* x, int32_t x_dtype, const int8_t* signs, int32_t n, int32_t T,
                         int32_t mode, float* y, uint16_t* x_op, void* stream);
 
-/* Draft GEMV/GEMM: z[t][m] = sum_k Q_base[m][k] x'[t][k] for t < T, in the rotated
- * output basis (POC recipe step 4, "the same but without y_r").  Reads the base buffer only.
- * x_op      activation operand from nest_rotate (T tokens).
- * z         fp32 [T][M] out.
- * workspace nest_workspace_bytes(M, K, T) bytes (see there). */
-nest_status nest_draft_gemv(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T,
-                            void* workspace, void* stream);
+/* Draft GEMV/GEMM: z[t][m] += sum_k Q_base[m][k] x'[t][k] for t < T, in the rotated
+ * output basis (POC recipe step 4: the draft forward is the verifier's without y_r).
+ * Reads the base buffer only.
+ * x_op  activation operand from nest_rotate (T tokens).
+ * z     fp32 [T][M], ACCUMULATED into: clear it first for a plain product.  The
+ *       128-column groups of a row are split across CTAs and each part is added with
+ *       fp32 atomics, so the order of those additions (and the last bits of z) may
+ *       differ between calls.  Calls that write the same z must not run concurrently
+ *       unless that accumulation is intended. */
+nest_status nest_draft_gemv(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* stream);
 
-/* Verify GEMM: z[t][m] = sum_k (Q_base + Q_resid)[m][k] x'[t][k] for t < T, one pass over
+/* Verify GEMM: z[t][m] += sum_k (Q_base + Q_resid)[m][k] x'[t][k] for t < T, one pass over
  * both buffers for all T tokens (POC recipe step 4: y_b + y_r before the output rotation).
  * Needs layer->resid_bits in {6, 7, 8}.  Arguments as nest_draft_gemv. */
-nest_status nest_verify_gemm(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T,
-                             void* workspace, void* stream);
+nest_status nest_verify_gemm(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* stream);
 
 /* Whole linear: y = S_o H_o (Q x'), x' = H_i S_i x (rotate in, GEMM, rotate out).
  * verify  0 = draft (base only), 1 = verify (base + residual).
  * x       [T][K] fp32 (x_dtype 0) or bf16 bits (x_dtype 1).
  * y       fp32 [T][M] out.
- * scratch nest_linear_scratch_bytes(M, K, T) bytes; its workspace part obeys the
- *         rules of nest_workspace_bytes (zero-filled once). */
+ * scratch nest_linear_scratch_bytes(M, K, T) bytes of device memory (operand and
+ *         accumulator; no initial contents needed).  Calls sharing a scratch buffer
+ *         must be ordered (one stream). */
 size_t nest_linear_scratch_bytes(int32_t M, int32_t K, int32_t T);
 nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype,
                         int32_t T, float* y, void* scratch, void* stream);

@@ -61,13 +61,13 @@ nest_status check_layer(const nest_layer* L, bool need_resid) {
     return NEST_OK;
 }
 
-nest_status run_gemm(const nest_layer* L, int bits, const uint16_t* xop, float* z, int T, void* ws, void* stream) {
+nest_status run_gemm(const nest_layer* L, int bits, const uint16_t* xop, float* z, int T, void* stream) {
     nest_status st = check_layer(L, bits != 0);
     if (st != NEST_OK) return st;
-    if (xop == nullptr || z == nullptr || ws == nullptr) return NEST_ERR_INVALID_ARG;
+    if (xop == nullptr || z == nullptr) return NEST_ERR_INVALID_ARG;
     if (T < 1) return NEST_ERR_INVALID_ARG;
     if (T > 64) return NEST_ERR_UNSUPPORTED;
-    if (!aligned16(xop) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(z) & 3u)) return NEST_ERR_MISALIGNED;
+    if (!aligned16(xop) || (reinterpret_cast<uintptr_t>(z) & 3u)) return NEST_ERR_MISALIGNED;
     if (!device_supported()) return NEST_ERR_UNSUPPORTED;
     const int sms = device_sms();
     if (sms <= 0) return NEST_ERR_CUDA;
@@ -76,14 +76,13 @@ nest_status run_gemm(const nest_layer* L, int bits, const uint16_t* xop, float* 
     a.resid = bits ? L->resid : nullptr;
     a.xop = xop;
     a.z = z;
-    a.counters = reinterpret_cast<int*>(ws);
-    a.partial = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + ws_counter_bytes(L->M));
     a.M = L->M;
     a.K = L->K;
     a.T = T;
     a.G = L->K / 128;
     a.units = (long long)n_tiles(L->M) * a.G;
-    long long grid = a.units < sms ? a.units : sms;
+    const long long slots = (long long)kGemmCtasPerSm * sms;   // every CTA resident at once
+    long long grid = a.units < slots ? a.units : slots;
     if (grid > kMaxGrid) grid = kMaxGrid;
     return from_cuda(launch_gemm(a, bits, (int)grid, as_stream(stream)));
 }
@@ -119,11 +118,6 @@ size_t nest_resid_bytes(int32_t M, int32_t K, int32_t bits) {
 size_t nest_xop_bytes(int32_t K, int32_t T) {
     if (K < 1 || K % 128 || T < 1 || T > 64) return 0;
     return (size_t)(K / 128) * 256 * n_pad(T);
-}
-
-size_t nest_workspace_bytes(int32_t M, int32_t K, int32_t T) {
-    if (M < 1 || K < 1 || K % 128 || T < 1 || T > 64) return 0;
-    return ws_counter_bytes(M) + ws_partial_bytes(M, K, T);
 }
 
 nest_status nest_quantize(const float* W, const int8_t* sign_out, const int8_t* sign_in, int32_t M, int32_t K,
@@ -175,6 +169,7 @@ nest_status nest_rotate(const void* x, int32_t x_dtype, const int8_t* signs, int
                         float* y, uint16_t* x_op, void* stream) {
     if (!x || !signs || (!y && !x_op)) return NEST_ERR_INVALID_ARG;
     if (n < 1 || T < 1) return NEST_ERR_INVALID_ARG;
+    if ((long long)n * T >= (1LL << 31)) return NEST_ERR_UNSUPPORTED;
     if ((x_dtype != 0 && x_dtype != 1) || (mode != 0 && mode != 1)) return NEST_ERR_INVALID_ARG;
     if (x_op != nullptr) {
         if (mode != 0) return NEST_ERR_INVALID_ARG;
@@ -183,26 +178,24 @@ nest_status nest_rotate(const void* x, int32_t x_dtype, const int8_t* signs, int
     }
     if ((reinterpret_cast<uintptr_t>(x) & (x_dtype == 1 ? 1u : 3u)) || (y && (reinterpret_cast<uintptr_t>(y) & 3u)))
         return NEST_ERR_MISALIGNED;
-    return from_cuda(launch_rotate(x, x_dtype, signs, n, T, mode, y, x_op, as_stream(stream)));
+    return from_cuda(launch_rotate(x, x_dtype, signs, n, T, mode, y, x_op, nullptr, 0, as_stream(stream)));
 }
 
-nest_status nest_draft_gemv(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* workspace,
-                            void* stream) {
-    return run_gemm(layer, 0, x_op, z, T, workspace, stream);
+nest_status nest_draft_gemv(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* stream) {
+    return run_gemm(layer, 0, x_op, z, T, stream);
 }
 
-nest_status nest_verify_gemm(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* workspace,
-                             void* stream) {
+nest_status nest_verify_gemm(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* stream) {
     if (layer != nullptr && layer->resid_bits == 0) return NEST_ERR_INVALID_ARG;
-    return run_gemm(layer, layer ? layer->resid_bits : 0, x_op, z, T, workspace, stream);
+    return run_gemm(layer, layer ? layer->resid_bits : 0, x_op, z, T, stream);
 }
 
-// scratch of nest_linear: [x_op][z][workspace], each 256-byte aligned
+// scratch of nest_linear: [x_op][z], each 256-byte aligned
 static size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t nest_linear_scratch_bytes(int32_t M, int32_t K, int32_t T) {
     if (M < 1 || K < 1 || K % 128 || T < 1 || T > 64) return 0;
-    return round256(nest_xop_bytes(K, T)) + round256((size_t)T * M * sizeof(float)) + nest_workspace_bytes(M, K, T);
+    return round256(nest_xop_bytes(K, T)) + round256((size_t)T * M * sizeof(float));
 }
 
 nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype, int32_t T, float* y,
@@ -217,10 +210,14 @@ nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, 
     uint8_t* s = reinterpret_cast<uint8_t*>(scratch);
     uint16_t* xop = reinterpret_cast<uint16_t*>(s);
     float* z = reinterpret_cast<float*>(s + round256(nest_xop_bytes(K, T)));
-    void* ws = s + round256(nest_xop_bytes(K, T)) + round256((size_t)T * M * sizeof(float));
-    st = nest_rotate(x, x_dtype, layer->sign_in, K, T, 0, nullptr, xop, stream);
-    if (st != NEST_OK) return st;
-    st = verify ? nest_verify_gemm(layer, xop, z, T, ws, stream) : nest_draft_gemv(layer, xop, z, T, ws, stream);
+    if ((x_dtype != 0 && x_dtype != 1) || (reinterpret_cast<uintptr_t>(x) & (x_dtype == 1 ? 1u : 3u)))
+        return x_dtype != 0 && x_dtype != 1 ? NEST_ERR_INVALID_ARG : NEST_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(y) & 3u)) return NEST_ERR_MISALIGNED;
+    // rotate in, writing the GEMM operand and clearing the accumulator z
+    cudaError_t e = launch_rotate(x, x_dtype, layer->sign_in, K, T, 0, nullptr, xop, z, (long long)T * M,
+                                  as_stream(stream));
+    if (e != cudaSuccess) return NEST_ERR_CUDA;
+    st = verify ? nest_verify_gemm(layer, xop, z, T, stream) : nest_draft_gemv(layer, xop, z, T, stream);
     if (st != NEST_OK) return st;
     return nest_rotate(z, 0, layer->sign_out, M, T, 1, y, nullptr, stream);
 }

@@ -21,10 +21,14 @@
 //                    memory (128 lanes x Np columns).
 //   epilogue       : warpgroup 0 reads D with tcgen05.ld and writes z.
 // Work split: the (tile, group) units, tile-major, are cut into equal
-// contiguous ranges, one per CTA ("stream-K").  A tile whose groups span
-// several CTAs is finished by whichever CTA arrives last: each contributor
-// writes its partial sums to the workspace and bumps a per-tile counter; the
-// last one adds the partials in CTA order (deterministic) and writes z.
+// contiguous ranges, one per CTA ("stream-K").  Every CTA adds the sums of
+// each row-tile segment it covers into z with fp32 reductions (z += ...), so a
+// tile split across CTAs needs no workspace and no inter-CTA handshake; the
+// order in which the split parts land is not fixed.
+// Launches use programmatic dependent launch: a CTA sets up its barriers and
+// tensor memory and starts streaming weights before the previous kernel in the
+// stream has finished; it waits for it (griddepcontrol.wait) only before it
+// reads the activation operand or touches z.
 #include "nest_device.cuh"
 #include "nest_internal.h"
 
@@ -42,34 +46,22 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
-// Bounded wait for a single thread.  Gives up after kWaitLimitNs or when the
-// CTA's abort flag is raised; on a timeout it raises the flag and the device
-// error flag.  `honour_abort == false` is used while draining in-flight copies.
-__device__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int* abort, bool honour_abort = true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (honour_abort && *abort) return false;
-        if ((it & 31u) == 31u && globaltimer() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            atomicExch(&g_nest_error, 1);
-            return false;
-        }
-    }
-}
-
-// Bounded wait for a whole warp; the result is the same on every lane.
-__device__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// Bounded wait for a whole warp (all 32 lanes converged); the result is the
+// same on every lane.  Gives up after kWaitLimitNs, or at once when another
+// role of the CTA has given up (*abort != 0) unless `honour_abort` is false
+// (used while draining in-flight copies and MMAs); on a timeout it raises the
+// CTA's abort flag and the device error flag.
+__device__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, bool honour_abort = true) {
     bool ok = mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, ok)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 0;; ++it) {
         if (!ok) ok = mbar_try_wait(bar, parity);
         if (__all_sync(0xffffffffu, ok)) return true;
-        const bool stop = (*abort != 0) || ((it & 31u) == 31u && globaltimer() - t0 > kWaitLimitNs);
+        const bool timed_out = (it & 31u) == 31u && globaltimer() - t0 > kWaitLimitNs;
+        const bool stop = timed_out || (honour_abort && *abort != 0);
         if (__any_sync(0xffffffffu, stop)) {
-            if ((threadIdx.x & 31) == 0) {
+            if (__any_sync(0xffffffffu, timed_out) && (threadIdx.x & 31) == 0) {
                 *abort = 1;
                 atomicExch(&g_nest_error, 1);
             }
@@ -80,24 +72,30 @@ __device__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
 
 template <int BITS, int NP>
 struct Cfg {
+    // Two CTAs share an SM: each has its own MMA issuer, so the gaps in one
+    // CTA's MMA stream (barrier waits, commits) are filled by the other's.
+    static constexpr int kCtasPerSm = 2;
     static constexpr int kResUnit = resid_unit_bytes(BITS);
-    static constexpr int kXBytes = 256 * NP;                // Np tokens x 128 columns of fp16
-    static constexpr int kStage = kBaseUnit + kResUnit + kXBytes;
-    static constexpr int kStagesRaw = (220 * 1024 - 1024) / kStage;
+    static constexpr int kWStage = kBaseUnit + kResUnit;     // packed weights of one unit
+    static constexpr int kXBytes = 256 * NP;                 // Np tokens x 128 columns of fp16
+    static constexpr int kTmemCols = 512 / kCtasPerSm;
+    static constexpr int kColA = 2 * NP;                     // A buffers after the two D buffers
+    static constexpr int kNumA = (kTmemCols - kColA) / 64;   // A buffers (64 TMEM columns) = activation slots
+    static constexpr int kXRing = kNumA * kXBytes;
+    static constexpr int kSmemBudget = 110 * 1024;
+    static constexpr int kStagesRaw = (kSmemBudget - 512 - kXRing) / kWStage;
     static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
-    static constexpr int kNumA = 6;                         // A buffers of 64 TMEM columns
-    static constexpr int kDeqWG = 2;                        // dequantising warpgroups
+    static constexpr int kDeqWG = 2;                         // dequantising warpgroups
     static constexpr int kProducerWarp = 4 * kDeqWG;
     static constexpr int kMmaWarp = 4 * kDeqWG + 1;
     static constexpr int kThreads = 32 * (4 * kDeqWG + 2);
-    static constexpr int kTmemCols = 512;
-    static constexpr int kColA = 128;                       // A buffers after the two D buffers
-    // barriers: full[S], empty[S], a_full[NA], a_empty[NA], d_full[2], d_empty[2], drain
-    static constexpr int kNumBars = 2 * kStages + 2 * kNumA + 5;
-    static constexpr int kSmemBytes = kStages * kStage + kNumBars * 8 + 16;
+    // barriers: full_w[S], empty_w[S], full_x[NA], a_full[NA], done[NA], d_full[2], d_empty[2], drain
+    static constexpr int kNumBars = 2 * kStages + 3 * kNumA + 5;
+    static constexpr int kSmemBytes = kStages * kWStage + kXRing + kNumBars * 8 + 16;
+    static_assert(kNumA >= 2, "tensor memory budget");
     static_assert(kStages >= 2, "stage too large");
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-    static_assert(kStage % 128 == 0, "stage alignment");
+    static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
+    static_assert(kWStage % 128 == 0 && kXBytes % 128 == 0, "stage alignment");
 };
 
 // Decode 64 columns (half h of the 128-column group) of row r of one unit into
@@ -192,38 +190,37 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NP]) {
 __device__ __forceinline__ long long unit_begin(int c, long long units, int grid) {
     return (long long)c * units / grid;
 }
-__device__ __forceinline__ int unit_owner(long long u, long long units, int grid) {
-    return (int)(((u + 1) * grid - 1) / units);
-}
 
 template <int BITS, int NP>
-__global__ void __launch_bounds__(Cfg<BITS, NP>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BITS, NP>::kThreads, Cfg<BITS, NP>::kCtasPerSm)
 k_nest_gemm(const GemmArgs p) {
     using C = Cfg<BITS, NP>;
     constexpr int S = C::kStages, NA = C::kNumA;
     extern __shared__ __align__(1024) uint8_t smem[];
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStage);
+    uint8_t* xring = smem + S * C::kWStage;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(xring + C::kXRing);
     const uint32_t bar0 = smem_u32(bars);
-    auto full = [&](int s) { return bar0 + 8u * s; };
-    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
-    auto a_full = [&](int a) { return bar0 + 8u * (2 * S + a); };
-    auto a_empty = [&](int a) { return bar0 + 8u * (2 * S + NA + a); };
-    auto d_full = [&](int d) { return bar0 + 8u * (2 * S + 2 * NA + d); };
-    auto d_empty = [&](int d) { return bar0 + 8u * (2 * S + 2 * NA + 2 + d); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * S + 2 * NA + 4);
+    auto full_w = [&](int s) { return bar0 + 8u * s; };
+    auto empty_w = [&](int s) { return bar0 + 8u * (S + s); };
+    auto full_x = [&](int a) { return bar0 + 8u * (2 * S + a); };
+    auto a_full = [&](int a) { return bar0 + 8u * (2 * S + NA + a); };
+    auto done = [&](int a) { return bar0 + 8u * (2 * S + 2 * NA + a); };
+    auto d_full = [&](int d) { return bar0 + 8u * (2 * S + 3 * NA + d); };
+    auto d_empty = [&](int d) { return bar0 + 8u * (2 * S + 3 * NA + 2 + d); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 3 * NA + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-    auto st_base = [&](int s) { return smem + s * C::kStage; };
-    auto st_res = [&](int s) { return smem + s * C::kStage + kBaseUnit; };
-    auto st_x = [&](int s) { return smem + s * C::kStage + kBaseUnit + C::kResUnit; };
+    auto st_base = [&](int s) { return smem + s * C::kWStage; };
+    auto st_res = [&](int s) { return smem + s * C::kWStage + kBaseUnit; };
+    auto st_x = [&](int a) { return xring + a * C::kXBytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
-        for (int a = 0; a < NA; ++a) { mbar_init(a_full(a), kRows); mbar_init(a_empty(a), 1); }
+        for (int s = 0; s < S; ++s) { mbar_init(full_w(s), 1); mbar_init(empty_w(s), kRows); }
+        for (int a = 0; a < NA; ++a) { mbar_init(full_x(a), 1); mbar_init(a_full(a), kRows); mbar_init(done(a), 1); }
         for (int d = 0; d < 2; ++d) { mbar_init(d_full(d), 1); mbar_init(d_empty(d), kRows); }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -237,66 +234,110 @@ k_nest_gemm(const GemmArgs p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dep_launch_dependents();
 
+    // this CTA's contiguous range of (tile, group) units
     const long long units = p.units;
     const int grid = gridDim.x, cta = blockIdx.x, G = p.G;
     const long long u0 = unit_begin(cta, units, grid);
     const int n = (int)(unit_begin(cta + 1, units, grid) - u0);
+    const int tile0 = (int)(u0 / G), g0 = (int)(u0 - (long long)tile0 * G);
 
     if (warp == C::kProducerWarp) {
-        if (lane == 0) {
-            int issued = 0;
-            for (int i = 0; i < n; ++i) {
-                const int s = i % S;
-                if (i >= S && !thread_wait(empty(s), ((i / S) - 1) & 1, abort_flag)) break;
-                const long long u = u0 + i;
-                const int g = (int)(u % G);
-                mbar_arrive_expect_tx(full(s), C::kStage);
-                bulk_g2s(smem_u32(st_base(s)), p.base + u * kBaseUnit, kBaseUnit, full(s));
-                if constexpr (BITS != 0)
-                    bulk_g2s(smem_u32(st_res(s)), p.resid + u * C::kResUnit, C::kResUnit, full(s));
-                bulk_g2s(smem_u32(st_x(s)), p.xop + (size_t)g * (C::kXBytes / 2), C::kXBytes, full(s));
-                ++issued;
+        const uint8_t* bsrc = p.base + u0 * kBaseUnit;
+        const uint8_t* rsrc = p.resid + u0 * C::kResUnit;
+        auto issue_w = [&](int i) {
+            const int s = i % S;
+            mbar_arrive_expect_tx(full_w(s), C::kWStage);
+            bulk_g2s(smem_u32(st_base(s)), bsrc + (size_t)i * kBaseUnit, kBaseUnit, full_w(s));
+            if constexpr (BITS != 0)
+                bulk_g2s(smem_u32(st_res(s)), rsrc + (size_t)i * C::kResUnit, C::kResUnit, full_w(s));
+        };
+        // weights do not depend on the previous kernel: fill the weight ring now
+        const int pre = n < S ? n : S;
+        if (lane == 0)
+            for (int i = 0; i < pre; ++i) issue_w(i);
+        __syncwarp();
+        grid_dep_wait();                     // the activation operand comes from the previous kernel
+        // Two independent rings: activation block of unit ix goes to slot ix % NA once unit
+        // ix - NA's MMAs are done; weights of unit iw go to stage iw % S once unit iw - S has
+        // been decoded.  Poll both so neither waits behind the other.
+        int iw = pre, ix = 0, g = g0;
+        uint64_t t_last = globaltimer();
+        while (ix < n || iw < n) {
+            bool moved = false;
+            if (ix < n) {
+                bool ready = ix < NA;
+                if (!ready && lane == 0) ready = mbar_test_wait(done(ix % NA), ((ix / NA) - 1) & 1);
+                if (__shfl_sync(0xffffffffu, ready, 0)) {
+                    if (lane == 0) {
+                        const int a = ix % NA;
+                        mbar_arrive_expect_tx(full_x(a), C::kXBytes);
+                        bulk_g2s(smem_u32(st_x(a)), p.xop + (size_t)g * (C::kXBytes / 2), C::kXBytes, full_x(a));
+                    }
+                    if (++g == G) g = 0;
+                    ++ix;
+                    moved = true;
+                }
             }
-            // every issued copy has landed before the CTA may leave
-            for (int j = issued > S ? issued - S : 0; j < issued; ++j)
-                thread_wait(full(j % S), (j / S) & 1, abort_flag, false);
+            if (iw < n) {
+                bool ready = false;
+                if (lane == 0) ready = mbar_test_wait(empty_w(iw % S), ((iw / S) - 1) & 1);
+                if (__shfl_sync(0xffffffffu, ready, 0)) {
+                    if (lane == 0) issue_w(iw);
+                    ++iw;
+                    moved = true;
+                }
+            }
+            if (moved) {
+                t_last = globaltimer();
+            } else {
+                __nanosleep(64);           // nothing to issue yet: back off the barrier words
+                const bool stop = (*abort_flag != 0) || (globaltimer() - t_last > kWaitLimitNs);
+                if (__shfl_sync(0xffffffffu, stop, 0)) {
+                    if (lane == 0 && *abort_flag == 0) { *abort_flag = 1; atomicExch(&g_nest_error, 1); }
+                    break;
+                }
+            }
         }
+        __syncwarp();
+        // every issued copy has landed before the CTA may leave
+        for (int j = iw > S ? iw - S : 0; j < iw; ++j) warp_wait(full_w(j % S), (j / S) & 1, abort_flag, false);
+        for (int j = ix > NA ? ix - NA : 0; j < ix; ++j) warp_wait(full_x(j % NA), (j / NA) & 1, abort_flag, false);
     } else if (warp == C::kMmaWarp) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(128, NP);
-            int seg = -1;
-            bool issued_any = false;
-            for (int i = 0; i < n; ++i) {
-                const long long u = u0 + i;
-                const int g = (int)(u % G);
-                const bool first = (i == 0) || g == 0;
-                const bool last = (i == n - 1) || g == G - 1;
-                if (first) {
-                    ++seg;
-                    if (seg >= 2 && !thread_wait(d_empty(seg & 1), ((seg >> 1) - 1) & 1, abort_flag)) break;
-                }
-                const int s = i % S, a = i % NA, d = seg & 1;
-                if (!thread_wait(full(s), (i / S) & 1, abort_flag)) break;
-                if (!thread_wait(a_full(a), (i / NA) & 1, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t xb = smem_u32(st_x(s));
+        constexpr uint32_t idesc = idesc_f16_f32(128, NP);
+        // B descriptor of activation slot 0, k-step 0; slot a adds a * kXBytes, k-step kk adds kk * NP * 32 bytes
+        const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(xring), (NP / 8) * 128, 128);
+        int seg = -1, g = g0;
+        bool issued_any = false;
+        for (int i = 0; i < n; ++i) {
+            const bool first = (i == 0) || g == 0;
+            const bool last = (i == n - 1) || g == G - 1;
+            if (first) {
+                ++seg;
+                if (seg >= 2 && !warp_wait(d_empty(seg & 1), ((seg >> 1) - 1) & 1, abort_flag)) break;
+            }
+            const int a = i % NA, d = seg & 1;
+            // a_full also covers the activation block: its warpgroup waited for full_x before arriving
+            if (!warp_wait(a_full(a), (i / NA) & 1, abort_flag)) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t bd = bdesc0 + (uint64_t)((a * C::kXBytes) >> 4);
+                const uint32_t ta = tmem + C::kColA + 64 * a, td = tmem + d * NP;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    // B block: core matrix (token block nb, column chunk c) at ((c * NP/8) + nb) * 128 bytes
-                    const uint64_t bdesc = smem_desc_noswizzle(xb + (2 * kk) * (NP / 8) * 128, (NP / 8) * 128, 128);
-                    mma_f16_ts(tmem + d * NP, tmem + C::kColA + 64 * a + 8 * kk, bdesc, idesc,
-                               (first && kk == 0) ? 0u : 1u);
-                }
-                issued_any = true;
-                tc_commit(empty(s));
-                tc_commit(a_empty(a));
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_f16_ts(td, ta + 8 * kk, bd + (uint64_t)(kk * NP * 2), idesc, (first && kk == 0) ? 0u : 1u);
+                tc_commit(done(a));
                 if (last) tc_commit(d_full(d));
             }
-            if (issued_any) {          // all MMAs finished before tensor memory is released
-                tc_commit(drain_bar);
-                thread_wait(drain_bar, 0, abort_flag, false);
-            }
+            __syncwarp();
+            issued_any = true;
+            if (++g == G) g = 0;
+        }
+        if (issued_any) {              // all MMAs finished before tensor memory is released
+            if (lane == 0) tc_commit(drain_bar);
+            __syncwarp();
+            warp_wait(drain_bar, 0, abort_flag, false);
         }
     } else {
         // dequantisation warpgroups; warpgroup 0 also runs the epilogues
@@ -304,18 +345,16 @@ k_nest_gemm(const GemmArgs p) {
         const int r = 32 * (warp & 3) + lane;               // row of the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const __half2 off2 = __float2half2_rn(1024.0f + (BITS ? (float)(1 << (BITS - 1)) : 0.0f));
-        int seg = -1;
-        bool ok = true;
-        for (int i = 0; i < n && ok; ++i) {
-            const long long u = u0 + i;
-            const int g = (int)(u % G);
-            const int tile = (int)(u / G);
-            if ((i == 0) || g == 0) ++seg;
+        int seg = -1, g = g0, tile = tile0;
+        bool dep_done = false;
+        for (int i = 0; i < n; ++i) {
+            const bool first = (i == 0) || g == 0;
+            const bool last = (i == n - 1) || g == G - 1;
+            if (first) ++seg;
             if (i % C::kDeqWG == wg) {
                 const int s = i % S, a = i % NA;
-                ok = warp_wait(full(s), (i / S) & 1, abort_flag);
-                if (ok && i >= NA) ok = warp_wait(a_empty(a), ((i / NA) - 1) & 1, abort_flag);
-                if (!ok) break;
+                if (!warp_wait(full_w(s), (i / S) & 1, abort_flag)) break;
+                if (i >= NA && !warp_wait(done(a), ((i / NA) - 1) & 1, abort_flag)) break;
                 tc_fence_after();
                 const uint8_t* sb = st_base(s);
                 const uint8_t* sr = st_res(s);
@@ -335,13 +374,15 @@ k_nest_gemm(const GemmArgs p) {
                     dequant_half<BITS>(sb, sr, r, hh, lut_lo, lut_hi, sr2, off2, w);
                     tmem_st32_wait(tmem + lane_base + C::kColA + 64 * a + 32 * hh, w);
                 }
+                mbar_arrive(empty_w(s));             // this thread is done with the weight stage
                 tc_fence_before();
+                // the MMA issuer waits on a_full alone, so a_full must also imply the activation block
+                if (!warp_wait(full_x(a), (i / NA) & 1, abort_flag)) break;
                 mbar_arrive(a_full(a));
             }
-            const bool last = (i == n - 1) || g == G - 1;
             if (wg == 0 && last) {
                 const int d = seg & 1;
-                if (!warp_wait(d_full(d), (seg >> 1) & 1, abort_flag)) { ok = false; break; }
+                if (!warp_wait(d_full(d), (seg >> 1) & 1, abort_flag)) break;
                 tc_fence_after();
                 float v[NP];
                 tmem_ld_cols<NP>(tmem + lane_base + d * NP, v);
@@ -349,50 +390,15 @@ k_nest_gemm(const GemmArgs p) {
                 mbar_arrive(d_empty(d));
                 const int m = tile * kRows + r;
                 const int T = p.T, M = p.M;
-                const bool whole = (g == G - 1) && (u - (long long)tile * G + 1 == (long long)G) &&
-                                   (u0 <= (long long)tile * G);
-                if (whole) {
-                    if (m < M) {
-#pragma unroll
-                        for (int t = 0; t < NP; ++t)
-                            if (t < T) p.z[(size_t)t * M + m] = v[t];
-                    }
-                } else {
-                    // partial tile: slot 0 for this CTA's first segment, 1 for its last
-                    const int slot = ((long long)tile * G <= u0) ? 0 : 1;
-                    float* part = p.partial + ((size_t)(2 * cta + slot) * T) * kRows;
+                if (!dep_done) { grid_dep_wait(); dep_done = true; }
+                if (m < M) {
+                    float* zp = p.z + m;
 #pragma unroll
                     for (int t = 0; t < NP; ++t)
-                        if (t < T) part[(size_t)t * kRows + r] = v[t];
-                    __threadfence();
-                    __syncwarp();
-                    const int c_lo = unit_owner((long long)tile * G, units, grid);
-                    const int c_hi = unit_owner((long long)tile * G + G - 1, units, grid);
-                    int* ctr = p.counters + 4 * tile + (warp & 3);
-                    int old = 0;
-                    if (lane == 0) old = atomicAdd(ctr, 1);
-                    old = __shfl_sync(0xffffffffu, old, 0);
-                    if (old == c_hi - c_lo) {
-                        __threadfence();
-                        float acc[NP];
-#pragma unroll
-                        for (int t = 0; t < NP; ++t) acc[t] = 0.0f;
-                        for (int c = c_lo; c <= c_hi; ++c) {
-                            const int sl = ((long long)tile * G <= unit_begin(c, units, grid)) ? 0 : 1;
-                            const float* pp = p.partial + ((size_t)(2 * c + sl) * T) * kRows;
-#pragma unroll
-                            for (int t = 0; t < NP; ++t)
-                                if (t < T) acc[t] += __ldcg(pp + (size_t)t * kRows + r);
-                        }
-                        if (m < M) {
-#pragma unroll
-                            for (int t = 0; t < NP; ++t)
-                                if (t < T) p.z[(size_t)t * M + m] = acc[t];
-                        }
-                        if (lane == 0) atomicExch(ctr, 0);
-                    }
+                        if (t < T) atomicAdd(zp + (size_t)t * M, v[t]);    // fire-and-forget reduction
                 }
             }
+            if (++g == G) { g = 0; ++tile; }
         }
     }
 
@@ -405,15 +411,14 @@ k_nest_gemm(const GemmArgs p) {
 template <int BITS, int NP>
 cudaError_t launch_t(const GemmArgs& a, int grid, cudaStream_t stream) {
     using C = Cfg<BITS, NP>;
-    static bool configured = false;       // per instantiation; attribute is per device context
+    static bool configured = false;       // the attribute is per function; set it on first use
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(k_nest_gemm<BITS, NP>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    k_nest_gemm<BITS, NP><<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_nest_gemm<BITS, NP>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, a);
 }
 
 template <int BITS>

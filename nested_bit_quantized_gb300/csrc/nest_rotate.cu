@@ -40,17 +40,25 @@ __device__ __forceinline__ void warp_fwht(float& v0, float& v1, int nbits, int l
 
 template <int MODE, bool BF16>
 __global__ void __launch_bounds__(kThreads)
-k_rotate(const void* __restrict__ x, const int8_t* __restrict__ signs, int n, long long total, int L,
-         float scale, float* __restrict__ y, uint16_t* __restrict__ xop, int NB) {
+k_rotate(const void* __restrict__ x, const int8_t* __restrict__ signs, unsigned n, unsigned total, int L,
+         float scale, float* __restrict__ y, uint16_t* __restrict__ xop, int NB, float* __restrict__ zero_out,
+         long long zero_count) {
     __shared__ float buf[64][65];
-    const long long seg0 = (long long)blockIdx.x * kSeg;
-    const long long rem = total - seg0;
-    const int count = rem < kSeg ? (int)rem : kSeg;
+    grid_dep_launch_dependents();
+    grid_dep_wait();                      // x may be the previous kernel's output; y may be its input
+    if (zero_out != nullptr) {            // clear the accumulator of the GEMM that follows
+        const long long per = (zero_count + gridDim.x - 1) / gridDim.x;
+        const long long lo = per * blockIdx.x, hi = lo + per < zero_count ? lo + per : zero_count;
+        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) zero_out[i] = 0.0f;
+    }
+    const unsigned seg0 = blockIdx.x * (unsigned)kSeg;
+    const unsigned rem = total - seg0;
+    const int count = rem < (unsigned)kSeg ? (int)rem : kSeg;
 
     for (int f = threadIdx.x; f < kSeg; f += kThreads) {
         float v = 0.0f;
         if (f < count) {
-            const long long idx = seg0 + f;
+            const unsigned idx = seg0 + f;
             if constexpr (BF16) v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(x)[idx]);
             else v = reinterpret_cast<const float*>(x)[idx];
             if constexpr (MODE == 0) v *= (float)signs[idx % n];
@@ -82,7 +90,7 @@ k_rotate(const void* __restrict__ x, const int8_t* __restrict__ signs, int n, lo
 
     if (y != nullptr) {
         for (int f = threadIdx.x; f < count; f += kThreads) {
-            const long long idx = seg0 + f;
+            const unsigned idx = seg0 + f;
             float v = buf[f >> 6][f & 63] * scale;
             if constexpr (MODE == 1) v *= (float)signs[idx % n];
             y[idx] = v;
@@ -92,8 +100,8 @@ k_rotate(const void* __restrict__ x, const int8_t* __restrict__ signs, int n, lo
         // eight consecutive columns of one token -> one 16-byte store into the operand layout
         for (int j = threadIdx.x; j < count / 8; j += kThreads) {
             const int f = 8 * j;
-            const long long idx = seg0 + f;
-            const int t = (int)(idx / n), k = (int)(idx % n);
+            const unsigned idx = seg0 + f;
+            const unsigned t = idx / n, k = idx - t * n;
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -118,22 +126,27 @@ int hadamard_block(int n) {
 }
 
 cudaError_t launch_rotate(const void* x, int x_dtype, const int8_t* signs, int n, int T, int mode,
-                          float* y, uint16_t* xop, cudaStream_t stream) {
+                          float* y, uint16_t* xop, float* zero_out, long long zero_count, cudaStream_t stream) {
     const int b = hadamard_block(n);
     int L = 0;
     while ((1 << L) < b) ++L;
     const float scale = (float)(1.0 / sqrt((double)b));
-    const long long total = (long long)T * n;
+    const unsigned total = (unsigned)T * (unsigned)n;     // the entry point keeps T * n < 2^31
     const int grid = (int)((total + kSeg - 1) / kSeg);
     const int NB = n_pad(T) / 8;
+    const dim3 g(grid), blk(kThreads);
     if (mode == 0) {
-        if (x_dtype == 1) k_rotate<0, true><<<grid, kThreads, 0, stream>>>(x, signs, n, total, L, scale, y, xop, NB);
-        else k_rotate<0, false><<<grid, kThreads, 0, stream>>>(x, signs, n, total, L, scale, y, xop, NB);
-    } else {
-        if (x_dtype == 1) k_rotate<1, true><<<grid, kThreads, 0, stream>>>(x, signs, n, total, L, scale, y, nullptr, NB);
-        else k_rotate<1, false><<<grid, kThreads, 0, stream>>>(x, signs, n, total, L, scale, y, nullptr, NB);
+        if (x_dtype == 1)
+            return launch_pdl(k_rotate<0, true>, g, blk, 0, stream, x, signs, (unsigned)n, total, L, scale, y, xop, NB,
+                              zero_out, zero_count);
+        return launch_pdl(k_rotate<0, false>, g, blk, 0, stream, x, signs, (unsigned)n, total, L, scale, y, xop, NB,
+                          zero_out, zero_count);
     }
-    return cudaGetLastError();
+    if (x_dtype == 1)
+        return launch_pdl(k_rotate<1, true>, g, blk, 0, stream, x, signs, (unsigned)n, total, L, scale, y,
+                          (uint16_t*)nullptr, NB, zero_out, zero_count);
+    return launch_pdl(k_rotate<1, false>, g, blk, 0, stream, x, signs, (unsigned)n, total, L, scale, y,
+                      (uint16_t*)nullptr, NB, zero_out, zero_count);
 }
 
 }  // namespace nest

@@ -54,14 +54,13 @@ def load() -> ctypes.CDLL:
         "nest_base_bytes": ([_I32, _I32], _SZ),
         "nest_resid_bytes": ([_I32, _I32, _I32], _SZ),
         "nest_xop_bytes": ([_I32, _I32], _SZ),
-        "nest_workspace_bytes": ([_I32, _I32, _I32], _SZ),
         "nest_linear_scratch_bytes": ([_I32, _I32, _I32], _SZ),
         "nest_quantize": ([_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P], _I32),
         "nest_pack": ([_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P], _I32),
         "nest_unpack": ([ctypes.POINTER(_Layer), _P, _P, _P, _P, _P], _I32),
         "nest_rotate": ([_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P], _I32),
-        "nest_draft_gemv": ([ctypes.POINTER(_Layer), _P, _P, _I32, _P, _P], _I32),
-        "nest_verify_gemm": ([ctypes.POINTER(_Layer), _P, _P, _I32, _P, _P], _I32),
+        "nest_draft_gemv": ([ctypes.POINTER(_Layer), _P, _P, _I32, _P], _I32),
+        "nest_verify_gemm": ([ctypes.POINTER(_Layer), _P, _P, _I32, _P], _I32),
         "nest_linear": ([ctypes.POINTER(_Layer), _I32, _P, _I32, _I32, _P, _P, _P], _I32),
         "nest_error_check": ([_P], _I32),
     }
@@ -116,10 +115,6 @@ def xop_bytes(K: int, T: int) -> int:
     return int(load().nest_xop_bytes(K, T))
 
 
-def workspace_bytes(M: int, K: int, T: int) -> int:
-    return int(load().nest_workspace_bytes(M, K, T))
-
-
 def linear_scratch_bytes(M: int, K: int, T: int) -> int:
     return int(load().nest_linear_scratch_bytes(M, K, T))
 
@@ -127,11 +122,6 @@ def linear_scratch_bytes(M: int, K: int, T: int) -> int:
 def _u8(n: int, device) -> torch.Tensor:
     # 16-byte aligned byte buffer (the caching allocator returns 512-byte aligned blocks)
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
-
-
-def new_workspace(M: int, K: int, T: int, device="cuda") -> torch.Tensor:
-    """A zero-filled GEMM workspace for shapes up to (M, K, T)."""
-    return torch.zeros(max(workspace_bytes(M, K, T), 16), dtype=torch.uint8, device=device)
 
 
 # ---------------------------------------------------------------------------
@@ -245,16 +235,16 @@ def new_xop(K: int, T: int, device="cuda") -> torch.Tensor:
 
 
 def gemm(layer: Layer, x_op: torch.Tensor, T: int, verify: bool, z: Optional[torch.Tensor] = None,
-         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """nest_verify_gemm (verify=True) or nest_draft_gemv: z [T][M] fp32 in the rotated basis."""
+         stream=None) -> torch.Tensor:
+    """nest_verify_gemm (verify=True) or nest_draft_gemv: z [T][M] fp32 in the rotated basis.
+
+    The library ACCUMULATES into z; a new z is zero-filled, a given z is added to."""
     dev = layer.base.device
     if z is None:
-        z = torch.empty((T, layer.M), dtype=torch.float32, device=dev)
-    if workspace is None:
-        workspace = new_workspace(layer.M, layer.K, T, dev)
+        z = torch.zeros((T, layer.M), dtype=torch.float32, device=dev)
     L = layer.c_struct()
     fn = load().nest_verify_gemm if verify else load().nest_draft_gemv
-    st = fn(ctypes.byref(L), _ptr(x_op), _ptr(z), T, _ptr(workspace), _stream(stream))
+    st = fn(ctypes.byref(L), _ptr(x_op), _ptr(z), T, _stream(stream))
     _check(st, "nest_verify_gemm" if verify else "nest_draft_gemv")
     return z
 
@@ -267,7 +257,7 @@ def linear(layer: Layer, x: torch.Tensor, verify: bool, y: Optional[torch.Tensor
     if y is None:
         y = torch.empty((T, layer.M), dtype=torch.float32, device=dev)
     if scratch is None:
-        scratch = torch.zeros(linear_scratch_bytes(layer.M, layer.K, T), dtype=torch.uint8, device=dev)
+        scratch = torch.empty(linear_scratch_bytes(layer.M, layer.K, T), dtype=torch.uint8, device=dev)
     dt = 1 if x.dtype == torch.bfloat16 else 0
     L = layer.c_struct()
     st = load().nest_linear(ctypes.byref(L), int(verify), _ptr(x), dt, T, _ptr(y), _ptr(scratch), _stream(stream))

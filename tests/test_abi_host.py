@@ -56,8 +56,8 @@ def test_sizes_reject_bad_shapes(lib):
     assert nest.xop_bytes(128, 65) == 0
     assert nest.xop_bytes(256, 1) == 2 * 256 * 16
     assert nest.xop_bytes(256, 17) == 2 * 256 * 32
-    assert nest.workspace_bytes(128, 128, 0) == 0
-    assert nest.linear_scratch_bytes(4096, 4096, 16) > nest.workspace_bytes(4096, 4096, 16)
+    assert nest.linear_scratch_bytes(128, 128, 0) == 0
+    assert nest.linear_scratch_bytes(4096, 4096, 16) == nest.xop_bytes(4096, 16) + 16 * 4096 * 4
 
 
 def _layer(M=256, K=512, bits=8, base=0x10000, resid=0x20000):
@@ -68,19 +68,19 @@ def test_gemm_argument_validation(lib):
     L = _layer()
     ok = ctypes.c_void_p(0x50000)
     f = lib.nest_verify_gemm
-    assert f(None, ok, ok, 16, ok, None) == 1                              # null layer
-    assert f(ctypes.byref(L), None, ok, 16, ok, None) == 1                 # null operand
-    assert f(ctypes.byref(L), ok, ok, 0, ok, None) == 1                    # T < 1
-    assert f(ctypes.byref(L), ok, ok, 65, ok, None) == 2                   # T > 64
-    assert f(ctypes.byref(_layer(K=200)), ok, ok, 4, ok, None) == 2         # K % 128
-    assert f(ctypes.byref(_layer(bits=5)), ok, ok, 4, ok, None) == 2        # bit width
-    assert f(ctypes.byref(_layer(bits=0)), ok, ok, 4, ok, None) == 1        # verify needs a residual
-    assert f(ctypes.byref(_layer(base=0x10001)), ok, ok, 4, ok, None) == 3  # misaligned base
-    assert f(ctypes.byref(L), ctypes.c_void_p(0x50008), ok, 4, ok, None) == 3
-    assert f(ctypes.byref(_layer(M=0)), ok, ok, 4, ok, None) == 1
+    assert f(None, ok, ok, 16, None) == 1                              # null layer
+    assert f(ctypes.byref(L), None, ok, 16, None) == 1                 # null operand
+    assert f(ctypes.byref(L), ok, ok, 0, None) == 1                    # T < 1
+    assert f(ctypes.byref(L), ok, ok, 65, None) == 2                   # T > 64
+    assert f(ctypes.byref(_layer(K=200)), ok, ok, 4, None) == 2         # K % 128
+    assert f(ctypes.byref(_layer(bits=5)), ok, ok, 4, None) == 2        # bit width
+    assert f(ctypes.byref(_layer(bits=0)), ok, ok, 4, None) == 1        # verify needs a residual
+    assert f(ctypes.byref(_layer(base=0x10001)), ok, ok, 4, None) == 3  # misaligned base
+    assert f(ctypes.byref(L), ctypes.c_void_p(0x50008), ok, 4, None) == 3
+    assert f(ctypes.byref(_layer(M=0)), ok, ok, 4, None) == 1
     d = lib.nest_draft_gemv
-    assert d(ctypes.byref(_layer(bits=0, resid=0)), ok, ok, 70, ok, None) == 2
-    assert d(ctypes.byref(_layer(bits=0, resid=0)), ok, None, 4, ok, None) == 1
+    assert d(ctypes.byref(_layer(bits=0, resid=0)), ok, ok, 70, None) == 2
+    assert d(ctypes.byref(_layer(bits=0, resid=0)), ok, None, 4, None) == 1
 
 
 def test_rotate_pack_quantize_validation(lib):

@@ -165,24 +165,44 @@ def test_linear_parity(dev, bits):
             parity(y, O.forward(q, s_o, s_i, xv, verify)["y"])
 
 
-def test_draft_is_bitexact_subset_of_verify(dev):
+def _close(a, b, rel=1e-6):
+    """Equal up to the order of the fp32 additions of the split K range."""
+    scale = np.sqrt(np.mean(np.asarray(b, np.float64) ** 2))
+    assert np.max(np.abs(np.asarray(a, np.float64) - b)) <= rel * 64 * scale
+
+
+def test_draft_is_subset_of_verify(dev):
+    # with a zero residual the verify kernel decodes the same fp16 weights as the draft
     M, K, bits = 512, 1024, 7
     W, s_o, s_i, q = ref_layer(M, K, bits)
     q0 = dict(q)
     q0["resid_codes"] = np.zeros_like(q["resid_codes"])
     lv = dev_layer(q0, bits, s_o, s_i, dev)
     x, _ = bf16_x(16, K, 7, dev)
-    assert np.array_equal(run_gemm(lv, x, True, dev), run_gemm(lv, x, False, dev))
+    _close(run_gemm(lv, x, True, dev), run_gemm(lv, x, False, dev))
 
 
-def test_deterministic_and_token_independent(dev):
+def test_gemm_accumulates_into_z(dev):
+    M, K, bits = 256, 512, 8
+    W, s_o, s_i, q = ref_layer(M, K, bits)
+    layer = dev_layer(q, bits, s_o, s_i, dev)
+    x, xv = bf16_x(4, K, 9, dev)
+    xop = nest.new_xop(K, 4, dev)
+    nest.rotate(x, layer.sign_in, 0, x_op=xop)
+    z0 = torch.full((4, M), 0.5, dtype=torch.float32, device=dev)
+    z = nest.gemm(layer, xop, 4, True, z=z0.clone())
+    ref = O.forward(q, s_o, s_i, xv, True)["z"]
+    parity(z.cpu().numpy() - 0.5, ref)
+
+
+def test_repeatable_and_token_independent(dev):
     M, K, bits = 1024, 2560, 7
     W, s_o, s_i, q = ref_layer(M, K, bits)
     layer = dev_layer(q, bits, s_o, s_i, dev)
     x, xv = bf16_x(16, K, 8, dev)
     a = run_gemm(layer, x, True, dev)
     b = run_gemm(layer, x, True, dev)
-    assert np.array_equal(a, b)
+    _close(a, b)
     for t in (0, 5, 15):
         one = run_gemm(layer, x[t:t + 1].contiguous(), True, dev)
         parity(one[0], a[t])
