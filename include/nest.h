@@ -171,6 +171,18 @@ nest_status nest_draft_gemv(const nest_layer* layer, const uint16_t* x_op, float
  * Needs layer->resid_bits in {6, 7, 8}.  Arguments as nest_draft_gemv. */
 nest_status nest_verify_gemm(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* stream);
 
+/* Grouped GEMMs: `count` (1..4) independent linears in ONE launch, e.g. the q/k/v
+ * projections or the gate/up projections of a decoder layer, which read the same input.
+ * Their (row tile, group) units are concatenated and split evenly over the CTAs, so the
+ * launch's start-up and tail are paid once.  layers: host array of `count` descriptors
+ * (for verify, all with the same resid_bits); x_ops, z: host arrays of `count` device
+ * pointers; each z[k] is fp32 [T][layers[k].M] and is accumulated into, as in
+ * nest_draft_gemv / nest_verify_gemm.  T is shared. */
+nest_status nest_draft_gemv_group(const nest_layer* layers, int32_t count, const uint16_t* const* x_ops,
+                                  float* const* z, int32_t T, void* stream);
+nest_status nest_verify_gemm_group(const nest_layer* layers, int32_t count, const uint16_t* const* x_ops,
+                                   float* const* z, int32_t T, void* stream);
+
 /* Whole linear: y = S_o H_o (Q x'), x' = H_i S_i x (rotate in, GEMM, rotate out).
  * verify  0 = draft (base only), 1 = verify (base + residual).
  * x       [T][K] fp32 (x_dtype 0) or bf16 bits (x_dtype 1).
@@ -181,6 +193,14 @@ nest_status nest_verify_gemm(const nest_layer* layer, const uint16_t* x_op, floa
 size_t nest_linear_scratch_bytes(int32_t M, int32_t K, int32_t T);
 nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype,
                         int32_t T, float* y, void* scratch, void* stream);
+
+/* Whole linears for `count` (1..4) independent layers in three launches (one grouped
+ * rotation in, one grouped GEMM, one grouped rotation out).  layers: host array; xs, ys:
+ * host arrays of device pointers ([T][K_k] inputs, [T][M_k] fp32 outputs); scratch:
+ * nest_linear_group_scratch_bytes(layers, count, T) bytes of device memory. */
+size_t nest_linear_group_scratch_bytes(const nest_layer* layers, int32_t count, int32_t T);
+nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t verify, const void* const* xs,
+                              int32_t x_dtype, int32_t T, float* const* ys, void* scratch, void* stream);
 
 /* Reads and clears the device-side error flag that kernels set when a pipeline
  * wait runs past its limit.  Synchronises `stream`.  Returns NEST_ERR_TIMEOUT if

@@ -61,28 +61,44 @@ nest_status check_layer(const nest_layer* L, bool need_resid) {
     return NEST_OK;
 }
 
-nest_status run_gemm(const nest_layer* L, int bits, const uint16_t* xop, float* z, int T, void* stream) {
-    nest_status st = check_layer(L, bits != 0);
-    if (st != NEST_OK) return st;
-    if (xop == nullptr || z == nullptr) return NEST_ERR_INVALID_ARG;
+// One launch over `count` independent linears (same residual width, same T).
+nest_status run_gemm_group(const nest_layer* layers, int count, bool verify, const uint16_t* const* xops,
+                           float* const* zs, int T, void* stream) {
+    if (layers == nullptr || xops == nullptr || zs == nullptr) return NEST_ERR_INVALID_ARG;
+    if (count < 1) return NEST_ERR_INVALID_ARG;
+    if (count > kMaxGemmTasks) return NEST_ERR_UNSUPPORTED;
     if (T < 1) return NEST_ERR_INVALID_ARG;
     if (T > 64) return NEST_ERR_UNSUPPORTED;
-    if (!aligned16(xop) || (reinterpret_cast<uintptr_t>(z) & 3u)) return NEST_ERR_MISALIGNED;
+    const int bits = verify ? layers[0].resid_bits : 0;
+    if (verify && bits == 0) return NEST_ERR_INVALID_ARG;
+    GemmArgs a = {};
+    a.ntasks = count;
+    a.T = T;
+    long long units = 0;
+    for (int k = 0; k < count; ++k) {
+        const nest_layer* L = &layers[k];
+        nest_status st = check_layer(L, verify);
+        if (st != NEST_OK) return st;
+        if (verify && L->resid_bits != bits) return NEST_ERR_INVALID_ARG;
+        if (xops[k] == nullptr || zs[k] == nullptr) return NEST_ERR_INVALID_ARG;
+        if (!aligned16(xops[k]) || (reinterpret_cast<uintptr_t>(zs[k]) & 3u)) return NEST_ERR_MISALIGNED;
+        GemmTask& t = a.task[k];
+        t.base = L->base;
+        t.resid = verify ? L->resid : nullptr;
+        t.xop = xops[k];
+        t.z = zs[k];
+        t.M = L->M;
+        t.G = L->K / 128;
+        t.tiles = n_tiles(L->M);
+        t.ubegin = units;
+        units += (long long)t.tiles * t.G;
+    }
+    a.units = units;
     if (!device_supported()) return NEST_ERR_UNSUPPORTED;
     const int sms = device_sms();
     if (sms <= 0) return NEST_ERR_CUDA;
-    GemmArgs a;
-    a.base = L->base;
-    a.resid = bits ? L->resid : nullptr;
-    a.xop = xop;
-    a.z = z;
-    a.M = L->M;
-    a.K = L->K;
-    a.T = T;
-    a.G = L->K / 128;
-    a.units = (long long)n_tiles(L->M) * a.G;
     const long long slots = (long long)kGemmCtasPerSm * sms;   // every CTA resident at once
-    long long grid = a.units < slots ? a.units : slots;
+    long long grid = units < slots ? units : slots;
     if (grid > kMaxGrid) grid = kMaxGrid;
     return from_cuda(launch_gemm(a, bits, (int)grid, as_stream(stream)));
 }
@@ -182,15 +198,24 @@ nest_status nest_rotate(const void* x, int32_t x_dtype, const int8_t* signs, int
 }
 
 nest_status nest_draft_gemv(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* stream) {
-    return run_gemm(layer, 0, x_op, z, T, stream);
+    return run_gemm_group(layer, 1, false, &x_op, &z, T, stream);
 }
 
 nest_status nest_verify_gemm(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* stream) {
-    if (layer != nullptr && layer->resid_bits == 0) return NEST_ERR_INVALID_ARG;
-    return run_gemm(layer, layer ? layer->resid_bits : 0, x_op, z, T, stream);
+    return run_gemm_group(layer, 1, true, &x_op, &z, T, stream);
 }
 
-// scratch of nest_linear: [x_op][z], each 256-byte aligned
+nest_status nest_draft_gemv_group(const nest_layer* layers, int32_t count, const uint16_t* const* x_ops,
+                                  float* const* z, int32_t T, void* stream) {
+    return run_gemm_group(layers, count, false, x_ops, z, T, stream);
+}
+
+nest_status nest_verify_gemm_group(const nest_layer* layers, int32_t count, const uint16_t* const* x_ops,
+                                   float* const* z, int32_t T, void* stream) {
+    return run_gemm_group(layers, count, true, x_ops, z, T, stream);
+}
+
+// scratch of nest_linear: [x_op][z], each 256-byte aligned; of nest_linear_group: one such pair per linear
 static size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t nest_linear_scratch_bytes(int32_t M, int32_t K, int32_t T) {
@@ -198,28 +223,58 @@ size_t nest_linear_scratch_bytes(int32_t M, int32_t K, int32_t T) {
     return round256(nest_xop_bytes(K, T)) + round256((size_t)T * M * sizeof(float));
 }
 
-nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype, int32_t T, float* y,
-                        void* scratch, void* stream) {
-    nest_status st = check_layer(layer, verify != 0);
-    if (st != NEST_OK) return st;
-    if (!x || !y || !scratch || !layer->sign_in || !layer->sign_out) return NEST_ERR_INVALID_ARG;
+size_t nest_linear_group_scratch_bytes(const nest_layer* layers, int32_t count, int32_t T) {
+    if (layers == nullptr || count < 1 || count > kMaxGemmTasks) return 0;
+    size_t total = 0;
+    for (int k = 0; k < count; ++k) {
+        const size_t b = nest_linear_scratch_bytes(layers[k].M, layers[k].K, T);
+        if (b == 0) return 0;
+        total += b;
+    }
+    return total;
+}
+
+nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t verify, const void* const* xs,
+                              int32_t x_dtype, int32_t T, float* const* ys, void* scratch, void* stream) {
+    if (layers == nullptr || xs == nullptr || ys == nullptr || scratch == nullptr) return NEST_ERR_INVALID_ARG;
+    if (count < 1) return NEST_ERR_INVALID_ARG;
+    if (count > kMaxGemmTasks) return NEST_ERR_UNSUPPORTED;
+    if (x_dtype != 0 && x_dtype != 1) return NEST_ERR_INVALID_ARG;
     if (T < 1) return NEST_ERR_INVALID_ARG;
     if (T > 64) return NEST_ERR_UNSUPPORTED;
     if (!aligned16(scratch)) return NEST_ERR_MISALIGNED;
-    const int M = layer->M, K = layer->K;
+    RotArgs rin = {}, rout = {};
+    const uint16_t* xops[kMaxGemmTasks];
+    float* zs[kMaxGemmTasks];
     uint8_t* s = reinterpret_cast<uint8_t*>(scratch);
-    uint16_t* xop = reinterpret_cast<uint16_t*>(s);
-    float* z = reinterpret_cast<float*>(s + round256(nest_xop_bytes(K, T)));
-    if ((x_dtype != 0 && x_dtype != 1) || (reinterpret_cast<uintptr_t>(x) & (x_dtype == 1 ? 1u : 3u)))
-        return x_dtype != 0 && x_dtype != 1 ? NEST_ERR_INVALID_ARG : NEST_ERR_MISALIGNED;
-    if ((reinterpret_cast<uintptr_t>(y) & 3u)) return NEST_ERR_MISALIGNED;
-    // rotate in, writing the GEMM operand and clearing the accumulator z
-    cudaError_t e = launch_rotate(x, x_dtype, layer->sign_in, K, T, 0, nullptr, xop, z, (long long)T * M,
-                                  as_stream(stream));
-    if (e != cudaSuccess) return NEST_ERR_CUDA;
-    st = verify ? nest_verify_gemm(layer, xop, z, T, stream) : nest_draft_gemv(layer, xop, z, T, stream);
+    for (int k = 0; k < count; ++k) {
+        const nest_layer* L = &layers[k];
+        nest_status st = check_layer(L, verify != 0);
+        if (st != NEST_OK) return st;
+        if (!L->sign_in || !L->sign_out || !xs[k] || !ys[k]) return NEST_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(xs[k]) & (x_dtype == 1 ? 1u : 3u)) || (reinterpret_cast<uintptr_t>(ys[k]) & 3u))
+            return NEST_ERR_MISALIGNED;
+        uint16_t* xop = reinterpret_cast<uint16_t*>(s);
+        float* z = reinterpret_cast<float*>(s + round256(nest_xop_bytes(L->K, T)));
+        s += nest_linear_scratch_bytes(L->M, L->K, T);
+        xops[k] = xop;
+        zs[k] = z;
+        // rotate in, writing the GEMM operand and clearing the accumulator z
+        rin.task[k] = RotTask{xs[k], L->sign_in, nullptr, xop, z, (long long)T * L->M, (unsigned)L->K};
+        // rotate out
+        rout.task[k] = RotTask{z, L->sign_out, ys[k], nullptr, nullptr, 0, (unsigned)L->M};
+    }
+    rin.ntasks = rout.ntasks = count;
+    if (launch_rotate_group(rin, x_dtype, 0, T, as_stream(stream)) != cudaSuccess) return NEST_ERR_CUDA;
+    nest_status st = run_gemm_group(layers, count, verify != 0, xops, zs, T, stream);
     if (st != NEST_OK) return st;
-    return nest_rotate(z, 0, layer->sign_out, M, T, 1, y, nullptr, stream);
+    if (launch_rotate_group(rout, 0, 1, T, as_stream(stream)) != cudaSuccess) return NEST_ERR_CUDA;
+    return NEST_OK;
+}
+
+nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype, int32_t T, float* y,
+                        void* scratch, void* stream) {
+    return nest_linear_group(layer, 1, verify, &x, x_dtype, T, &y, scratch, stream);
 }
 
 nest_status nest_error_check(void* stream) {

@@ -191,9 +191,29 @@ __device__ __forceinline__ long long unit_begin(int c, long long units, int grid
     return (long long)c * units / grid;
 }
 
+// Position in the concatenated unit range of a grouped launch: task k, row tile, group g.
+struct UnitCursor {
+    int k, tile, g;
+    __device__ __forceinline__ void init(const GemmArgs& p, long long u) {
+        k = 0;
+        while (k + 1 < p.ntasks && p.task[k + 1].ubegin <= u) ++k;
+        const long long l = u - p.task[k].ubegin;
+        tile = (int)(l / p.task[k].G);
+        g = (int)(l - (long long)tile * p.task[k].G);
+    }
+    __device__ __forceinline__ void next(const GemmArgs& p) {
+        if (++g == p.task[k].G) {
+            g = 0;
+            if (++tile == p.task[k].tiles) { tile = 0; ++k; }
+        }
+    }
+    __device__ __forceinline__ long long local(const GemmArgs& p) const { return (long long)tile * p.task[k].G + g; }
+    __device__ __forceinline__ bool group_end(const GemmArgs& p) const { return g == p.task[k].G - 1; }
+};
+
 template <int BITS, int NP>
 __global__ void __launch_bounds__(Cfg<BITS, NP>::kThreads, Cfg<BITS, NP>::kCtasPerSm)
-k_nest_gemm(const GemmArgs p) {
+k_nest_gemm(const __grid_constant__ GemmArgs p) {
     using C = Cfg<BITS, NP>;
     constexpr int S = C::kStages, NA = C::kNumA;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -236,33 +256,39 @@ k_nest_gemm(const GemmArgs p) {
     const uint32_t tmem = *tmem_slot;
     grid_dep_launch_dependents();
 
-    // this CTA's contiguous range of (tile, group) units
+    // this CTA's contiguous range of units (tasks, row tiles, groups concatenated)
     const long long units = p.units;
-    const int grid = gridDim.x, cta = blockIdx.x, G = p.G;
-    const long long u0 = unit_begin(cta, units, grid);
-    const int n = (int)(unit_begin(cta + 1, units, grid) - u0);
-    const int tile0 = (int)(u0 / G), g0 = (int)(u0 - (long long)tile0 * G);
+    const int grid = gridDim.x;
+    const long long u0 = unit_begin(blockIdx.x, units, grid);
+    const int n = (int)(unit_begin(blockIdx.x + 1, units, grid) - u0);
+    UnitCursor start;
+    start.init(p, u0);
 
     if (warp == C::kProducerWarp) {
-        const uint8_t* bsrc = p.base + u0 * kBaseUnit;
-        const uint8_t* rsrc = p.resid + u0 * C::kResUnit;
+        UnitCursor cw = start;               // next unit whose weights are fetched
         auto issue_w = [&](int i) {
             const int s = i % S;
+            const GemmTask& t = p.task[cw.k];
+            const long long lu = cw.local(p);
             mbar_arrive_expect_tx(full_w(s), C::kWStage);
-            bulk_g2s(smem_u32(st_base(s)), bsrc + (size_t)i * kBaseUnit, kBaseUnit, full_w(s));
+            bulk_g2s(smem_u32(st_base(s)), t.base + lu * kBaseUnit, kBaseUnit, full_w(s));
             if constexpr (BITS != 0)
-                bulk_g2s(smem_u32(st_res(s)), rsrc + (size_t)i * C::kResUnit, C::kResUnit, full_w(s));
+                bulk_g2s(smem_u32(st_res(s)), t.resid + lu * C::kResUnit, C::kResUnit, full_w(s));
+            cw.next(p);
         };
         // weights do not depend on the previous kernel: fill the weight ring now
         const int pre = n < S ? n : S;
-        if (lane == 0)
-            for (int i = 0; i < pre; ++i) issue_w(i);
+        for (int i = 0; i < pre; ++i) {
+            if (lane == 0) issue_w(i);
+            else cw.next(p);
+        }
         __syncwarp();
         grid_dep_wait();                     // the activation operand comes from the previous kernel
         // Two independent rings: activation block of unit ix goes to slot ix % NA once unit
         // ix - NA's MMAs are done; weights of unit iw go to stage iw % S once unit iw - S has
         // been decoded.  Poll both so neither waits behind the other.
-        int iw = pre, ix = 0, g = g0;
+        int iw = pre, ix = 0;
+        UnitCursor cx = start;               // next unit whose activation block is fetched
         uint64_t t_last = globaltimer();
         while (ix < n || iw < n) {
             bool moved = false;
@@ -273,9 +299,10 @@ k_nest_gemm(const GemmArgs p) {
                     if (lane == 0) {
                         const int a = ix % NA;
                         mbar_arrive_expect_tx(full_x(a), C::kXBytes);
-                        bulk_g2s(smem_u32(st_x(a)), p.xop + (size_t)g * (C::kXBytes / 2), C::kXBytes, full_x(a));
+                        bulk_g2s(smem_u32(st_x(a)), p.task[cx.k].xop + (size_t)cx.g * (C::kXBytes / 2), C::kXBytes,
+                                 full_x(a));
                     }
-                    if (++g == G) g = 0;
+                    cx.next(p);
                     ++ix;
                     moved = true;
                 }
@@ -285,6 +312,7 @@ k_nest_gemm(const GemmArgs p) {
                 if (lane == 0) ready = mbar_test_wait(empty_w(iw % S), ((iw / S) - 1) & 1);
                 if (__shfl_sync(0xffffffffu, ready, 0)) {
                     if (lane == 0) issue_w(iw);
+                    else cw.next(p);
                     ++iw;
                     moved = true;
                 }
@@ -308,11 +336,12 @@ k_nest_gemm(const GemmArgs p) {
         constexpr uint32_t idesc = idesc_f16_f32(128, NP);
         // B descriptor of activation slot 0, k-step 0; slot a adds a * kXBytes, k-step kk adds kk * NP * 32 bytes
         const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(xring), (NP / 8) * 128, 128);
-        int seg = -1, g = g0;
+        int seg = -1;
+        UnitCursor cu = start;
         bool issued_any = false;
         for (int i = 0; i < n; ++i) {
-            const bool first = (i == 0) || g == 0;
-            const bool last = (i == n - 1) || g == G - 1;
+            const bool first = (i == 0) || cu.g == 0;
+            const bool last = (i == n - 1) || cu.group_end(p);
             if (first) {
                 ++seg;
                 if (seg >= 2 && !warp_wait(d_empty(seg & 1), ((seg >> 1) - 1) & 1, abort_flag)) break;
@@ -332,7 +361,7 @@ k_nest_gemm(const GemmArgs p) {
             }
             __syncwarp();
             issued_any = true;
-            if (++g == G) g = 0;
+            cu.next(p);
         }
         if (issued_any) {              // all MMAs finished before tensor memory is released
             if (lane == 0) tc_commit(drain_bar);
@@ -345,11 +374,12 @@ k_nest_gemm(const GemmArgs p) {
         const int r = 32 * (warp & 3) + lane;               // row of the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const __half2 off2 = __float2half2_rn(1024.0f + (BITS ? (float)(1 << (BITS - 1)) : 0.0f));
-        int seg = -1, g = g0, tile = tile0;
+        int seg = -1;
+        UnitCursor cu = start;
         bool dep_done = false;
         for (int i = 0; i < n; ++i) {
-            const bool first = (i == 0) || g == 0;
-            const bool last = (i == n - 1) || g == G - 1;
+            const bool first = (i == 0) || cu.g == 0;
+            const bool last = (i == n - 1) || cu.group_end(p);
             if (first) ++seg;
             if (i % C::kDeqWG == wg) {
                 const int s = i % S, a = i % NA;
@@ -388,17 +418,18 @@ k_nest_gemm(const GemmArgs p) {
                 tmem_ld_cols<NP>(tmem + lane_base + d * NP, v);
                 tc_fence_before();
                 mbar_arrive(d_empty(d));
-                const int m = tile * kRows + r;
-                const int T = p.T, M = p.M;
+                const GemmTask& task = p.task[cu.k];
+                const int m = cu.tile * kRows + r;
+                const int T = p.T, M = task.M;
                 if (!dep_done) { grid_dep_wait(); dep_done = true; }
                 if (m < M) {
-                    float* zp = p.z + m;
+                    float* zp = task.z + m;
 #pragma unroll
                     for (int t = 0; t < NP; ++t)
                         if (t < T) atomicAdd(zp + (size_t)t * M, v[t]);    // fire-and-forget reduction
                 }
             }
-            if (++g == G) { g = 0; ++tile; }
+            cu.next(p);
         }
     }
 

@@ -8,14 +8,41 @@
 
 namespace nest {
 
-// Arguments of one draft/verify GEMM launch.
-struct GemmArgs {
+constexpr int kMaxTasks = 4;           // linears in one grouped launch
+
+// One linear of a grouped draft/verify GEMM launch.
+struct GemmTask {
     const uint8_t* base;      // packed base units
     const uint8_t* resid;     // packed residual units (verify only)
     const uint16_t* xop;      // activation operand
     float* z;                 // [T][M] output, accumulated into
-    int M, K, T, G;           // G = K / 128
-    long long units;          // row tiles * G
+    int M, G, tiles;          // G = K / 128, tiles = ceil(M / 128)
+    long long ubegin;         // index of the task's first unit in the launch's unit range
+};
+
+// Arguments of one grouped launch: the tasks' (tile, group) units are concatenated.
+struct GemmArgs {
+    GemmTask task[kMaxTasks];
+    int ntasks, T;
+    long long units;          // total units of all tasks
+};
+
+// One set of vectors of a grouped rotation launch (see launch_rotate).
+struct RotTask {
+    const void* x;
+    const int8_t* signs;
+    float* y;
+    uint16_t* xop;
+    float* zero_out;
+    long long zero_count;
+    unsigned n, total;        // vector length, T * n
+    int L, NB, cta_begin;     // log2 block size, operand token blocks, first CTA of the task
+    float scale;
+};
+
+struct RotArgs {
+    RotTask task[kMaxTasks];
+    int ntasks;
 };
 
 constexpr int kMaxGrid = 1024;
@@ -44,12 +71,16 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int bits, int grid, cudaStream_t stream);
+constexpr int kMaxGemmTasks = kMaxTasks;
 cudaError_t read_and_clear_error(int* flag, cudaStream_t stream);
 
 // zero_out (optional): a buffer of zero_count floats the kernel also clears (the
 // accumulator of the GEMM that follows it).
 cudaError_t launch_rotate(const void* x, int x_dtype, const int8_t* signs, int n, int T, int mode,
                           float* y, uint16_t* xop, float* zero_out, long long zero_count, cudaStream_t stream);
+// Rotation of several vector sets in one launch (same mode and input type); fills the
+// tasks' L, NB, scale, total and cta_begin.
+cudaError_t launch_rotate_group(RotArgs& a, int x_dtype, int mode, int T, cudaStream_t stream);
 
 cudaError_t launch_pack(const uint8_t* bc, const uint16_t* bs, const int8_t* rc, const uint16_t* rs,
                         int M, int K, int bits, uint8_t* base_out, uint8_t* resid_out, cudaStream_t stream);

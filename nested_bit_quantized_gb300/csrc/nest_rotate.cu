@@ -40,30 +40,49 @@ __device__ __forceinline__ void warp_fwht(float& v0, float& v1, int nbits, int l
 
 template <int MODE, bool BF16>
 __global__ void __launch_bounds__(kThreads)
-k_rotate(const void* __restrict__ x, const int8_t* __restrict__ signs, unsigned n, unsigned total, int L,
-         float scale, float* __restrict__ y, uint16_t* __restrict__ xop, int NB, float* __restrict__ zero_out,
-         long long zero_count) {
+k_rotate(const __grid_constant__ RotArgs args) {
     __shared__ float buf[64][65];
     grid_dep_launch_dependents();
+    int k = 0;                            // the vector set this CTA works on
+    while (k + 1 < args.ntasks && args.task[k + 1].cta_begin <= (int)blockIdx.x) ++k;
+    const RotTask& tk = args.task[k];
+    const void* __restrict__ x = tk.x;
+    const int8_t* __restrict__ signs = tk.signs;
+    const unsigned n = tk.n, total = tk.total;
+    const int L = tk.L, NB = tk.NB;
+    const float scale = tk.scale;
+    float* __restrict__ y = tk.y;
+    uint16_t* __restrict__ xop = tk.xop;
+    const unsigned cta = blockIdx.x - tk.cta_begin;
+    const unsigned nctas = (total + kSeg - 1) / kSeg;
     grid_dep_wait();                      // x may be the previous kernel's output; y may be its input
-    if (zero_out != nullptr) {            // clear the accumulator of the GEMM that follows
-        const long long per = (zero_count + gridDim.x - 1) / gridDim.x;
-        const long long lo = per * blockIdx.x, hi = lo + per < zero_count ? lo + per : zero_count;
-        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) zero_out[i] = 0.0f;
+    if (tk.zero_out != nullptr) {         // clear the accumulator of the GEMM that follows
+        const long long per = (tk.zero_count + nctas - 1) / nctas;
+        const long long lo = per * cta, hi = lo + per < tk.zero_count ? lo + per : tk.zero_count;
+        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) tk.zero_out[i] = 0.0f;
     }
-    const unsigned seg0 = blockIdx.x * (unsigned)kSeg;
+    const unsigned seg0 = cta * (unsigned)kSeg;
     const unsigned rem = total - seg0;
     const int count = rem < (unsigned)kSeg ? (int)rem : kSeg;
 
-    for (int f = threadIdx.x; f < kSeg; f += kThreads) {
-        float v = 0.0f;
+    // all loads of this thread in flight together, then into shared memory
+    constexpr int kPer = kSeg / kThreads;
+    float v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int f = threadIdx.x + j * kThreads;
+        v[j] = 0.0f;
         if (f < count) {
             const unsigned idx = seg0 + f;
-            if constexpr (BF16) v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(x)[idx]);
-            else v = reinterpret_cast<const float*>(x)[idx];
-            if constexpr (MODE == 0) v *= (float)signs[idx % n];
+            if constexpr (BF16) v[j] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(x)[idx]);
+            else v[j] = reinterpret_cast<const float*>(x)[idx];
+            if constexpr (MODE == 0) v[j] *= (float)signs[idx % n];
         }
-        buf[f >> 6][f & 63] = v;
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int f = threadIdx.x + j * kThreads;
+        buf[f >> 6][f & 63] = v[j];
     }
     __syncthreads();
 
@@ -89,11 +108,16 @@ k_rotate(const void* __restrict__ x, const int8_t* __restrict__ signs, unsigned 
     }
 
     if (y != nullptr) {
-        for (int f = threadIdx.x; f < count; f += kThreads) {
-            const unsigned idx = seg0 + f;
-            float v = buf[f >> 6][f & 63] * scale;
-            if constexpr (MODE == 1) v *= (float)signs[idx % n];
-            y[idx] = v;
+        float sg[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int f = threadIdx.x + j * kThreads;
+            sg[j] = (MODE == 1 && f < count) ? (float)signs[(seg0 + f) % n] : 1.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int f = threadIdx.x + j * kThreads;
+            if (f < count) y[seg0 + f] = buf[f >> 6][f & 63] * scale * sg[j];
         }
     }
     if (MODE == 0 && xop != nullptr) {
@@ -125,28 +149,40 @@ int hadamard_block(int n) {
     return b;
 }
 
+cudaError_t launch_rotate_group(RotArgs& a, int x_dtype, int mode, int T, cudaStream_t stream) {
+    int ctas = 0;
+    for (int k = 0; k < a.ntasks; ++k) {
+        RotTask& t = a.task[k];
+        const int b = hadamard_block((int)t.n);
+        int L = 0;
+        while ((1 << L) < b) ++L;
+        t.L = L;
+        t.scale = (float)(1.0 / sqrt((double)b));
+        t.total = (unsigned)T * t.n;                     // the entry points keep T * n < 2^31
+        t.NB = n_pad(T) / 8;
+        t.cta_begin = ctas;
+        ctas += (int)((t.total + kSeg - 1) / kSeg);
+    }
+    const dim3 g(ctas), blk(kThreads);
+    if (mode == 0)
+        return x_dtype == 1 ? launch_pdl(k_rotate<0, true>, g, blk, 0, stream, a)
+                            : launch_pdl(k_rotate<0, false>, g, blk, 0, stream, a);
+    return x_dtype == 1 ? launch_pdl(k_rotate<1, true>, g, blk, 0, stream, a)
+                        : launch_pdl(k_rotate<1, false>, g, blk, 0, stream, a);
+}
+
 cudaError_t launch_rotate(const void* x, int x_dtype, const int8_t* signs, int n, int T, int mode,
                           float* y, uint16_t* xop, float* zero_out, long long zero_count, cudaStream_t stream) {
-    const int b = hadamard_block(n);
-    int L = 0;
-    while ((1 << L) < b) ++L;
-    const float scale = (float)(1.0 / sqrt((double)b));
-    const unsigned total = (unsigned)T * (unsigned)n;     // the entry point keeps T * n < 2^31
-    const int grid = (int)((total + kSeg - 1) / kSeg);
-    const int NB = n_pad(T) / 8;
-    const dim3 g(grid), blk(kThreads);
-    if (mode == 0) {
-        if (x_dtype == 1)
-            return launch_pdl(k_rotate<0, true>, g, blk, 0, stream, x, signs, (unsigned)n, total, L, scale, y, xop, NB,
-                              zero_out, zero_count);
-        return launch_pdl(k_rotate<0, false>, g, blk, 0, stream, x, signs, (unsigned)n, total, L, scale, y, xop, NB,
-                          zero_out, zero_count);
-    }
-    if (x_dtype == 1)
-        return launch_pdl(k_rotate<1, true>, g, blk, 0, stream, x, signs, (unsigned)n, total, L, scale, y,
-                          (uint16_t*)nullptr, NB, zero_out, zero_count);
-    return launch_pdl(k_rotate<1, false>, g, blk, 0, stream, x, signs, (unsigned)n, total, L, scale, y,
-                      (uint16_t*)nullptr, NB, zero_out, zero_count);
+    RotArgs a = {};
+    a.ntasks = 1;
+    a.task[0].x = x;
+    a.task[0].signs = signs;
+    a.task[0].y = y;
+    a.task[0].xop = mode == 0 ? xop : nullptr;
+    a.task[0].zero_out = zero_out;
+    a.task[0].zero_count = zero_count;
+    a.task[0].n = (unsigned)n;
+    return launch_rotate_group(a, x_dtype, mode, T, stream);
 }
 
 }  // namespace nest

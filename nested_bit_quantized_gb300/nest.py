@@ -62,6 +62,11 @@ def load() -> ctypes.CDLL:
         "nest_draft_gemv": ([ctypes.POINTER(_Layer), _P, _P, _I32, _P], _I32),
         "nest_verify_gemm": ([ctypes.POINTER(_Layer), _P, _P, _I32, _P], _I32),
         "nest_linear": ([ctypes.POINTER(_Layer), _I32, _P, _I32, _I32, _P, _P, _P], _I32),
+        "nest_draft_gemv_group": ([ctypes.POINTER(_Layer), _I32, ctypes.POINTER(_P), ctypes.POINTER(_P), _I32, _P], _I32),
+        "nest_verify_gemm_group": ([ctypes.POINTER(_Layer), _I32, ctypes.POINTER(_P), ctypes.POINTER(_P), _I32, _P], _I32),
+        "nest_linear_group_scratch_bytes": ([ctypes.POINTER(_Layer), _I32, _I32], _SZ),
+        "nest_linear_group": ([ctypes.POINTER(_Layer), _I32, _I32, ctypes.POINTER(_P), _I32, _I32,
+                               ctypes.POINTER(_P), _P, _P], _I32),
         "nest_error_check": ([_P], _I32),
     }
     for name, (args, res) in sig.items():
@@ -267,3 +272,50 @@ def linear(layer: Layer, x: torch.Tensor, verify: bool, y: Optional[torch.Tensor
 
 def error_check(stream=None) -> None:
     _check(load().nest_error_check(_stream(stream)), "nest_error_check")
+
+
+# ---------------------------------------------------------------------------
+# grouped launches (independent linears in one launch)
+# ---------------------------------------------------------------------------
+
+def _layers(layers):
+    arr = (_Layer * len(layers))()
+    for i, L in enumerate(layers):
+        arr[i] = L.c_struct()
+    return arr
+
+
+def _ptrs(ts):
+    return (_P * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def gemm_group(layers, x_ops, T: int, verify: bool, zs=None, stream=None):
+    """nest_verify_gemm_group / nest_draft_gemv_group: one launch over up to 4 linears.
+    Accumulates into zs (new zs are zero-filled)."""
+    dev = layers[0].base.device
+    if zs is None:
+        zs = [torch.zeros((T, L.M), dtype=torch.float32, device=dev) for L in layers]
+    arr = _layers(layers)
+    fn = load().nest_verify_gemm_group if verify else load().nest_draft_gemv_group
+    st = fn(arr, len(layers), _ptrs(x_ops), _ptrs(zs), T, _stream(stream))
+    _check(st, "nest_verify_gemm_group" if verify else "nest_draft_gemv_group")
+    return zs
+
+
+def linear_group_scratch_bytes(layers, T: int) -> int:
+    return int(load().nest_linear_group_scratch_bytes(_layers(layers), len(layers), T))
+
+
+def linear_group(layers, xs, verify: bool, ys=None, scratch: Optional[torch.Tensor] = None, stream=None):
+    """nest_linear_group: y_k = S_o H_o (Q_k (H_i S_i x_k)) for up to 4 linears in 3 launches."""
+    T = xs[0].shape[0]
+    dev = layers[0].base.device
+    if ys is None:
+        ys = [torch.empty((T, L.M), dtype=torch.float32, device=dev) for L in layers]
+    if scratch is None:
+        scratch = torch.empty(linear_group_scratch_bytes(layers, T), dtype=torch.uint8, device=dev)
+    dt = 1 if xs[0].dtype == torch.bfloat16 else 0
+    st = load().nest_linear_group(_layers(layers), len(layers), int(verify), _ptrs(xs), dt, T, _ptrs(ys),
+                                  _ptr(scratch), _stream(stream))
+    _check(st, "nest_linear_group")
+    return ys

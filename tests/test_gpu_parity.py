@@ -165,6 +165,27 @@ def test_linear_parity(dev, bits):
             parity(y, O.forward(q, s_o, s_i, xv, verify)["y"])
 
 
+@pytest.mark.parametrize("bits", [7, 8])
+def test_grouped_gemm_and_linear_parity(dev, bits):
+    shapes = [(384, 512), (200, 1024), (1280, 384)]          # ragged M, different K per linear
+    refs = [ref_layer(M, K, bits, seed=11 + i) for i, (M, K) in enumerate(shapes)]
+    layers = [dev_layer(q, bits, so, si, dev) for (W, so, si, q) in refs]
+    for T in (1, 16, 40):
+        xs = [bf16_x(T, K, 60 + i + T, dev) for i, (M, K) in enumerate(shapes)]
+        xops = []
+        for L, (x, _) in zip(layers, xs):
+            xop = nest.new_xop(L.K, T, dev)
+            nest.rotate(x, L.sign_in, 0, x_op=xop)
+            xops.append(xop)
+        for verify in (False, True):
+            zs = nest.gemm_group(layers, xops, T, verify)
+            for (W, so, si, q), (x, xv), z in zip(refs, xs, zs):
+                parity(z.cpu().numpy(), O.forward(q, so, si, xv, verify)["z"])
+            ys = nest.linear_group(layers, [x for x, _ in xs], verify)
+            for (W, so, si, q), (x, xv), y in zip(refs, xs, ys):
+                parity(y.cpu().numpy(), O.forward(q, so, si, xv, verify)["y"])
+
+
 def _close(a, b, rel=1e-6):
     """Equal up to the order of the fp32 additions of the split K range."""
     scale = np.sqrt(np.mean(np.asarray(b, np.float64) ** 2))
