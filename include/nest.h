@@ -202,6 +202,21 @@ size_t nest_linear_group_scratch_bytes(const nest_layer* layers, int32_t count, 
 nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t verify, const void* const* xs,
                               int32_t x_dtype, int32_t T, float* const* ys, void* scratch, void* stream);
 
+/* nest_linear without caller scratch, for callers that cannot allocate device memory
+ * (a process whose memory pool is fixed at start-up, a plain C caller without an
+ * allocator, a loop that cannot afford cudaMalloc's implicit synchronisation).  None of
+ * the source pages has a counterpart; this is a library convenience.  Arguments as
+ * nest_linear minus `scratch`: the operand and the accumulator live in one fixed 8 MiB
+ * array of the library's device memory, held by every GPU that loads the library until
+ * the process exits.  Shapes with nest_linear_scratch_bytes(M, K, T) > 8 MiB return
+ * NEST_ERR_UNSUPPORTED without launching.  The first call on a device looks up the
+ * array's address for that device (make that call before any stream capture).  Calls
+ * share the array: calls whose work overlaps on the GPU (other streams or threads) race
+ * and must be serialised by the caller; nothing needs clearing between calls.  Allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine). */
+nest_status nest_linear_static(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype,
+                               int32_t T, float* y, void* stream);
+
 /* Reads and clears the device-side error flag that kernels set when a pipeline
  * wait runs past its limit.  Synchronises `stream`.  Returns NEST_ERR_TIMEOUT if
  * the flag was set, NEST_ERR_CUDA on a CUDA error, NEST_OK otherwise. */
