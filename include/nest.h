@@ -202,6 +202,26 @@ size_t nest_linear_group_scratch_bytes(const nest_layer* layers, int32_t count, 
 nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t verify, const void* const* xs,
                               int32_t x_dtype, int32_t T, float* const* ys, void* scratch, void* stream);
 
+/* Glue between chained linears, fused with the rotations on both sides of it:
+ *   y = S_o H_o z_a  (or the elementwise product y_a * y_b of two linears' outputs, e.g. gate * up),
+ *   h = bf16(y / rms(y)) per token (unit-RMS rescale standing in for the normalisation
+ *       between linears, then the bf16 cast),
+ *   and for each of n_next (0..3) next linears j: x'_j = H_i S_i h written as its GEMM operand.
+ * The rotations are those of POC recipe steps 1 and 4 (feedman.me/posts/wZBTJ); the chaining
+ * and the RMS rescale are the chained-layer workload's reading, not the pages'.
+ * z_a, z_b      fp32 [T][M] GEMM accumulators (rotated basis); z_b / sign_out_b may be NULL.
+ * sign_out_a/b  S_o of those linears (int8 [M]).
+ * y             optional fp32 [T][M] out: the un-rotated output (the product when z_b is given).
+ * next          host array of n_next layer descriptors; each must have K == M (its sign_in is used).
+ * x_ops         host array of n_next operand buffers (out, nest_xop_bytes(M, T) bytes each).
+ * z_next        NULL, or host array of n_next accumulators (fp32 [T][next[j].M], or NULL entries)
+ *               that are cleared here for the GEMMs that follow.
+ * Limits: T <= 64, M % 128 == 0 when n_next > 0, M <= 29000 (one token's two vectors in
+ * shared memory). */
+nest_status nest_chain(const float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,
+                       int32_t M, int32_t T, float* y, const nest_layer* next, int32_t n_next,
+                       uint16_t* const* x_ops, float* const* z_next, void* stream);
+
 /* nest_linear without caller scratch, for callers that cannot allocate device memory
  * (a process whose memory pool is fixed at start-up, a plain C caller without an
  * allocator, a loop that cannot afford cudaMalloc's implicit synchronisation).  None of

@@ -1,0 +1,84 @@
+"""Chained decoder layer on the device: the order of library calls only.
+
+A layer of seven linears (q, k, v, o, gate, up, down) is run as grouped GEMMs
+joined by nest_chain, which fuses each output rotation, the unit-RMS rescale
+and bf16 cast standing in for the normalisation between linears, and the next
+linears' input rotations.  q, k, v read the layer input; o reads q's output;
+gate and up read o's output; down reads gate * up; the next layer reads down's
+output.  The k and v outputs are rotated back and kept (the KV-cache stand-in).
+Every step runs in libnest; this module only allocates buffers and sequences
+the calls.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Dict, List, Optional
+
+import torch
+
+from . import nest
+
+NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+class LayerBuffers:
+    """Operands, accumulators and outputs of one layer for a fixed T."""
+
+    def __init__(self, lin: Dict[str, nest.Layer], T: int, device):
+        self.T = T
+        self.xop = {n: nest.new_xop(lin[n].K, T, device) for n in NAMES}
+        self.z = {n: torch.zeros((T, lin[n].M), dtype=torch.float32, device=device) for n in NAMES}
+        self.y = {n: torch.empty((T, lin[n].M), dtype=torch.float32, device=device) for n in ("k", "v", "down")}
+
+
+def chain(z_a, s_a, z_b, s_b, T: int, y=None, nexts: Optional[List[nest.Layer]] = None, x_ops=None, z_next=None,
+          stream=None):
+    """nest_chain (see include/nest.h)."""
+    lib = nest.load()
+    if not hasattr(lib, "_chain_sig"):
+        lib.nest_chain.argtypes = [nest._P, nest._P, nest._P, nest._P, nest._I32, nest._I32, nest._P,
+                                   ctypes.POINTER(nest._Layer), nest._I32, ctypes.POINTER(nest._P),
+                                   ctypes.POINTER(nest._P), nest._P]
+        lib.nest_chain.restype = nest._I32
+        lib._chain_sig = True
+    nexts = nexts or []
+    M = z_a.shape[1]
+    arr = nest._layers(nexts) if nexts else None
+    xo = nest._ptrs(x_ops) if nexts else None
+    zn = nest._ptrs(z_next) if z_next else None
+    st = lib.nest_chain(nest._ptr(z_a), nest._ptr(s_a), nest._ptr(z_b), nest._ptr(s_b), M, T, nest._ptr(y),
+                        arr, len(nexts), xo, zn, nest._stream(stream))
+    nest._check(st, "nest_chain")
+
+
+def layer_input(lin: Dict[str, nest.Layer], x: torch.Tensor, buf: LayerBuffers, stream=None):
+    """Rotate the layer input into the q, k, v operands and clear their accumulators."""
+    for n in ("q", "k", "v"):
+        nest.rotate(x, lin[n].sign_in, 0, x_op=buf.xop[n], stream=stream)
+        buf.z[n].zero_()
+
+
+def layer_forward(lin: Dict[str, nest.Layer], buf: LayerBuffers, verify: bool,
+                  next_lin: Optional[Dict[str, nest.Layer]] = None, next_buf: Optional[LayerBuffers] = None,
+                  stream=None):
+    """One layer from prepared q/k/v operands.  Feeds next_lin's q/k/v operands, or writes
+    buf.y['down'] when this is the last layer."""
+    T = buf.T
+    g = lambda names: nest.gemm_group([lin[n] for n in names], [buf.xop[n] for n in names], T, verify,
+                                      zs=[buf.z[n] for n in names], stream=stream)
+    g(("q", "k", "v"))
+    chain(buf.z["q"], lin["q"].sign_out, None, None, T, None, [lin["o"]], [buf.xop["o"]], [buf.z["o"]], stream)
+    for n in ("k", "v"):
+        nest.rotate(buf.z[n], lin[n].sign_out, 1, y=buf.y[n], stream=stream)
+    g(("o",))
+    chain(buf.z["o"], lin["o"].sign_out, None, None, T, None, [lin["gate"], lin["up"]],
+          [buf.xop["gate"], buf.xop["up"]], [buf.z["gate"], buf.z["up"]], stream)
+    g(("gate", "up"))
+    chain(buf.z["gate"], lin["gate"].sign_out, buf.z["up"], lin["up"].sign_out, T, None, [lin["down"]],
+          [buf.xop["down"]], [buf.z["down"]], stream)
+    g(("down",))
+    if next_lin is None:
+        chain(buf.z["down"], lin["down"].sign_out, None, None, T, buf.y["down"], stream=stream)
+    else:
+        chain(buf.z["down"], lin["down"].sign_out, None, None, T, buf.y["down"], [next_lin[n] for n in ("q", "k", "v")],
+              [next_buf.xop[n] for n in ("q", "k", "v")], [next_buf.z[n] for n in ("q", "k", "v")], stream)

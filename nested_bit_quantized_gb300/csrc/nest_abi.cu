@@ -277,6 +277,40 @@ nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, 
     return nest_linear_group(layer, 1, verify, &x, x_dtype, T, &y, scratch, stream);
 }
 
+nest_status nest_chain(const float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,
+                       int32_t M, int32_t T, float* y, const nest_layer* next, int32_t n_next,
+                       uint16_t* const* x_ops, float* const* z_next, void* stream) {
+    if (z_a == nullptr || sign_out_a == nullptr) return NEST_ERR_INVALID_ARG;
+    if ((z_b == nullptr) != (sign_out_b == nullptr)) return NEST_ERR_INVALID_ARG;
+    if (M < 1 || T < 1 || n_next < 0) return NEST_ERR_INVALID_ARG;
+    if (T > 64 || n_next > kMaxChainNext) return NEST_ERR_UNSUPPORTED;
+    if (n_next == 0 && y == nullptr) return NEST_ERR_INVALID_ARG;
+    if (n_next > 0 && (next == nullptr || x_ops == nullptr)) return NEST_ERR_INVALID_ARG;
+    if (n_next > 0 && M % 128) return NEST_ERR_UNSUPPORTED;
+    if (chain_smem_bytes(M) > 227 * 1024) return NEST_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(z_a) & 3u) || (z_b && (reinterpret_cast<uintptr_t>(z_b) & 3u)) ||
+        (y && (reinterpret_cast<uintptr_t>(y) & 3u)))
+        return NEST_ERR_MISALIGNED;
+    ChainArgs c = {};
+    c.za = z_a;
+    c.sa = sign_out_a;
+    c.zb = z_b;
+    c.sb = sign_out_b;
+    c.y = y;
+    c.nnext = n_next;
+    c.M = M;
+    c.T = T;
+    for (int j = 0; j < n_next; ++j) {
+        const nest_layer& L = next[j];
+        if (L.K != M || L.sign_in == nullptr || x_ops[j] == nullptr) return NEST_ERR_INVALID_ARG;
+        if (!aligned16(x_ops[j])) return NEST_ERR_MISALIGNED;
+        float* zn = z_next ? z_next[j] : nullptr;
+        if (zn && (reinterpret_cast<uintptr_t>(zn) & 3u)) return NEST_ERR_MISALIGNED;
+        c.next[j] = ChainNext{L.sign_in, x_ops[j], zn, zn ? (long long)T * L.M : 0};
+    }
+    return from_cuda(launch_chain(c, as_stream(stream)));
+}
+
 nest_status nest_error_check(void* stream) {
     int flag = 0;
     cudaError_t e = read_and_clear_error(&flag, as_stream(stream));

@@ -165,6 +165,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 // ---------------------------------------------------------------------------
+// fast Walsh-Hadamard butterflies
+// ---------------------------------------------------------------------------
+
+// Butterflies over the low `nbits` bits of a 64-element warp vector:
+// element `lane` in v0, element `lane + 32` in v1 (unnormalised Sylvester order).
+__device__ __forceinline__ void warp_fwht(float& v0, float& v1, int nbits, int lane) {
+    const int lane_bits = nbits < 5 ? nbits : 5;
+    for (int s = 0; s < lane_bits; ++s) {
+        const int m = 1 << s;
+        const float o0 = __shfl_xor_sync(0xffffffffu, v0, m);
+        const float o1 = __shfl_xor_sync(0xffffffffu, v1, m);
+        const bool upper = (lane & m) != 0;
+        v0 = upper ? o0 - v0 : v0 + o0;
+        v1 = upper ? o1 - v1 : v1 + o1;
+    }
+    if (nbits >= 6) {
+        const float a = v0 + v1, b = v0 - v1;
+        v0 = a;
+        v1 = b;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // small integer / half helpers
 // ---------------------------------------------------------------------------
 

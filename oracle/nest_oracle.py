@@ -302,3 +302,43 @@ def bits_per_weight(base: bool, resid_bits: int | None) -> float:
     if resid_bits:
         bpw += resid_bits + 16 / GROUP
     return bpw
+
+
+# ----------------------------------------------------------------------------
+# chained decoder layer (the chained-layer workload's reading; not on the pages)
+# ----------------------------------------------------------------------------
+
+def round_bf16(a) -> np.ndarray:
+    """Round float64 values to bfloat16 (8 significant bits, round half to even)."""
+    a = np.asarray(a, dtype=np.float64)
+    m, e = np.frexp(a)                        # a = m * 2**e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
+
+
+def chain_glue(y_a: np.ndarray, y_b: np.ndarray | None = None) -> np.ndarray:
+    """Input of the next linear: h = y_a (or y_a * y_b, e.g. gate * up), rescaled to unit
+    RMS per token (row) as a stand-in for the normalisation between linears, then cast to
+    bf16.  Returns the bf16 values as float64 [T][M]."""
+    h = np.asarray(y_a, np.float64) if y_b is None else np.asarray(y_a, np.float64) * np.asarray(y_b, np.float64)
+    rms = np.sqrt(np.mean(h * h, axis=1, keepdims=True))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        h = np.where(rms > 0, h / rms, 0.0)
+    return round_bf16(h)
+
+
+def decoder_layer_forward(lin: Dict[str, tuple], x: np.ndarray, verify: bool) -> Dict[str, np.ndarray]:
+    """One chained decoder layer.  lin maps q, k, v, o, gate, up, down to
+    (quantized layer dict, S_o, S_i).  q, k, v read x; o reads q's output; gate and up
+    read o's output; down reads gate * up; every intermediate goes through chain_glue.
+    Returns each linear's y and the next layer's input."""
+    out = {}
+    fwd = lambda name, xin: forward(lin[name][0], lin[name][1], lin[name][2], xin, verify)["y"]
+    for n in ("q", "k", "v"):
+        out[n] = fwd(n, x)
+    out["o"] = fwd("o", chain_glue(out["q"]))
+    xg = chain_glue(out["o"])
+    out["gate"] = fwd("gate", xg)
+    out["up"] = fwd("up", xg)
+    out["down"] = fwd("down", chain_glue(out["gate"], out["up"]))
+    out["next"] = chain_glue(out["down"])
+    return out

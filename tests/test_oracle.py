@@ -394,3 +394,27 @@ def test_pack_hand_worked_examples():
     assert all(_word(pr, 0, 0, w) == 0 for w in range(17, 24))
     # bit 6 of u is 1 for every column (u = 64 and u = 127): words 24..27 all ones
     assert all(_word(pr, 0, 0, w) == 0xFFFFFFFF for w in range(24, 28))
+
+
+# ----------------------------------------------------------------------------
+# chained-layer glue
+# ----------------------------------------------------------------------------
+
+def test_round_bf16_matches_library_conversion():
+    import torch
+    rng = np.random.default_rng(30)
+    a = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32).astype(np.float64)
+    a[:4] = [0.0, -0.0, 1.0, 1.0 + 2.0 ** -8]          # exact tie rounds to even
+    ref = torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(O.round_bf16(a), ref)
+
+
+def test_chain_glue_unit_rms_and_product():
+    rng = np.random.default_rng(31)
+    ya, yb = rng.normal(size=(3, 256)) * 5.0, rng.normal(size=(3, 256))
+    h = O.chain_glue(ya)
+    assert np.allclose(np.sqrt(np.mean(h * h, axis=1)), 1.0, atol=4e-3)      # bf16 rounding only
+    hp = O.chain_glue(ya, yb)
+    p = ya * yb
+    assert np.allclose(hp, p / np.sqrt(np.mean(p * p, axis=1, keepdims=True)), rtol=2 ** -8, atol=0)
+    assert np.array_equal(O.chain_glue(np.zeros((1, 128))), np.zeros((1, 128)))
