@@ -367,6 +367,117 @@ def run_gpu(args, rank, world):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------
+# chained 31B-class layers: one layer (draft T=1, verify T=64) or the 60-layer spec cycle
+# ----------------------------------------------------------------------------
+
+def run_stack(args):
+    import numpy as np
+    import torch
+    from nested_bit_quantized_gb300 import build as nb
+    from nested_bit_quantized_gb300 import chain, nest, synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    nb.build()
+    nest.load()
+    cycle = args.workload == "stack_31b"
+    n_layers = args.layers if args.layers else (60 if cycle else 1)
+    stack = synth.stack_31b(n_layers)
+    bits = 8
+    work = torch.empty(max(l.M * l.K for l in stack[0]), dtype=torch.float64, device=dev)
+    lin = []
+    for layer in stack:
+        d = {}
+        for l in layer:
+            W = synth.weights_device(l.M, l.K, l.w_seed, l.outliers, dev)
+            s_o, s_i = synth.sign_pair(l.M, l.K, l.sign_seed)
+            so, si = torch.from_numpy(s_o).to(dev), torch.from_numpy(s_i).to(dev)
+            q = nest.quantize(W, so, si, bits, work=work[:l.M * l.K].view(l.M, l.K))
+            d[l.name.split(".")[-1]] = nest.pack(q["base_codes"], q["base_scales"], q["resid_codes"], q["resid_scales"],
+                                                 bits, so, si)
+            del W, q
+        lin.append(d)
+    del work
+    torch.cuda.synchronize()
+    T_d, T_v = (1, 16) if cycle else (1, 64)
+    hidden = stack[0][0].K
+    xs = {}
+    for T in (T_d, T_v):
+        b, _ = synth.activations(T, hidden, 31 + T)
+        xs[T] = torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+    bufs = {T: [chain.LayerBuffers(d, T, dev) for d in lin] for T in (T_d, T_v)}
+
+    def run_pass(T, verify):
+        chain.layer_input(lin[0], xs[T], bufs[T][0])
+        for i in range(n_layers):
+            nxt = i + 1 < n_layers
+            chain.layer_forward(lin[i], bufs[T][i], verify, lin[i + 1] if nxt else None,
+                                bufs[T][i + 1] if nxt else None)
+
+    gamma = 8 if cycle else 1
+    def step():
+        for _ in range(gamma):
+            run_pass(T_d, False)
+        run_pass(T_v, True)
+
+    stream = torch.cuda.Stream(device=dev)
+    graphs = {}
+    with torch.cuda.stream(stream):
+        for name, fn in (("step", step), ("draft", lambda: run_pass(T_d, False)), ("verify", lambda: run_pass(T_v, True))):
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            graphs[name] = g
+    torch.cuda.synchronize()
+    nest.error_check()
+
+    def timed(g, reps, warm):
+        for _ in range(warm):
+            g.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            s.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    def lbytes(T, verify):
+        return sum(lin_bytes(l.M, l.K, T, bits if verify else 0) for layer in stack for l in layer)
+
+    with ClockSampler(dev.index) as clk:
+        ms = timed(graphs["step"], args.steps, args.warmup)
+    ms_d = timed(graphs["draft"], max(3, args.steps), args.warmup)
+    ms_v = timed(graphs["verify"], max(3, args.steps), args.warmup)
+    nest.error_check()
+    step_bytes = gamma * lbytes(T_d, False) + lbytes(T_v, True)
+    hbm, src = peaks()
+    line = {
+        "metric": METRIC, "value": step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": (f"31B-class stack, {n_layers} chained layers (q 8192x5376, k/v 4096x5376, o 5376x8192, "
+                                f"gate/up 21504x5376, down 5376x21504), 2-bit base + 8-bit residual; step = "
+                                f"{gamma} draft pass(es) at T={T_d} + 1 verify pass at T={T_v}"),
+                   "resident_weight_GB": sum(weight_bytes(l.M, l.K, bits) for layer in stack for l in layer) / 1e9,
+                   "l2": "inputs larger than L2 (every linear streams 0.1-0.4 GB)", "accumulate": "f32"},
+        "draft_pass": {"T": T_d, "ms": ms_d, "us_per_layer": 1e3 * ms_d / n_layers,
+                       "GBps": lbytes(T_d, False) / (ms_d * 1e-3) / 1e9},
+        "verify_pass": {"T": T_v, "ms": ms_v, "us_per_layer": 1e3 * ms_v / n_layers,
+                        "GBps": lbytes(T_v, True) / (ms_v * 1e-3) / 1e9,
+                        "frac_of_measured_hbm": lbytes(T_v, True) / (ms_v * 1e-3) / 1e9 / hbm},
+        "ideal_ms_at_measured_hbm": step_bytes / (hbm * 1e9) * 1e3,
+        "gpu_launches": (gamma + 1) * (3 + 10 * n_layers) * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -375,6 +486,10 @@ def main():
     ap.add_argument("--impl", default="nest", choices=["nest", "reference"])
     ap.add_argument("--copies", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "decoder_31b", "stack_31b"],
+                    help="mlp_triplet_4b (default, the metric's workload), one chained 31B-class layer, "
+                         "or the 60-layer 31B-class speculative cycle")
+    ap.add_argument("--layers", type=int, default=0, help="layers of the 31B-class stack (default 1 or 60)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -382,6 +497,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.workload != WORKLOAD:
+        run_stack(args)
     else:
         run_gpu(args, rank, world if "RANK" in os.environ else 1)
 

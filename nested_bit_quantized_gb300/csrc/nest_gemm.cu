@@ -94,6 +94,7 @@ struct Cfg {
     static constexpr int kSmemBytes = kStages * kWStage + kXRing + kNumBars * 8 + 16;
     static_assert(kNumA >= 2, "tensor memory budget");
     static_assert(kStages >= 2, "stage too large");
+    static_assert(kStages % kDeqWG == 0 || kStages >= kNumA, "weight-stage phase order needs S >= NA when S is odd");
     static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
     static_assert(kWStage % 128 == 0 && kXBytes % 128 == 0, "stage alignment");
 };
@@ -383,8 +384,15 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
             if (first) ++seg;
             if (i % C::kDeqWG == wg) {
                 const int s = i % S, a = i % NA;
-                if (!warp_wait(full_w(s), (i / S) & 1, abort_flag)) break;
+                // Order matters when S is odd: stage s then alternates between the two
+                // warpgroups, and a parity wait cannot tell phase k+1 from phase k-1.  The
+                // wait on done(a) for unit i-NA comes first: its MMAs were issued after
+                // the a_full of unit i-S (S >= NA), so every thread that consumed unit i-S
+                // has already seen full_w(s) complete, and the phase this wait tests is the
+                // next one.  Unit i+1's copy can land before unit i's, so without this the
+                // warpgroup of unit i+S could read a stage that is still being filled.
                 if (i >= NA && !warp_wait(done(a), ((i / NA) - 1) & 1, abort_flag)) break;
+                if (!warp_wait(full_w(s), (i / S) & 1, abort_flag)) break;
                 tc_fence_after();
                 const uint8_t* sb = st_base(s);
                 const uint8_t* sr = st_res(s);
