@@ -472,7 +472,7 @@ def run_stack(args):
                         "GBps": lbytes(T_v, True) / (ms_v * 1e-3) / 1e9,
                         "frac_of_measured_hbm": lbytes(T_v, True) / (ms_v * 1e-3) / 1e9 / hbm},
         "ideal_ms_at_measured_hbm": step_bytes / (hbm * 1e9) * 1e3,
-        "gpu_launches": (gamma + 1) * (3 + 10 * n_layers) * args.steps,
+        "gpu_launches": (gamma + 1) * 13 * n_layers * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

@@ -203,24 +203,48 @@ nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t v
                               int32_t x_dtype, int32_t T, float* const* ys, void* scratch, void* stream);
 
 /* Glue between chained linears, fused with the rotations on both sides of it:
- *   y = S_o H_o z_a  (or the elementwise product y_a * y_b of two linears' outputs, e.g. gate * up),
- *   h = bf16(y / rms(y)) per token (unit-RMS rescale standing in for the normalisation
- *       between linears, then the bf16 cast),
- *   and for each of n_next (0..3) next linears j: x'_j = H_i S_i h written as its GEMM operand.
+ *   h = S_o H_o z_a  (or the elementwise product h_a * h_b of two linears' outputs, e.g. gate * up),
+ *   h' = bf16(h / rms(h)) per token (unit-RMS rescale standing in for the normalisation
+ *        between linears, then the bf16 cast),
+ *   and for each of n_next (0..3) next linears j: x'_j = H_i S_i h' written as its GEMM operand.
  * The rotations are those of POC recipe steps 1 and 4 (feedman.me/posts/wZBTJ); the chaining
  * and the RMS rescale are the chained-layer workload's reading, not the pages'.
- * z_a, z_b      fp32 [T][M] GEMM accumulators (rotated basis); z_b / sign_out_b may be NULL.
+ * Two launches (rotation out with per-segment sums of squares; rescale, cast and rotation in).
+ * z_a           fp32 [T][M] GEMM accumulator of linear a (rotated basis).  When y is NULL, h
+ *               overwrites z_a.
+ * z_b           NULL, or the accumulator of the product partner (fp32 [T][M], read only);
+ *               sign_out_b is NULL exactly when z_b is.  z_b must differ from z_a and y.
  * sign_out_a/b  S_o of those linears (int8 [M]).
- * y             optional fp32 [T][M] out: the un-rotated output (the product when z_b is given).
+ * y             NULL, or fp32 [T][M] out: h (the product when z_b is given), kept by the caller.
  * next          host array of n_next layer descriptors; each must have K == M (its sign_in is used).
  * x_ops         host array of n_next operand buffers (out, nest_xop_bytes(M, T) bytes each).
  * z_next        NULL, or host array of n_next accumulators (fp32 [T][next[j].M], or NULL entries)
  *               that are cleared here for the GEMMs that follow.
- * Limits: T <= 64, M % 128 == 0 when n_next > 0, M <= 29000 (one token's two vectors in
- * shared memory). */
-nest_status nest_chain(const float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,
+ * work          nest_chain_work_bytes(M, T) bytes of device memory, no initial contents; calls
+ *               whose work may overlap on the GPU need separate work buffers.
+ * Limits: T <= 64, M * T < 2^31, M % 128 == 0 when n_next > 0. */
+size_t nest_chain_work_bytes(int32_t M, int32_t T);
+nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,
                        int32_t M, int32_t T, float* y, const nest_layer* next, int32_t n_next,
-                       uint16_t* const* x_ops, float* const* z_next, void* stream);
+                       uint16_t* const* x_ops, float* const* z_next, float* work, void* stream);
+
+/* Grouped rotation: `count` (1..4) independent nest_rotate calls sharing x_dtype, T and mode,
+ * in ONE launch (e.g. one layer input rotated into the q, k and v operands, or the k and v
+ * outputs rotated back).  Each task may also clear a buffer of zero_count floats (e.g. the
+ * accumulator of the GEMM that reads its operand), which saves a separate fill launch.
+ * Task fields have nest_rotate's meaning and limits; zero_out may be NULL when zero_count
+ * is 0 and must not overlap any other buffer of the call. */
+typedef struct {
+    const void* x;          /* [T][n] fp32 or bf16 bits */
+    const int8_t* signs;    /* int8 [n] */
+    int32_t n;
+    float* y;               /* fp32 [T][n] out, or NULL */
+    uint16_t* x_op;         /* operand out (mode 0), or NULL */
+    float* zero_out;        /* cleared here, or NULL */
+    int64_t zero_count;     /* floats to clear */
+} nest_rotate_task;
+nest_status nest_rotate_group(const nest_rotate_task* tasks, int32_t count, int32_t x_dtype, int32_t T,
+                              int32_t mode, void* stream);
 
 /* nest_linear without caller scratch, for callers that cannot allocate device memory
  * (a process whose memory pool is fixed at start-up, a plain C caller without an

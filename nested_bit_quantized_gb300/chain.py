@@ -11,7 +11,6 @@ the calls.
 """
 from __future__ import annotations
 
-import ctypes
 from typing import Dict, List, Optional
 
 import torch
@@ -22,40 +21,42 @@ NAMES = ("q", "k", "v", "o", "gate", "up", "down")
 
 
 class LayerBuffers:
-    """Operands, accumulators and outputs of one layer for a fixed T."""
+    """Operands, accumulators, outputs and glue work space of one layer for a fixed T."""
 
     def __init__(self, lin: Dict[str, nest.Layer], T: int, device):
         self.T = T
         self.xop = {n: nest.new_xop(lin[n].K, T, device) for n in NAMES}
         self.z = {n: torch.zeros((T, lin[n].M), dtype=torch.float32, device=device) for n in NAMES}
         self.y = {n: torch.empty((T, lin[n].M), dtype=torch.float32, device=device) for n in ("k", "v", "down")}
+        wb = max(chain_work_bytes(lin[n].M, T) for n in NAMES)
+        self.work = torch.empty(wb // 4, dtype=torch.float32, device=device)
 
 
-def chain(z_a, s_a, z_b, s_b, T: int, y=None, nexts: Optional[List[nest.Layer]] = None, x_ops=None, z_next=None,
-          stream=None):
-    """nest_chain (see include/nest.h)."""
+def chain_work_bytes(M: int, T: int) -> int:
+    return int(nest.load().nest_chain_work_bytes(M, T))
+
+
+def chain(z_a, s_a, z_b, s_b, T: int, work: torch.Tensor, y=None, nexts: Optional[List[nest.Layer]] = None,
+          x_ops=None, z_next=None, stream=None):
+    """nest_chain (see include/nest.h).  Without y, the glue output overwrites z_a."""
     lib = nest.load()
-    if not hasattr(lib, "_chain_sig"):
-        lib.nest_chain.argtypes = [nest._P, nest._P, nest._P, nest._P, nest._I32, nest._I32, nest._P,
-                                   ctypes.POINTER(nest._Layer), nest._I32, ctypes.POINTER(nest._P),
-                                   ctypes.POINTER(nest._P), nest._P]
-        lib.nest_chain.restype = nest._I32
-        lib._chain_sig = True
     nexts = nexts or []
     M = z_a.shape[1]
+    if work.numel() * 4 < chain_work_bytes(M, T):
+        raise ValueError("work buffer too small")
     arr = nest._layers(nexts) if nexts else None
     xo = nest._ptrs(x_ops) if nexts else None
     zn = nest._ptrs(z_next) if z_next else None
     st = lib.nest_chain(nest._ptr(z_a), nest._ptr(s_a), nest._ptr(z_b), nest._ptr(s_b), M, T, nest._ptr(y),
-                        arr, len(nexts), xo, zn, nest._stream(stream))
+                        arr, len(nexts), xo, zn, nest._ptr(work), nest._stream(stream))
     nest._check(st, "nest_chain")
 
 
 def layer_input(lin: Dict[str, nest.Layer], x: torch.Tensor, buf: LayerBuffers, stream=None):
-    """Rotate the layer input into the q, k, v operands and clear their accumulators."""
-    for n in ("q", "k", "v"):
-        nest.rotate(x, lin[n].sign_in, 0, x_op=buf.xop[n], stream=stream)
-        buf.z[n].zero_()
+    """Rotate the layer input into the q, k, v operands and clear their accumulators (one launch)."""
+    names = ("q", "k", "v")
+    nest.rotate_group([x] * 3, [lin[n].sign_in for n in names], 0, x_ops=[buf.xop[n] for n in names],
+                      zero=[buf.z[n] for n in names], stream=stream)
 
 
 def layer_forward(lin: Dict[str, nest.Layer], buf: LayerBuffers, verify: bool,
@@ -67,18 +68,20 @@ def layer_forward(lin: Dict[str, nest.Layer], buf: LayerBuffers, verify: bool,
     g = lambda names: nest.gemm_group([lin[n] for n in names], [buf.xop[n] for n in names], T, verify,
                                       zs=[buf.z[n] for n in names], stream=stream)
     g(("q", "k", "v"))
-    chain(buf.z["q"], lin["q"].sign_out, None, None, T, None, [lin["o"]], [buf.xop["o"]], [buf.z["o"]], stream)
-    for n in ("k", "v"):
-        nest.rotate(buf.z[n], lin[n].sign_out, 1, y=buf.y[n], stream=stream)
+    chain(buf.z["q"], lin["q"].sign_out, None, None, T, buf.work, None, [lin["o"]], [buf.xop["o"]], [buf.z["o"]],
+          stream)
+    nest.rotate_group([buf.z["k"], buf.z["v"]], [lin["k"].sign_out, lin["v"].sign_out], 1,
+                      ys=[buf.y["k"], buf.y["v"]], stream=stream)
     g(("o",))
-    chain(buf.z["o"], lin["o"].sign_out, None, None, T, None, [lin["gate"], lin["up"]],
+    chain(buf.z["o"], lin["o"].sign_out, None, None, T, buf.work, None, [lin["gate"], lin["up"]],
           [buf.xop["gate"], buf.xop["up"]], [buf.z["gate"], buf.z["up"]], stream)
     g(("gate", "up"))
-    chain(buf.z["gate"], lin["gate"].sign_out, buf.z["up"], lin["up"].sign_out, T, None, [lin["down"]],
+    chain(buf.z["gate"], lin["gate"].sign_out, buf.z["up"], lin["up"].sign_out, T, buf.work, None, [lin["down"]],
           [buf.xop["down"]], [buf.z["down"]], stream)
     g(("down",))
     if next_lin is None:
-        chain(buf.z["down"], lin["down"].sign_out, None, None, T, buf.y["down"], stream=stream)
+        chain(buf.z["down"], lin["down"].sign_out, None, None, T, buf.work, buf.y["down"], stream=stream)
     else:
-        chain(buf.z["down"], lin["down"].sign_out, None, None, T, buf.y["down"], [next_lin[n] for n in ("q", "k", "v")],
-              [next_buf.xop[n] for n in ("q", "k", "v")], [next_buf.z[n] for n in ("q", "k", "v")], stream)
+        chain(buf.z["down"], lin["down"].sign_out, None, None, T, buf.work, buf.y["down"],
+              [next_lin[n] for n in ("q", "k", "v")], [next_buf.xop[n] for n in ("q", "k", "v")],
+              [next_buf.z[n] for n in ("q", "k", "v")], stream)

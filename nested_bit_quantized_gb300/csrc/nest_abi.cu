@@ -277,26 +277,32 @@ nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, 
     return nest_linear_group(layer, 1, verify, &x, x_dtype, T, &y, scratch, stream);
 }
 
-nest_status nest_chain(const float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,
+size_t nest_chain_work_bytes(int32_t M, int32_t T) {
+    if (M < 1 || T < 1 || T > 64) return 0;
+    return round256((size_t)T * glue_segments(M) * sizeof(float));
+}
+
+nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,
                        int32_t M, int32_t T, float* y, const nest_layer* next, int32_t n_next,
-                       uint16_t* const* x_ops, float* const* z_next, void* stream) {
-    if (z_a == nullptr || sign_out_a == nullptr) return NEST_ERR_INVALID_ARG;
+                       uint16_t* const* x_ops, float* const* z_next, float* work, void* stream) {
+    if (z_a == nullptr || sign_out_a == nullptr || work == nullptr) return NEST_ERR_INVALID_ARG;
     if ((z_b == nullptr) != (sign_out_b == nullptr)) return NEST_ERR_INVALID_ARG;
+    if (z_b == z_a || (y != nullptr && y == z_b)) return NEST_ERR_INVALID_ARG;
     if (M < 1 || T < 1 || n_next < 0) return NEST_ERR_INVALID_ARG;
     if (T > 64 || n_next > kMaxChainNext) return NEST_ERR_UNSUPPORTED;
-    if (n_next == 0 && y == nullptr) return NEST_ERR_INVALID_ARG;
+    if ((long long)M * T >= (1LL << 31)) return NEST_ERR_UNSUPPORTED;
     if (n_next > 0 && (next == nullptr || x_ops == nullptr)) return NEST_ERR_INVALID_ARG;
     if (n_next > 0 && M % 128) return NEST_ERR_UNSUPPORTED;
-    if (chain_smem_bytes(M) > 227 * 1024) return NEST_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(z_a) & 3u) || (z_b && (reinterpret_cast<uintptr_t>(z_b) & 3u)) ||
-        (y && (reinterpret_cast<uintptr_t>(y) & 3u)))
+        (y && (reinterpret_cast<uintptr_t>(y) & 3u)) || (reinterpret_cast<uintptr_t>(work) & 3u))
         return NEST_ERR_MISALIGNED;
-    ChainArgs c = {};
+    GlueArgs c = {};
     c.za = z_a;
     c.sa = sign_out_a;
     c.zb = z_b;
     c.sb = sign_out_b;
-    c.y = y;
+    c.h = y != nullptr ? y : z_a;
+    c.work = work;
     c.nnext = n_next;
     c.M = M;
     c.T = T;
@@ -306,9 +312,44 @@ nest_status nest_chain(const float* z_a, const int8_t* sign_out_a, const float* 
         if (!aligned16(x_ops[j])) return NEST_ERR_MISALIGNED;
         float* zn = z_next ? z_next[j] : nullptr;
         if (zn && (reinterpret_cast<uintptr_t>(zn) & 3u)) return NEST_ERR_MISALIGNED;
-        c.next[j] = ChainNext{L.sign_in, x_ops[j], zn, zn ? (long long)T * L.M : 0};
+        c.next[j] = GlueNext{L.sign_in, x_ops[j], zn, zn ? (long long)T * L.M : 0};
     }
-    return from_cuda(launch_chain(c, as_stream(stream)));
+    return from_cuda(launch_glue(c, as_stream(stream)));
+}
+
+nest_status nest_rotate_group(const nest_rotate_task* tasks, int32_t count, int32_t x_dtype, int32_t T,
+                              int32_t mode, void* stream) {
+    if (tasks == nullptr || count < 1 || T < 1) return NEST_ERR_INVALID_ARG;
+    if (count > kMaxTasks) return NEST_ERR_UNSUPPORTED;
+    if ((x_dtype != 0 && x_dtype != 1) || (mode != 0 && mode != 1)) return NEST_ERR_INVALID_ARG;
+    RotArgs a = {};
+    a.ntasks = count;
+    long long ctas = 0;
+    for (int k = 0; k < count; ++k) {
+        const nest_rotate_task& r = tasks[k];
+        if (!r.x || !r.signs || (!r.y && !r.x_op) || r.n < 1) return NEST_ERR_INVALID_ARG;
+        if ((long long)r.n * T >= (1LL << 31)) return NEST_ERR_UNSUPPORTED;
+        if (r.x_op != nullptr) {
+            if (mode != 0) return NEST_ERR_INVALID_ARG;
+            if (r.n % 128 || T > 64) return NEST_ERR_UNSUPPORTED;
+            if (!aligned16(r.x_op)) return NEST_ERR_MISALIGNED;
+        }
+        if ((reinterpret_cast<uintptr_t>(r.x) & (x_dtype == 1 ? 1u : 3u)) ||
+            (r.y && (reinterpret_cast<uintptr_t>(r.y) & 3u)))
+            return NEST_ERR_MISALIGNED;
+        if (r.zero_count < 0 || (r.zero_count > 0 && r.zero_out == nullptr)) return NEST_ERR_INVALID_ARG;
+        if (r.zero_out && (reinterpret_cast<uintptr_t>(r.zero_out) & 3u)) return NEST_ERR_MISALIGNED;
+        ctas += ((long long)r.n * T + 4095) / 4096;
+        a.task[k].x = r.x;
+        a.task[k].signs = r.signs;
+        a.task[k].y = r.y;
+        a.task[k].xop = r.x_op;
+        a.task[k].zero_out = r.zero_count > 0 ? r.zero_out : nullptr;
+        a.task[k].zero_count = r.zero_count;
+        a.task[k].n = (unsigned)r.n;
+    }
+    if (ctas >= (1LL << 31)) return NEST_ERR_UNSUPPORTED;
+    return from_cuda(launch_rotate_group(a, x_dtype, mode, T, as_stream(stream)));
 }
 
 nest_status nest_error_check(void* stream) {

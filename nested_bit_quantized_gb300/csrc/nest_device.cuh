@@ -187,6 +187,59 @@ __device__ __forceinline__ void warp_fwht(float& v0, float& v1, int nbits, int l
     }
 }
 
+// Block-diagonal FWHT (unnormalised, blocks of 2^L, 0 <= L <= 12) of the 4096 values
+// of a 64 x 64 shared-memory tile, value f at tile[f / 64][f % 64]: butterflies over
+// index bits 0..5 along rows, then bits 6..11 along columns (the padding column keeps
+// the column pass free of bank conflicts).  Every thread of the CTA (THREADS of them)
+// calls it; the tile is complete on return.
+template <int THREADS>
+__device__ __forceinline__ void tile_fwht(float (*tile)[65], int L) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L1 = L < 6 ? L : 6;
+    if (L1 > 0) {
+        for (int row = warp; row < 64; row += THREADS / 32) {
+            float v0 = tile[row][lane], v1 = tile[row][lane + 32];
+            warp_fwht(v0, v1, L1, lane);
+            tile[row][lane] = v0;
+            tile[row][lane + 32] = v1;
+        }
+        __syncthreads();
+    }
+    if (L > 6) {
+        for (int col = warp; col < 64; col += THREADS / 32) {
+            float v0 = tile[lane][col], v1 = tile[lane + 32][col];
+            warp_fwht(v0, v1, L - 6, lane);
+            tile[lane][col] = v0;
+            tile[lane + 32][col] = v1;
+        }
+        __syncthreads();
+    }
+}
+
+// Sum over all THREADS threads of the CTA; every thread gets the total.  red: 32 floats
+// of shared memory.
+template <int THREADS>
+__device__ __forceinline__ float cta_sum(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = lane < THREADS / 32 ? red[lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    __syncthreads();
+    return t;
+}
+
+// Offset in bytes of token t, columns k..k+7 (k % 8 == 0) in the fp16 GEMM operand of
+// NB token blocks: per 128-column group g, core matrices of 8 tokens x 8 columns (16-byte
+// rows), column-block c major, token block minor.
+__device__ __forceinline__ size_t xop_offset(int k, int t, int NB) {
+    const int g = k >> 7, c = (k & 127) >> 3;
+    return (size_t)g * 2048 * NB + ((size_t)(c * NB + (t >> 3)) * 8 + (t & 7)) * 16;
+}
+
 // ---------------------------------------------------------------------------
 // small integer / half helpers
 // ---------------------------------------------------------------------------

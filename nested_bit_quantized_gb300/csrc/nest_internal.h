@@ -83,25 +83,26 @@ cudaError_t launch_rotate(const void* x, int x_dtype, const int8_t* signs, int n
 cudaError_t launch_rotate_group(RotArgs& a, int x_dtype, int mode, int T, cudaStream_t stream);
 
 // Glue between chained linears (nest_chain): see nest_chain.cu.
-struct ChainNext {
+struct GlueNext {
     const int8_t* sign_in;    // S_i of the next linear (length M)
     uint16_t* xop;            // its GEMM operand (out)
     float* zero_out;          // its GEMM accumulator, cleared here (optional)
     long long zero_count;
 };
-struct ChainArgs {
+constexpr int kMaxChainNext = 3;
+struct GlueArgs {
     const float* za;          // accumulator of linear a, [T][M], rotated basis
     const int8_t* sa;         // S_o of linear a
     const float* zb;          // optional product partner (same M)
     const int8_t* sb;
-    float* y;                 // optional un-rotated output (the product when zb is given)
-    ChainNext next[3];
-    int nnext, M, T, L, NB;
+    float* h;                 // glue output before the RMS rescale, [T][M] (may be za)
+    float* work;              // [T][nseg] segment sums of squares
+    GlueNext next[kMaxChainNext];
+    int nnext, M, T, L, NB, nseg;
     float scale;
 };
-constexpr int kMaxChainNext = 3;
-size_t chain_smem_bytes(int M);
-cudaError_t launch_chain(ChainArgs& a, cudaStream_t stream);
+int glue_segments(int M);     // 4096-element segments per token
+cudaError_t launch_glue(GlueArgs& a, cudaStream_t stream);
 
 cudaError_t launch_pack(const uint8_t* bc, const uint16_t* bs, const int8_t* rc, const uint16_t* rs,
                         int M, int K, int bits, uint8_t* base_out, uint8_t* resid_out, cudaStream_t stream);

@@ -67,26 +67,7 @@ k_rotate(const __grid_constant__ RotArgs args) {
     }
     __syncthreads();
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L1 = L < 6 ? L : 6;
-    if (L1 > 0) {
-        for (int row = warp; row < 64; row += kThreads / 32) {
-            float v0 = buf[row][lane], v1 = buf[row][lane + 32];
-            warp_fwht(v0, v1, L1, lane);
-            buf[row][lane] = v0;
-            buf[row][lane + 32] = v1;
-        }
-        __syncthreads();
-    }
-    if (L > 6) {
-        for (int col = warp; col < 64; col += kThreads / 32) {
-            float v0 = buf[lane][col], v1 = buf[lane + 32][col];
-            warp_fwht(v0, v1, L - 6, lane);
-            buf[lane][col] = v0;
-            buf[lane + 32][col] = v1;
-        }
-        __syncthreads();
-    }
+    tile_fwht<kThreads>(buf, L);
 
     if (y != nullptr) {
         float sg[kPer];
@@ -114,9 +95,8 @@ k_rotate(const __grid_constant__ RotArgs args) {
                 const float b = buf[(f + 2 * e + 1) >> 6][(f + 2 * e + 1) & 63] * scale;
                 w[e] = h2_as_u32(__floats2half2_rn(a, b));
             }
-            const int g = k >> 7, c = (k & 127) >> 3;
-            const size_t off = (size_t)g * 2048 * NB + ((size_t)(c * NB + (t >> 3)) * 8 + (t & 7)) * 16;
-            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(xop) + off) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(xop) + xop_offset(k, t, NB)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
 }

@@ -33,6 +33,12 @@ class _Layer(ctypes.Structure):
                 ("base", _P), ("resid", _P), ("sign_out", _P), ("sign_in", _P)]
 
 
+class RotateTask(ctypes.Structure):
+    """nest_rotate_task: one set of vectors of a grouped rotation."""
+    _fields_ = [("x", _P), ("signs", _P), ("n", _I32), ("y", _P), ("x_op", _P), ("zero_out", _P),
+                ("zero_count", ctypes.c_int64)]
+
+
 _lib = None
 
 
@@ -67,6 +73,10 @@ def load() -> ctypes.CDLL:
         "nest_linear_group_scratch_bytes": ([ctypes.POINTER(_Layer), _I32, _I32], _SZ),
         "nest_linear_group": ([ctypes.POINTER(_Layer), _I32, _I32, ctypes.POINTER(_P), _I32, _I32,
                                ctypes.POINTER(_P), _P, _P], _I32),
+        "nest_chain_work_bytes": ([_I32, _I32], _SZ),
+        "nest_chain": ([_P, _P, _P, _P, _I32, _I32, _P, ctypes.POINTER(_Layer), _I32, ctypes.POINTER(_P),
+                        ctypes.POINTER(_P), _P, _P], _I32),
+        "nest_rotate_group": ([ctypes.POINTER(RotateTask), _I32, _I32, _I32, _I32, _P], _I32),
         "nest_error_check": ([_P], _I32),
     }
     for name, (args, res) in sig.items():
@@ -233,6 +243,27 @@ def rotate(x: torch.Tensor, signs: torch.Tensor, mode: int, y: Optional[torch.Te
     st = load().nest_rotate(_ptr(x), dt, _ptr(signs), n, T, mode, _ptr(y), _ptr(x_op), _stream(stream))
     _check(st, "nest_rotate")
     return y, x_op
+
+
+def rotate_group(xs, signs, mode: int, ys=None, x_ops=None, zero=None, stream=None):
+    """nest_rotate_group: up to 4 rotations (same dtype, T and mode) in one launch.
+    xs, signs: lists; ys / x_ops: lists (entries may be None) or None; zero: list of
+    fp32 tensors (or None entries) cleared by the same launch."""
+    n_t = len(xs)
+    ys = ys or [None] * n_t
+    x_ops = x_ops or [None] * n_t
+    zero = zero or [None] * n_t
+    dt = 1 if xs[0].dtype == torch.bfloat16 else 0
+    T = xs[0].shape[0]
+    arr = (RotateTask * n_t)()
+    for i, (x, s, y, xo, z) in enumerate(zip(xs, signs, ys, x_ops, zero)):
+        if x.dtype != xs[0].dtype or x.shape[0] != T:
+            raise ValueError("all inputs of a grouped rotation share dtype and T")
+        _dev(x, x.dtype, "x")
+        _dev(s, torch.int8, "signs")
+        arr[i] = RotateTask(_ptr(x), _ptr(s), x.shape[1], _ptr(y), _ptr(xo), _ptr(z), 0 if z is None else z.numel())
+    st = load().nest_rotate_group(arr, n_t, dt, T, mode, _stream(stream))
+    _check(st, "nest_rotate_group")
 
 
 def new_xop(K: int, T: int, device="cuda") -> torch.Tensor:

@@ -112,6 +112,37 @@ def test_rotate_pack_quantize_validation(lib):
     assert q(ctypes.c_void_p(0x50004), ok, ok, 128, 128, 8, ok, ok, ok, ok, ok, None) == 3
 
 
+def test_chain_and_rotate_group_validation(lib):
+    ok = ctypes.c_void_p(0x50000)
+    assert lib.nest_chain_work_bytes(5376, 64) == 256 * ((64 * 2 * 4 + 255) // 256)
+    assert lib.nest_chain_work_bytes(21504, 64) == 64 * 6 * 4
+    assert lib.nest_chain_work_bytes(100, 65) == 0
+    L = nest._Layer(256, 512, 0, 0x50000, None, 0x50000, 0x50000)
+    nx = (nest._Layer * 1)(L)
+    xo = (ctypes.c_void_p * 1)(0x50000)
+    c = lib.nest_chain
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, None, None) == 1       # work missing
+    assert c(ok, ok, ok, None, 512, 4, None, nx, 1, xo, None, ok, None) == 1         # partner sign missing
+    assert c(ok, ok, ok, ok, 512, 4, None, nx, 1, xo, None, ok, None) == 1           # z_b aliases z_a
+    assert c(ok, ok, None, None, 512, 65, None, nx, 1, xo, None, ok, None) == 2      # T > 64
+    assert c(ok, ok, None, None, 640, 4, None, nx, 1, xo, None, ok, None) == 1       # next K != M
+    assert c(ok, ok, None, None, 500, 4, None, nx, 1, xo, None, ok, None) == 2       # operand needs M % 128
+    assert c(ok, ok, None, None, 512, 4, None, nx, 4, xo, None, ok, None) == 2       # more than 3 next
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, ctypes.c_void_p(0x50002), None) == 3
+    T = nest.RotateTask
+    one = (T * 1)(T(0x50000, 0x50000, 128, 0x50000, None, None, 0))
+    g = lib.nest_rotate_group
+    assert g(one, 0, 1, 4, 0, None) == 1
+    assert g(one, 5, 1, 4, 0, None) == 2
+    assert g(one, 1, 2, 4, 0, None) == 1                                                # dtype
+    bad = (T * 1)(T(0x50000, 0x50000, 128, 0x50000, None, None, 16))
+    assert g(bad, 1, 1, 4, 0, None) == 1                                                # zero_count without buffer
+    opr = (T * 1)(T(0x50000, 0x50000, 100, None, 0x50000, None, 0))
+    assert g(opr, 1, 1, 4, 0, None) == 2                                                # operand needs n % 128
+    mis = (T * 1)(T(0x50000, 0x50000, 128, None, 0x50008, None, 0))
+    assert g(mis, 1, 1, 4, 0, None) == 3
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(nest, "_lib", None)
     monkeypatch.setattr(nest._build, "LIB", str(tmp_path / "missing.so"))

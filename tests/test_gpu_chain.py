@@ -38,29 +38,64 @@ def dev():
     return d
 
 
-@pytest.mark.parametrize("M,T,product", [(512, 1, False), (5376, 17, True), (3840, 64, False), (8192, 5, True)])
-def test_chain_kernel(dev, M, T, product):
+@pytest.mark.parametrize("M,T,product,in_place,n_next", [
+    (512, 1, False, False, 2), (5376, 17, True, False, 2), (3840, 64, False, True, 2), (8192, 5, True, True, 1),
+    (21504, 3, True, False, 1), (300, 4, True, False, 0), (4096, 2, False, True, 3)])
+def test_chain_kernel(dev, M, T, product, in_place, n_next):
+    """Out-rotation (+ product), RMS rescale, bf16 cast and next in-rotations; ragged last
+    4096-element segments (5376, 21504), a segment shorter than one (300, 3840), h in place."""
     rng = np.random.default_rng(M + T)
     za = rng.normal(size=(T, M)).astype(np.float32)
     zb = rng.normal(size=(T, M)).astype(np.float32) if product else None
     sa, sb = synth.signs(M, 1), synth.signs(M, 2)
-    nxt = [synth.signs(M, 3 + j) for j in range(2)]
-    y = torch.empty((T, M), dtype=torch.float32, device=dev)
-    # two next linears reading h (their descriptors only need K == M and S_i)
+    nxt = [synth.signs(M, 3 + j) for j in range(n_next)]
+    za_d = to_dev(za, torch, dev)
+    y = None if in_place else torch.empty((T, M), dtype=torch.float32, device=dev)
+    # next linears reading h (their descriptors only need K == M and S_i)
     dummy = torch.zeros(16, dtype=torch.uint8, device=dev)
-    layers = [nest.Layer(128, M, 0, dummy, None, to_dev(sa, torch, dev), to_dev(s, torch, dev)) for s in nxt]
+    layers = [nest.Layer(1000 + 24 * j, M, 0, dummy, None, to_dev(sa, torch, dev), to_dev(s, torch, dev))
+              for j, s in enumerate(nxt)]
     xops = [nest.new_xop(M, T, dev) for _ in nxt]
-    zn = [torch.full((T, 128), 7.0, device=dev) for _ in nxt]
-    chain.chain(to_dev(za, torch, dev), to_dev(sa, torch, dev), to_dev(zb, torch, dev) if product else None,
-                to_dev(sb, torch, dev) if product else None, T, y, layers, xops, zn)
+    zn = [torch.full((T, L.M), 7.0, device=dev) for L in layers]
+    work = torch.full((chain.chain_work_bytes(M, T) // 4,), float("nan"), device=dev)
+    chain.chain(za_d, to_dev(sa, torch, dev), to_dev(zb, torch, dev) if product else None,
+                to_dev(sb, torch, dev) if product else None, T, work, y, layers, xops, zn)
     ya = O.unrotate_outputs(za, sa)
     yref = ya * O.unrotate_outputs(zb, sb) if product else ya
-    parity(y.cpu().numpy(), yref)
+    parity((za_d if in_place else y).cpu().numpy(), yref)
     h = O.chain_glue(ya, O.unrotate_outputs(zb, sb) if product else None)
     for s, xop in zip(nxt, xops):
         parity(decode_xop(xop.cpu().numpy(), M, T).astype(np.float64), O.rotate_activations(h, s))
     for z in zn:
         assert torch.count_nonzero(z).item() == 0
+    nest.error_check()
+
+
+def test_rotate_group_matches_single_calls(dev):
+    """nest_rotate_group: three operands of one input plus cleared accumulators, and two
+    output rotations, each equal to the single-call result."""
+    T, K = 9, 5376
+    xb, xv = synth.activations(T, K, 5)
+    x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    signs = [to_dev(synth.signs(K, 40 + j), torch, dev) for j in range(3)]
+    ops = [nest.new_xop(K, T, dev).zero_() for _ in range(3)]          # padding tokens stay 0
+    zs = [torch.full((T, 777 + j), 3.0, device=dev) for j in range(3)]
+    nest.rotate_group([x] * 3, signs, 0, x_ops=ops, zero=zs)
+    for s, op, z in zip(signs, ops, zs):
+        one = nest.new_xop(K, T, dev).zero_()
+        nest.rotate(x, s, 0, x_op=one)
+        assert torch.equal(op[:one.numel()], one)
+        assert torch.count_nonzero(z).item() == 0
+    M = [8192, 3840]
+    zin = [torch.randn((T, m), device=dev) for m in M]
+    so = [to_dev(synth.signs(m, 50 + j), torch, dev) for j, m in enumerate(M)]
+    ys = [torch.empty((T, m), device=dev) for m in M]
+    nest.rotate_group(zin, so, 1, ys=ys)
+    for z, s, y in zip(zin, so, ys):
+        ref = torch.empty_like(y)
+        nest.rotate(z, s, 1, y=ref)
+        assert torch.equal(y, ref)
+    nest.error_check()
 
 
 SMALL = dict(hidden=512, inter=1024, q=512, kv=256)
