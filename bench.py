@@ -36,6 +36,7 @@ METRIC = "verify GEMM effective HBM GB/s and µs/layer at T=16 (vs T=1), % of 8 
 WORKLOAD = "mlp_triplet_4b"
 BITS = 7
 T_VERIFY, T_DRAFT = 16, 1
+SWEEP_T = (1, 4, 8, 16, 32, 64)
 
 
 def lin_bytes(M, K, T, bits):
@@ -295,6 +296,39 @@ def run_gpu(args, rank, world):
                      "launches": n_launch}
     hbm, src = peaks()
 
+    # GEMM-only sweep over T (draft and verify), same copies and launch groups
+    sweep = []
+    if not args.no_sweep:
+        for T in SWEEP_T:
+            sx = {k: nest.new_xop(l.K, T, dev) for k, l in enumerate(layers[0])}
+            sz = {k: torch.zeros((T, l.M), dtype=torch.float32, device=dev) for k, l in enumerate(layers[0])}
+            for k, l in enumerate(layers[0]):
+                b, _ = synth.activations(T, l.K, wl.x_seed + 7 * T + k)
+                nest.rotate(torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16), l.sign_in, 0,
+                            x_op=sx[k])
+            rec = {"T": T}
+            for verify in (False, True):
+                def fn():
+                    for trip in layers:
+                        for grp in groups:
+                            nest.gemm_group([trip[k] for k in grp], [sx[k] for k in grp], T, verify,
+                                            zs=[sz[k] for k in grp])
+                with torch.cuda.stream(stream):
+                    fn()
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        fn()
+                reps = 20
+                per = timed(g, reps, 3) / reps * 1e3 / n_lin
+                by = sum(lin_bytes(L.M, L.K, T, BITS if verify else 0) for L in layers[0]) / 3
+                key = "verify" if verify else "draft"
+                rec[key + "_us"] = per
+                rec[key + "_GBps"] = by / (per * 1e-6) / 1e9
+                del g
+            sweep.append(rec)
+        nest.error_check()
+
     # end to end through the public API: pinned host inputs in, the last verify output back
     host_x = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in xs.items()}
     for k in xs:
@@ -355,6 +389,7 @@ def run_gpu(args, rank, world):
                          "achieved": ach,
                          "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": src,
                          "traffic": None},
+            "sweep": sweep,
             "cpu_baseline": cpu,
             "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -486,6 +521,7 @@ def main():
     ap.add_argument("--impl", default="nest", choices=["nest", "reference"])
     ap.add_argument("--copies", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the GEMM-only sweep over T")
     ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "decoder_31b", "stack_31b"],
                     help="mlp_triplet_4b (default, the metric's workload), one chained 31B-class layer, "
                          "or the 60-layer 31B-class speculative cycle")

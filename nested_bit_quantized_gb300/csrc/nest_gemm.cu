@@ -29,6 +29,8 @@
 // tensor memory and starts streaming weights before the previous kernel in the
 // stream has finished; it waits for it (griddepcontrol.wait) only before it
 // reads the activation operand or touches z.
+#include <cstdlib>
+
 #include "nest_device.cuh"
 #include "nest_internal.h"
 
@@ -447,6 +449,407 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
     if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// Register-fragment GEMM for few tokens (T <= 8 * NT): mma.sync m16n8k16.
+//
+// With N = 8..16 tokens a tcgen05.mma of 128 x N x 16 costs a fixed issue time
+// that does not shrink with N, and one thread issues all of a CTA's MMAs.  Here
+// every warp decodes its weights straight into mma.sync A fragments (no tensor
+// memory, no MMA thread, no hand-off), so the weight rate is set by the decode
+// ALU work and the memory pipe.
+//
+// K order inside a fragment.  mma.sync sums over its 16 k indices in any order,
+// so the k index a thread's fragment slot stands for may be any column, as long
+// as the B fragment uses the same one.  Thread (g, q) of a warp (g = lane / 4,
+// q = lane % 4) takes, in k-step s of half h, the four columns 4Q .. 4Q+3 with
+// Q = 16h + 4q + s.  In the packed unit those are exactly the four codes that
+// word q of the row's half-h base vector holds at bit offset 2s, and residual
+// word Q - 16h; the B fragment is x'[token][4Q .. 4Q+3], eight contiguous bytes
+// of the operand.  So the kernel reads the same packed layout and operand as
+// the tcgen05 kernel, each byte once.
+//
+// Scales are applied in fp32 per (row, group): the base fragment holds the
+// unscaled fp16 levels, the residual fragment the integer codes q (exact in
+// fp16), each summed into its own fp32 accumulator by the MMA, then
+//   z += s_b * sum(L[c] x') + s_r * sum(q x').
+//
+// Copies.  A 1-D bulk copy costs a CTA about the same time whether it moves 2 KB
+// or 8 KB, so a copy of one 4 KB unit caps a CTA far below its share of HBM
+// bandwidth.  A stage therefore holds up to KU consecutive units of one row tile
+// (contiguous in the packed buffers and, group after group, in the operand), each
+// part fetched by one copy.  With T <= 8 the activation is not staged at all:
+// the B fragments are read from global memory, the next unit's while the current
+// one is decoded, so the only copies are the weights'.
+//
+// Pipeline: one producer warp fills a ring of S stages.  Two teams of four warps
+// take alternate units of each stage; every compute warp waits for every stage in
+// order and releases it, so each barrier phase is waited in order by the same
+// warps.  Warp w of a team owns rows 32w .. 32w+31 of a unit (two 16-row slabs);
+// partial sums of a row tile are added into z with fp32 reductions when the
+// team's next unit starts another tile.
+// ---------------------------------------------------------------------------
+
+template <int BITS, int NT>
+struct RfCfg {
+    static constexpr int kCtasPerSm = NT >= 4 ? 1 : 2;       // 32 tokens need the registers of a whole SM
+    static constexpr int kNB = NT < 2 ? 2 : NT;              // operand token blocks (n_pad / 8)
+    static constexpr bool kStageX = NT >= 2;                 // T <= 8 reads its B fragments from global memory
+    static constexpr int kXBytes = kStageX ? 2048 * kNB : 0; // one group of the operand
+    static constexpr int kResUnit = resid_unit_bytes(BITS);
+    static constexpr int kUnit = kBaseUnit + kResUnit + kXBytes;
+    static constexpr int kSmemBudget = kCtasPerSm == 1 ? 220 * 1024 : 110 * 1024;
+    static constexpr int kAvail = kSmemBudget - 512;
+    static constexpr int kKURaw = kAvail / (4 * kUnit);      // room for two stages per team
+    static constexpr int kKU = kKURaw > 4 ? 4 : (kKURaw < 1 ? 1 : kKURaw);   // units per stage
+    static constexpr int kStageBytes = kKU * kUnit;
+    static constexpr int kStagesRaw = kAvail / kStageBytes;
+    static constexpr int kStages = (kStagesRaw > 8 ? 8 : kStagesRaw) & ~1;   // even: a stage keeps its team
+    static constexpr int kResOff = kKU * kBaseUnit;          // parts of a stage: bases, residuals, operand
+    static constexpr int kXOff = kResOff + kKU * kResUnit;
+    static constexpr int kTeams = 2;
+    static constexpr int kWarpsPerTeam = 4;
+    static constexpr int kComputeWarps = kTeams * kWarpsPerTeam;
+    static constexpr int kProducerWarp = kComputeWarps;
+    static constexpr int kThreads = 32 * (kComputeWarps + 1);
+    static constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStages * 8 + 16;
+    static_assert(kStages >= 2 * kTeams, "stage too large");
+    static_assert(kStageBytes % 128 == 0 && kResOff % 16 == 0 && kXOff % 16 == 0, "stage alignment");
+    static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
+};
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ld_cg_v4(const void* ptr) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
+    return v;
+}
+
+// Residual words of one row and half for thread q: everything the four k-steps need.
+template <int BITS>
+struct ResidWords {
+    uint32_t w[4];
+    __device__ __forceinline__ void load(const uint8_t* sr, int r, int h, int q) {
+        if constexpr (BITS == 8) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sr + ((4 * h + q) * kRows + r) * 16);
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        } else if constexpr (BITS == 6 || BITS == 7) {
+            const uint2 lo = *reinterpret_cast<const uint2*>(sr + ((2 * h + (q >> 1)) * kRows + r) * 16 + 8 * (q & 1));
+            w[0] = lo.x;
+            w[1] = lo.y;
+            w[2] = *reinterpret_cast<const uint32_t*>(sr + ((4 + h) * kRows + r) * 16 + 4 * q);
+            w[3] = BITS == 7 ? *reinterpret_cast<const uint32_t*>(sr + (6 * kRows + r) * 16 + 8 * h + 4 * (q >> 1)) : 0u;
+        }
+    }
+    // offset-binary residual codes of columns 4Q .. 4Q+3, Q = 16h + 4q + s, one per byte
+    __device__ __forceinline__ uint32_t codes(int s, int q) const {
+        if constexpr (BITS == 8) {
+            return w[s];
+        } else {
+            const uint32_t lo = ((s < 2 ? w[0] : w[1]) >> (4 * (s & 1))) & 0x0F0F0F0Fu;
+            const uint32_t ms = (s < 2 ? (w[2] << (4 - 2 * s)) : (w[2] >> (2 * s - 4))) & 0x30303030u;
+            uint32_t u = lo | ms;
+            if constexpr (BITS == 7) {
+                const int ph = 4 * (q & 1) + s;
+                u |= (ph < 7 ? (w[3] << (6 - ph)) : (w[3] >> 1)) & 0x40404040u;
+            }
+            return u;
+        }
+    }
+};
+
+// Units in the chunk that starts at cursor c: at most ku, at most `left`, never past the row tile.
+__device__ __forceinline__ int chunk_len(const GemmArgs& p, const UnitCursor& c, int left, int ku) {
+    const int in_tile = p.task[c.k].G - c.g;
+    const int l = left < ku ? left : ku;
+    return l < in_tile ? l : in_tile;
+}
+
+template <int BITS, int NT>
+__global__ void __launch_bounds__(RfCfg<BITS, NT>::kThreads, RfCfg<BITS, NT>::kCtasPerSm)
+k_nest_rf(const __grid_constant__ GemmArgs p) {
+    using C = RfCfg<BITS, NT>;
+    constexpr int S = C::kStages, KU = C::kKU;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S);
+    auto stage = [&](int s) { return smem + s * C::kStageBytes; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), C::kWarpsPerTeam); }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    grid_dep_launch_dependents();
+
+    const long long units = p.units;
+    const int grid = gridDim.x;
+    const long long u0 = unit_begin(blockIdx.x, units, grid);
+    const int n = (int)(unit_begin(blockIdx.x + 1, units, grid) - u0);
+    UnitCursor start;
+    start.init(p, u0);
+
+    if (warp == C::kProducerWarp) {
+        // chunk j holds units [i, i + kc) of this CTA, starting at cursor c
+        auto issue_w = [&](int j, const UnitCursor& c, int kc) {
+            const int s = j % S;
+            const GemmTask& t = p.task[c.k];
+            const long long lu = c.local(p);
+            mbar_arrive_expect_tx(full(s), kc * C::kUnit);
+            bulk_g2s(smem_u32(stage(s)), t.base + lu * kBaseUnit, kc * kBaseUnit, full(s));
+            if constexpr (BITS != 0)
+                bulk_g2s(smem_u32(stage(s) + C::kResOff), t.resid + lu * C::kResUnit, kc * C::kResUnit, full(s));
+        };
+        auto issue_x = [&](int j, const UnitCursor& c, int kc) {
+            if constexpr (C::kStageX)
+                bulk_g2s(smem_u32(stage(j % S) + C::kXOff), p.task[c.k].xop + (size_t)c.g * (C::kXBytes / 2),
+                         kc * C::kXBytes, full(j % S));
+        };
+        UnitCursor cw = start;
+        int i = 0, j = 0;
+        while (j < S && i < n) {             // weights do not depend on the previous kernel: start them now
+            const int kc = chunk_len(p, cw, n - i, KU);
+            if (lane == 0) issue_w(j, cw, kc);
+            for (int u = 0; u < kc; ++u) cw.next(p);
+            i += kc;
+            ++j;
+        }
+        grid_dep_wait();                     // the activation operand comes from the previous kernel
+        {
+            UnitCursor cx = start;
+            int ii = 0;
+            for (int jj = 0; jj < j; ++jj) {
+                const int kc = chunk_len(p, cx, n - ii, KU);
+                if (lane == 0) issue_x(jj, cx, kc);
+                for (int u = 0; u < kc; ++u) cx.next(p);
+                ii += kc;
+            }
+        }
+        uint64_t t_last = globaltimer();
+        while (i < n) {
+            bool ready = false;
+            if (lane == 0) ready = mbar_test_wait(empty(j % S), ((j / S) - 1) & 1);
+            if (__shfl_sync(0xffffffffu, ready, 0)) {
+                const int kc = chunk_len(p, cw, n - i, KU);
+                if (lane == 0) { issue_w(j, cw, kc); issue_x(j, cw, kc); }
+                for (int u = 0; u < kc; ++u) cw.next(p);
+                i += kc;
+                ++j;
+                t_last = globaltimer();
+            } else {
+                __nanosleep(64);
+                const bool stop = (*abort_flag != 0) || (globaltimer() - t_last > kWaitLimitNs);
+                if (__shfl_sync(0xffffffffu, stop, 0)) {
+                    if (lane == 0 && *abort_flag == 0) { *abort_flag = 1; atomicExch(&g_nest_error, 1); }
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+        // every issued copy has landed before the CTA may leave
+        for (int jj = j > S ? j - S : 0; jj < j; ++jj) warp_wait(full(jj % S), (jj / S) & 1, abort_flag, false);
+        return;
+    }
+
+    const int team = warp / C::kWarpsPerTeam, wq = warp % C::kWarpsPerTeam;
+    const int g = lane >> 2, q = lane & 3;
+    const int T = p.T;
+    uint32_t lut_lo, lut_hi;                  // unscaled fp16 levels: low bytes, high bytes
+    {
+        uint32_t hv[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) hv[c] = __half_as_ushort(__float2half_rn(level_f(c)));
+        lut_lo = (hv[0] & 0xFFu) | ((hv[1] & 0xFFu) << 8) | ((hv[2] & 0xFFu) << 16) | ((hv[3] & 0xFFu) << 24);
+        lut_hi = (hv[0] >> 8) | ((hv[1] >> 8) << 8) | ((hv[2] >> 8) << 16) | ((hv[3] >> 8) << 24);
+    }
+    const __half2 off2 = __float2half2_rn(1024.0f + (BITS ? (float)(1 << (BITS - 1)) : 0.0f));
+    float zacc[2][NT][4];
+#pragma unroll
+    for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) zacc[sl][nt][e] = 0.0f;
+
+    grid_dep_wait();                          // the operand and z come from / are cleared by the previous kernel
+
+    // T <= 8: B fragments x'[g][4Q .. 4Q+7] (token block 0) straight from global memory
+    auto load_bx = [&](const uint16_t* xop, int grp, uint4 (&dst)[2][2]) {
+        const uint8_t* xg = reinterpret_cast<const uint8_t*>(xop) + (size_t)grp * 4096;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp)
+                dst[h][pp] = g < T ? ld_cg_v4(xg + ((8 * h + 2 * q + pp) * 16 + g) * 16) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto advance = [&](UnitCursor& c, int m) {
+        for (int u = 0; u < m; ++u) c.next(p);
+    };
+    uint4 bxg[2][2];
+
+    // Chunks go to the teams in turn (chunk j -> team j % 2); S is even, so a stage always
+    // belongs to the same team.  cj / i: cursor and unit index of chunk j's first unit.
+    UnitCursor cj = start;
+    int i = 0, j = 0;
+    if constexpr (!C::kStageX) {
+        UnitCursor c0 = start;
+        if (team == 1 && n > 0) advance(c0, chunk_len(p, start, n, KU));
+        if (team == 0 ? n > 0 : chunk_len(p, start, n, KU) < n) load_bx(p.task[c0.k].xop, c0.g, bxg);
+    }
+    while (i < n) {
+        const int kc = chunk_len(p, cj, n - i, KU);
+        UnitCursor c1 = cj;
+        advance(c1, kc);
+        const int i1 = i + kc;
+        if ((j % C::kTeams) == team) {
+            const int s_ = j % S;
+            if (!warp_wait(full(s_), (j / S) & 1, abort_flag)) break;
+            // the team's next chunk, j + 2: where its partial sums go, and its first operand block
+            const int kc1 = i1 < n ? chunk_len(p, c1, n - i1, KU) : 0;
+            UnitCursor c2 = c1;
+            advance(c2, kc1);
+            const bool has_next = i1 + kc1 < n;
+            const bool flush = !has_next || c2.k != cj.k || c2.tile != cj.tile;
+            const GemmTask& task = p.task[cj.k];
+            for (int u = 0; u < kc; ++u) {
+                uint4 bxn[2][2];
+                if constexpr (!C::kStageX) {
+                    if (u + 1 < kc) load_bx(task.xop, cj.g + u + 1, bxn);
+                    else if (has_next) load_bx(p.task[c2.k].xop, c2.g, bxn);
+                }
+                const uint8_t* sb = stage(s_) + u * kBaseUnit;
+                const uint8_t* sr = stage(s_) + C::kResOff + u * C::kResUnit;
+                const uint8_t* sx = stage(s_) + C::kXOff + u * C::kXBytes;
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    const int r0 = 32 * wq + 16 * sl + g, r1 = r0 + 8;
+                    uint32_t bw0[2], bw1[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        bw0[h] = *reinterpret_cast<const uint32_t*>(sb + (h * kRows + r0) * 16 + 4 * q);
+                        bw1[h] = *reinterpret_cast<const uint32_t*>(sb + (h * kRows + r1) * 16 + 4 * q);
+                    }
+                    const float sb0 = __half2float(*reinterpret_cast<const __half*>(sb + 4096 + 2 * r0));
+                    const float sb1 = __half2float(*reinterpret_cast<const __half*>(sb + 4096 + 2 * r1));
+                    float sr0 = 0.0f, sr1 = 0.0f;
+                    if constexpr (BITS != 0) {
+                        sr0 = __half2float(*reinterpret_cast<const __half*>(sr + 2048 * BITS + 2 * r0));
+                        sr1 = __half2float(*reinterpret_cast<const __half*>(sr + 2048 * BITS + 2 * r1));
+                    }
+                    float db[NT][4], dr[NT][4];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) { db[nt][e] = 0.0f; dr[nt][e] = 0.0f; }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        ResidWords<BITS> rw0, rw1;
+                        if constexpr (BITS != 0) { rw0.load(sr, r0, h, q); rw1.load(sr, r1, h, q); }
+#pragma unroll
+                        for (int pp = 0; pp < 2; ++pp) {
+                            // B fragments of k-steps 2pp and 2pp+1: x'[8nt + g][4Q .. 4Q+7], Q = 16h + 4q + 2pp
+                            uint4 bx[NT];
+                            if constexpr (C::kStageX) {
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    bx[nt] = *reinterpret_cast<const uint4*>(
+                                        sx + (((8 * h + 2 * q + pp) * C::kNB + nt) * 8 + g) * 16);
+                            } else {
+                                bx[0] = bxg[h][pp];
+                            }
+#pragma unroll
+                            for (int s2 = 0; s2 < 2; ++s2) {
+                                const int s = 2 * pp + s2;
+                                const uint32_t v0 = (bw0[h] >> (2 * s)) & 0x03030303u;
+                                const uint32_t v1 = (bw1[h] >> (2 * s)) & 0x03030303u;
+                                const uint32_t sel0 = v0 * 0x11u + 0x40404040u, sel1 = v1 * 0x11u + 0x40404040u;
+                                const uint32_t a0 = prmt(lut_lo, lut_hi, sel0), a2 = prmt(lut_lo, lut_hi, sel0 >> 16);
+                                const uint32_t a1 = prmt(lut_lo, lut_hi, sel1), a3 = prmt(lut_lo, lut_hi, sel1 >> 16);
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    mma16816(db[nt], a0, a1, a2, a3, s2 ? bx[nt].z : bx[nt].x, s2 ? bx[nt].w : bx[nt].y);
+                                if constexpr (BITS != 0) {
+                                    const uint32_t u0 = rw0.codes(s, q), u1 = rw1.codes(s, q);
+                                    const uint32_t q0 = h2_as_u32(__hsub2(u32_as_h2(prmt(u0, 0x64646464u, 0x5140u)), off2));
+                                    const uint32_t q2 = h2_as_u32(__hsub2(u32_as_h2(prmt(u0, 0x64646464u, 0x7362u)), off2));
+                                    const uint32_t q1 = h2_as_u32(__hsub2(u32_as_h2(prmt(u1, 0x64646464u, 0x5140u)), off2));
+                                    const uint32_t q3 = h2_as_u32(__hsub2(u32_as_h2(prmt(u1, 0x64646464u, 0x7362u)), off2));
+#pragma unroll
+                                    for (int nt = 0; nt < NT; ++nt)
+                                        mma16816(dr[nt], q0, q1, q2, q3, s2 ? bx[nt].z : bx[nt].x, s2 ? bx[nt].w : bx[nt].y);
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        zacc[sl][nt][0] += sb0 * db[nt][0] + sr0 * dr[nt][0];
+                        zacc[sl][nt][1] += sb0 * db[nt][1] + sr0 * dr[nt][1];
+                        zacc[sl][nt][2] += sb1 * db[nt][2] + sr1 * dr[nt][2];
+                        zacc[sl][nt][3] += sb1 * db[nt][3] + sr1 * dr[nt][3];
+                    }
+                }
+                if constexpr (!C::kStageX) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int pp = 0; pp < 2; ++pp) bxg[h][pp] = bxn[h][pp];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(s_));     // this warp is done with the stage
+            if (flush) {
+                const int M = task.M;
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    const int m0 = cj.tile * kRows + 32 * wq + 16 * sl + g, m1 = m0 + 8;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int t0 = 8 * nt + 2 * q, t1 = t0 + 1;
+                        if (m0 < M) {
+                            if (t0 < T) atomicAdd(task.z + (size_t)t0 * M + m0, zacc[sl][nt][0]);
+                            if (t1 < T) atomicAdd(task.z + (size_t)t1 * M + m0, zacc[sl][nt][1]);
+                        }
+                        if (m1 < M) {
+                            if (t0 < T) atomicAdd(task.z + (size_t)t0 * M + m1, zacc[sl][nt][2]);
+                            if (t1 < T) atomicAdd(task.z + (size_t)t1 * M + m1, zacc[sl][nt][3]);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) zacc[sl][nt][e] = 0.0f;
+                    }
+                }
+            }
+        }
+        cj = c1;
+        i = i1;
+        ++j;
+    }
+}
+
+template <int BITS, int NT>
+cudaError_t launch_rf(const GemmArgs& a, int grid, cudaStream_t stream) {
+    using C = RfCfg<BITS, NT>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k_nest_rf<BITS, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch_pdl(k_nest_rf<BITS, NT>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, a);
+}
+
 template <int BITS, int NP>
 cudaError_t launch_t(const GemmArgs& a, int grid, cudaStream_t stream) {
     using C = Cfg<BITS, NP>;
@@ -460,8 +863,27 @@ cudaError_t launch_t(const GemmArgs& a, int grid, cudaStream_t stream) {
     return launch_pdl(k_nest_gemm<BITS, NP>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, a);
 }
 
+// Kernel choice, from measurements on GB300 (a 128 x N x 16 tcgen05.mma costs a
+// fixed ~50 cycles to issue whatever N is; mma.sync m16n8k16 runs ~0.47 per cycle
+// per SM): the draft (base only) at T <= 8 on the register-fragment kernel, where
+// the 2-bit decode and not the MMA issue bounds it; everything else on tcgen05,
+// which is faster for the verify at every T.  NEST_GEMM_PATH=tc or =rf in the
+// environment forces one kernel (rf up to 32 tokens), for measuring one against
+// the other.
+int path_override() {
+    const char* e = getenv("NEST_GEMM_PATH");
+    return (e && e[0] == 't') ? 1 : (e && e[0] == 'r') ? 2 : 0;
+}
+
 template <int BITS>
 cudaError_t launch_bits(const GemmArgs& a, int grid, cudaStream_t stream) {
+    const int ov = path_override();
+    const bool rf = ov == 2 ? a.T <= 32 : (ov == 0 && BITS == 0 && a.T <= 8);
+    if (rf) {
+        if (a.T <= 8) return launch_rf<BITS, 1>(a, grid, stream);
+        if (a.T <= 16) return launch_rf<BITS, 2>(a, grid, stream);
+        return launch_rf<BITS, 4>(a, grid, stream);
+    }
     if (a.T <= 16) return launch_t<BITS, 16>(a, grid, stream);
     if (a.T <= 32) return launch_t<BITS, 32>(a, grid, stream);
     return launch_t<BITS, 64>(a, grid, stream);

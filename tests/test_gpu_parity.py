@@ -186,6 +186,25 @@ def test_grouped_gemm_and_linear_parity(dev, bits):
                 parity(y.cpu().numpy(), O.forward(q, so, si, xv, verify)["y"])
 
 
+@pytest.mark.parametrize("bits", [0, 6, 7, 8])
+def test_register_fragment_and_tcgen05_paths(dev, bits, monkeypatch):
+    """Both GEMM kernels on the same inputs: the register-fragment (mma.sync) kernel that
+    serves T <= 16 by default, forced up to T = 32, and the tcgen05 kernel forced down to
+    T = 1; each against the oracle."""
+    M, K = 1280, 2560
+    W, s_o, s_i, q = ref_layer(M, K, bits or 7, seed=5)
+    layer = dev_layer(q, bits or 7, s_o, s_i, dev)
+    verify = bits != 0
+    for T in (1, 3, 8, 9, 16, 17, 32):
+        x, xv = bf16_x(T, K, 90 + T, dev)
+        ref = O.forward(q, s_o, s_i, xv, verify)["z"]
+        for path in ("rf", "tc"):
+            monkeypatch.setenv("NEST_GEMM_PATH", path)
+            parity(run_gemm(layer, x, verify, dev), ref)
+    monkeypatch.delenv("NEST_GEMM_PATH")
+    nest.error_check()
+
+
 def _close(a, b, rel=1e-6):
     """Equal up to the order of the fp32 additions of the split K range."""
     scale = np.sqrt(np.mean(np.asarray(b, np.float64) ** 2))
