@@ -37,6 +37,22 @@ WORKLOAD = "mlp_triplet_4b"
 BITS = 7
 T_VERIFY, T_DRAFT = 16, 1
 SWEEP_T = (1, 4, 8, 16, 32, 64)
+# DRAM bytes per linear of the roofline kernel, from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum of a grouped gate+up verify launch at T=16, divided by its two
+# linears).  Valid only for the kernel source it was taken on: reported as null otherwise.
+NCU_TRAFFIC = {"src": "nested_bit_quantized_gb300/csrc/nest_gemm.cu",
+               "sha256": "e0557ee2d6dd7fb4c01cd409f5bc940ca92a1d12173d204aa4ebb6cc005afad2",
+               "bytes_per_linear": (59.045120e6 + 0.092928e6) / 2}
+
+
+def ncu_traffic():
+    import hashlib
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), NCU_TRAFFIC["src"])
+    try:
+        digest = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return NCU_TRAFFIC["bytes_per_linear"] if digest == NCU_TRAFFIC["sha256"] else None
 
 
 def lin_bytes(M, K, T, bits):
@@ -388,7 +404,8 @@ def run_gpu(args, rank, world):
             "roofline": {"bound": "hbm", "kernel": "k_nest_gemm<7,16> (verify, T=16; gate+up grouped, down alone)",
                          "achieved": ach,
                          "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": src,
-                         "traffic": None},
+                         "traffic": ncu_traffic(), "traffic_unit": "DRAM bytes per linear (ncu)",
+                         "algorithmic_bytes_per_linear": v16["bytes_per_gemm"]},
             "sweep": sweep,
             "cpu_baseline": cpu,
             "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
