@@ -342,3 +342,113 @@ def decoder_layer_forward(lin: Dict[str, tuple], x: np.ndarray, verify: bool) ->
     out["down"] = fwd("down", chain_glue(out["gate"], out["up"]))
     out["next"] = chain_glue(out["down"])
     return out
+
+
+# ----------------------------------------------------------------------------
+# BitNest W4/W8 nested weights (BitNest: Bit-Nested Speculative Decoding for
+# Memory-Efficient LLM Inference Acceleration, Section 3.2 and Appendix A.1,
+# Eq. (5)-(10); dual-plane storage, Section 3.3)
+# ----------------------------------------------------------------------------
+
+W4_QMIN, W4_QMAX = -8, 7
+
+
+def quantize_w4(Wr: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """W4 base, Eq. (5): group-wise (g = 128) signed 4-bit codes q4 in [-8, 7]
+    and a scale s4 per (row, group), so that W_draft = q4 * s4 (Eq. (6)).
+
+    The paper builds the base with GPTQ, which needs calibration data; the RTN
+    base is taken instead (a reading): s4 = fp16(max|W'| / 7), the symmetric
+    rule the paper states for its KV cache (Eq. (11)), and q4 = clip(rint(W'/s4),
+    -8, 7) with round-half-to-even.  A zero group gets s4 = 0 and q4 = 0.
+
+    Returns (q4 int8 [M][K], s4 float16 [M][K/128])."""
+    Wr = np.asarray(Wr, dtype=np.float64)
+    M, K = Wr.shape
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 128")
+    G = K // GROUP
+    blocks = Wr.reshape(M, G, GROUP)
+    amax = np.max(np.abs(blocks), axis=2)
+    s16 = to_fp16(amax / 7.0)
+    s = s16.astype(np.float64)
+    q = np.zeros((M, G, GROUP), dtype=np.int64)
+    nz = s > 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.clip(np.rint(blocks / s[:, :, None]), W4_QMIN, W4_QMAX)
+    q[nz] = r[nz].astype(np.int64)
+    return q.reshape(M, K).astype(np.int8), s16
+
+
+def refine_w4w8(Wr: np.ndarray, q4: np.ndarray, s4: np.ndarray) -> np.ndarray:
+    """Fixed-base refinement, Eq. (7)-(9): dW = W' - q4 s4 (Eq. (7)),
+    s_ref = s4 / 16 (Eq. (8)), and
+
+        q_r = clip(round(dW / s_ref), 0, 7)    where q4 == -8,
+        q_r = clip(round(dW / s_ref), -8, 7)   elsewhere             (Eq. (9)),
+
+    so that 16 q4 + q_r never leaves the signed 8-bit range.  round is
+    round-half-to-even (a reading); s_ref = 0 gives q_r = 0.
+
+    Returns q_r int8 [M][K]."""
+    Wr = np.asarray(Wr, dtype=np.float64)
+    M, K = Wr.shape
+    G = K // GROUP
+    dW = Wr - dequant_w4(q4, s4)
+    s_ref = (s4.astype(np.float64) / 16.0)[:, :, None]
+    lo = np.where(q4.reshape(M, G, GROUP) == W4_QMIN, 0, -8)
+    q = np.zeros((M, G, GROUP), dtype=np.int64)
+    nz = np.broadcast_to(s_ref > 0, (M, G, GROUP))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.rint(dW.reshape(M, G, GROUP) / s_ref)
+    r = np.minimum(np.maximum(r, lo), 7)
+    q[nz] = r[nz].astype(np.int64)
+    return q.reshape(M, K).astype(np.int8)
+
+
+def dequant_w4(q4: np.ndarray, s4: np.ndarray) -> np.ndarray:
+    """W_draft = q4 * s4, Eq. (6) (float64 [M][K])."""
+    M, K = q4.shape
+    G = K // GROUP
+    return (q4.reshape(M, G, GROUP).astype(np.float64) * s4.astype(np.float64)[:, :, None]).reshape(M, K)
+
+
+def dequant_w8(q4: np.ndarray, s4: np.ndarray, qr: np.ndarray) -> np.ndarray:
+    """W_target = (16 q4 + q_r) s_ref with s_ref = s4 / 16, Eq. (10) (float64 [M][K])."""
+    M, K = q4.shape
+    G = K // GROUP
+    c8 = 16 * q4.reshape(M, G, GROUP).astype(np.int64) + qr.reshape(M, G, GROUP).astype(np.int64)
+    return (c8.astype(np.float64) * (s4.astype(np.float64) / 16.0)[:, :, None]).reshape(M, K)
+
+
+def quantize_layer_w4w8(W: np.ndarray, s_o: np.ndarray, s_i: np.ndarray) -> Dict[str, np.ndarray]:
+    """Rotate (the same two-sided randomized Hadamard rotation as the 2-bit path,
+    standing in for the paper's folded function-preserving rotations), then the
+    W4 base and its fixed-base 4-bit refinement."""
+    Wr = rotate_weights(W, s_o, s_i)
+    q4, s4 = quantize_w4(Wr)
+    qr = refine_w4w8(Wr, q4, s4)
+    return {"Wr": Wr, "q4": q4, "s4": s4, "qr": qr}
+
+
+def forward_w4w8(layer: Dict[str, np.ndarray], s_o: np.ndarray, s_i: np.ndarray,
+                 x: np.ndarray, verify: bool) -> Dict[str, np.ndarray]:
+    """x' = H_i S_i x; draft z = W_draft x', verify z = W_target x' (rotated basis);
+    y = S_o H_o z.  The draft reads the base plane only (Section 3.3)."""
+    xr = rotate_activations(x, s_i)
+    W = dequant_w8(layer["q4"], layer["s4"], layer["qr"]) if verify else dequant_w4(layer["q4"], layer["s4"])
+    z = xr @ W.T
+    return {"x_rot": xr, "z": z, "y": unrotate_outputs(z, s_o)}
+
+
+def forward_rows_w4w8(rows: Dict[str, np.ndarray], xr: np.ndarray, verify: bool) -> np.ndarray:
+    """z for a subset of output rows, given x'."""
+    W = dequant_w8(rows["q4"], rows["s4"], rows["qr"]) if verify else dequant_w4(rows["q4"], rows["s4"])
+    return np.asarray(xr, np.float64) @ W.T
+
+
+def bits_per_weight_w4w8(verify: bool) -> float:
+    """Dual-plane storage (Section 3.3): the base plane holds 4 bits per weight plus
+    the fp16 group scale; the refinement plane 4 bits per weight and no scale
+    (s_ref is derived from s4)."""
+    return 4 + 16 / GROUP + (4 if verify else 0)

@@ -37,6 +37,10 @@ def _load():
         lib.ref_unpack_base.argtypes, lib.ref_unpack_base.restype = [P, I, I, P, P], None
         lib.ref_pack_resid.argtypes, lib.ref_pack_resid.restype = [P, P, I, I, I, P], I
         lib.ref_unpack_resid.argtypes, lib.ref_unpack_resid.restype = [P, I, I, I, P, P], I
+        lib.ref_w4_bytes.argtypes, lib.ref_w4_bytes.restype = [I, I], S
+        lib.ref_w4ref_bytes.argtypes, lib.ref_w4ref_bytes.restype = [I, I], S
+        lib.ref_pack_w4w8.argtypes, lib.ref_pack_w4w8.restype = [P, P, P, I, I, P, P], None
+        lib.ref_unpack_w4w8.argtypes, lib.ref_unpack_w4w8.restype = [P, P, I, I, P, P, P], None
         _lib = lib
     return _lib
 
@@ -87,3 +91,38 @@ def unpack_resid(packed: np.ndarray, M: int, K: int, bits: int):
     if _load().ref_unpack_resid(_ptr(packed), M, K, bits, _ptr(codes), _ptr(sc)):
         raise ValueError("bits must be 6, 7 or 8")
     return codes, sc
+
+
+def w4_bytes(M: int, K: int) -> int:
+    return int(_load().ref_w4_bytes(M, K))
+
+
+def w4ref_bytes(M: int, K: int) -> int:
+    return int(_load().ref_w4ref_bytes(M, K))
+
+
+def pack_w4w8(q4: np.ndarray, s4: np.ndarray, qr: np.ndarray | None):
+    """Dual-plane W4/W8 packing: returns (base plane bytes, refinement plane bytes or None)."""
+    q4 = np.ascontiguousarray(q4, dtype=np.int8)
+    sc = np.ascontiguousarray(np.asarray(s4).view(np.uint16))
+    M, K = q4.shape
+    base = np.empty(w4_bytes(M, K), dtype=np.uint8)
+    ref = None
+    qrp = None
+    if qr is not None:
+        qrp = np.ascontiguousarray(qr, dtype=np.int8)
+        ref = np.empty(w4ref_bytes(M, K), dtype=np.uint8)
+    _load().ref_pack_w4w8(_ptr(q4), _ptr(sc), _ptr(qrp) if qrp is not None else None, M, K, _ptr(base),
+                          _ptr(ref) if ref is not None else None)
+    return base, ref
+
+
+def unpack_w4w8(base: np.ndarray, ref: np.ndarray | None, M: int, K: int):
+    base = np.ascontiguousarray(base, dtype=np.uint8)
+    q4 = np.zeros((M, K), dtype=np.int8)
+    qr = np.zeros((M, K), dtype=np.int8)
+    sc = np.zeros((M, K // 128), dtype=np.uint16)
+    refp = np.ascontiguousarray(ref, dtype=np.uint8) if ref is not None else None
+    _load().ref_unpack_w4w8(_ptr(base), _ptr(refp) if refp is not None else None, M, K, _ptr(q4), _ptr(sc),
+                            _ptr(qr))
+    return q4, sc, (qr if ref is not None else None)

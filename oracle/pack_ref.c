@@ -187,3 +187,75 @@ int ref_unpack_resid(const uint8_t* packed, int M, int K, int bits, int8_t* code
         }
     return 0;
 }
+
+/*
+ * BitNest W4/W8 dual-plane storage (BitNest paper, Section 3.3: the base and the
+ * refinement codes in two independently packed 4-bit planes, N/2 bytes each for
+ * N weights, the refinement without scale metadata).  Same unit grid as above.
+ *
+ * W4 base unit (8448 bytes), stored value u4 = q4 + 8 (0..15):
+ *   bytes [0, 8192): a row's 64 bytes as 16 words, chunk-major (word w of row r at
+ *                    byte ((w/4)*128 + r)*16 + (w%4)*4); word w holds columns
+ *                    8w..8w+7, column 8w + 4h + q in bits 8q + 4h .. 8q + 4h + 3.
+ *   bytes [8192, 8448): fp16 s4 of row r at 8192 + 2r.
+ * Refinement unit (8192 bytes): the same nibble layout with u_r = q_r + 8.
+ * Rows past M hold q4 = q_r = 0 and scale 0.
+ */
+size_t ref_w4_unit_bytes(void) { return 8192 + 256; }
+size_t ref_w4ref_unit_bytes(void) { return 8192; }
+
+size_t ref_w4_bytes(int M, int K) { return n_tiles(M) * (size_t)(K / GROUP) * ref_w4_unit_bytes(); }
+size_t ref_w4ref_bytes(int M, int K) { return n_tiles(M) * (size_t)(K / GROUP) * ref_w4ref_unit_bytes(); }
+
+static void nib_put(uint8_t* unit, int r, int j, uint32_t u) {
+    int j8 = j % 8;
+    set_bits(unit, r, j / 8, 8 * (j8 % 4) + 4 * (j8 / 4), u & 15u);
+}
+
+static uint32_t nib_get(const uint8_t* unit, int r, int j) {
+    int j8 = j % 8;
+    return get_bits(unit, r, j / 8, 8 * (j8 % 4) + 4 * (j8 / 4), 15u);
+}
+
+void ref_pack_w4w8(const int8_t* q4, const uint16_t* s4, const int8_t* qr, int M, int K,
+                   uint8_t* base_out, uint8_t* ref_out) {
+    int G = K / GROUP;
+    memset(base_out, 0, ref_w4_bytes(M, K));
+    if (ref_out) memset(ref_out, 0, ref_w4ref_bytes(M, K));
+    for (size_t t = 0; t < n_tiles(M); ++t)
+        for (int g = 0; g < G; ++g) {
+            uint8_t* bu = base_out + (t * G + g) * ref_w4_unit_bytes();
+            uint8_t* ru = ref_out ? ref_out + (t * G + g) * ref_w4ref_unit_bytes() : NULL;
+            for (int r = 0; r < ROWS; ++r) {
+                size_t m = t * ROWS + r;
+                int valid = m < (size_t)M;
+                for (int j = 0; j < GROUP; ++j) {
+                    size_t i = m * K + (size_t)g * GROUP + j;
+                    nib_put(bu, r, j, (uint32_t)((valid ? q4[i] : 0) + 8));
+                    if (ru) nib_put(ru, r, j, (uint32_t)((valid ? qr[i] : 0) + 8));
+                }
+                uint16_t s = valid ? s4[m * G + g] : 0;
+                bu[8192 + 2 * r] = (uint8_t)s;
+                bu[8192 + 2 * r + 1] = (uint8_t)(s >> 8);
+            }
+        }
+}
+
+void ref_unpack_w4w8(const uint8_t* base, const uint8_t* ref, int M, int K, int8_t* q4, uint16_t* s4, int8_t* qr) {
+    int G = K / GROUP;
+    for (size_t t = 0; t < n_tiles(M); ++t)
+        for (int g = 0; g < G; ++g) {
+            const uint8_t* bu = base + (t * G + g) * ref_w4_unit_bytes();
+            const uint8_t* ru = ref ? ref + (t * G + g) * ref_w4ref_unit_bytes() : NULL;
+            for (int r = 0; r < ROWS; ++r) {
+                size_t m = t * ROWS + r;
+                if (m >= (size_t)M) continue;
+                for (int j = 0; j < GROUP; ++j) {
+                    size_t i = m * K + (size_t)g * GROUP + j;
+                    q4[i] = (int8_t)((int)nib_get(bu, r, j) - 8);
+                    if (ru) qr[i] = (int8_t)((int)nib_get(ru, r, j) - 8);
+                }
+                s4[m * G + g] = (uint16_t)(bu[8192 + 2 * r] | (bu[8192 + 2 * r + 1] << 8));
+            }
+        }
+}

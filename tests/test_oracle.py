@@ -418,3 +418,149 @@ def test_chain_glue_unit_rms_and_product():
     p = ya * yb
     assert np.allclose(hp, p / np.sqrt(np.mean(p * p, axis=1, keepdims=True)), rtol=2 ** -8, atol=0)
     assert np.array_equal(O.chain_glue(np.zeros((1, 128))), np.zeros((1, 128)))
+
+
+# ----------------------------------------------------------------------------
+# BitNest W4/W8 nested weights (BitNest paper, Section 3.2-3.3, Appendix A.1)
+# ----------------------------------------------------------------------------
+
+def _rotated(M, K, seed):
+    W = synth.weights(M, K, seed, "entries")
+    s_o, s_i = synth.sign_pair(M, K, seed + 1)
+    return O.rotate_weights(W, s_o, s_i)
+
+
+def test_w4_base_is_nearest_of_the_16_levels():
+    """Eq. (5): brute force over all 16 codes; the scale makes max|W'| land on +-7."""
+    Wr = _rotated(24, 256, 901)
+    q4, s4 = O.quantize_w4(Wr)
+    M, K = Wr.shape
+    s = np.repeat(s4.astype(np.float64), 128, axis=1)
+    cand = np.arange(-8, 8)[None, None, :] * s[:, :, None]
+    err = np.abs(Wr[:, :, None] - cand)
+    best = err.min(axis=2)
+    got = np.abs(Wr - q4.astype(np.float64) * s)
+    assert np.allclose(got, best, rtol=0, atol=1e-15)
+    amax = np.abs(Wr).reshape(M, 2, 128).max(axis=2)
+    assert np.all(np.abs(s4.astype(np.float64) * 7 - amax) <= amax * 2.0 ** -11)
+    assert q4.min() >= -7 and q4.max() <= 7        # symmetric RTN never needs -8
+    top = np.abs(Wr).reshape(M, 2, 128).argmax(axis=2)
+    assert np.all(np.abs(np.take_along_axis(q4.reshape(M, 2, 128).astype(int), top[:, :, None], 2)) == 7)
+
+
+def test_w4w8_refinement_is_nearest_allowed_code():
+    """Eq. (7)-(9): brute force over the allowed refinement codes, s_ref = s4 / 16."""
+    Wr = _rotated(16, 384, 903)
+    q4, s4 = O.quantize_w4(Wr)
+    qr = O.refine_w4w8(Wr, q4, s4)
+    dW = Wr - O.dequant_w4(q4, s4)
+    sref = np.repeat(s4.astype(np.float64) / 16, 128, axis=1)
+    cand = np.arange(-8, 8)[None, None, :] * sref[:, :, None]
+    best = np.abs(dW[:, :, None] - cand).min(axis=2)
+    assert np.allclose(np.abs(dW - qr * sref), best, rtol=0, atol=1e-15)
+    # the error is at most s_ref, and at most s_ref / 2 where no clip at +7 happened
+    E = np.abs(Wr - O.dequant_w8(q4, s4, qr))
+    assert np.all(E <= sref * (1 + 1e-12))
+    unclipped = dW / sref < 7.5
+    assert np.all(E[unclipped] <= sref[unclipped] / 2 * (1 + 1e-12))
+
+
+def test_w4w8_asymmetric_clip_at_minus_eight():
+    """Eq. (9): where q4 = -8 the refinement is clipped to [0, 7], so 16 q4 + q_r >= -128."""
+    s4 = np.full((1, 1), 0.5, dtype=np.float16)          # s_ref = 1/32
+    q4 = np.full((1, 128), -7, dtype=np.int8)
+    q4[0, :64] = -8
+    Wr = q4.astype(np.float64) * 0.5 - 3.2 / 32           # dW / s_ref = -3.2 everywhere
+    Wr[0, 10] = -8 * 0.5 + 5.4 / 32                       # dW / s_ref = +5.4 under q4 = -8
+    qr = O.refine_w4w8(Wr, q4, s4)
+    assert np.all(qr[0, :64][np.arange(64) != 10] == 0)    # clipped at 0
+    assert qr[0, 10] == 5
+    assert np.all(qr[0, 64:] == -3)                       # q4 > -8: ordinary rounding
+    # every admissible (q4, q_r) pair composes to a signed 8-bit code; the unclipped rule would not
+    codes = [16 * a + b for a in range(-8, 8) for b in (range(0, 8) if a == -8 else range(-8, 8))]
+    assert min(codes) == -128 and max(codes) == 119 and len(set(codes)) == len(codes)
+    assert 16 * -8 + -8 < -128
+
+
+def test_w8_target_identity_and_exact_subset():
+    """Eq. (10): q4 s4 + q_r s_ref == (16 q4 + q_r) s_ref exactly; q_r = 0 gives the draft."""
+    Wr = _rotated(8, 256, 905)
+    q4, s4 = O.quantize_w4(Wr)
+    qr = O.refine_w4w8(Wr, q4, s4)
+    sref = np.repeat(s4.astype(np.float64) / 16, 128, axis=1)
+    two_terms = O.dequant_w4(q4, s4) + qr.astype(np.float64) * sref
+    assert np.array_equal(two_terms, O.dequant_w8(q4, s4, qr))
+    assert np.array_equal(O.dequant_w8(q4, s4, np.zeros_like(qr)), O.dequant_w4(q4, s4))
+
+
+def test_w4w8_zero_group_and_storage():
+    Wr = _rotated(4, 256, 907)
+    Wr[1, 128:] = 0.0
+    q4, s4 = O.quantize_w4(Wr)
+    qr = O.refine_w4w8(Wr, q4, s4)
+    assert s4[1, 1] == 0 and np.all(q4[1, 128:] == 0) and np.all(qr[1, 128:] == 0)
+    # dual-plane storage (Section 3.3): N/2 bytes per plane, the scale only on the base
+    assert O.bits_per_weight_w4w8(False) == 4.125 and O.bits_per_weight_w4w8(True) == 8.125
+
+
+def test_w4w8_forward_bruteforce_and_error_order():
+    """Triple loop on a tiny case against the dense path, and the target's output error
+    is about 1/16 of the draft's (one extra 4-bit refinement of the same scale)."""
+    M, K, T = 16, 128, 3
+    W = synth.weights(M, K, 909, "entries")
+    s_o, s_i = synth.sign_pair(M, K, 910)
+    lay = O.quantize_layer_w4w8(W, s_o, s_i)
+    _, x = synth.activations(T, K, 911)
+    for verify in (False, True):
+        out = O.forward_w4w8(lay, s_o, s_i, x, verify)
+        Wd = O.dequant_w8(lay["q4"], lay["s4"], lay["qr"]) if verify else O.dequant_w4(lay["q4"], lay["s4"])
+        z = np.zeros((T, M))
+        for t in range(T):
+            for m in range(M):
+                z[t, m] = sum(Wd[m, k] * out["x_rot"][t, k] for k in range(K))
+        assert np.allclose(out["z"], z, rtol=1e-12, atol=1e-12)
+    M, K = 64, 512
+    W = synth.weights(M, K, 913, "entries")
+    s_o, s_i = synth.sign_pair(M, K, 914)
+    lay = O.quantize_layer_w4w8(W, s_o, s_i)
+    _, x = synth.activations(8, K, 915)
+    ref = x @ W.T
+    e4 = np.linalg.norm(O.forward_w4w8(lay, s_o, s_i, x, False)["y"] - ref)
+    e8 = np.linalg.norm(O.forward_w4w8(lay, s_o, s_i, x, True)["y"] - ref)
+    assert 8 < e4 / e8 < 32
+
+
+@pytest.mark.parametrize("M,K", [(128, 128), (200, 384), (1, 256)])
+def test_w4w8_pack_roundtrip(M, K):
+    rng = np.random.default_rng(M + K)
+    q4 = rng.integers(-8, 8, size=(M, K)).astype(np.int8)
+    qr = rng.integers(-8, 8, size=(M, K)).astype(np.int8)
+    s4 = rng.uniform(1e-3, 1e-1, size=(M, K // 128)).astype(np.float16)
+    base, ref = P.pack_w4w8(q4, s4, qr)
+    tiles = (M + 127) // 128
+    assert base.size == tiles * (K // 128) * 8448 and ref.size == tiles * (K // 128) * 8192
+    u4, us, ur = P.unpack_w4w8(base, ref, M, K)
+    assert np.array_equal(u4, q4) and np.array_equal(ur, qr) and np.array_equal(us, s4.view(np.uint16))
+    b2, r2 = P.pack_w4w8(q4, s4, None)
+    assert r2 is None and np.array_equal(b2, base)
+
+
+def test_w4w8_pack_hand_worked_examples():
+    """Nibble positions written out by hand from the layout description."""
+    M, K = 2, 128
+    q4 = np.zeros((M, K), dtype=np.int8)
+    qr = np.zeros((M, K), dtype=np.int8)
+    q4[0, 0] = 3        # u = 11: row 0, word 0, bits 0..3    -> byte 0 low nibble
+    q4[0, 4] = -2       # u = 6:  row 0, word 0, bits 4..7    -> byte 0 high nibble
+    q4[1, 9] = -8       # u = 0:  row 1, word 1, bits 8..11   -> byte (0*128+1)*16 + 4 + 1, low nibble
+    q4[0, 127] = 7      # u = 15: row 0, word 15 (chunk 3, word 3), bits 28..31 -> byte (3*128)*16 + 12 + 3
+    qr[1, 33] = 5       # u = 13: row 1, word 4 (chunk 1, word 0), bits 8..11 -> byte (128+1)*16 + 1
+    s4 = np.zeros((M, 1), dtype=np.float16)
+    s4[1, 0] = 1.0      # 0x3C00 at 8192 + 2
+    base, ref = P.pack_w4w8(q4, s4, qr)
+    assert base[0] == 0x6B
+    assert base[16 + 5] & 0x0F == 0x0 and base[16 + 5] >> 4 == 0x8
+    assert base[3 * 128 * 16 + 15] >> 4 == 0xF
+    assert ref[(128 + 1) * 16 + 1] & 0x0F == 0xD
+    assert base[8192 + 2] == 0x00 and base[8192 + 3] == 0x3C
+    assert base[17] == 0x88                      # untouched columns hold q = 0 (u = 8)
