@@ -55,9 +55,18 @@ def ncu_traffic():
     return NCU_TRAFFIC["bytes_per_linear"] if digest == NCU_TRAFFIC["sha256"] else None
 
 
+def bits_per_weight(bits):
+    """Algorithmic weight bits per weight.  bits: 0 = 2-bit base alone (draft), 6/7/8 = base +
+    b-bit residual (verify), 40 = W4 base alone (draft), 48 = W4 base + 4-bit refinement (verify)."""
+    if bits == 40:
+        return 4.125
+    if bits == 48:
+        return 8.125
+    return 2.125 + ((bits + 0.125) if bits else 0.0)
+
+
 def lin_bytes(M, K, T, bits):
-    w = M * K * (2.125 + ((bits + 0.125) if bits else 0.0)) / 8.0
-    return w + 2.0 * T * K + 4.0 * T * M
+    return M * K * bits_per_weight(bits) / 8.0 + 2.0 * T * K + 4.0 * T * M
 
 
 def weight_bytes(M, K, bits):
@@ -199,6 +208,8 @@ def run_gpu(args, rank, world):
 
     wl = synth.WORKLOADS[WORKLOAD]
     C = args.copies
+    w4w8 = args.codec == "w4w8"
+    DC, VC = (40, 48) if w4w8 else (0, BITS)      # byte accounting of the draft and verify passes
     # quantise and pack C copies of the triplet on the device
     layers = []
     work = None
@@ -210,10 +221,14 @@ def run_gpu(args, rank, world):
             s_o, s_i = synth.sign_pair(lin.M, lin.K, lin.sign_seed + 2 * c)
             if work is None or work.numel() < lin.M * lin.K:
                 work = torch.empty(lin.M * lin.K, dtype=torch.float64, device=dev)
-            q = nest.quantize(W, torch.from_numpy(s_o).to(dev), torch.from_numpy(s_i).to(dev), BITS,
-                              work=work[:lin.M * lin.K].view(lin.M, lin.K))
-            trip.append(nest.pack(q["base_codes"], q["base_scales"], q["resid_codes"], q["resid_scales"], BITS,
-                                  torch.from_numpy(s_o).to(dev), torch.from_numpy(s_i).to(dev)))
+            so, si = torch.from_numpy(s_o).to(dev), torch.from_numpy(s_i).to(dev)
+            if w4w8:
+                q = nest.quantize_w4w8(W, so, si, work=work[:lin.M * lin.K].view(lin.M, lin.K))
+                trip.append(nest.pack_w4w8(q["q4"], q["s4"], q["qr"], so, si))
+            else:
+                q = nest.quantize(W, so, si, BITS, work=work[:lin.M * lin.K].view(lin.M, lin.K))
+                trip.append(nest.pack(q["base_codes"], q["base_scales"], q["resid_codes"], q["resid_scales"], BITS,
+                                      so, si))
             del W, q
         layers.append(trip)
     del work
@@ -293,7 +308,7 @@ def run_gpu(args, rank, world):
         return ms
 
     n_lin = 3 * C
-    step_bytes = sum(lin_bytes(L.M, L.K, T_DRAFT, 0) + lin_bytes(L.M, L.K, T_VERIFY, BITS)
+    step_bytes = sum(lin_bytes(L.M, L.K, T_DRAFT, DC) + lin_bytes(L.M, L.K, T_VERIFY, VC)
                      for trip in layers for L in trip)
     with ClockSampler(local) as clk:
         ms = timed(graphs["step"], args.steps, args.warmup)
@@ -302,7 +317,7 @@ def run_gpu(args, rank, world):
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
 
     sub = {}
-    for name, T, bits in (("v16", T_VERIFY, BITS), ("v1", T_DRAFT, BITS), ("d1", T_DRAFT, 0)):
+    for name, T, bits in (("v16", T_VERIFY, VC), ("v1", T_DRAFT, VC), ("d1", T_DRAFT, DC)):
         reps = max(3, args.steps)
         tms = timed(graphs[name], reps, max(3, args.warmup)) / reps
         per = tms * 1e3 / n_lin                   # us per linear (all three linears move equal bytes)
@@ -337,7 +352,7 @@ def run_gpu(args, rank, world):
                         fn()
                 reps = 20
                 per = timed(g, reps, 3) / reps * 1e3 / n_lin
-                by = sum(lin_bytes(L.M, L.K, T, BITS if verify else 0) for L in layers[0]) / 3
+                by = sum(lin_bytes(L.M, L.K, T, VC if verify else DC) for L in layers[0]) / 3
                 key = "verify" if verify else "draft"
                 rec[key + "_us"] = per
                 rec[key + "_GBps"] = by / (per * 1e-6) / 1e9
@@ -390,9 +405,12 @@ def run_gpu(args, rank, world):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "config": {"workload": "mlp_triplet_4b: gate/up 9728x2560, down 2560x9728, 2-bit base + 7-bit "
-                                   "residual, g128 fp16 scales; draft T=1 then verify T=16 per step",
-                       "copies": C, "resident_weight_GB": C * sum(weight_bytes(l.M, l.K, BITS) for l in wl.linears) / 1e9,
+            "config": {"workload": ("mlp_triplet_4b: gate/up 9728x2560, down 2560x9728, "
+                                    + ("BitNest W4 base + 4-bit refinement (W8 target), g128 fp16 scales"
+                                       if w4w8 else "2-bit base + 7-bit residual, g128 fp16 scales")
+                                    + "; draft T=1 then verify T=16 per step"),
+                       "copies": C,
+                       "resident_weight_GB": C * sum(l.M * l.K * bits_per_weight(VC) / 8 for l in wl.linears) / 1e9,
                        "l2": f"inputs larger than L2: {C} distinct quantised triplet copies per pass",
                        "accumulate": "f32", "parallelism": f"replicas x{world}",
                        "launch_groups": "gate+up in one grouped launch (same input), down alone"},
@@ -401,10 +419,11 @@ def run_gpu(args, rank, world):
             "verify_T1": {"us_per_gemm": v1["us_per_gemm"], "GBps": v1["GBps"]},
             "t16_over_t1": v16["us_per_gemm"] / v1["us_per_gemm"],
             "draft_T1": {"us_per_gemm": d1["us_per_gemm"], "GBps": d1["GBps"]},
-            "roofline": {"bound": "hbm", "kernel": "k_nest_gemm<7,16> (verify, T=16; gate+up grouped, down alone)",
+            "roofline": {"bound": "hbm",
+                         "kernel": f"k_nest_gemm<{VC},16> (verify, T=16; gate+up grouped, down alone)",
                          "achieved": ach,
                          "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": src,
-                         "traffic": ncu_traffic(), "traffic_unit": "DRAM bytes per linear (ncu)",
+                         "traffic": None if w4w8 else ncu_traffic(), "traffic_unit": "DRAM bytes per linear (ncu)",
                          "algorithmic_bytes_per_linear": v16["bytes_per_gemm"]},
             "sweep": sweep,
             "cpu_baseline": cpu,
@@ -539,6 +558,9 @@ def main():
     ap.add_argument("--copies", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the GEMM-only sweep over T")
+    ap.add_argument("--codec", default="l2", choices=["l2", "w4w8"],
+                    help="weight codec of the default workload: l2 (2-bit base + 7-bit residual, the metric's) "
+                         "or w4w8 (BitNest W4 base + 4-bit refinement)")
     ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "decoder_31b", "stack_31b"],
                     help="mlp_triplet_4b (default, the metric's workload), one chained 31B-class layer, "
                          "or the 60-layer 31B-class speculative cycle")

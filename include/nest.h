@@ -64,15 +64,21 @@ typedef enum {
     NEST_ERR_TIMEOUT = 5        /* a kernel gave up waiting on a pipeline barrier (nest_error_check) */
 } nest_status;
 
+/* Weight codecs. */
+#define NEST_CODEC_L2 0   /* 2-bit Lloyd-Max base + b-bit uniform residual (POC recipe steps 2, 3) */
+#define NEST_CODEC_W4W8 1 /* BitNest W4 base + 4-bit refinement at s4/16, dual planes (BitNest 3.2, 3.3) */
+
 /* A packed layer.  Plain descriptor; the pointers are device pointers owned by the caller. */
 typedef struct {
     int32_t M;                  /* d_out, >= 1 */
     int32_t K;                  /* d_in, multiple of 128 */
-    int32_t resid_bits;         /* 6, 7 or 8; 0 = base only (draft-only layer) */
-    const uint8_t* base;        /* nest_base_bytes(M, K) bytes */
-    const uint8_t* resid;       /* nest_resid_bytes(M, K, resid_bits) bytes, or NULL if resid_bits == 0 */
+    int32_t resid_bits;         /* NEST_CODEC_L2: 6, 7 or 8; NEST_CODEC_W4W8: 4; 0 = base only (draft-only layer) */
+    const uint8_t* base;        /* nest_base_bytes(M, K) (L2) or nest_w4_base_bytes(M, K) (W4W8) bytes */
+    const uint8_t* resid;       /* nest_resid_bytes(M, K, resid_bits) (L2) or nest_w4_ref_bytes(M, K) (W4W8)
+                                   bytes, or NULL if resid_bits == 0 */
     const int8_t* sign_out;     /* S_o, M entries of +-1 */
     const int8_t* sign_in;      /* S_i, K entries of +-1 */
+    int32_t codec;              /* NEST_CODEC_L2 (0, the default of a zeroed descriptor) or NEST_CODEC_W4W8 */
 } nest_layer;
 
 /* Human-readable name of a status. */
@@ -89,6 +95,11 @@ size_t nest_base_bytes(int32_t M, int32_t K);
 
 /* Bytes of the packed residual buffer: ceil(M/128) * (K/128) * (2048*bits + 256). */
 size_t nest_resid_bytes(int32_t M, int32_t K, int32_t bits);
+
+/* BitNest W4/W8 dual planes (NEST_CODEC_W4W8): ceil(M/128) * (K/128) units of 8448 bytes
+ * (4-bit base codes + fp16 scales s4) and of 8192 bytes (4-bit refinement codes). */
+size_t nest_w4_base_bytes(int32_t M, int32_t K);
+size_t nest_w4_ref_bytes(int32_t M, int32_t K);
 
 /* Bytes of the activation operand for K columns and T tokens: (K/128) * 256 * Np. */
 size_t nest_xop_bytes(int32_t K, int32_t T);
@@ -137,6 +148,27 @@ nest_status nest_pack(const uint8_t* base_codes, const uint16_t* base_scales,
                       int32_t M, int32_t K, int32_t bits,
                       uint8_t* base_out, uint8_t* resid_out, void* stream);
 
+/* BitNest W4/W8 offline quantizer (BitNest paper, Eq. (5)-(10)): rotate W as
+ * nest_quantize does, then per (row, 128-group) s4 = fp16(max|W'| / 7), q4 =
+ * clip(rint(W'/s4), -8, 7) (an RTN base: GPTQ needs calibration data), and
+ * q_r = clip(rint((W' - q4 s4) / (s4/16)), q4 == -8 ? 0 : -8, 7), all in fp64.
+ * work: M*K doubles (16-byte aligned).  q4, q_r: int8 [M][K] (q_r may be NULL: base only);
+ * s4: fp16 bits [M][K/128]. */
+nest_status nest_quantize_w4w8(const float* W, const int8_t* sign_out, const int8_t* sign_in,
+                               int32_t M, int32_t K, double* work, int8_t* q4, uint16_t* s4, int8_t* q_r,
+                               void* stream);
+
+/* Dual-plane packing of W4/W8 codes.  q4 in [-8, 7], q_r in [-8, 7] (NULL: no refinement
+ * plane, and ref_out may be NULL).  Unit layout (row r, 32-bit little-endian words, word w
+ * of row r at unit byte ((w/4)*128 + r)*16 + (w%4)*4): word w holds columns 8w..8w+7,
+ * column 8w + 4k + j in bits 8j + 4k .. 8j + 4k + 3, stored as code + 8; the base unit's
+ * fp16 s4 of row r at byte 8192 + 2r.  Rows past M hold code 0 and scale 0. */
+nest_status nest_pack_w4w8(const int8_t* q4, const uint16_t* s4, const int8_t* q_r, int32_t M, int32_t K,
+                           uint8_t* base_out, uint8_t* ref_out, void* stream);
+
+/* Inverse of nest_pack_w4w8 (tests).  q_r may be NULL. */
+nest_status nest_unpack_w4w8(const nest_layer* layer, int8_t* q4, uint16_t* s4, int8_t* q_r, void* stream);
+
 /* Inverse of nest_pack (used by tests).  resid_* may be NULL when layer->resid_bits == 0. */
 nest_status nest_unpack(const nest_layer* layer, uint8_t* base_codes, uint16_t* base_scales,
                         int8_t* resid_codes, uint16_t* resid_scales, void* stream);
@@ -157,7 +189,9 @@ nest_status nest_rotate(const void* x, int32_t x_dtype, const int8_t* signs, int
 
 /* Draft GEMV/GEMM: z[t][m] += sum_k Q_base[m][k] x'[t][k] for t < T, in the rotated
  * output basis (POC recipe step 4: the draft forward is the verifier's without y_r).
- * Reads the base buffer only.
+ * Reads the base buffer only.  For NEST_CODEC_W4W8 layers Q_base = q4 s4 (BitNest
+ * Eq. (6)) and the verify below uses Q = (16 q4 + q_r) s4/16 (Eq. (10)).  A grouped
+ * launch takes layers of one codec.
  * x_op  activation operand from nest_rotate (T tokens).
  * z     fp32 [T][M], ACCUMULATED into: clear it first for a plain product.  The
  *       128-column groups of a row are split across CTAs and each part is added with

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/nest.h"
+#include "nest_device.cuh"
 #include "nest_internal.h"
 
 using namespace nest;
@@ -51,6 +52,15 @@ nest_status check_layer(const nest_layer* L, bool need_resid) {
     if (L->K % 128 != 0) return NEST_ERR_UNSUPPORTED;
     if (L->base == nullptr) return NEST_ERR_INVALID_ARG;
     if (!aligned16(L->base)) return NEST_ERR_MISALIGNED;
+    if (L->codec == NEST_CODEC_W4W8) {
+        if (L->resid_bits != 0 && L->resid_bits != 4) return NEST_ERR_UNSUPPORTED;
+        if (need_resid) {
+            if (L->resid_bits != 4 || L->resid == nullptr) return NEST_ERR_INVALID_ARG;
+            if (!aligned16(L->resid)) return NEST_ERR_MISALIGNED;
+        }
+        return NEST_OK;
+    }
+    if (L->codec != NEST_CODEC_L2) return NEST_ERR_UNSUPPORTED;
     if (need_resid) {
         if (!bits_ok(L->resid_bits)) return L->resid_bits == 0 ? NEST_ERR_INVALID_ARG : NEST_ERR_UNSUPPORTED;
         if (L->resid == nullptr) return NEST_ERR_INVALID_ARG;
@@ -69,8 +79,11 @@ nest_status run_gemm_group(const nest_layer* layers, int count, bool verify, con
     if (count > kMaxGemmTasks) return NEST_ERR_UNSUPPORTED;
     if (T < 1) return NEST_ERR_INVALID_ARG;
     if (T > 64) return NEST_ERR_UNSUPPORTED;
+    const int codec = layers[0].codec;
     const int bits = verify ? layers[0].resid_bits : 0;
     if (verify && bits == 0) return NEST_ERR_INVALID_ARG;
+    // kernel codec: 0 / 6 / 7 / 8 (2-bit base, residual width) or 40 / 48 (W4 draft / W8 target)
+    const int kcodec = codec == NEST_CODEC_W4W8 ? (verify ? 48 : 40) : bits;
     GemmArgs a = {};
     a.ntasks = count;
     a.T = T;
@@ -79,7 +92,7 @@ nest_status run_gemm_group(const nest_layer* layers, int count, bool verify, con
         const nest_layer* L = &layers[k];
         nest_status st = check_layer(L, verify);
         if (st != NEST_OK) return st;
-        if (verify && L->resid_bits != bits) return NEST_ERR_INVALID_ARG;
+        if (L->codec != codec || (verify && L->resid_bits != bits)) return NEST_ERR_INVALID_ARG;
         if (xops[k] == nullptr || zs[k] == nullptr) return NEST_ERR_INVALID_ARG;
         if (!aligned16(xops[k]) || (reinterpret_cast<uintptr_t>(zs[k]) & 3u)) return NEST_ERR_MISALIGNED;
         GemmTask& t = a.task[k];
@@ -100,7 +113,7 @@ nest_status run_gemm_group(const nest_layer* layers, int count, bool verify, con
     const long long slots = (long long)kGemmCtasPerSm * sms;   // every CTA resident at once
     long long grid = units < slots ? units : slots;
     if (grid > kMaxGrid) grid = kMaxGrid;
-    return from_cuda(launch_gemm(a, bits, (int)grid, as_stream(stream)));
+    return from_cuda(launch_gemm(a, kcodec, (int)grid, as_stream(stream)));
 }
 
 }  // namespace
@@ -129,6 +142,48 @@ size_t nest_base_bytes(int32_t M, int32_t K) {
 size_t nest_resid_bytes(int32_t M, int32_t K, int32_t bits) {
     if (M < 1 || K < 1 || K % 128 || !bits_ok(bits)) return 0;
     return (size_t)n_tiles(M) * (K / 128) * (2048 * (size_t)bits + 256);
+}
+
+size_t nest_w4_base_bytes(int32_t M, int32_t K) {
+    if (M < 1 || K < 1 || K % 128) return 0;
+    return (size_t)n_tiles(M) * (K / 128) * kW4BaseUnit;
+}
+
+size_t nest_w4_ref_bytes(int32_t M, int32_t K) {
+    if (M < 1 || K < 1 || K % 128) return 0;
+    return (size_t)n_tiles(M) * (K / 128) * kW4RefUnit;
+}
+
+nest_status nest_quantize_w4w8(const float* W, const int8_t* sign_out, const int8_t* sign_in, int32_t M, int32_t K,
+                               double* work, int8_t* q4, uint16_t* s4, int8_t* q_r, void* stream) {
+    if (!W || !sign_out || !sign_in || !work || !q4 || !s4) return NEST_ERR_INVALID_ARG;
+    if (M < 1 || K < 1) return NEST_ERR_INVALID_ARG;
+    if (K % 128) return NEST_ERR_UNSUPPORTED;
+    if (!aligned16(W) || !aligned16(work)) return NEST_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(s4) & 1u) return NEST_ERR_MISALIGNED;
+    if ((long long)M * (K / hadamard_block(K)) > 0x7fffffffLL) return NEST_ERR_UNSUPPORTED;
+    return from_cuda(launch_quantize_w4w8(W, sign_out, sign_in, M, K, work, q4, s4, q_r, as_stream(stream)));
+}
+
+nest_status nest_pack_w4w8(const int8_t* q4, const uint16_t* s4, const int8_t* q_r, int32_t M, int32_t K,
+                           uint8_t* base_out, uint8_t* ref_out, void* stream) {
+    if (!q4 || !s4 || !base_out) return NEST_ERR_INVALID_ARG;
+    if (q_r != nullptr && ref_out == nullptr) return NEST_ERR_INVALID_ARG;
+    if (M < 1 || K < 1) return NEST_ERR_INVALID_ARG;
+    if (K % 128) return NEST_ERR_UNSUPPORTED;
+    if (!aligned16(base_out) || (q_r && !aligned16(ref_out))) return NEST_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(s4) & 1u) return NEST_ERR_MISALIGNED;
+    return from_cuda(launch_pack_w4w8(q4, s4, q_r, M, K, base_out, q_r ? ref_out : nullptr, as_stream(stream)));
+}
+
+nest_status nest_unpack_w4w8(const nest_layer* layer, int8_t* q4, uint16_t* s4, int8_t* q_r, void* stream) {
+    if (layer == nullptr || layer->codec != NEST_CODEC_W4W8) return NEST_ERR_INVALID_ARG;
+    nest_status st = check_layer(layer, q_r != nullptr);
+    if (st != NEST_OK) return st;
+    if (!q4 || !s4) return NEST_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(s4) & 1u) return NEST_ERR_MISALIGNED;
+    return from_cuda(launch_unpack_w4w8(layer->base, q_r ? layer->resid : nullptr, layer->M, layer->K, q4, s4, q_r,
+                                        as_stream(stream)));
 }
 
 size_t nest_xop_bytes(int32_t K, int32_t T) {
@@ -169,6 +224,7 @@ nest_status nest_pack(const uint8_t* base_codes, const uint16_t* base_scales, co
 
 nest_status nest_unpack(const nest_layer* layer, uint8_t* base_codes, uint16_t* base_scales, int8_t* resid_codes,
                         uint16_t* resid_scales, void* stream) {
+    if (layer != nullptr && layer->codec != NEST_CODEC_L2) return NEST_ERR_INVALID_ARG;
     nest_status st = check_layer(layer, false);
     if (st != NEST_OK) return st;
     const int bits = layer->resid_bits;

@@ -12,6 +12,9 @@ constexpr int kRows = 128;           // output rows per tile (one TMEM lane each
 constexpr int kGroup = 128;          // columns per quantisation group
 constexpr int kBaseUnit = 4096 + 256;
 __host__ __device__ constexpr int resid_unit_bytes(int bits) { return bits ? 2048 * bits + 256 : 0; }
+// W4/W8 dual-plane units (BitNest section 3.3): 4-bit base codes + fp16 scales, 4-bit refinement codes
+constexpr int kW4BaseUnit = 8192 + 256;
+constexpr int kW4RefUnit = 8192;
 constexpr int kHadCap = 4096;
 
 // Levels of the 2-bit base, ascending (the Gaussian 4-level Lloyd-Max set).

@@ -72,13 +72,25 @@ __device__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, bo
     }
 }
 
+// Weight codecs of the GEMM kernels (template parameter BITS):
+//   0        2-bit Lloyd-Max base only (draft)
+//   6, 7, 8  2-bit base + b-bit uniform residual (verify)
+//   40       BitNest W4 base only (draft)
+//   48       BitNest W4 base + 4-bit refinement, the W8 target (verify)
+__host__ __device__ constexpr bool is_w4(int codec) { return codec >= 40; }
+__host__ __device__ constexpr int base_unit_bytes(int codec) { return is_w4(codec) ? kW4BaseUnit : kBaseUnit; }
+__host__ __device__ constexpr int second_unit_bytes(int codec) {
+    return codec == 48 ? kW4RefUnit : (is_w4(codec) ? 0 : resid_unit_bytes(codec));
+}
+
 template <int BITS, int NP>
 struct Cfg {
     // Two CTAs share an SM: each has its own MMA issuer, so the gaps in one
     // CTA's MMA stream (barrier waits, commits) are filled by the other's.
     static constexpr int kCtasPerSm = 2;
-    static constexpr int kResUnit = resid_unit_bytes(BITS);
-    static constexpr int kWStage = kBaseUnit + kResUnit;     // packed weights of one unit
+    static constexpr int kBaseBytes = base_unit_bytes(BITS);
+    static constexpr int kResUnit = second_unit_bytes(BITS);
+    static constexpr int kWStage = kBaseBytes + kResUnit;    // packed weights of one unit
     static constexpr int kXBytes = 256 * NP;                 // Np tokens x 128 columns of fp16
     static constexpr int kTmemCols = 512 / kCtasPerSm;
     static constexpr int kColA = 2 * NP;                     // A buffers after the two D buffers
@@ -100,6 +112,44 @@ struct Cfg {
     static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
     static_assert(kWStage % 128 == 0 && kXBytes % 128 == 0, "stage alignment");
 };
+
+// W4/W8: decode 64 columns (half h) of row r into 32 fp16x2 registers, w = c * s4 with
+// c = q4 (draft) or 16 q4 + q_r (verify; the epilogue applies the 1/16 of s_ref = s4/16).
+// Word w of a row's nibble plane holds columns 8w..8w+7 (column 8w + 4k + j in bits
+// 8j + 4k), so for Q = 16h + qd the four columns 4Q..4Q+3 are the k = qd & 1 nibbles of
+// word 8h + qd/2.  With offset nibbles u4 = q4 + 8, u_r = q_r + 8 the byte u4 * 16 + u_r
+// equals 16 q4 + q_r + 136, so one shift and one masked select build four target codes.
+template <int BITS>
+__device__ __forceinline__ void dequant_half_w4(const uint8_t* sb, const uint8_t* sr, int r, int h, __half2 s2,
+                                                __half2 off2, uint32_t (&out)[32]) {
+    uint32_t bw[8], rw[8];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sb + ((2 * h + c) * kRows + r) * 16);
+        bw[4 * c] = v.x; bw[4 * c + 1] = v.y; bw[4 * c + 2] = v.z; bw[4 * c + 3] = v.w;
+        if constexpr (BITS == 48) {
+            const uint4 u = *reinterpret_cast<const uint4*>(sr + ((2 * h + c) * kRows + r) * 16);
+            rw[4 * c] = u.x; rw[4 * c + 1] = u.y; rw[4 * c + 2] = u.z; rw[4 * c + 3] = u.w;
+        }
+    }
+#pragma unroll
+    for (int qd = 0; qd < 16; ++qd) {
+        const uint32_t wb = bw[qd >> 1];
+        uint32_t b4;
+        if constexpr (BITS == 48) {
+            const uint32_t wr = rw[qd >> 1];
+            b4 = (qd & 1) ? ((wb & 0xF0F0F0F0u) | ((wr >> 4) & 0x0F0F0F0Fu))
+                          : (((wb << 4) & 0xF0F0F0F0u) | (wr & 0x0F0F0F0Fu));
+        } else {
+            b4 = (qd & 1) ? ((wb >> 4) & 0x0F0F0F0Fu) : (wb & 0x0F0F0F0Fu);
+        }
+        // 1024 + byte as fp16 (exact), minus 1024 + offset, times s4
+        const __half2 c01 = __hsub2(u32_as_h2(prmt(b4, 0x64646464u, 0x5140u)), off2);
+        const __half2 c23 = __hsub2(u32_as_h2(prmt(b4, 0x64646464u, 0x7362u)), off2);
+        out[2 * qd] = h2_as_u32(__hmul2(c01, s2));
+        out[2 * qd + 1] = h2_as_u32(__hmul2(c23, s2));
+    }
+}
 
 // Decode 64 columns (half h of the 128-column group) of row r of one unit into
 // 32 fp16x2 registers: w = s_b * L[code] (+ s_r * q).
@@ -236,7 +286,7 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     auto st_base = [&](int s) { return smem + s * C::kWStage; };
-    auto st_res = [&](int s) { return smem + s * C::kWStage + kBaseUnit; };
+    auto st_res = [&](int s) { return smem + s * C::kWStage + C::kBaseBytes; };
     auto st_x = [&](int a) { return xring + a * C::kXBytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -274,8 +324,8 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
             const GemmTask& t = p.task[cw.k];
             const long long lu = cw.local(p);
             mbar_arrive_expect_tx(full_w(s), C::kWStage);
-            bulk_g2s(smem_u32(st_base(s)), t.base + lu * kBaseUnit, kBaseUnit, full_w(s));
-            if constexpr (BITS != 0)
+            bulk_g2s(smem_u32(st_base(s)), t.base + lu * C::kBaseBytes, C::kBaseBytes, full_w(s));
+            if constexpr (C::kResUnit != 0)
                 bulk_g2s(smem_u32(st_res(s)), t.resid + lu * C::kResUnit, C::kResUnit, full_w(s));
             cw.next(p);
         };
@@ -376,7 +426,10 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
         const int wg = warp >> 2;
         const int r = 32 * (warp & 3) + lane;               // row of the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const __half2 off2 = __float2half2_rn(1024.0f + (BITS ? (float)(1 << (BITS - 1)) : 0.0f));
+        // magic-number offsets: 1024 + the stored offset of the codes
+        const __half2 off2 = __float2half2_rn(
+            1024.0f + (BITS == 48 ? 136.0f : BITS == 40 ? 8.0f : (BITS ? (float)(1 << (BITS - 1)) : 0.0f)));
+        constexpr float kOutScale = BITS == 48 ? 0.0625f : 1.0f;     // s_ref = s4 / 16
         int seg = -1;
         UnitCursor cu = start;
         bool dep_done = false;
@@ -398,21 +451,31 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
                 tc_fence_after();
                 const uint8_t* sb = st_base(s);
                 const uint8_t* sr = st_res(s);
-                const float s_b = __half2float(*reinterpret_cast<const __half*>(sb + 4096 + 2 * r));
-                // scaled levels as fp16, low bytes in lut_lo and high bytes in lut_hi
-                uint32_t h[4];
+                if constexpr (is_w4(BITS)) {
+                    const __half2 s2 = __half2half2(*reinterpret_cast<const __half*>(sb + 8192 + 2 * r));
 #pragma unroll
-                for (int c = 0; c < 4; ++c) h[c] = __half_as_ushort(__float2half_rn(s_b * level_f(c)));
-                const uint32_t lut_lo = (h[0] & 0xFFu) | ((h[1] & 0xFFu) << 8) | ((h[2] & 0xFFu) << 16) | ((h[3] & 0xFFu) << 24);
-                const uint32_t lut_hi = (h[0] >> 8) | ((h[1] >> 8) << 8) | ((h[2] >> 8) << 16) | ((h[3] >> 8) << 24);
-                __half2 sr2 = __float2half2_rn(0.0f);
-                if constexpr (BITS != 0)
-                    sr2 = __half2half2(*reinterpret_cast<const __half*>(sr + 2048 * BITS + 2 * r));
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t w[32];
+                        dequant_half_w4<BITS>(sb, sr, r, hh, s2, off2, w);
+                        tmem_st32_wait(tmem + lane_base + C::kColA + 64 * a + 32 * hh, w);
+                    }
+                } else {
+                    const float s_b = __half2float(*reinterpret_cast<const __half*>(sb + 4096 + 2 * r));
+                    // scaled levels as fp16, low bytes in lut_lo and high bytes in lut_hi
+                    uint32_t h[4];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t w[32];
-                    dequant_half<BITS>(sb, sr, r, hh, lut_lo, lut_hi, sr2, off2, w);
-                    tmem_st32_wait(tmem + lane_base + C::kColA + 64 * a + 32 * hh, w);
+                    for (int c = 0; c < 4; ++c) h[c] = __half_as_ushort(__float2half_rn(s_b * level_f(c)));
+                    const uint32_t lut_lo = (h[0] & 0xFFu) | ((h[1] & 0xFFu) << 8) | ((h[2] & 0xFFu) << 16) | ((h[3] & 0xFFu) << 24);
+                    const uint32_t lut_hi = (h[0] >> 8) | ((h[1] >> 8) << 8) | ((h[2] >> 8) << 16) | ((h[3] >> 8) << 24);
+                    __half2 sr2 = __float2half2_rn(0.0f);
+                    if constexpr (BITS != 0)
+                        sr2 = __half2half2(*reinterpret_cast<const __half*>(sr + 2048 * BITS + 2 * r));
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t w[32];
+                        dequant_half<BITS>(sb, sr, r, hh, lut_lo, lut_hi, sr2, off2, w);
+                        tmem_st32_wait(tmem + lane_base + C::kColA + 64 * a + 32 * hh, w);
+                    }
                 }
                 mbar_arrive(empty_w(s));             // this thread is done with the weight stage
                 tc_fence_before();
@@ -436,7 +499,7 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
                     float* zp = task.z + m;
 #pragma unroll
                     for (int t = 0; t < NP; ++t)
-                        if (t < T) atomicAdd(zp + (size_t)t * M, v[t]);    // fire-and-forget reduction
+                        if (t < T) atomicAdd(zp + (size_t)t * M, v[t] * kOutScale);   // fire-and-forget reduction
                 }
             }
             cu.next(p);
@@ -877,12 +940,14 @@ int path_override() {
 
 template <int BITS>
 cudaError_t launch_bits(const GemmArgs& a, int grid, cudaStream_t stream) {
-    const int ov = path_override();
-    const bool rf = ov == 2 ? a.T <= 32 : (ov == 0 && BITS == 0 && a.T <= 8);
-    if (rf) {
-        if (a.T <= 8) return launch_rf<BITS, 1>(a, grid, stream);
-        if (a.T <= 16) return launch_rf<BITS, 2>(a, grid, stream);
-        return launch_rf<BITS, 4>(a, grid, stream);
+    if constexpr (!is_w4(BITS)) {
+        const int ov = path_override();
+        const bool rf = ov == 2 ? a.T <= 32 : (ov == 0 && BITS == 0 && a.T <= 8);
+        if (rf) {
+            if (a.T <= 8) return launch_rf<BITS, 1>(a, grid, stream);
+            if (a.T <= 16) return launch_rf<BITS, 2>(a, grid, stream);
+            return launch_rf<BITS, 4>(a, grid, stream);
+        }
     }
     if (a.T <= 16) return launch_t<BITS, 16>(a, grid, stream);
     if (a.T <= 32) return launch_t<BITS, 32>(a, grid, stream);
@@ -897,6 +962,8 @@ cudaError_t launch_gemm(const GemmArgs& a, int bits, int grid, cudaStream_t stre
         case 6: return launch_bits<6>(a, grid, stream);
         case 7: return launch_bits<7>(a, grid, stream);
         case 8: return launch_bits<8>(a, grid, stream);
+        case 40: return launch_bits<40>(a, grid, stream);
+        case 48: return launch_bits<48>(a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -109,6 +109,13 @@ cudaError_t launch_pack(const uint8_t* bc, const uint16_t* bs, const int8_t* rc,
 cudaError_t launch_unpack(const uint8_t* base, const uint8_t* resid, int M, int K, int bits,
                           uint8_t* bc, uint16_t* bs, int8_t* rc, uint16_t* rs, cudaStream_t stream);
 
+cudaError_t launch_pack_w4w8(const int8_t* q4, const uint16_t* s4, const int8_t* qr, int M, int K,
+                             uint8_t* base_out, uint8_t* ref_out, cudaStream_t stream);
+cudaError_t launch_unpack_w4w8(const uint8_t* base, const uint8_t* ref, int M, int K, int8_t* q4, uint16_t* s4,
+                               int8_t* qr, cudaStream_t stream);
+cudaError_t launch_quantize_w4w8(const float* W, const int8_t* so, const int8_t* si, int M, int K, double* work,
+                                 int8_t* q4, uint16_t* s4, int8_t* qr, cudaStream_t stream);
+
 cudaError_t launch_quantize(const float* W, const int8_t* so, const int8_t* si, int M, int K, int bits,
                             double* work, uint8_t* bc, uint16_t* bs, int8_t* rc, uint16_t* rs,
                             cudaStream_t stream);

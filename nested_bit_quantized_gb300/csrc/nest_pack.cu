@@ -113,6 +113,53 @@ __global__ void k_unpack(const uint8_t* __restrict__ base, const uint8_t* __rest
     }
 }
 
+// W4/W8 dual-plane storage (BitNest, section 3.3): one thread per (unit, row, nibble
+// word); word w of a row holds columns 8w..8w+7, column 8w + 4h + q in bits 8q + 4h.
+// Stored nibble u = code + 8.  The base plane carries the fp16 scale s4 of each row at
+// byte 8192 + 2r of its unit; the refinement plane has no scale.
+__global__ void k_pack_nib(const int8_t* __restrict__ codes, const uint16_t* __restrict__ scales, int M, int K,
+                           long long n_items, size_t unit_bytes, uint8_t* __restrict__ out) {
+    const int G = K / kGroup;
+    for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < n_items;
+         it += (long long)gridDim.x * blockDim.x) {
+        const int w = (int)(it & 15);
+        const int r = (int)((it >> 4) & 127);
+        const long long unit = it >> 11;
+        const int tile = (int)(unit / G), g = (int)(unit % G);
+        const int m = tile * kRows + r;
+        const bool valid = m < M;
+        const int8_t* c = codes + (size_t)(valid ? m : 0) * K + (size_t)g * kGroup + 8 * w;
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) word |= (((uint32_t)((valid ? (int)c[j] : 0) + 8)) & 15u) << (8 * (j & 3) + 4 * (j >> 2));
+        uint8_t* u = out + unit * unit_bytes;
+        *reinterpret_cast<uint32_t*>(u + word_off(r, w)) = word;
+        if (scales != nullptr && w == 0)
+            *reinterpret_cast<uint16_t*>(u + 8192 + 2 * r) = valid ? scales[(size_t)m * G + g] : (uint16_t)0;
+    }
+}
+
+// one thread per weight (test path)
+__global__ void k_unpack_w4w8(const uint8_t* __restrict__ base, const uint8_t* __restrict__ ref, int M, int K,
+                              int8_t* __restrict__ q4, uint16_t* __restrict__ s4, int8_t* __restrict__ qr) {
+    const int G = K / kGroup;
+    const long long total = (long long)M * K;
+    for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < total;
+         it += (long long)gridDim.x * blockDim.x) {
+        const int m = (int)(it / K), k = (int)(it % K);
+        const int tile = m / kRows, r = m % kRows, g = k / kGroup, j = k % kGroup;
+        const long long unit = (long long)tile * G + g;
+        const int j8 = j & 7, sh = 8 * (j8 & 3) + 4 * (j8 >> 2);
+        const uint8_t* ub = base + unit * kW4BaseUnit;
+        q4[it] = (int8_t)((int)((rd_word(ub, r, j >> 3) >> sh) & 15u) - 8);
+        if (j == 0) s4[(size_t)m * G + g] = *reinterpret_cast<const uint16_t*>(ub + 8192 + 2 * r);
+        if (ref != nullptr) {
+            const uint8_t* ur = ref + unit * kW4RefUnit;
+            qr[it] = (int8_t)((int)((rd_word(ur, r, j >> 3) >> sh) & 15u) - 8);
+        }
+    }
+}
+
 int grid_for(long long items, int threads) {
     long long g = (items + threads - 1) / threads;
     return (int)(g < 65535 * 16 ? (g < 1 ? 1 : g) : 65535 * 16);
@@ -136,6 +183,26 @@ cudaError_t launch_unpack(const uint8_t* base, const uint8_t* resid, int M, int 
                           uint8_t* bc, uint16_t* bs, int8_t* rc, uint16_t* rs, cudaStream_t stream) {
     const long long total = (long long)M * K;
     k_unpack<<<grid_for(total, 256), 256, 0, stream>>>(base, resid, M, K, bits, bc, bs, rc, rs);
+    return cudaGetLastError();
+}
+
+}  // namespace nest
+
+namespace nest {
+
+cudaError_t launch_pack_w4w8(const int8_t* q4, const uint16_t* s4, const int8_t* qr, int M, int K,
+                             uint8_t* base_out, uint8_t* ref_out, cudaStream_t stream) {
+    const long long units = (long long)n_tiles(M) * (K / kGroup);
+    const long long n = units * kRows * 16;
+    k_pack_nib<<<grid_for(n, 256), 256, 0, stream>>>(q4, s4, M, K, n, kW4BaseUnit, base_out);
+    if (qr != nullptr) k_pack_nib<<<grid_for(n, 256), 256, 0, stream>>>(qr, nullptr, M, K, n, kW4RefUnit, ref_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_w4w8(const uint8_t* base, const uint8_t* ref, int M, int K, int8_t* q4, uint16_t* s4,
+                               int8_t* qr, cudaStream_t stream) {
+    const long long total = (long long)M * K;
+    k_unpack_w4w8<<<grid_for(total, 256), 256, 0, stream>>>(base, ref, M, K, q4, s4, qr);
     return cudaGetLastError();
 }
 

@@ -128,16 +128,47 @@ __global__ void k_q_quant(const double* __restrict__ wr, int M, int K, int bits,
     if (lane == 0) rs[m * G + g] = __half_as_ushort(sr16);
 }
 
+// BitNest W4/W8 (Eq. (5)-(10) of the BitNest paper, RTN base): one warp per (row,
+// group), 4 consecutive columns per lane.  s4 = fp16(max|W'| / 7); q4 = clip(rint(W'/s4),
+// -8, 7); dW = W' - q4 s4; s_ref = s4 / 16; q_r = clip(rint(dW / s_ref), q4 == -8 ? 0 : -8, 7).
+__global__ void k_q_w4w8(const double* __restrict__ wr, int M, int K, int8_t* __restrict__ q4,
+                         uint16_t* __restrict__ s4, int8_t* __restrict__ qr) {
+    const int G = K / kGroup;
+    const long long wid = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= (long long)M * G) return;
+    const long long m = wid / G;
+    const int g = (int)(wid % G);
+    const long long col = (long long)g * kGroup + 4 * lane;
+    double v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = wr[m * K + col + e];
+    const double amax = warp_max(fmax(fmax(fabs(v[0]), fabs(v[1])), fmax(fabs(v[2]), fabs(v[3]))));
+    const __half s16 = __double2half(amax / 7.0);
+    const double s = (double)__half2float(s16);
+    const double sref = s / 16.0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        int a = 0, b = 0;
+        if (s > 0.0) {
+            a = (int)fmin(fmax(rint(v[e] / s), -8.0), 7.0);
+            const double t = rint((v[e] - (double)a * s) / sref);
+            b = (int)fmin(fmax(t, a == -8 ? 0.0 : -8.0), 7.0);
+        }
+        q4[m * K + col + e] = (int8_t)a;
+        if (qr != nullptr) qr[m * K + col + e] = (int8_t)b;
+    }
+    if (lane == 0) s4[m * G + g] = __half_as_ushort(s16);
+}
+
 int grid_for(long long items, int threads) {
     long long g = (items + threads - 1) / threads;
     return (int)(g < 65535 * 16 ? (g < 1 ? 1 : g) : 65535 * 16);
 }
 
-}  // namespace
-
-cudaError_t launch_quantize(const float* W, const int8_t* so, const int8_t* si, int M, int K, int bits,
-                            double* work, uint8_t* bc, uint16_t* bs, int8_t* rc, uint16_t* rs,
-                            cudaStream_t stream) {
+// W' = H_o S_o W S_i H_i in fp64 into `work` (the rotation both quantizers start from)
+void rotate_stage(const float* W, const int8_t* so, const int8_t* si, int M, int K, double* work,
+                  cudaStream_t stream) {
     const int b_in = hadamard_block(K), b_out = hadamard_block(M);
     const int thr_rows = b_in >= 512 ? 256 : (b_in / 2 > 32 ? b_in / 2 : 32);
     k_q_rows<<<(unsigned)((long long)M * (K / b_in)), thr_rows, b_in * sizeof(double), stream>>>(
@@ -150,8 +181,24 @@ cudaError_t launch_quantize(const float* W, const int8_t* so, const int8_t* si, 
             k_q_cols<<<grid_for((long long)(M / 2) * K, 256), 256, 0, stream>>>(
                 work, so, M, K, h, h == 1 ? 1 : 0, (2 * h == b_out) ? sc : 1.0);
     }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const float* W, const int8_t* so, const int8_t* si, int M, int K, int bits,
+                            double* work, uint8_t* bc, uint16_t* bs, int8_t* rc, uint16_t* rs,
+                            cudaStream_t stream) {
+    rotate_stage(W, so, si, M, K, work, stream);
     const long long warps = (long long)M * (K / kGroup);
     k_q_quant<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, stream>>>(work, M, K, bits, bc, bs, rc, rs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_w4w8(const float* W, const int8_t* so, const int8_t* si, int M, int K, double* work,
+                                 int8_t* q4, uint16_t* s4, int8_t* qr, cudaStream_t stream) {
+    rotate_stage(W, so, si, M, K, work, stream);
+    const long long warps = (long long)M * (K / kGroup);
+    k_q_w4w8<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, stream>>>(work, M, K, q4, s4, qr);
     return cudaGetLastError();
 }
 

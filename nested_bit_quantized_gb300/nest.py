@@ -28,9 +28,12 @@ class NestError(RuntimeError):
         self.status = status
 
 
+CODEC_L2, CODEC_W4W8 = 0, 1     # nest_layer.codec (include/nest.h)
+
+
 class _Layer(ctypes.Structure):
     _fields_ = [("M", _I32), ("K", _I32), ("resid_bits", _I32),
-                ("base", _P), ("resid", _P), ("sign_out", _P), ("sign_in", _P)]
+                ("base", _P), ("resid", _P), ("sign_out", _P), ("sign_in", _P), ("codec", _I32)]
 
 
 class RotateTask(ctypes.Structure):
@@ -74,6 +77,11 @@ def load() -> ctypes.CDLL:
         "nest_linear_group": ([ctypes.POINTER(_Layer), _I32, _I32, ctypes.POINTER(_P), _I32, _I32,
                                ctypes.POINTER(_P), _P, _P], _I32),
         "nest_chain_work_bytes": ([_I32, _I32], _SZ),
+        "nest_w4_base_bytes": ([_I32, _I32], _SZ),
+        "nest_w4_ref_bytes": ([_I32, _I32], _SZ),
+        "nest_quantize_w4w8": ([_P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P], _I32),
+        "nest_pack_w4w8": ([_P, _P, _P, _I32, _I32, _P, _P, _P], _I32),
+        "nest_unpack_w4w8": ([ctypes.POINTER(_Layer), _P, _P, _P, _P], _I32),
         "nest_chain": ([_P, _P, _P, _P, _I32, _I32, _P, ctypes.POINTER(_Layer), _I32, ctypes.POINTER(_P),
                         ctypes.POINTER(_P), _P, _P], _I32),
         "nest_rotate_group": ([ctypes.POINTER(RotateTask), _I32, _I32, _I32, _I32, _P], _I32),
@@ -176,11 +184,12 @@ class Layer:
     resid: Optional[torch.Tensor]
     sign_out: torch.Tensor
     sign_in: torch.Tensor
+    codec: int = CODEC_L2
 
     def c_struct(self) -> _Layer:
         return _Layer(self.M, self.K, self.bits, self.base.data_ptr(),
                       self.resid.data_ptr() if self.resid is not None else None,
-                      self.sign_out.data_ptr(), self.sign_in.data_ptr())
+                      self.sign_out.data_ptr(), self.sign_in.data_ptr(), self.codec)
 
     @property
     def weight_bytes(self) -> int:
@@ -200,6 +209,52 @@ def pack(base_codes: torch.Tensor, base_scales: torch.Tensor, resid_codes: Optio
                           M, K, bits, _ptr(base), _ptr(resid), _stream(stream))
     _check(st, "nest_pack")
     return Layer(M, K, bits, base, resid, sign_out, sign_in)
+
+
+def quantize_w4w8(W: torch.Tensor, sign_out: torch.Tensor, sign_in: torch.Tensor, refine: bool = True,
+                  work: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """BitNest W4/W8 quantizer on the device (nest_quantize_w4w8): q4, s4 (fp16 bits), q_r."""
+    _dev(W, torch.float32, "W")
+    _dev(sign_out, torch.int8, "sign_out")
+    _dev(sign_in, torch.int8, "sign_in")
+    M, K = W.shape
+    dev = W.device
+    if work is None:
+        work = torch.empty((M, K), dtype=torch.float64, device=dev)
+    out = {"q4": torch.empty((M, K), dtype=torch.int8, device=dev),
+           "s4": torch.empty((M, K // 128), dtype=torch.int16, device=dev),
+           "qr": torch.empty((M, K), dtype=torch.int8, device=dev) if refine else None}
+    st = load().nest_quantize_w4w8(_ptr(W), _ptr(sign_out), _ptr(sign_in), M, K, _ptr(work), _ptr(out["q4"]),
+                                   _ptr(out["s4"]), _ptr(out["qr"]), _stream(stream))
+    _check(st, "nest_quantize_w4w8")
+    return out
+
+
+def pack_w4w8(q4: torch.Tensor, s4: torch.Tensor, qr: Optional[torch.Tensor], sign_out: torch.Tensor,
+              sign_in: torch.Tensor, stream=None) -> Layer:
+    """Dual-plane packing (nest_pack_w4w8); a layer of codec W4W8 (resid_bits 4, or 0 without q_r)."""
+    _dev(q4, torch.int8, "q4")
+    M, K = q4.shape
+    dev = q4.device
+    lib = load()
+    base = _u8(int(lib.nest_w4_base_bytes(M, K)), dev)
+    ref = _u8(int(lib.nest_w4_ref_bytes(M, K)), dev) if qr is not None else None
+    st = lib.nest_pack_w4w8(_ptr(q4), _ptr(s4), _ptr(qr), M, K, _ptr(base), _ptr(ref), _stream(stream))
+    _check(st, "nest_pack_w4w8")
+    return Layer(M, K, 4 if qr is not None else 0, base, ref, sign_out, sign_in, CODEC_W4W8)
+
+
+def unpack_w4w8(layer: Layer, stream=None) -> dict:
+    """Inverse of pack_w4w8 (nest_unpack_w4w8)."""
+    dev = layer.base.device
+    out = {"q4": torch.empty((layer.M, layer.K), dtype=torch.int8, device=dev),
+           "s4": torch.empty((layer.M, layer.K // 128), dtype=torch.int16, device=dev),
+           "qr": torch.empty((layer.M, layer.K), dtype=torch.int8, device=dev) if layer.resid is not None else None}
+    L = layer.c_struct()
+    st = load().nest_unpack_w4w8(ctypes.byref(L), _ptr(out["q4"]), _ptr(out["s4"]), _ptr(out["qr"]),
+                                 _stream(stream))
+    _check(st, "nest_unpack_w4w8")
+    return out
 
 
 def unpack(layer: Layer, stream=None) -> dict:

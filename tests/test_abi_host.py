@@ -148,3 +148,36 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(nest._build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         nest.load()
+
+
+def test_w4w8_sizes_and_validation(lib):
+    for M, K in [(128, 128), (200, 384), (1, 256), (21504, 5376)]:
+        assert lib.nest_w4_base_bytes(M, K) == P.w4_bytes(M, K)
+        assert lib.nest_w4_ref_bytes(M, K) == P.w4ref_bytes(M, K)
+    assert lib.nest_w4_base_bytes(128, 100) == 0
+    ok = ctypes.c_void_p(0x50000)
+    q = lib.nest_quantize_w4w8
+    assert q(None, ok, ok, 128, 128, ok, ok, ok, ok, None) == 1
+    assert q(ok, ok, ok, 128, 100, ok, ok, ok, ok, None) == 2
+    assert q(ok, ok, ok, 128, 128, ok, ok, ctypes.c_void_p(0x50001), ok, None) == 3
+    p = lib.nest_pack_w4w8
+    assert p(ok, ok, ok, 128, 128, ok, None, None) == 1              # refinement codes without a plane
+    assert p(ok, ok, None, 128, 100, ok, None, None) == 2
+    assert p(ok, ok, None, 128, 128, ctypes.c_void_p(0x50008), None, None) == 3
+    # layer validation: codec and refinement width
+    xo = (ctypes.c_void_p * 1)(0x50000)
+    zs = (ctypes.c_void_p * 1)(0x60000)
+    bad = (nest._Layer * 1)(nest._Layer(256, 512, 6, 0x50000, 0x50000, 0x30000, 0x40000, nest.CODEC_W4W8))
+    assert lib.nest_verify_gemm_group(bad, 1, xo, zs, 4, None) == 2
+    nocodec = (nest._Layer * 1)(nest._Layer(256, 512, 4, 0x50000, 0x50000, 0x30000, 0x40000, 7))
+    assert lib.nest_draft_gemv_group(nocodec, 1, xo, zs, 4, None) == 2
+    noref = (nest._Layer * 1)(nest._Layer(256, 512, 0, 0x50000, None, 0x30000, 0x40000, nest.CODEC_W4W8))
+    assert lib.nest_verify_gemm_group(noref, 1, xo, zs, 4, None) == 1
+    mixed = (nest._Layer * 2)(nest._Layer(256, 512, 4, 0x50000, 0x50000, 0x30000, 0x40000, nest.CODEC_W4W8),
+                              nest._Layer(256, 512, 0, 0x50000, None, 0x30000, 0x40000, nest.CODEC_L2))
+    xo2 = (ctypes.c_void_p * 2)(0x50000, 0x50000)
+    zs2 = (ctypes.c_void_p * 2)(0x60000, 0x60000)
+    assert lib.nest_draft_gemv_group(mixed, 2, xo2, zs2, 4, None) == 1
+    u = lib.nest_unpack_w4w8
+    assert u(ctypes.byref(nest._Layer(256, 512, 4, 0x50000, 0x50000, 0x30000, 0x40000, nest.CODEC_L2)),
+             ok, ok, ok, None) == 1
