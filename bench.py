@@ -37,6 +37,7 @@ WORKLOAD = "mlp_triplet_4b"
 BITS = 7
 T_VERIFY, T_DRAFT = 16, 1
 SWEEP_T = (1, 4, 8, 16, 32, 64)
+PREFILL_T = (128, 256)
 # DRAM bytes per linear of the roofline kernel, from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum of a grouped gate+up verify launch at T=16, divided by its two
 # linears).  Valid only for the kernel source it was taken on: reported as null otherwise.
@@ -80,6 +81,16 @@ def peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def tensor_peak():
+    """Dense fp16 tensor peak in TFLOP/s: the measured bf16 burst figure (fp16 and bf16 have
+    the same nominal dense rate), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -360,6 +371,39 @@ def run_gpu(args, rank, world):
             sweep.append(rec)
         nest.error_check()
 
+    # prefill-size verify (T = 128, 256): a dense contraction on tcgen05, measured as TFLOP/s
+    prefill = []
+    if not args.no_sweep:
+        tpk, tsrc = tensor_peak()
+        for T in PREFILL_T:
+            sx = {k: nest.new_xop(l.K, T, dev) for k, l in enumerate(layers[0])}
+            sz = {k: torch.zeros((T, l.M), dtype=torch.float32, device=dev) for k, l in enumerate(layers[0])}
+            for k, l in enumerate(layers[0]):
+                b, _ = synth.activations(T, l.K, wl.x_seed + 7 * T + k)
+                nest.rotate(torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16), l.sign_in, 0,
+                            x_op=sx[k])
+
+            def fn():
+                for trip in layers:
+                    for grp in groups:
+                        nest.gemm_group([trip[k] for k in grp], [sx[k] for k in grp], T, True,
+                                        zs=[sz[k] for k in grp])
+            with torch.cuda.stream(stream):
+                fn()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fn()
+            reps = 10
+            per = timed(g, reps, 3) / reps * 1e3 / n_lin
+            flops = sum(2.0 * L.M * L.K * T for L in layers[0]) / 3
+            by = sum(lin_bytes(L.M, L.K, T, VC) for L in layers[0]) / 3
+            tf = flops / (per * 1e-6) / 1e12
+            prefill.append({"T": T, "verify_us": per, "GBps": by / (per * 1e-6) / 1e9, "TFLOPs": tf,
+                            "frac_of_tensor_peak": tf / tpk, "tensor_peak": tpk, "peak_source": tsrc})
+            del g
+        nest.error_check()
+
     # end to end through the public API: pinned host inputs in, the last verify output back
     host_x = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in xs.items()}
     for k in xs:
@@ -426,6 +470,7 @@ def run_gpu(args, rank, world):
                          "traffic": None if w4w8 else ncu_traffic(), "traffic_unit": "DRAM bytes per linear (ncu)",
                          "algorithmic_bytes_per_linear": v16["bytes_per_gemm"]},
             "sweep": sweep,
+            "prefill": prefill,
             "cpu_baseline": cpu,
             "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -30,7 +30,7 @@
  *     (NEST_ERR_MISALIGNED otherwise).
  *   - Inputs and outputs must not overlap.
  *   - Supported envelope of the GEMMs: K % 128 == 0, any M >= 1,
- *     1 <= T <= 64.  Device: compute capability 10.3 (sm_103a).
+ *     1 <= T <= 256.  Device: compute capability 10.3 (sm_103a).
  *
  * Storage format (packed buffers): arrays of UNITS, one unit per (tile of
  * 128 output rows, 128-column group), tile-major.  A base unit is 4352 bytes
@@ -40,7 +40,7 @@
  *
  * Activation operand ("x_op"): the rotated activations x' = H_i S_i x in
  * fp16, laid out as the GEMM reads them: per 128-column group g, a block of
- * 256*Np bytes (Np = T rounded up to 16, 32 or 64); inside it, the fp16
+ * 256*Np bytes (Np = T rounded up to 16, 32, 64, 128 or 256); inside it, the fp16
  * value of token t, column k = 128 g + 8 c + e sits at byte
  * ((c * Np/8 + t/8) * 8 + t%8) * 16 + 2 e.  Rows t >= T are never read
  * into an output.
@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
     NEST_OK = 0,
     NEST_ERR_INVALID_ARG = 1,   /* null pointer, negative or zero size, bad enum */
-    NEST_ERR_UNSUPPORTED = 2,   /* outside the supported envelope (K % 128, T > 64, bits, device) */
+    NEST_ERR_UNSUPPORTED = 2,   /* outside the supported envelope (K % 128, T > 256, bits, device) */
     NEST_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
     NEST_ERR_CUDA = 4,          /* a CUDA runtime call or a launch failed */
     NEST_ERR_TIMEOUT = 5        /* a kernel gave up waiting on a pipeline barrier (nest_error_check) */
@@ -182,7 +182,7 @@ nest_status nest_unpack(const nest_layer* layer, uint8_t* base_codes, uint16_t* 
  * x        [T][n], fp32 (x_dtype 0) or bf16 bits (x_dtype 1); T * n < 2^31.
  * signs    int8 [n] +-1 (natural alignment).
  * y        fp32 [T][n] out, or NULL.
- * x_op     activation operand out (mode 0 only, n % 128 == 0, T <= 64), or NULL.
+ * x_op     activation operand out (mode 0 only, n % 128 == 0, T <= 256), or NULL.
  * At least one of y, x_op must be given.  n >= 1, T >= 1. */
 nest_status nest_rotate(const void* x, int32_t x_dtype, const int8_t* signs, int32_t n, int32_t T,
                         int32_t mode, float* y, uint16_t* x_op, void* stream);
@@ -256,7 +256,7 @@ nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t v
  *               that are cleared here for the GEMMs that follow.
  * work          nest_chain_work_bytes(M, T) bytes of device memory, no initial contents; calls
  *               whose work may overlap on the GPU need separate work buffers.
- * Limits: T <= 64, M * T < 2^31, M % 128 == 0 when n_next > 0. */
+ * Limits: T <= 256, M * T < 2^31, M % 128 == 0 when n_next > 0. */
 size_t nest_chain_work_bytes(int32_t M, int32_t T);
 nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,
                        int32_t M, int32_t T, float* y, const nest_layer* next, int32_t n_next,

@@ -78,7 +78,7 @@ nest_status run_gemm_group(const nest_layer* layers, int count, bool verify, con
     if (count < 1) return NEST_ERR_INVALID_ARG;
     if (count > kMaxGemmTasks) return NEST_ERR_UNSUPPORTED;
     if (T < 1) return NEST_ERR_INVALID_ARG;
-    if (T > 64) return NEST_ERR_UNSUPPORTED;
+    if (T > kMaxT) return NEST_ERR_UNSUPPORTED;
     const int codec = layers[0].codec;
     const int bits = verify ? layers[0].resid_bits : 0;
     if (verify && bits == 0) return NEST_ERR_INVALID_ARG;
@@ -110,7 +110,7 @@ nest_status run_gemm_group(const nest_layer* layers, int count, bool verify, con
     if (!device_supported()) return NEST_ERR_UNSUPPORTED;
     const int sms = device_sms();
     if (sms <= 0) return NEST_ERR_CUDA;
-    const long long slots = (long long)kGemmCtasPerSm * sms;   // every CTA resident at once
+    const long long slots = (long long)gemm_ctas_per_sm(T) * sms;   // every CTA resident at once
     long long grid = units < slots ? units : slots;
     if (grid > kMaxGrid) grid = kMaxGrid;
     return from_cuda(launch_gemm(a, kcodec, (int)grid, as_stream(stream)));
@@ -187,7 +187,7 @@ nest_status nest_unpack_w4w8(const nest_layer* layer, int8_t* q4, uint16_t* s4, 
 }
 
 size_t nest_xop_bytes(int32_t K, int32_t T) {
-    if (K < 1 || K % 128 || T < 1 || T > 64) return 0;
+    if (K < 1 || K % 128 || T < 1 || T > kMaxT) return 0;
     return (size_t)(K / 128) * 256 * n_pad(T);
 }
 
@@ -245,7 +245,7 @@ nest_status nest_rotate(const void* x, int32_t x_dtype, const int8_t* signs, int
     if ((x_dtype != 0 && x_dtype != 1) || (mode != 0 && mode != 1)) return NEST_ERR_INVALID_ARG;
     if (x_op != nullptr) {
         if (mode != 0) return NEST_ERR_INVALID_ARG;
-        if (n % 128 || T > 64) return NEST_ERR_UNSUPPORTED;
+        if (n % 128 || T > kMaxT) return NEST_ERR_UNSUPPORTED;
         if (!aligned16(x_op)) return NEST_ERR_MISALIGNED;
     }
     if ((reinterpret_cast<uintptr_t>(x) & (x_dtype == 1 ? 1u : 3u)) || (y && (reinterpret_cast<uintptr_t>(y) & 3u)))
@@ -275,7 +275,7 @@ nest_status nest_verify_gemm_group(const nest_layer* layers, int32_t count, cons
 static size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t nest_linear_scratch_bytes(int32_t M, int32_t K, int32_t T) {
-    if (M < 1 || K < 1 || K % 128 || T < 1 || T > 64) return 0;
+    if (M < 1 || K < 1 || K % 128 || T < 1 || T > kMaxT) return 0;
     return round256(nest_xop_bytes(K, T)) + round256((size_t)T * M * sizeof(float));
 }
 
@@ -297,7 +297,7 @@ nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t v
     if (count > kMaxGemmTasks) return NEST_ERR_UNSUPPORTED;
     if (x_dtype != 0 && x_dtype != 1) return NEST_ERR_INVALID_ARG;
     if (T < 1) return NEST_ERR_INVALID_ARG;
-    if (T > 64) return NEST_ERR_UNSUPPORTED;
+    if (T > kMaxT) return NEST_ERR_UNSUPPORTED;
     if (!aligned16(scratch)) return NEST_ERR_MISALIGNED;
     RotArgs rin = {}, rout = {};
     const uint16_t* xops[kMaxGemmTasks];
@@ -334,7 +334,7 @@ nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, 
 }
 
 size_t nest_chain_work_bytes(int32_t M, int32_t T) {
-    if (M < 1 || T < 1 || T > 64) return 0;
+    if (M < 1 || T < 1 || T > kMaxT) return 0;
     return round256((size_t)T * glue_segments(M) * sizeof(float));
 }
 
@@ -345,7 +345,7 @@ nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, c
     if ((z_b == nullptr) != (sign_out_b == nullptr)) return NEST_ERR_INVALID_ARG;
     if (z_b == z_a || (y != nullptr && y == z_b)) return NEST_ERR_INVALID_ARG;
     if (M < 1 || T < 1 || n_next < 0) return NEST_ERR_INVALID_ARG;
-    if (T > 64 || n_next > kMaxChainNext) return NEST_ERR_UNSUPPORTED;
+    if (T > kMaxT || n_next > kMaxChainNext) return NEST_ERR_UNSUPPORTED;
     if ((long long)M * T >= (1LL << 31)) return NEST_ERR_UNSUPPORTED;
     if (n_next > 0 && (next == nullptr || x_ops == nullptr)) return NEST_ERR_INVALID_ARG;
     if (n_next > 0 && M % 128) return NEST_ERR_UNSUPPORTED;
@@ -387,7 +387,7 @@ nest_status nest_rotate_group(const nest_rotate_task* tasks, int32_t count, int3
         if ((long long)r.n * T >= (1LL << 31)) return NEST_ERR_UNSUPPORTED;
         if (r.x_op != nullptr) {
             if (mode != 0) return NEST_ERR_INVALID_ARG;
-            if (r.n % 128 || T > 64) return NEST_ERR_UNSUPPORTED;
+            if (r.n % 128 || T > kMaxT) return NEST_ERR_UNSUPPORTED;
             if (!aligned16(r.x_op)) return NEST_ERR_MISALIGNED;
         }
         if ((reinterpret_cast<uintptr_t>(r.x) & (x_dtype == 1 ? 1u : 3u)) ||

@@ -85,26 +85,32 @@ __host__ __device__ constexpr int second_unit_bytes(int codec) {
 
 template <int BITS, int NP>
 struct Cfg {
-    // Two CTAs share an SM: each has its own MMA issuer, so the gaps in one
-    // CTA's MMA stream (barrier waits, commits) are filled by the other's.
-    static constexpr int kCtasPerSm = 2;
+    // Up to 64 tokens two CTAs share an SM: each has its own MMA issuer, so the gaps
+    // in one CTA's MMA stream (barrier waits, commits) are filled by the other's.
+    // 128 and 256 tokens (prefill-size trees) take a whole SM: its 512 tensor-memory
+    // columns hold the 128 x Np accumulator(s) and the A buffers, and 220 KB of shared
+    // memory the 32-64 KB activation blocks.
+    static constexpr int kCtasPerSm = NP >= 128 ? 1 : 2;
     static constexpr int kBaseBytes = base_unit_bytes(BITS);
     static constexpr int kResUnit = second_unit_bytes(BITS);
     static constexpr int kWStage = kBaseBytes + kResUnit;    // packed weights of one unit
     static constexpr int kXBytes = 256 * NP;                 // Np tokens x 128 columns of fp16
     static constexpr int kTmemCols = 512 / kCtasPerSm;
-    static constexpr int kColA = 2 * NP;                     // A buffers after the two D buffers
-    static constexpr int kNumA = (kTmemCols - kColA) / 64;   // A buffers (64 TMEM columns) = activation slots
+    static constexpr int kNumD = NP >= 256 ? 1 : 2;          // accumulator buffers
+    static constexpr int kColA = kNumD * NP;                 // A buffers after the D buffers
+    static constexpr int kNumARaw = (kTmemCols - kColA) / 64;
+    static constexpr int kMaxA = NP >= 256 ? 2 : (NP >= 128 ? 3 : 8);   // activation slots the smem holds
+    static constexpr int kNumA = kNumARaw < kMaxA ? kNumARaw : kMaxA;   // A buffers (64 columns) = activation slots
     static constexpr int kXRing = kNumA * kXBytes;
-    static constexpr int kSmemBudget = 110 * 1024;
+    static constexpr int kSmemBudget = kCtasPerSm == 1 ? 220 * 1024 : 110 * 1024;
     static constexpr int kStagesRaw = (kSmemBudget - 512 - kXRing) / kWStage;
     static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
     static constexpr int kDeqWG = 2;                         // dequantising warpgroups
     static constexpr int kProducerWarp = 4 * kDeqWG;
     static constexpr int kMmaWarp = 4 * kDeqWG + 1;
     static constexpr int kThreads = 32 * (4 * kDeqWG + 2);
-    // barriers: full_w[S], empty_w[S], full_x[NA], a_full[NA], done[NA], d_full[2], d_empty[2], drain
-    static constexpr int kNumBars = 2 * kStages + 3 * kNumA + 5;
+    // barriers: full_w[S], empty_w[S], full_x[NA], a_full[NA], done[NA], d_full[ND], d_empty[ND], drain
+    static constexpr int kNumBars = 2 * kStages + 3 * kNumA + 2 * kNumD + 1;
     static constexpr int kSmemBytes = kStages * kWStage + kXRing + kNumBars * 8 + 16;
     static_assert(kNumA >= 2, "tensor memory budget");
     static_assert(kStages >= 2, "stage too large");
@@ -279,9 +285,10 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
     auto full_x = [&](int a) { return bar0 + 8u * (2 * S + a); };
     auto a_full = [&](int a) { return bar0 + 8u * (2 * S + NA + a); };
     auto done = [&](int a) { return bar0 + 8u * (2 * S + 2 * NA + a); };
+    constexpr int ND = C::kNumD;
     auto d_full = [&](int d) { return bar0 + 8u * (2 * S + 3 * NA + d); };
-    auto d_empty = [&](int d) { return bar0 + 8u * (2 * S + 3 * NA + 2 + d); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * S + 3 * NA + 4);
+    auto d_empty = [&](int d) { return bar0 + 8u * (2 * S + 3 * NA + ND + d); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 3 * NA + 2 * ND);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -294,7 +301,7 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) { mbar_init(full_w(s), 1); mbar_init(empty_w(s), kRows); }
         for (int a = 0; a < NA; ++a) { mbar_init(full_x(a), 1); mbar_init(a_full(a), kRows); mbar_init(done(a), 1); }
-        for (int d = 0; d < 2; ++d) { mbar_init(d_full(d), 1); mbar_init(d_empty(d), kRows); }
+        for (int d = 0; d < ND; ++d) { mbar_init(d_full(d), 1); mbar_init(d_empty(d), kRows); }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -397,9 +404,9 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
             const bool last = (i == n - 1) || cu.group_end(p);
             if (first) {
                 ++seg;
-                if (seg >= 2 && !warp_wait(d_empty(seg & 1), ((seg >> 1) - 1) & 1, abort_flag)) break;
+                if (seg >= ND && !warp_wait(d_empty(seg % ND), ((seg / ND) - 1) & 1, abort_flag)) break;
             }
-            const int a = i % NA, d = seg & 1;
+            const int a = i % NA, d = seg % ND;
             // a_full also covers the activation block: its warpgroup waited for full_x before arriving
             if (!warp_wait(a_full(a), (i / NA) & 1, abort_flag)) break;
             tc_fence_after();
@@ -484,22 +491,40 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
                 mbar_arrive(a_full(a));
             }
             if (wg == 0 && last) {
-                const int d = seg & 1;
-                if (!warp_wait(d_full(d), (seg >> 1) & 1, abort_flag)) break;
+                const int d = seg % ND;
+                if (!warp_wait(d_full(d), (seg / ND) & 1, abort_flag)) break;
                 tc_fence_after();
-                float v[NP];
-                tmem_ld_cols<NP>(tmem + lane_base + d * NP, v);
-                tc_fence_before();
-                mbar_arrive(d_empty(d));
                 const GemmTask& task = p.task[cu.k];
                 const int m = cu.tile * kRows + r;
                 const int T = p.T, M = task.M;
-                if (!dep_done) { grid_dep_wait(); dep_done = true; }
-                if (m < M) {
-                    float* zp = task.z + m;
+                float* zp = task.z + m;
+                if constexpr (NP <= 64) {
+                    float v[NP];
+                    tmem_ld_cols<NP>(tmem + lane_base + d * NP, v);
+                    tc_fence_before();
+                    mbar_arrive(d_empty(d));
+                    if (!dep_done) { grid_dep_wait(); dep_done = true; }
+                    if (m < M) {
 #pragma unroll
-                    for (int t = 0; t < NP; ++t)
-                        if (t < T) atomicAdd(zp + (size_t)t * M, v[t] * kOutScale);   // fire-and-forget reduction
+                        for (int t = 0; t < NP; ++t)
+                            if (t < T) atomicAdd(zp + (size_t)t * M, v[t] * kOutScale);   // fire-and-forget reduction
+                    }
+                } else {
+                    // 32 accumulator columns at a time; the buffer is released after the last load
+                    if (!dep_done) { grid_dep_wait(); dep_done = true; }
+                    for (int c0 = 0; c0 < NP; c0 += 32) {
+                        float v[32];
+                        tmem_ld_cols<32>(tmem + lane_base + d * NP + c0, v);
+                        if (c0 + 32 == NP) {
+                            tc_fence_before();
+                            mbar_arrive(d_empty(d));
+                        }
+                        if (m < M) {
+#pragma unroll
+                            for (int t = 0; t < 32; ++t)
+                                if (c0 + t < T) atomicAdd(zp + (size_t)(c0 + t) * M, v[t] * kOutScale);
+                        }
+                    }
                 }
             }
             cu.next(p);
@@ -951,7 +976,9 @@ cudaError_t launch_bits(const GemmArgs& a, int grid, cudaStream_t stream) {
     }
     if (a.T <= 16) return launch_t<BITS, 16>(a, grid, stream);
     if (a.T <= 32) return launch_t<BITS, 32>(a, grid, stream);
-    return launch_t<BITS, 64>(a, grid, stream);
+    if (a.T <= 64) return launch_t<BITS, 64>(a, grid, stream);
+    if (a.T <= 128) return launch_t<BITS, 128>(a, grid, stream);
+    return launch_t<BITS, 256>(a, grid, stream);
 }
 
 }  // namespace
@@ -967,6 +994,8 @@ cudaError_t launch_gemm(const GemmArgs& a, int bits, int grid, cudaStream_t stre
         default: return cudaErrorInvalidValue;
     }
 }
+
+int gemm_ctas_per_sm(int T) { return T > 64 ? 1 : kGemmCtasPerSm; }
 
 cudaError_t read_and_clear_error(int* flag, cudaStream_t stream) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_nest_error, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);

@@ -49,7 +49,9 @@ constexpr int kMaxGrid = 1024;
 constexpr int kGemmCtasPerSm = 2;     // resident GEMM CTAs per SM (matches the kernel's launch bounds)
 
 inline int n_tiles(int M) { return (M + 127) / 128; }
-inline int n_pad(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
+constexpr int kMaxT = 256;                // tokens per call (verify trees up to prefill-size chunks)
+inline int n_pad(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : (T <= 64 ? 64 : (T <= 128 ? 128 : 256))); }
+int gemm_ctas_per_sm(int T);              // resident CTAs per SM of the GEMM launched for T tokens
 
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel in the stream is still running; it must call

@@ -56,7 +56,7 @@ extern "C" nest_status nest_linear_static(const nest_layer* layer, int32_t verif
     if (layer == nullptr || x == nullptr || y == nullptr) return NEST_ERR_INVALID_ARG;
     if (layer->M < 1 || layer->K < 1 || T < 1) return NEST_ERR_INVALID_ARG;
     const size_t need = nest_linear_scratch_bytes(layer->M, layer->K, T);
-    if (need == 0) return NEST_ERR_UNSUPPORTED;               // K % 128 != 0 or T > 64
+    if (need == 0) return NEST_ERR_UNSUPPORTED;               // K % 128 != 0 or T > 256
     if (need > kStaticScratchBytes) return NEST_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     const nest_status st = scratch_for_current_device(&scratch);

@@ -27,7 +27,7 @@ def to_dev(a, torch, dev):
 
 
 def n_pad(T):
-    return 16 if T <= 16 else (32 if T <= 32 else 64)
+    return next(n for n in (16, 32, 64, 128, 256) if T <= n)
 
 
 def decode_xop(buf, K, T):

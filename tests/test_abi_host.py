@@ -53,7 +53,8 @@ def test_sizes_match_reference_packer(lib, M, K, bits):
 def test_sizes_reject_bad_shapes(lib):
     assert nest.base_bytes(128, 100) == 0
     assert nest.resid_bytes(128, 128, 5) == 0
-    assert nest.xop_bytes(128, 65) == 0
+    assert nest.xop_bytes(128, 257) == 0
+    assert nest.xop_bytes(128, 65) == 256 * 128 and nest.xop_bytes(256, 200) == 2 * 256 * 256
     assert nest.xop_bytes(256, 1) == 2 * 256 * 16
     assert nest.xop_bytes(256, 17) == 2 * 256 * 32
     assert nest.linear_scratch_bytes(128, 128, 0) == 0
@@ -71,7 +72,7 @@ def test_gemm_argument_validation(lib):
     assert f(None, ok, ok, 16, None) == 1                              # null layer
     assert f(ctypes.byref(L), None, ok, 16, None) == 1                 # null operand
     assert f(ctypes.byref(L), ok, ok, 0, None) == 1                    # T < 1
-    assert f(ctypes.byref(L), ok, ok, 65, None) == 2                   # T > 64
+    assert f(ctypes.byref(L), ok, ok, 257, None) == 2                  # T > 256
     assert f(ctypes.byref(_layer(K=200)), ok, ok, 4, None) == 2         # K % 128
     assert f(ctypes.byref(_layer(bits=5)), ok, ok, 4, None) == 2        # bit width
     assert f(ctypes.byref(_layer(bits=0)), ok, ok, 4, None) == 1        # verify needs a residual
@@ -98,7 +99,7 @@ def test_rotate_pack_quantize_validation(lib):
     assert r(ok, 1, ok, 128, 4, 2, ok, None, None) == 1          # mode
     assert r(ok, 1, ok, 128, 4, 0, None, None, None) == 1        # no output
     assert r(ok, 1, ok, 100, 4, 0, None, ok, None) == 2          # operand needs n % 128
-    assert r(ok, 1, ok, 128, 65, 0, None, ok, None) == 2         # operand needs T <= 64
+    assert r(ok, 1, ok, 128, 257, 0, None, ok, None) == 2        # operand needs T <= 256
     assert r(ok, 1, ok, 128, 4, 1, None, ok, None) == 1          # operand only on the input side
     assert r(ok, 1, ok, 128, 4, 0, None, ctypes.c_void_p(0x50002), None) == 3
     p = lib.nest_pack
@@ -116,7 +117,7 @@ def test_chain_and_rotate_group_validation(lib):
     ok = ctypes.c_void_p(0x50000)
     assert lib.nest_chain_work_bytes(5376, 64) == 256 * ((64 * 2 * 4 + 255) // 256)
     assert lib.nest_chain_work_bytes(21504, 64) == 64 * 6 * 4
-    assert lib.nest_chain_work_bytes(100, 65) == 0
+    assert lib.nest_chain_work_bytes(100, 257) == 0
     L = nest._Layer(256, 512, 0, 0x50000, None, 0x50000, 0x50000)
     nx = (nest._Layer * 1)(L)
     xo = (ctypes.c_void_p * 1)(0x50000)
@@ -124,7 +125,7 @@ def test_chain_and_rotate_group_validation(lib):
     assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, None, None) == 1       # work missing
     assert c(ok, ok, ok, None, 512, 4, None, nx, 1, xo, None, ok, None) == 1         # partner sign missing
     assert c(ok, ok, ok, ok, 512, 4, None, nx, 1, xo, None, ok, None) == 1           # z_b aliases z_a
-    assert c(ok, ok, None, None, 512, 65, None, nx, 1, xo, None, ok, None) == 2      # T > 64
+    assert c(ok, ok, None, None, 512, 257, None, nx, 1, xo, None, ok, None) == 2     # T > 256
     assert c(ok, ok, None, None, 640, 4, None, nx, 1, xo, None, ok, None) == 1       # next K != M
     assert c(ok, ok, None, None, 500, 4, None, nx, 1, xo, None, ok, None) == 2       # operand needs M % 128
     assert c(ok, ok, None, None, 512, 4, None, nx, 4, xo, None, ok, None) == 2       # more than 3 next

@@ -40,7 +40,7 @@ def dev():
 
 @pytest.mark.parametrize("M,T,product,in_place,n_next", [
     (512, 1, False, False, 2), (5376, 17, True, False, 2), (3840, 64, False, True, 2), (8192, 5, True, True, 1),
-    (21504, 3, True, False, 1), (300, 4, True, False, 0), (4096, 2, False, True, 3)])
+    (21504, 3, True, False, 1), (300, 4, True, False, 0), (4096, 2, False, True, 3), (5376, 160, True, False, 2)])
 def test_chain_kernel(dev, M, T, product, in_place, n_next):
     """Out-rotation (+ product), RMS rescale, bf16 cast and next in-rotations; ragged last
     4096-element segments (5376, 21504), a segment shorter than one (300, 3840), h in place."""

@@ -309,3 +309,32 @@ def test_full_size_sampled_rows(dev, name, idx, T):
 
 def test_error_flag_clear(dev):
     nest.error_check()
+
+
+# ----------------------------------------------------------------------------
+# prefill-size token counts (65..256): one CTA per SM, N up to 256 per MMA
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,bits", [(200, 384, 7), (1280, 1024, 8), (129, 256, 6)])
+def test_gemm_parity_prefill(dev, M, K, bits):
+    W, s_o, s_i, q = ref_layer(M, K, bits, seed=13)
+    layer = dev_layer(q, bits, s_o, s_i, dev)
+    for T in (65, 100, 128, 129, 200, 256):
+        x, xv = bf16_x(T, K, 110 + T, dev)
+        for verify in (False, True):
+            z = run_gemm(layer, x, verify, dev)
+            parity(z, O.forward(q, s_o, s_i, xv, verify)["z"])
+    nest.error_check()
+
+
+def test_linear_and_group_prefill(dev):
+    shapes = [(384, 512), (200, 1024)]
+    refs = [ref_layer(M, K, 7, seed=21 + i) for i, (M, K) in enumerate(shapes)]
+    layers = [dev_layer(q, 7, so, si, dev) for (W, so, si, q) in refs]
+    for T in (96, 256):
+        xs = [bf16_x(T, K, 130 + i + T, dev) for i, (M, K) in enumerate(shapes)]
+        for verify in (False, True):
+            ys = nest.linear_group(layers, [x for x, _ in xs], verify)
+            for (W, so, si, q), (x, xv), y in zip(refs, xs, ys):
+                parity(y.cpu().numpy(), O.forward(q, so, si, xv, verify)["y"])
+    nest.error_check()

@@ -137,3 +137,17 @@ def test_draft_is_exact_subset(dev):
     b = nest.gemm(L, xop, 16, True).cpu().numpy().astype(np.float64)
     scale = np.sqrt(np.mean(a * a))
     assert np.max(np.abs(a - b)) <= 1e-6 * 64 * scale
+
+
+def test_w4w8_prefill(dev):
+    M, K = 640, 1024
+    q4, s4, qr = _codes(M, K, 90)
+    s_o, s_i = synth.sign_pair(M, K, 91)
+    L = _layer(q4, s4, qr, s_o, s_i, dev)
+    lay = {"q4": q4, "s4": s4, "qr": qr}
+    for T in (128, 256):
+        xb, xv = synth.activations(T, K, 92 + T)
+        x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+        for verify in (False, True):
+            parity(nest.linear(L, x, verify).cpu().numpy(), O.forward_w4w8(lay, s_o, s_i, xv, verify)["y"])
+    nest.error_check()
