@@ -452,3 +452,81 @@ def bits_per_weight_w4w8(verify: bool) -> float:
     the fp16 group scale; the refinement plane 4 bits per weight and no scale
     (s_ref is derived from s4)."""
     return 4 + 16 / GROUP + (4 if verify else 0)
+
+
+# ----------------------------------------------------------------------------
+# Nested KV4/KV8 cache (BitNest paper, Section 3.4 and Appendix A.2, Eq. (11)-(14))
+# ----------------------------------------------------------------------------
+
+KV_DIM = 128
+
+
+def kv_quantize(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Online per-token, per-KV-head symmetric RTN of vectors x[..., d] (d = 128):
+
+        s = max_i |x_i| / 7,  q4 = clip(round(x / s), -8, 7)                         (Eq. (11))
+        q_r = clip(round((x - q4 s) / (s / 16)), -8, 7)                                (Eq. (13))
+
+    Readings: s is stored as fp16 and used as that fp16 value; round is half-to-even;
+    the decisions are taken in fp32 (the pages fix no precision; fp32 is the kernel's),
+    each operation rounded on its own (no fused multiply-add).  A zero vector gets s = 0
+    and zero codes.
+
+    Returns (q4 int8 [..., d], q_r int8 [..., d], s float16 [...])."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    s16 = (amax / np.float32(7.0)).astype(np.float32).astype(np.float16)
+    s = s16.astype(np.float32)[..., None]
+    nz = s > 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q4 = np.where(nz, np.clip(np.rint(x32 / s), -8, 7), 0).astype(np.float32)
+        sref = s / np.float32(16.0)
+        res = (x32 - (q4 * s).astype(np.float32)).astype(np.float32)
+        qr = np.where(nz, np.clip(np.rint(res / sref), -8, 7), 0)
+    return q4.astype(np.int8), qr.astype(np.int8), s16
+
+
+def kv_dequant(q4: np.ndarray, qr: np.ndarray, s16: np.ndarray, view: int) -> np.ndarray:
+    """KV4 view q4 s (Eq. (12)) or KV8 view (16 q4 + q_r) s / 16 (Eq. (14)), float64."""
+    s = s16.astype(np.float64)[..., None]
+    if view == 4:
+        return q4.astype(np.float64) * s
+    return (16 * q4.astype(np.int64) + qr.astype(np.int64)).astype(np.float64) * (s / 16.0)
+
+
+def kv_attention(q: np.ndarray, k: Tuple[np.ndarray, np.ndarray, np.ndarray],
+                 v: Tuple[np.ndarray, np.ndarray, np.ndarray], L: int, view: int, recent_n: int) -> np.ndarray:
+    """Decode attention over a nested cache, float64.
+
+    q: [T][Hq][d] queries of the T newest tokens (already written at positions L-T..L-1);
+    k, v: (q4, q_r, s) with q4/q_r [Hkv][Lmax][d] and s [Hkv][Lmax].  Query head h reads
+    KV head h // (Hq / Hkv) (grouped-query attention).  Query t sees positions
+    [0, L - T + t + 1) (causal), with scores q.k / sqrt(d) and a softmax over them.
+    View 8 reads KV8 everywhere (verification); view 4 reads the KV4 base (drafting)
+    except the newest recent_n positions of the cache, j >= L - recent_n, which are read
+    at KV8 (the Recent-N policy of Appendix A.2).
+
+    Returns out [T][Hq][d]."""
+    q = np.asarray(q, dtype=np.float64)
+    T, Hq, d = q.shape
+    Hkv = k[0].shape[0]
+    G = Hq // Hkv
+    K8 = kv_dequant(k[0][:, :L], k[1][:, :L], k[2][:, :L], 8)
+    V8 = kv_dequant(v[0][:, :L], v[1][:, :L], v[2][:, :L], 8)
+    if view == 4:
+        K4 = kv_dequant(k[0][:, :L], k[1][:, :L], k[2][:, :L], 4)
+        V4 = kv_dequant(v[0][:, :L], v[1][:, :L], v[2][:, :L], 4)
+        hi = np.arange(L) >= L - recent_n
+        Kv = np.where(hi[None, :, None], K8, K4)
+        Vv = np.where(hi[None, :, None], V8, V4)
+    else:
+        Kv, Vv = K8, V8
+    out = np.zeros((T, Hq, d))
+    for t in range(T):
+        n = L - T + t + 1
+        for h in range(Hq):
+            kh = h // G
+            sc = Kv[kh, :n] @ q[t, h] / math.sqrt(d)
+            p = np.exp(sc - sc.max())
+            out[t, h] = (p / p.sum()) @ Vv[kh, :n]
+    return out

@@ -564,3 +564,64 @@ def test_w4w8_pack_hand_worked_examples():
     assert ref[(128 + 1) * 16 + 1] & 0x0F == 0xD
     assert base[8192 + 2] == 0x00 and base[8192 + 3] == 0x3C
     assert base[17] == 0x88                      # untouched columns hold q = 0 (u = 8)
+
+
+# ----------------------------------------------------------------------------
+# nested KV4/KV8 cache (BitNest paper, Section 3.4, Appendix A.2)
+# ----------------------------------------------------------------------------
+
+def test_kv_quantize_nearest_codes_and_views():
+    """Eq. (11)-(14): the base is the nearest of 16 levels of s, the refinement the nearest
+    of 16 levels of s/16 around it; KV8 = (16 q4 + q_r) s/16 exactly equals q4 s + q_r s/16."""
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=(6, 4, 128)).astype(np.float32) * rng.uniform(0.1, 4, size=(6, 4, 1)).astype(np.float32)
+    q4, qr, s16 = O.kv_quantize(x)
+    s = s16.astype(np.float64)[..., None]
+    amax = np.abs(x).max(axis=-1)
+    assert np.all(np.abs(s16.astype(np.float64) * 7 - amax) <= amax * 2.0 ** -10)
+    levels = np.arange(-8, 8)
+    e4 = np.abs(x[..., None] - levels * s[..., None])
+    assert np.allclose(np.abs(x - q4 * s), e4.min(axis=-1), rtol=0, atol=1e-6 * amax.max())
+    r = x - q4 * s
+    er = np.abs(r[..., None] - levels * (s / 16)[..., None])
+    assert np.allclose(np.abs(r - qr * s / 16), er.min(axis=-1), rtol=0, atol=1e-6 * amax.max())
+    k8 = O.kv_dequant(q4, qr, s16, 8)
+    assert np.array_equal(k8, O.kv_dequant(q4, qr, s16, 4) + qr * (s / 16))
+    assert np.all(np.abs(x - k8) <= s / 16 * (1 + 1e-6))                 # <= s_ref (clip at +7), ~s_ref/2 typical
+    assert np.abs(x - k8).mean() < np.abs(x - O.kv_dequant(q4, qr, s16, 4)).mean() / 8
+    assert q4.min() >= -7                                                  # s = max/7 never needs -8
+    z = np.zeros((1, 128), np.float32)
+    zq4, zqr, zs = O.kv_quantize(z)
+    assert zs[0] == 0 and not zq4.any() and not zqr.any()
+
+
+def test_kv_attention_bruteforce_and_policies():
+    """Causal GQA decode attention against explicit loops; Recent-N = 0 is the pure KV4 view,
+    Recent-N >= L the pure KV8 view; a one-position window reduces to that value."""
+    rng = np.random.default_rng(7)
+    Hkv, G, L, T, d = 2, 3, 11, 3, 128
+    kx = rng.normal(size=(Hkv, 16, d)).astype(np.float32)
+    vx = rng.normal(size=(Hkv, 16, d)).astype(np.float32)
+    k = O.kv_quantize(kx)
+    v = O.kv_quantize(vx)
+    q = rng.normal(size=(T, Hkv * G, d))
+    out = O.kv_attention(q, k, v, L, 8, 0)
+    K8 = O.kv_dequant(*k, 8)
+    V8 = O.kv_dequant(*v, 8)
+    for t in range(T):
+        for h in range(Hkv * G):
+            n = L - T + t + 1
+            w = [math.exp(sum(K8[h // G, j, i] * q[t, h, i] for i in range(d)) / math.sqrt(d)) for j in range(n)]
+            ref = sum(w[j] * V8[h // G, j] for j in range(n)) / sum(w)
+            assert np.allclose(out[t, h], ref, rtol=1e-10, atol=1e-12)
+    assert np.allclose(O.kv_attention(q, k, v, L, 4, L), out, rtol=0, atol=1e-14)
+    o4 = O.kv_attention(q, k, v, L, 4, 0)
+    K4 = O.kv_dequant(*k, 4)
+    V4 = O.kv_dequant(*v, 4)
+    sc = K4[0, :L - T + 1] @ q[0, 0] / math.sqrt(d)
+    p = np.exp(sc - sc.max())
+    assert np.allclose(o4[0, 0], p / p.sum() @ V4[0, :L - T + 1], rtol=1e-12)
+    one = O.kv_attention(q[:1], k, v, 1, 4, 0)
+    assert np.allclose(one[0, 0], V4[0, 0], rtol=1e-12)
+    mixed = O.kv_attention(q, k, v, L, 4, 3)
+    assert not np.allclose(mixed, o4) and not np.allclose(mixed, out)
