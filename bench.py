@@ -594,6 +594,80 @@ def run_stack(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------
+# nested KV4/KV8 cache: decode attention at a 31B-class head configuration
+# ----------------------------------------------------------------------------
+
+def run_kv(args):
+    import numpy as np
+    import torch
+    from nested_bit_quantized_gb300 import build as nb
+    from nested_bit_quantized_gb300 import nest
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    nb.build()
+    nest.load()
+    Hq, Hkv, d = 64, 32, 128                      # q 8192 = 64 x 128, k/v 4096 = 32 x 128
+    L = args.context
+    copies = 2                                    # two layers' caches, alternating (>= L2 for KV4 at 32K)
+    g = torch.Generator(device=dev).manual_seed(7)
+    caches = []
+    for c in range(copies):
+        kc, vc = nest.KVCache(Hkv, L, dev), nest.KVCache(Hkv, L, dev)
+        for s0 in range(0, L, 4096):
+            n = min(4096, L - s0)
+            nest.kv_write(kc, torch.randn((n, Hkv, d), generator=g, device=dev), s0)
+            nest.kv_write(vc, torch.randn((n, Hkv, d), generator=g, device=dev), s0)
+        caches.append((kc, vc))
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    hbm, _ = peaks()
+    recs = []
+    for name, T, view, rn in (("draft KV4", 1, 4, 0), ("draft KV4 + Recent-1024", 1, 4, 1024),
+                              ("verify KV8", 16, 8, 0), ("draft KV8", 1, 8, 0)):
+        q = torch.randn((T, Hq, d), generator=g, device=dev).to(torch.bfloat16)
+        out = torch.empty((T, Hq, d), dtype=torch.float32, device=dev)
+        work = torch.empty(int(nest.load().nest_kv_attention_work_bytes(T, Hq, Hkv, L)) // 4 + 1,
+                           dtype=torch.float32, device=dev)
+
+        def fn():
+            for kc, vc in caches:
+                nest.kv_attention(q, kc, vc, L, view, rn, out=out, work=work)
+        with torch.cuda.stream(stream):
+            fn()
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                fn()
+        for _ in range(3):
+            gr.replay()
+        torch.cuda.synchronize()
+        reps = max(10, args.steps)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            s.record(stream)
+            for _ in range(reps):
+                gr.replay()
+            e.record(stream)
+        torch.cuda.synchronize()
+        us = s.elapsed_time(e) * 1e3 / reps / copies
+        hi = min(rn, L) if view == 4 else L
+        per_pos = (64 + 2) * 2 if view == 4 else (128 + 2) * 2        # K and V rows read per position
+        by = Hkv * ((L - hi) * per_pos + hi * (128 + 2) * 2) + T * Hq * d * (2 + 4)
+        recs.append({"case": name, "T": T, "us_per_layer": us, "GBps": by / (us * 1e-6) / 1e9,
+                     "frac_of_measured_hbm": by / (us * 1e-6) / 1e9 / hbm, "bytes": by})
+        del gr
+    nest.error_check()
+    line = {"metric": "nested KV-cache decode attention, effective HBM GB/s per layer", "value": recs[0]["GBps"],
+            "unit": "GB/s", "n_gpus": 1, "higher_is_better": True, "dtype": "f32 (4-bit planes)",
+            "data": "synthetic",
+            "config": {"workload": f"KV4/KV8 nested cache, Hq={Hq}, Hkv={Hkv}, d={d}, context {L}, "
+                                   f"{copies} layers' caches alternating"},
+            "cases": recs}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -606,7 +680,8 @@ def main():
     ap.add_argument("--codec", default="l2", choices=["l2", "w4w8"],
                     help="weight codec of the default workload: l2 (2-bit base + 7-bit residual, the metric's) "
                          "or w4w8 (BitNest W4 base + 4-bit refinement)")
-    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "decoder_31b", "stack_31b"],
+    ap.add_argument("--context", type=int, default=32768, help="context length of --workload kv_31b")
+    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "decoder_31b", "stack_31b", "kv_31b"],
                     help="mlp_triplet_4b (default, the metric's workload), one chained 31B-class layer, "
                          "or the 60-layer 31B-class speculative cycle")
     ap.add_argument("--layers", type=int, default=0, help="layers of the 31B-class stack (default 1 or 60)")
@@ -617,6 +692,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.workload == "kv_31b":
+        run_kv(args)
     elif args.workload != WORKLOAD:
         run_stack(args)
     else:

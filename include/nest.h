@@ -295,6 +295,49 @@ nest_status nest_rotate_group(const nest_rotate_task* tasks, int32_t count, int3
 nest_status nest_linear_static(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype,
                                int32_t T, float* y, void* stream);
 
+/* ---- nested KV4/KV8 cache (BitNest paper, Section 3.4, Appendix A.2) ------ */
+
+/* One cache (keys or values) of H heads x Lmax positions, head dimension 128.
+ *   base  [H][Lmax][64] bytes: byte i of a row holds dims 2i (low nibble) and 2i+1
+ *                              (high nibble) as q4 + 8;
+ *   ref   [H][Lmax][64] bytes: the refinement codes q_r + 8, same layout;
+ *   scale [H][Lmax] fp16 bits: s = max|x| / 7 of the row.
+ * base and ref 16-byte aligned, scale 2-byte aligned; nest_kv_plane_bytes(H, Lmax)
+ * bytes each for base and ref, 2*H*Lmax bytes for scale. */
+typedef struct {
+    uint8_t* base;
+    uint8_t* ref;
+    uint16_t* scale;
+    int32_t H;
+    int32_t Lmax;
+} nest_kv_cache;
+
+size_t nest_kv_plane_bytes(int32_t H, int32_t Lmax);
+
+/* Quantise-on-write (Eq. (11), (13)): the key or value vectors x [T][H][128] (fp32 for
+ * x_dtype 0, bf16 bits for 1) of T new tokens are stored at positions pos0 .. pos0+T-1:
+ * s = fp16(max|x| / 7), q4 = clip(rint(x / s), -8, 7), q_r = clip(rint((x - q4 s) /
+ * (s / 16)), -8, 7), decided in fp32 with each operation rounded on its own.
+ * Needs 0 <= pos0, pos0 + T <= Lmax, 1 <= T. */
+nest_status nest_kv_write(const void* x, int32_t x_dtype, int32_t T, const nest_kv_cache* cache, int32_t pos0,
+                          void* stream);
+
+/* Decode attention over the nested caches (grouped-query: query head h reads KV head
+ * h / (Hq / Hkv)).  q [T][Hq][128] (fp32 or bf16 bits per q_dtype) are the queries of
+ * the T newest tokens, whose keys and values are already written at positions
+ * L-T .. L-1; query t sees positions 0 .. L-T+t (causal), scores q.k / sqrt(128),
+ * softmax, out [T][Hq][128] fp32 = sum p v.
+ * view 8: the KV8 view (16 q4 + q_r) s / 16 everywhere (verification);
+ * view 4: the KV4 view q4 s (drafting), except positions >= L - recent_n, read at KV8
+ *         (the Recent-N policy; recent_n = 0 is pure KV4).
+ * work: nest_kv_attention_work_bytes(T, Hq, Hkv, L) bytes of device memory (no
+ * initial contents); two launches (position splits, then their combination).
+ * Needs Hq % Hkv == 0, k->H == v->H == Hkv, k->Lmax == v->Lmax, T <= L <= Lmax. */
+size_t nest_kv_attention_work_bytes(int32_t T, int32_t Hq, int32_t Hkv, int32_t L);
+nest_status nest_kv_attention(const void* q, int32_t q_dtype, int32_t T, int32_t Hq, const nest_kv_cache* k,
+                              const nest_kv_cache* v, int32_t L, int32_t view, int32_t recent_n, float* out,
+                              float* work, void* stream);
+
 /* Reads and clears the device-side error flag that kernels set when a pipeline
  * wait runs past its limit.  Synchronises `stream`.  Returns NEST_ERR_TIMEOUT if
  * the flag was set, NEST_ERR_CUDA on a CUDA error, NEST_OK otherwise. */

@@ -408,6 +408,76 @@ nest_status nest_rotate_group(const nest_rotate_task* tasks, int32_t count, int3
     return from_cuda(launch_rotate_group(a, x_dtype, mode, T, as_stream(stream)));
 }
 
+size_t nest_kv_plane_bytes(int32_t H, int32_t Lmax) {
+    if (H < 1 || Lmax < 1) return 0;
+    return (size_t)H * Lmax * 64;
+}
+
+static nest_status check_kv(const nest_kv_cache* c) {
+    if (c == nullptr || !c->base || !c->ref || !c->scale) return NEST_ERR_INVALID_ARG;
+    if (c->H < 1 || c->Lmax < 1) return NEST_ERR_INVALID_ARG;
+    if (!aligned16(c->base) || !aligned16(c->ref) || (reinterpret_cast<uintptr_t>(c->scale) & 1u))
+        return NEST_ERR_MISALIGNED;
+    return NEST_OK;
+}
+
+nest_status nest_kv_write(const void* x, int32_t x_dtype, int32_t T, const nest_kv_cache* cache, int32_t pos0,
+                          void* stream) {
+    nest_status st = check_kv(cache);
+    if (st != NEST_OK) return st;
+    if (x == nullptr || T < 1 || pos0 < 0 || (x_dtype != 0 && x_dtype != 1)) return NEST_ERR_INVALID_ARG;
+    if ((long long)pos0 + T > cache->Lmax) return NEST_ERR_INVALID_ARG;
+    if ((long long)T * cache->H * 32 >= (1LL << 31)) return NEST_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(x) & (x_dtype == 1 ? 1u : 3u)) return NEST_ERR_MISALIGNED;
+    return from_cuda(launch_kv_write(x, x_dtype, T, cache->H, pos0, cache->Lmax, cache->base, cache->ref,
+                                     cache->scale, as_stream(stream)));
+}
+
+size_t nest_kv_attention_work_bytes(int32_t T, int32_t Hq, int32_t Hkv, int32_t L) {
+    if (T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || L < T) return 0;
+    const int sms = device_sms();
+    if (sms <= 0) return 0;
+    const int G = Hq / Hkv;
+    const int rows = kv_rows_per_tile();
+    const long long tiles = ((long long)T * G + rows - 1) / rows;
+    const long long ns = kv_splits(T, G, Hkv, L, sms);
+    return (size_t)Hkv * tiles * ns * rows * (128 + 2) * sizeof(float);
+}
+
+nest_status nest_kv_attention(const void* q, int32_t q_dtype, int32_t T, int32_t Hq, const nest_kv_cache* k,
+                              const nest_kv_cache* v, int32_t L, int32_t view, int32_t recent_n, float* out,
+                              float* work, void* stream) {
+    nest_status st = check_kv(k);
+    if (st == NEST_OK) st = check_kv(v);
+    if (st != NEST_OK) return st;
+    if (!q || !out || !work || T < 1 || Hq < 1 || (q_dtype != 0 && q_dtype != 1)) return NEST_ERR_INVALID_ARG;
+    if (view != 4 && view != 8) return NEST_ERR_INVALID_ARG;
+    if (recent_n < 0) return NEST_ERR_INVALID_ARG;
+    const int Hkv = k->H;
+    if (v->H != Hkv || Hq % Hkv) return NEST_ERR_INVALID_ARG;
+    if (L < T || L > k->Lmax || L > v->Lmax) return NEST_ERR_INVALID_ARG;
+    if ((long long)T * (Hq / Hkv) > 65535LL * kv_rows_per_tile()) return NEST_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(q) & (q_dtype == 1 ? 1u : 3u)) || (reinterpret_cast<uintptr_t>(out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(work) & 3u))
+        return NEST_ERR_MISALIGNED;
+    if (!device_supported()) return NEST_ERR_UNSUPPORTED;
+    const int sms = device_sms();
+    if (sms <= 0) return NEST_ERR_CUDA;
+    KvAttnArgs a = {};
+    a.q = q;
+    a.q_bf16 = q_dtype;
+    a.kbase = k->base; a.kref = k->ref; a.kscale = k->scale;
+    a.vbase = v->base; a.vref = v->ref; a.vscale = v->scale;
+    a.out = out;
+    a.work = work;
+    a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.L = L;
+    if (k->Lmax != v->Lmax) return NEST_ERR_INVALID_ARG;
+    a.Lmax = k->Lmax;
+    a.view = view;
+    a.recent_n = recent_n;
+    return from_cuda(launch_kv_attention(a, sms, as_stream(stream)));
+}
+
 nest_status nest_error_check(void* stream) {
     int flag = 0;
     cudaError_t e = read_and_clear_error(&flag, as_stream(stream));

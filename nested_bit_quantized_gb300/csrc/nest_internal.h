@@ -124,4 +124,20 @@ cudaError_t launch_quantize(const float* W, const int8_t* so, const int8_t* si, 
 
 int hadamard_block(int n);
 
+// Nested KV cache (nest_kv.cu).
+struct KvAttnArgs {
+    const void* q;            // [T][Hq][128] queries
+    int q_bf16;
+    const uint8_t *kbase, *kref, *vbase, *vref;
+    const uint16_t *kscale, *vscale;
+    float* out;               // [T][Hq][128]
+    float* work;              // per (head, tile, split, row): max, sum, 128 partial outputs
+    int T, Hq, Hkv, G, L, Lmax, view, recent_n, nsplit, ntiles;
+};
+cudaError_t launch_kv_write(const void* x, int bf16, int T, int H, int pos0, int Lmax, uint8_t* base, uint8_t* ref,
+                            uint16_t* scale, cudaStream_t stream);
+cudaError_t launch_kv_attention(KvAttnArgs& a, int sms, cudaStream_t stream);
+int kv_rows_per_tile();
+int kv_splits(int T, int G, int Hkv, int L, int sms);
+
 }  // namespace nest

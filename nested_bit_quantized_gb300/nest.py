@@ -31,6 +31,10 @@ class NestError(RuntimeError):
 CODEC_L2, CODEC_W4W8 = 0, 1     # nest_layer.codec (include/nest.h)
 
 
+class _KvCache(ctypes.Structure):
+    _fields_ = [("base", _P), ("ref", _P), ("scale", _P), ("H", _I32), ("Lmax", _I32)]
+
+
 class _Layer(ctypes.Structure):
     _fields_ = [("M", _I32), ("K", _I32), ("resid_bits", _I32),
                 ("base", _P), ("resid", _P), ("sign_out", _P), ("sign_in", _P), ("codec", _I32)]
@@ -85,6 +89,11 @@ def load() -> ctypes.CDLL:
         "nest_chain": ([_P, _P, _P, _P, _I32, _I32, _P, ctypes.POINTER(_Layer), _I32, ctypes.POINTER(_P),
                         ctypes.POINTER(_P), _P, _P], _I32),
         "nest_rotate_group": ([ctypes.POINTER(RotateTask), _I32, _I32, _I32, _I32, _P], _I32),
+        "nest_kv_plane_bytes": ([_I32, _I32], _SZ),
+        "nest_kv_write": ([_P, _I32, _I32, ctypes.POINTER(_KvCache), _I32, _P], _I32),
+        "nest_kv_attention_work_bytes": ([_I32, _I32, _I32, _I32], _SZ),
+        "nest_kv_attention": ([_P, _I32, _I32, _I32, ctypes.POINTER(_KvCache), ctypes.POINTER(_KvCache), _I32, _I32,
+                               _I32, _P, _P, _P], _I32),
         "nest_error_check": ([_P], _I32),
     }
     for name, (args, res) in sig.items():
@@ -405,3 +414,52 @@ def linear_group(layers, xs, verify: bool, ys=None, scratch: Optional[torch.Tens
                                   _ptr(scratch), _stream(stream))
     _check(st, "nest_linear_group")
     return ys
+
+
+# ----------------------------------------------------------------------------
+# nested KV4/KV8 cache
+# ----------------------------------------------------------------------------
+
+class KVCache:
+    """One nested cache (keys or values): base and refinement nibble planes and fp16 scales
+    for H heads x Lmax positions of dimension 128 (nest_kv_cache)."""
+
+    def __init__(self, H: int, Lmax: int, device="cuda"):
+        n = int(load().nest_kv_plane_bytes(H, Lmax))
+        if n == 0:
+            raise ValueError("bad cache shape")
+        self.H, self.Lmax = H, Lmax
+        self.base = torch.zeros(n, dtype=torch.uint8, device=device)
+        self.ref = torch.zeros(n, dtype=torch.uint8, device=device)
+        self.scale = torch.zeros(H * Lmax, dtype=torch.int16, device=device)
+
+    def c_struct(self) -> _KvCache:
+        return _KvCache(self.base.data_ptr(), self.ref.data_ptr(), self.scale.data_ptr(), self.H, self.Lmax)
+
+
+def kv_write(cache: KVCache, x: torch.Tensor, pos0: int, stream=None):
+    """nest_kv_write: store x [T][H][128] (fp32 or bf16) at positions pos0 .. pos0+T-1."""
+    dt = 1 if x.dtype == torch.bfloat16 else 0
+    _dev(x, x.dtype, "x")
+    C = cache.c_struct()
+    st = load().nest_kv_write(_ptr(x), dt, x.shape[0], ctypes.byref(C), pos0, _stream(stream))
+    _check(st, "nest_kv_write")
+
+
+def kv_attention(q: torch.Tensor, k: KVCache, v: KVCache, L: int, view: int, recent_n: int = 0,
+                 out: Optional[torch.Tensor] = None, work: Optional[torch.Tensor] = None, stream=None):
+    """nest_kv_attention: q [T][Hq][128] -> out [T][Hq][128] fp32."""
+    T, Hq, d = q.shape
+    dt = 1 if q.dtype == torch.bfloat16 else 0
+    _dev(q, q.dtype, "q")
+    lib = load()
+    if out is None:
+        out = torch.empty((T, Hq, d), dtype=torch.float32, device=q.device)
+    if work is None:
+        work = torch.empty(int(lib.nest_kv_attention_work_bytes(T, Hq, k.H, L)) // 4 + 1, dtype=torch.float32,
+                           device=q.device)
+    K, V = k.c_struct(), v.c_struct()
+    st = lib.nest_kv_attention(_ptr(q), dt, T, Hq, ctypes.byref(K), ctypes.byref(V), L, view, recent_n, _ptr(out),
+                               _ptr(work), _stream(stream))
+    _check(st, "nest_kv_attention")
+    return out

@@ -182,3 +182,22 @@ def test_w4w8_sizes_and_validation(lib):
     u = lib.nest_unpack_w4w8
     assert u(ctypes.byref(nest._Layer(256, 512, 4, 0x50000, 0x50000, 0x30000, 0x40000, nest.CODEC_L2)),
              ok, ok, ok, None) == 1
+
+
+def test_kv_cache_validation(lib):
+    assert lib.nest_kv_plane_bytes(8, 100) == 8 * 100 * 64 and lib.nest_kv_plane_bytes(0, 4) == 0
+    C = nest._KvCache(0x50000, 0x60000, 0x70000, 4, 64)
+    w = lib.nest_kv_write
+    ok = ctypes.c_void_p(0x50000)
+    assert w(ok, 0, 8, ctypes.byref(C), 60, None) == 1                    # past Lmax
+    assert w(ok, 2, 8, ctypes.byref(C), 0, None) == 1                     # dtype
+    assert w(ctypes.c_void_p(0x50002), 0, 8, ctypes.byref(C), 0, None) == 3
+    bad = nest._KvCache(0x50008, 0x60000, 0x70000, 4, 64)
+    assert w(ok, 0, 8, ctypes.byref(bad), 0, None) == 3
+    a = lib.nest_kv_attention
+    V = nest._KvCache(0x50000, 0x60000, 0x70000, 4, 64)
+    assert a(ok, 0, 2, 6, ctypes.byref(C), ctypes.byref(V), 32, 8, 0, ok, ok, None) == 1   # Hq % Hkv
+    assert a(ok, 0, 2, 8, ctypes.byref(C), ctypes.byref(V), 32, 5, 0, ok, ok, None) == 1   # view
+    assert a(ok, 0, 2, 8, ctypes.byref(C), ctypes.byref(V), 1, 8, 0, ok, ok, None) == 1    # L < T
+    assert a(ok, 0, 2, 8, ctypes.byref(C), ctypes.byref(V), 65, 8, 0, ok, ok, None) == 1   # L > Lmax
+    assert a(ok, 0, 2, 8, ctypes.byref(C), ctypes.byref(V), 32, 4, -1, ok, ok, None) == 1  # recent_n
