@@ -2,6 +2,7 @@
 // argument validation, launch configuration, and status codes.  No entry
 // point allocates memory or synchronises (except nest_error_check).
 #include <cstdint>
+#include <cstdlib>
 #include <cuda_runtime.h>
 
 #include "../../include/nest.h"
@@ -475,6 +476,8 @@ nest_status nest_kv_attention(const void* q, int32_t q_dtype, int32_t T, int32_t
     a.Lmax = k->Lmax;
     a.view = view;
     a.recent_n = recent_n;
+    const char* impl = getenv("NEST_KV_IMPL");            // "cuda": the CUDA-core kernel, for measurement
+    a.impl = (impl && impl[0] == 'c') ? 1 : 0;
     return from_cuda(launch_kv_attention(a, sms, as_stream(stream)));
 }
 

@@ -133,6 +133,7 @@ struct KvAttnArgs {
     float* out;               // [T][Hq][128]
     float* work;              // per (head, tile, split, row): max, sum, 128 partial outputs
     int T, Hq, Hkv, G, L, Lmax, view, recent_n, nsplit, ntiles;
+    int impl;                 // 0 tensor cores, 1 CUDA cores
 };
 cudaError_t launch_kv_write(const void* x, int bf16, int T, int H, int pos0, int Lmax, uint8_t* base, uint8_t* ref,
                             uint16_t* scale, cudaStream_t stream);

@@ -265,29 +265,361 @@ k_kv_attn(const __grid_constant__ KvAttnArgs a) {
     }
 }
 
-// out[t][h*G+g][:] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits
-__global__ void k_kv_combine(const __grid_constant__ KvAttnArgs a) {
+// ---------------------------------------------------------------------------
+// Tensor-core decode attention (mma.sync m16n8k16), 16 positions per warp step.
+//
+// QK: S[pos][row] = K[pos][:] . Q[row][:] with A = the key codes (16 positions x 16 dims
+// per k-step), B = the queries (16 dims x 8 rows).  The dims inside a k-step may be taken
+// in any order shared by A and B: thread q of a quad takes, in k-step s, dims
+// 32q + 4s .. 32q + 4s + 3, so over the 8 k-steps it reads bytes 16q .. 16q+15 of its two
+// key rows -- one 16-byte load per row, the quad reading the row's 64 bytes.
+// One code path serves both views: the byte (u4 << 4) | u_r minus 136 is the KV8 code
+// 16 q4 + q_r, and a position read at KV4 takes u_r = 8, giving 16 q4; every position's
+// scale is then s / 16, applied to its scores (keys) and to its probabilities (values).
+// PV: O^T[dim][row] += V^T[dim][pos] P^T[pos][row]: A = V^T loaded with ldmatrix.trans
+// from the block's values decoded to fp16 in shared memory, B = P^T from the score
+// fragments transposed in registers with movmatrix.
+// ---------------------------------------------------------------------------
+
+constexpr int kTcWarps = 4;
+constexpr int kTcThreads = 32 * kTcWarps;
+constexpr int kVPitch = 272;              // bytes per position row of a warp's fp16 value block (bank-conflict free)
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    return h2_as_u32(__floats2half2_rn(lo, hi));
+}
+
+__device__ __forceinline__ void mma16816f(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+// Four KV8 codes c = 16 u4 + u_r - 136 of one 32-bit base word and one refinement word
+// (dims 8w .. 8w+7 of a row, byte i = dims 2i | 2i+1), as fp16 pairs in dim order:
+// out[0] = (d0, d1), out[1] = (d2, d3), out[2] = (d4, d5), out[3] = (d6, d7).
+__device__ __forceinline__ void codes8(uint32_t b, uint32_t r, uint32_t (&out)[4]) {
+    // byte per dim: even dims from the low nibbles, odd dims from the high nibbles
+    const uint32_t ev = ((b << 4) & 0xF0F0F0F0u) | (r & 0x0F0F0F0Fu);          // dims 0, 2, 4, 6
+    const uint32_t od = (b & 0xF0F0F0F0u) | ((r >> 4) & 0x0F0F0F0Fu);          // dims 1, 3, 5, 7
+    const uint32_t p01 = prmt(ev, od, 0x5140u);                                 // dims 0, 1, 2, 3
+    const uint32_t p23 = prmt(ev, od, 0x7362u);                                 // dims 4, 5, 6, 7
+    const __half2 off = __float2half2_rn(1024.0f + 136.0f);
+    out[0] = h2_as_u32(__hsub2(u32_as_h2(prmt(p01, 0x64646464u, 0x5140u)), off));
+    out[1] = h2_as_u32(__hsub2(u32_as_h2(prmt(p01, 0x64646464u, 0x7362u)), off));
+    out[2] = h2_as_u32(__hsub2(u32_as_h2(prmt(p23, 0x64646464u, 0x5140u)), off));
+    out[3] = h2_as_u32(__hsub2(u32_as_h2(prmt(p23, 0x64646464u, 0x7362u)), off));
+}
+
+template <int NRT>
+constexpr int kv_tc_smem() {
+    constexpr int v = kTcWarps * 16 * kVPitch, o = kTcWarps * 8 * NRT * (kD + 1) * 4;
+    return (v > o ? v : o) + 2 * kTcWarps * 8 * NRT * 4;
+}
+
+template <int NRT>
+__global__ void __launch_bounds__(kTcThreads, 2)
+k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
+    constexpr int NRm = 8 * NRT;          // query rows per CTA
+    // dynamic shared memory: the warps' fp16 value blocks, later reused for the merge of
+    // the warps' outputs; the warps' softmax states after the larger of the two
+    extern __shared__ __align__(16) uint8_t dsm[];
+    constexpr int kVBytes = kTcWarps * 16 * kVPitch;
+    constexpr int kOBytes = kTcWarps * NRm * (kD + 1) * 4;
+    constexpr int kFront = kVBytes > kOBytes ? kVBytes : kOBytes;
+    uint8_t (*svb)[16 * kVPitch] = reinterpret_cast<uint8_t (*)[16 * kVPitch]>(dsm);
+    float (*so)[NRm][kD + 1] = reinterpret_cast<float (*)[NRm][kD + 1]>(dsm);
+    float (*sm)[NRm] = reinterpret_cast<float (*)[NRm]>(dsm + kFront);
+    float (*sl)[NRm] = reinterpret_cast<float (*)[NRm]>(dsm + kFront + kTcWarps * NRm * 4);
+    grid_dep_launch_dependents();
+    const int h = blockIdx.x, split = blockIdx.y, tile = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int R = a.T * a.G;
+    const int r0 = tile * NRm;
+    const int per = (a.L + a.nsplit - 1) / a.nsplit;
+    const int p0 = split * per, p1 = p0 + per < a.L ? p0 + per : a.L;
+    const size_t hrow = (size_t)h * a.Lmax;
+    const int recent0 = a.L - a.recent_n;
+    grid_dep_wait();
+
+    // B fragments of the queries (fp16, scaled by log2(e) / sqrt(d)), rows 8nt + g
+    uint32_t qb[NRT][8][2];
+    const float qscale = 1.4426950408889634f / sqrtf((float)kD);
+#pragma unroll
+    for (int nt = 0; nt < NRT; ++nt) {
+        const int row = r0 + 8 * nt + g;
+        const bool ok = row < R;
+        const int t = ok ? row / a.G : 0, gg = ok ? row % a.G : 0;
+        const size_t qi = ((size_t)t * a.Hq + (size_t)h * a.G + gg) * kD;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int dd = 32 * q + 4 * s + e;
+                float x = 0.0f;
+                if (ok) x = a.q_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.q)[qi + dd])
+                                     : reinterpret_cast<const float*>(a.q)[qi + dd];
+                v[e] = x * qscale;
+            }
+            qb[nt][s][0] = pack_h2(v[0], v[1]);
+            qb[nt][s][1] = pack_h2(v[2], v[3]);
+        }
+    }
+    // visible positions of the thread's two rows per n-tile (rows 8nt + 2q, 8nt + 2q + 1)
+    int vis[NRT][2];
+#pragma unroll
+    for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int row = r0 + 8 * nt + 2 * q + e;
+            vis[nt][e] = row < R ? a.L - a.T + row / a.G + 1 : 0;
+        }
+
+    float m[NRT][2], l[NRT][2], o[NRT][8][4];
+#pragma unroll
+    for (int nt = 0; nt < NRT; ++nt) {
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.0f;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) o[nt][dt][0] = o[nt][dt][1] = o[nt][dt][2] = o[nt][dt][3] = 0.0f;
+    }
+    uint8_t* vblk = svb[warp];
+    const uint32_t vblk_s = smem_u32(vblk);
+    // ldmatrix row addresses of matrix i/8, row i%8: positions (i%8) + 8*((i/8)/2), dims +8*((i/8)%2)
+    const int lm = lane >> 3, lr = lane & 7;
+    const uint32_t lda = vblk_s + (uint32_t)((lr + 8 * (lm >> 1)) * kVPitch + 16 * (lm & 1));
+
+    // Raw words of one 16-position block: keys (rows g, g+8; bytes 16q..16q+15) and values
+    // (position lane/2, dims 64*(lane&1) ..), base and refinement planes.  The next block's
+    // words are loaded before the current block is decoded.
+    struct Blk {
+        uint4 kb[2], kr[2], vb[2], vr[2];
+    };
+    auto load_blk = [&](int pb, Blk& B) {
+        const uint4 z = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int p = pb + g + 8 * e;
+            B.kb[e] = z;
+            B.kr[e] = z;
+            if (p < p1) {
+                B.kb[e] = *reinterpret_cast<const uint4*>(a.kbase + (hrow + p) * (kD / 2) + 16 * q);
+                if (a.view == 8 || p >= recent0)
+                    B.kr[e] = *reinterpret_cast<const uint4*>(a.kref + (hrow + p) * (kD / 2) + 16 * q);
+            }
+        }
+        const int p = pb + (lane >> 1);
+        const int half = lane & 1;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            B.vb[c] = z;
+            B.vr[c] = z;
+            if (p < p1) {
+                B.vb[c] = *reinterpret_cast<const uint4*>(a.vbase + (hrow + p) * (kD / 2) + 32 * half + 16 * c);
+                if (a.view == 8 || p >= recent0)
+                    B.vr[c] = *reinterpret_cast<const uint4*>(a.vref + (hrow + p) * (kD / 2) + 32 * half + 16 * c);
+            }
+        }
+    };
+    Blk nxt;
+    if (p0 + 16 * warp < p1) load_blk(p0 + 16 * warp, nxt);
+
+    for (int pb = p0 + 16 * warp; pb < p1; pb += 16 * kTcWarps) {
+        const Blk cur = nxt;
+        if (pb + 16 * kTcWarps < p1) load_blk(pb + 16 * kTcWarps, nxt);
+        const uint4* kb = cur.kb;
+        const uint4* kr = cur.kr;
+        float ks[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int p = pb + g + 8 * e;
+            ks[e] = p < p1 ? __half2float(__ushort_as_half(a.kscale[hrow + p])) * 0.0625f : 0.0f;
+        }
+        // ---- values: thread lane decodes position pb + lane/2, dims 64*(lane&1) .. +63 into fp16 ----
+        {
+            const int half = lane & 1;
+            uint8_t* dst = vblk + (lane >> 1) * kVPitch + 128 * half;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t bw[4] = {cur.vb[c].x, cur.vb[c].y, cur.vb[c].z, cur.vb[c].w};
+                const uint32_t rw[4] = {cur.vr[c].x, cur.vr[c].y, cur.vr[c].z, cur.vr[c].w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t cv[4];
+                    codes8(bw[w], rw[w], cv);
+                    *reinterpret_cast<uint4*>(dst + 64 * c + 16 * w) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
+                }
+            }
+        }
+        __syncwarp();
+
+        // ---- scores S[pos][row] ----
+        uint32_t ka[8][4];                    // A fragments: rows g (a0, a2), g + 8 (a1, a3) per k-step
+        {
+            const uint32_t b0w[4] = {kb[0].x, kb[0].y, kb[0].z, kb[0].w};
+            const uint32_t r0w[4] = {kr[0].x, kr[0].y, kr[0].z, kr[0].w};
+            const uint32_t b1w[4] = {kb[1].x, kb[1].y, kb[1].z, kb[1].w};
+            const uint32_t r1w[4] = {kr[1].x, kr[1].y, kr[1].z, kr[1].w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {     // word w: dims 32q + 8w .. +7 = k-steps 2w, 2w+1
+                uint32_t c0[4], c1[4];
+                codes8(b0w[w], r0w[w], c0);
+                codes8(b1w[w], r1w[w], c1);
+                ka[2 * w][0] = c0[0]; ka[2 * w][2] = c0[1]; ka[2 * w][1] = c1[0]; ka[2 * w][3] = c1[1];
+                ka[2 * w + 1][0] = c0[2]; ka[2 * w + 1][2] = c0[3]; ka[2 * w + 1][1] = c1[2]; ka[2 * w + 1][3] = c1[3];
+            }
+        }
+        float vsc[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int p = pb + g + 8 * e;
+            vsc[e] = p < p1 ? __half2float(__ushort_as_half(a.vscale[hrow + p])) * 0.0625f : 0.0f;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NRT; ++nt) {
+            float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int s = 0; s < 8; s += 2) {      // two independent accumulation chains
+                mma16816f(sc, ka[s][0], ka[s][1], ka[s][2], ka[s][3], qb[nt][s][0], qb[nt][s][1]);
+                mma16816f(sc2, ka[s + 1][0], ka[s + 1][1], ka[s + 1][2], ka[s + 1][3], qb[nt][s + 1][0],
+                          qb[nt][s + 1][1]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
+            // sc: (pos g, rows 2q, 2q+1), (pos g+8, rows 2q, 2q+1); scale, mask
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int pe = pb + g + 8 * (e >> 1), re = e & 1;
+                sc[e] = (pe < p1 && pe < vis[nt][re]) ? sc[e] * ks[e >> 1] : -INFINITY;
+            }
+            float pr[4];
+#pragma unroll
+            for (int re = 0; re < 2; ++re) {
+                float mx = fmaxf(sc[re], sc[2 + re]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float mn = fmaxf(m[nt][re], mx);
+                const float corr = mn == -INFINITY ? 1.0f : exp2f(m[nt][re] - mn);
+                const float e0 = sc[re] == -INFINITY ? 0.0f : exp2f(sc[re] - mn);
+                const float e1 = sc[2 + re] == -INFINITY ? 0.0f : exp2f(sc[2 + re] - mn);
+                float sum = e0 + e1;
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                l[nt][re] = l[nt][re] * corr + sum;
+                m[nt][re] = mn;
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) { o[nt][dt][re] *= corr; o[nt][dt][2 + re] *= corr; }
+                pr[re] = e0 * vsc[0];
+                pr[2 + re] = e1 * vsc[1];
+            }
+            // B fragments of P^T: b0 = positions 2q, 2q+1 of row g; b1 = positions 2q+8, 2q+9
+            const uint32_t pb0 = movmatrix_trans(pack_h2(pr[0], pr[1]));
+            const uint32_t pb1 = movmatrix_trans(pack_h2(pr[2], pr[3]));
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(lda + 32 * dt, v0, v1, v2, v3);
+                mma16816f(o[nt][dt], v0, v1, v2, v3, pb0, pb1);
+            }
+        }
+        __syncwarp();
+    }
+
+    // o[nt][dt]: (dim 16dt + g, rows 2q, 2q+1), (dim 16dt + g + 8, rows 2q, 2q+1) of the n-tile
+    __syncthreads();                          // every warp is done with its value block (aliased below)
+#pragma unroll
+    for (int nt = 0; nt < NRT; ++nt) {
+#pragma unroll
+        for (int re = 0; re < 2; ++re) {
+            const int rr = 8 * nt + 2 * q + re;
+            if (g == 0) { sm[warp][rr] = m[nt][re]; sl[warp][rr] = l[nt][re]; }
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+                so[warp][rr][16 * dt + g] = o[nt][dt][re];
+                so[warp][rr][16 * dt + g + 8] = o[nt][dt][2 + re];
+            }
+        }
+    }
+    __syncthreads();
+    const int nr = R - r0 < NRm ? R - r0 : NRm;
+    for (int i = threadIdx.x; i < nr * kD; i += kTcThreads) {
+        const int rr = i / kD, dd = i % kD;
+        float M = -INFINITY;
+        for (int w2 = 0; w2 < kTcWarps; ++w2) M = fmaxf(M, sm[w2][rr]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+            for (int w2 = 0; w2 < kTcWarps; ++w2) {
+                const float f = sm[w2][rr] == -INFINITY ? 0.0f : exp2f(sm[w2][rr] - M);
+                L += f * sl[w2][rr];
+                O += f * so[w2][rr][dd];
+            }
+        }
+        const int rg = r0 + rr;            // row within the head
+        const int tile16 = rg / kRowsPerTile, r16 = rg % kRowsPerTile;
+        const size_t slot = (((size_t)h * a.ntiles + tile16) * a.nsplit + split) * kRowsPerTile + r16;
+        float* wp = a.work + slot * (kD + 2);
+        wp[2 + dd] = O;
+        if (dd == 0) { wp[0] = M; wp[1] = L; }
+    }
+}
+
+// out[t][h*G+g][:] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits.
+// The splits' (max, sum) pairs are read in parallel into shared memory first, so the
+// per-dim pass below issues independent loads.
+constexpr int kMaxSplits = 1024;
+__global__ void __launch_bounds__(128) k_kv_combine(const __grid_constant__ KvAttnArgs a) {
+    __shared__ float sw[kMaxSplits];          // weight 2^(m_s - M) of each split
+    __shared__ float red[4];
     grid_dep_launch_dependents();
     const int h = blockIdx.x, row = blockIdx.y;     // row = t * G + g
     grid_dep_wait();
     const int tile = row / kRowsPerTile, rr = row % kRowsPerTile;
     const int t = row / a.G, g = row % a.G;
-    for (int dd = threadIdx.x; dd < kD; dd += blockDim.x) {
-        float M = -INFINITY;
-        for (int s = 0; s < a.nsplit; ++s) {
-            const size_t slot = (((size_t)h * a.ntiles + tile) * a.nsplit + s) * kRowsPerTile + rr;
-            M = fmaxf(M, a.work[slot * (kD + 2)]);
-        }
-        float L = 0.0f, O = 0.0f;
-        for (int s = 0; s < a.nsplit; ++s) {
-            const size_t slot = (((size_t)h * a.ntiles + tile) * a.nsplit + s) * kRowsPerTile + rr;
-            const float* wp = a.work + slot * (kD + 2);
-            const float f = wp[0] == -INFINITY ? 0.0f : exp2f(wp[0] - M);
-            L += f * wp[1];
-            O += f * wp[2 + dd];
-        }
-        a.out[((size_t)t * a.Hq + (size_t)h * a.G + g) * kD + dd] = L > 0.0f ? O / L : 0.0f;
+    auto slot = [&](int s) { return (((size_t)h * a.ntiles + tile) * a.nsplit + s) * kRowsPerTile + rr; };
+    float mloc = -INFINITY;
+    for (int s = threadIdx.x; s < a.nsplit; s += blockDim.x) {
+        const float ms = a.work[slot(s) * (kD + 2)];
+        sw[s] = ms;
+        mloc = fmaxf(mloc, ms);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mloc;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
+    float lloc = 0.0f;
+    for (int s = threadIdx.x; s < a.nsplit; s += blockDim.x) {
+        const float f = sw[s] == -INFINITY ? 0.0f : exp2f(sw[s] - M);
+        sw[s] = f;
+        lloc += f * a.work[slot(s) * (kD + 2) + 1];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lloc;
+    __syncthreads();
+    const float L = (red[0] + red[1]) + (red[2] + red[3]);
+    const int dd = threadIdx.x;                     // one output dim per thread (128 threads)
+    float O = 0.0f;
+#pragma unroll 8
+    for (int s = 0; s < a.nsplit; ++s) O += sw[s] * a.work[slot(s) * (kD + 2) + 2 + dd];
+    a.out[((size_t)t * a.Hq + (size_t)h * a.G + g) * kD + dd] = L > 0.0f ? O / L : 0.0f;
 }
 
 }  // namespace
@@ -303,13 +635,14 @@ cudaError_t launch_kv_write(const void* x, int bf16, int T, int H, int pos0, int
 int kv_rows_per_tile() { return kRowsPerTile; }
 
 // Position splits: enough CTAs for eight per SM (many loads in flight), at least 128
-// positions (one 32-position tile per warp) per split.
+// positions per split, at most kMaxSplits.
 int kv_splits(int T, int G, int Hkv, int L, int sms) {
     const int tiles = (T * G + kRowsPerTile - 1) / kRowsPerTile;
     const int base = Hkv * tiles;
     int ns = (8 * sms + base - 1) / base;
     const int by_len = (L + 127) / 128;
     ns = ns < by_len ? ns : by_len;
+    ns = ns < kMaxSplits ? ns : kMaxSplits;     // the combine holds one weight per split in shared memory
     return ns < 1 ? 1 : ns;
 }
 
@@ -318,11 +651,22 @@ cudaError_t launch_kv_attention(KvAttnArgs& a, int sms, cudaStream_t stream) {
     a.ntiles = (R + kRowsPerTile - 1) / kRowsPerTile;
     a.nsplit = kv_splits(a.T, a.Hq / a.Hkv, a.Hkv, a.L, sms);
     const int rows = R < kRowsPerTile ? R : kRowsPerTile;
-    const dim3 grid(a.Hkv, a.nsplit, a.ntiles), blk(kAttnThreads);
-    cudaError_t e = rows <= 2   ? launch_pdl(k_kv_attn<2>, grid, blk, 0, stream, a)
-                    : rows <= 4 ? launch_pdl(k_kv_attn<4>, grid, blk, 0, stream, a)
-                    : rows <= 8 ? launch_pdl(k_kv_attn<8>, grid, blk, 0, stream, a)
-                                : launch_pdl(k_kv_attn<16>, grid, blk, 0, stream, a);
+    cudaError_t e;
+    if (a.impl == 1) {                        // CUDA-core kernel (kept for measurement)
+        const dim3 grid(a.Hkv, a.nsplit, a.ntiles), blk(kAttnThreads);
+        e = rows <= 2   ? launch_pdl(k_kv_attn<2>, grid, blk, 0, stream, a)
+            : rows <= 4 ? launch_pdl(k_kv_attn<4>, grid, blk, 0, stream, a)
+            : rows <= 8 ? launch_pdl(k_kv_attn<8>, grid, blk, 0, stream, a)
+                        : launch_pdl(k_kv_attn<16>, grid, blk, 0, stream, a);
+    } else {                                  // tensor cores: 8 or 16 rows per CTA
+        if (rows <= 8) {
+            const dim3 grid(a.Hkv, a.nsplit, (R + 7) / 8), blk(kTcThreads);
+            e = launch_pdl(k_kv_attn_tc<1>, grid, blk, kv_tc_smem<1>(), stream, a);
+        } else {
+            const dim3 grid(a.Hkv, a.nsplit, a.ntiles), blk(kTcThreads);
+            e = launch_pdl(k_kv_attn_tc<2>, grid, blk, kv_tc_smem<2>(), stream, a);
+        }
+    }
     if (e != cudaSuccess) return e;
     return launch_pdl(k_kv_combine, dim3(a.Hkv, R), dim3(kD), 0, stream, a);
 }

@@ -94,3 +94,26 @@ def test_kv_attention_bf16_queries_and_long_context(dev):
         got = nest.kv_attention(qt, kc, vc, L, view, 128).cpu().numpy()
         parity(got.reshape(-1, 128), O.kv_attention(q, k, v, L, view, 128).reshape(-1, 128))
     nest.error_check()
+
+
+@pytest.mark.parametrize("impl", ["cuda", "tc"])
+def test_kv_attention_both_kernels(dev, impl, monkeypatch):
+    """The tensor-core kernel (default) and the CUDA-core kernel on the same cache, rows
+    per KV head from 1 to 40 (one and several 8- and 16-row tiles)."""
+    monkeypatch.setenv("NEST_KV_IMPL", impl)
+    rng = np.random.default_rng(21)
+    Hkv, L = 3, 500
+    kx = rng.normal(size=(L, Hkv, 128)).astype(np.float32)
+    vx = rng.normal(size=(L, Hkv, 128)).astype(np.float32)
+    kc, vc = nest.KVCache(Hkv, L, dev), nest.KVCache(Hkv, L, dev)
+    nest.kv_write(kc, torch.from_numpy(kx).to(dev), 0)
+    nest.kv_write(vc, torch.from_numpy(vx).to(dev), 0)
+    k = O.kv_quantize(np.transpose(kx, (1, 0, 2)))
+    v = O.kv_quantize(np.transpose(vx, (1, 0, 2)))
+    for T, G in ((1, 1), (3, 3), (9, 1), (5, 8)):
+        q = rng.normal(size=(T, Hkv * G, 128)).astype(np.float32)
+        for view, rn in ((8, 0), (4, 17)):
+            got = nest.kv_attention(torch.from_numpy(q).to(dev), kc, vc, L, view, rn).cpu().numpy()
+            parity(got.reshape(-1, 128), O.kv_attention(q, k, v, L, view, rn).reshape(-1, 128))
+    monkeypatch.delenv("NEST_KV_IMPL")
+    nest.error_check()
