@@ -303,7 +303,8 @@ nest_status nest_linear_static(const nest_layer* layer, int32_t verify, const vo
  *   ref   [H][Lmax][64] bytes: the refinement codes q_r + 8, same layout;
  *   scale [H][Lmax] fp16 bits: s = max|x| / 7 of the row.
  * base and ref 16-byte aligned, scale 2-byte aligned; nest_kv_plane_bytes(H, Lmax)
- * bytes each for base and ref, 2*H*Lmax bytes for scale. */
+ * bytes each for base and ref, 2*H*Lmax bytes for scale.  A plane holds fewer than
+ * 2^32 bytes (H * Lmax < 2^26); larger caches give NEST_ERR_UNSUPPORTED. */
 typedef struct {
     uint8_t* base;
     uint8_t* ref;

@@ -417,6 +417,7 @@ size_t nest_kv_plane_bytes(int32_t H, int32_t Lmax) {
 static nest_status check_kv(const nest_kv_cache* c) {
     if (c == nullptr || !c->base || !c->ref || !c->scale) return NEST_ERR_INVALID_ARG;
     if (c->H < 1 || c->Lmax < 1) return NEST_ERR_INVALID_ARG;
+    if ((long long)c->H * c->Lmax >= (1LL << 26)) return NEST_ERR_UNSUPPORTED;   // 32-bit plane offsets
     if (!aligned16(c->base) || !aligned16(c->ref) || (reinterpret_cast<uintptr_t>(c->scale) & 1u))
         return NEST_ERR_MISALIGNED;
     return NEST_OK;

@@ -9,6 +9,8 @@
 //   scale [H][Lmax]:     fp16 s = max|x| / 7.
 // The KV4 view reads base + scale (66 bytes per row), the KV8 view base + ref + scale
 // (130 bytes per row): the draft never touches the refinement plane.
+#include <type_traits>
+
 #include "nest_device.cuh"
 #include "nest_internal.h"
 
@@ -269,16 +271,21 @@ k_kv_attn(const __grid_constant__ KvAttnArgs a) {
 // Tensor-core decode attention (mma.sync m16n8k16), 16 positions per warp step.
 //
 // QK: S[pos][row] = K[pos][:] . Q[row][:] with A = the key codes (16 positions x 16 dims
-// per k-step), B = the queries (16 dims x 8 rows).  The dims inside a k-step may be taken
-// in any order shared by A and B: thread q of a quad takes, in k-step s, dims
-// 32q + 4s .. 32q + 4s + 3, so over the 8 k-steps it reads bytes 16q .. 16q+15 of its two
-// key rows -- one 16-byte load per row, the quad reading the row's 64 bytes.
-// One code path serves both views: the byte (u4 << 4) | u_r minus 136 is the KV8 code
-// 16 q4 + q_r, and a position read at KV4 takes u_r = 8, giving 16 q4; every position's
-// scale is then s / 16, applied to its scores (keys) and to its probabilities (values).
+// per k-step), B = the queries (16 dims x 8 rows).  A dot product may take its dims in any
+// order shared by both operands, and the decode below is cheapest when each 32-bit word of
+// a row (dims 8w .. 8w+7, byte i = dims 2i | 2i+1) comes out as the fp16 pairs
+// (8w + j, 8w + j + 4), j = 0..3.  Thread q of a quad owns bytes 16q .. 16q+15 of its two
+// key rows (one 16-byte load per row, the quad reading the row's 64 bytes); word w of
+// them feeds k-steps 2w (pairs j = 0, 1) and 2w + 1 (pairs j = 2, 3), and the query
+// fragments are packed in the same order.
+// Codes: the byte (u4 << 4) | u_r minus 136 is the KV8 code 16 q4 + q_r, and a position
+// read at KV4 takes u_r = 8, giving 16 q4, so every position's scale is s / 16, applied to
+// its scores (keys) and to its probabilities (values).  Blocks read wholly at KV4 take a
+// shorter decode of the base word alone.
 // PV: O^T[dim][row] += V^T[dim][pos] P^T[pos][row]: A = V^T loaded with ldmatrix.trans
-// from the block's values decoded to fp16 in shared memory, B = P^T from the score
-// fragments transposed in registers with movmatrix.
+// from the block's values decoded to fp16 in shared memory (each 8-dim group in the pair
+// order above, undone when the output is written), B = P^T from the score fragments
+// transposed in registers with movmatrix.
 // ---------------------------------------------------------------------------
 
 constexpr int kTcWarps = 4;
@@ -309,20 +316,38 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, u
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
-// Four KV8 codes c = 16 u4 + u_r - 136 of one 32-bit base word and one refinement word
-// (dims 8w .. 8w+7 of a row, byte i = dims 2i | 2i+1), as fp16 pairs in dim order:
-// out[0] = (d0, d1), out[1] = (d2, d3), out[2] = (d4, d5), out[3] = (d6, d7).
-__device__ __forceinline__ void codes8(uint32_t b, uint32_t r, uint32_t (&out)[4]) {
-    // byte per dim: even dims from the low nibbles, odd dims from the high nibbles
-    const uint32_t ev = ((b << 4) & 0xF0F0F0F0u) | (r & 0x0F0F0F0Fu);          // dims 0, 2, 4, 6
-    const uint32_t od = (b & 0xF0F0F0F0u) | ((r >> 4) & 0x0F0F0F0Fu);          // dims 1, 3, 5, 7
-    const uint32_t p01 = prmt(ev, od, 0x5140u);                                 // dims 0, 1, 2, 3
-    const uint32_t p23 = prmt(ev, od, 0x7362u);                                 // dims 4, 5, 6, 7
+// One 32-bit base word b and refinement word r (dims 8w .. 8w+7 of a row, byte i = dims
+// 2i | 2i+1) as the fp16 codes 16 u4 + u_r - 136 in pairs out[j] = (dim j, dim j + 4).
+__device__ __forceinline__ void dec8(uint32_t b, uint32_t r, uint32_t (&out)[4]) {
+    const uint32_t ev = ((b << 4) & 0xF0F0F0F0u) | (r & 0x0F0F0F0Fu);          // byte i: dim 2i
+    const uint32_t od = (b & 0xF0F0F0F0u) | ((r >> 4) & 0x0F0F0F0Fu);          // byte i: dim 2i + 1
     const __half2 off = __float2half2_rn(1024.0f + 136.0f);
-    out[0] = h2_as_u32(__hsub2(u32_as_h2(prmt(p01, 0x64646464u, 0x5140u)), off));
-    out[1] = h2_as_u32(__hsub2(u32_as_h2(prmt(p01, 0x64646464u, 0x7362u)), off));
-    out[2] = h2_as_u32(__hsub2(u32_as_h2(prmt(p23, 0x64646464u, 0x5140u)), off));
-    out[3] = h2_as_u32(__hsub2(u32_as_h2(prmt(p23, 0x64646464u, 0x7362u)), off));
+    out[0] = h2_as_u32(__hsub2(u32_as_h2(prmt(ev, 0x64646464u, 0x4240u)), off));   // dims 0, 4
+    out[1] = h2_as_u32(__hsub2(u32_as_h2(prmt(od, 0x64646464u, 0x4240u)), off));   // dims 1, 5
+    out[2] = h2_as_u32(__hsub2(u32_as_h2(prmt(ev, 0x64646464u, 0x4341u)), off));   // dims 2, 6
+    out[3] = h2_as_u32(__hsub2(u32_as_h2(prmt(od, 0x64646464u, 0x4341u)), off));   // dims 3, 7
+}
+
+// The same word read at KV4 (u_r = 8): 16 u4 - 128 in the same pair order.  A nibble in
+// bits 0-3 of an fp16 with exponent field 0x64 reads as 1024 + u4, one in bits 4-7 as
+// 1024 + 16 u4; both are mapped to 16 u4 - 128 exactly by one fp16 operation.
+__device__ __forceinline__ void dec4(uint32_t b, uint32_t (&out)[4]) {
+    const uint32_t b8 = b >> 8;
+    const __half2 x16 = __float2half2_rn(16.0f), o16 = __float2half2_rn(-16.0f * 1024.0f - 128.0f);
+    const __half2 o1 = __float2half2_rn(1024.0f + 128.0f);
+    out[0] = h2_as_u32(__hfma2(u32_as_h2((b & 0x000F000Fu) | 0x64006400u), x16, o16));    // dims 0, 4
+    out[1] = h2_as_u32(__hsub2(u32_as_h2((b & 0x00F000F0u) | 0x64006400u), o1));          // dims 1, 5
+    out[2] = h2_as_u32(__hfma2(u32_as_h2((b8 & 0x000F000Fu) | 0x64006400u), x16, o16));   // dims 2, 6
+    out[3] = h2_as_u32(__hsub2(u32_as_h2((b8 & 0x00F000F0u) | 0x64006400u), o1));         // dims 3, 7
+}
+
+// Dim of slot x of the decoded order (pairs (j, j + 4) inside each group of 8).
+__device__ __forceinline__ int slot_dim(int x) { return (x & ~7) | ((x >> 1) & 3) | ((x & 1) << 2); }
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 template <int NRT>
@@ -332,7 +357,7 @@ constexpr int kv_tc_smem() {
 }
 
 template <int NRT>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, NRT == 1 ? 4 : 2)
 k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
     constexpr int NRm = 8 * NRT;          // query rows per CTA
     // dynamic shared memory: the warps' fp16 value blocks, later reused for the merge of
@@ -367,18 +392,20 @@ k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
         const int t = ok ? row / a.G : 0, gg = ok ? row % a.G : 0;
         const size_t qi = ((size_t)t * a.Hq + (size_t)h * a.G + gg) * kD;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            float v[4];
+        for (int w = 0; w < 4; ++w) {
+            float v[8];                       // dims 32q + 8w .. +7
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int dd = 32 * q + 4 * s + e;
+            for (int e = 0; e < 8; ++e) {
+                const int dd = 32 * q + 8 * w + e;
                 float x = 0.0f;
                 if (ok) x = a.q_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.q)[qi + dd])
                                      : reinterpret_cast<const float*>(a.q)[qi + dd];
                 v[e] = x * qscale;
             }
-            qb[nt][s][0] = pack_h2(v[0], v[1]);
-            qb[nt][s][1] = pack_h2(v[2], v[3]);
+            qb[nt][2 * w][0] = pack_h2(v[0], v[4]);
+            qb[nt][2 * w][1] = pack_h2(v[1], v[5]);
+            qb[nt][2 * w + 1][0] = pack_h2(v[2], v[6]);
+            qb[nt][2 * w + 1][1] = pack_h2(v[3], v[7]);
         }
     }
     // visible positions of the thread's two rows per n-tile (rows 8nt + 2q, 8nt + 2q + 1)
@@ -391,6 +418,9 @@ k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
             vis[nt][e] = row < R ? a.L - a.T + row / a.G + 1 : 0;
         }
 
+    // positions below vis_all are inside the split and visible to every row of the CTA
+    const int vis_r0 = a.L - a.T + r0 / a.G + 1;     // row r0 (the CTA's earliest token) sees the fewest
+    const int vis_all = vis_r0 < p1 ? vis_r0 : p1;
     float m[NRT][2], l[NRT][2], o[NRT][8][4];
 #pragma unroll
     for (int nt = 0; nt < NRT; ++nt) {
@@ -406,127 +436,211 @@ k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
     const uint32_t lda = vblk_s + (uint32_t)((lr + 8 * (lm >> 1)) * kVPitch + 16 * (lm & 1));
 
     // Raw words of one 16-position block: keys (rows g, g+8; bytes 16q..16q+15) and values
-    // (position lane/2, dims 64*(lane&1) ..), base and refinement planes.  The next block's
-    // words are loaded before the current block is decoded.
+    // (position lane/2, dims 64*(lane&1) ..), base and refinement planes, and the fp16
+    // scales of positions g, g+8.  The next block's value words are loaded as soon as the
+    // current ones are decoded, its key words as soon as the scores are issued, so one
+    // set of registers carries both with a full iteration of lead time.
     struct Blk {
         uint4 kb[2], kr[2], vb[2], vr[2];
+        uint16_t ks[2], vs[2];
     };
-    auto load_blk = [&](int pb, Blk& B) {
-        const uint4 z = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+    const uint4 z8 = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+    // per-lane 32-bit offsets of position 0 of the head (a plane holds fewer than 2^32
+    // bytes); a block at pb adds pb rows.  The plane pointers stay kernel parameters.
+    const bool view8 = a.view == 8;
+    const uint32_t krow = (uint32_t)((hrow + g) * (kD / 2)) + 16u * q;
+    const uint32_t vrow = (uint32_t)((hrow + (lane >> 1)) * (kD / 2)) + 32u * (lane & 1);
+    const uint32_t srow = (uint32_t)(hrow + g);
+    auto ld16 = [](const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); };
+    // Key words of the block at pb.  Whole blocks inside the split take unguarded loads; the
+    // refinement words are read only where the block's decode uses them (every position
+    // at KV8, or the Recent-N window), other positions of a straddling block read u_r = 8.
+    auto load_k = [&](int pb, Blk& B) {
+        const bool need_ref = view8 || pb + 15 >= recent0;
+        if (pb + 16 <= p1) {
+            const uint32_t o = krow + (uint32_t)pb * (kD / 2);
+            B.kb[0] = ld16(a.kbase + o);
+            B.kb[1] = ld16(a.kbase + o + 8 * (kD / 2));
+            B.ks[0] = a.kscale[srow + pb];
+            B.ks[1] = a.kscale[srow + pb + 8];
+            if (need_ref) {
+                const bool all = view8 || pb >= recent0;
+                B.kr[0] = (all || pb + g >= recent0) ? ld16(a.kref + o) : z8;
+                B.kr[1] = (all || pb + g + 8 >= recent0) ? ld16(a.kref + o + 8 * (kD / 2)) : z8;
+            }
+            return;
+        }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int p = pb + g + 8 * e;
-            B.kb[e] = z;
-            B.kr[e] = z;
+            const uint32_t o = krow + (uint32_t)(pb + 8 * e) * (kD / 2);
+            B.kb[e] = z8;
+            B.kr[e] = z8;
+            B.ks[e] = 0;
             if (p < p1) {
-                B.kb[e] = *reinterpret_cast<const uint4*>(a.kbase + (hrow + p) * (kD / 2) + 16 * q);
-                if (a.view == 8 || p >= recent0)
-                    B.kr[e] = *reinterpret_cast<const uint4*>(a.kref + (hrow + p) * (kD / 2) + 16 * q);
+                B.kb[e] = ld16(a.kbase + o);
+                if (view8 || p >= recent0) B.kr[e] = ld16(a.kref + o);
+                B.ks[e] = a.kscale[srow + pb + 8 * e];
             }
         }
+    };
+    auto load_v = [&](int pb, Blk& B) {
+        const bool need_ref = view8 || pb + 15 >= recent0;
         const int p = pb + (lane >> 1);
-        const int half = lane & 1;
+        const uint32_t o = vrow + (uint32_t)pb * (kD / 2);
+        if (pb + 16 <= p1) {
+            B.vb[0] = ld16(a.vbase + o);
+            B.vb[1] = ld16(a.vbase + o + 16);
+            B.vs[0] = a.vscale[srow + pb];
+            B.vs[1] = a.vscale[srow + pb + 8];
+            if (need_ref) {
+                const bool use = view8 || p >= recent0;
+                B.vr[0] = use ? ld16(a.vref + o) : z8;
+                B.vr[1] = use ? ld16(a.vref + o + 16) : z8;
+            }
+            return;
+        }
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            B.vb[c] = z;
-            B.vr[c] = z;
+            B.vb[c] = z8;
+            B.vr[c] = z8;
             if (p < p1) {
-                B.vb[c] = *reinterpret_cast<const uint4*>(a.vbase + (hrow + p) * (kD / 2) + 32 * half + 16 * c);
-                if (a.view == 8 || p >= recent0)
-                    B.vr[c] = *reinterpret_cast<const uint4*>(a.vref + (hrow + p) * (kD / 2) + 32 * half + 16 * c);
+                B.vb[c] = ld16(a.vbase + o + 16 * c);
+                if (view8 || p >= recent0) B.vr[c] = ld16(a.vref + o + 16 * c);
             }
         }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) B.vs[e] = pb + g + 8 * e < p1 ? a.vscale[srow + pb + 8 * e] : (uint16_t)0;
     };
-    Blk nxt;
-    if (p0 + 16 * warp < p1) load_blk(p0 + 16 * warp, nxt);
+    Blk buf;
+    int pb = p0 + 16 * warp;                  // this warp's current block
+    if (pb < p1) {
+        load_k(pb, buf);
+        load_v(pb, buf);
+    }
 
-    for (int pb = p0 + 16 * warp; pb < p1; pb += 16 * kTcWarps) {
-        const Blk cur = nxt;
-        if (pb + 16 * kTcWarps < p1) load_blk(pb + 16 * kTcWarps, nxt);
-        const uint4* kb = cur.kb;
-        const uint4* kr = cur.kr;
-        float ks[2];
+    // One 16-position block.  DEC: 0 decodes the base words alone (a block wholly read at
+    // KV4), 1 base + refinement (KV8, or a KV4 read's Recent-N window, where positions
+    // outside the window carry u_r = 8), 2 picks one of the two at run time.  MASK: the
+    // block may hold positions past the split's end or past some row's causal limit.
+    auto step = [&](auto dec_c, auto mask_c) {
+        constexpr int DEC = decltype(dec_c)::value;
+        constexpr bool MASK = decltype(mask_c)::value;
+        const int pn = pb + 16 * kTcWarps;    // the warp's next block
+        const bool kv8 = DEC == 1 || (DEC == 2 && (view8 || pb + 15 >= recent0));
+        float ks[2], vsc[2];                  // zero past the split's end
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int p = pb + g + 8 * e;
-            ks[e] = p < p1 ? __half2float(__ushort_as_half(a.kscale[hrow + p])) * 0.0625f : 0.0f;
+            ks[e] = __half2float(__ushort_as_half(buf.ks[e])) * 0.0625f;
+            vsc[e] = __half2float(__ushort_as_half(buf.vs[e])) * 0.0625f;
         }
         // ---- values: thread lane decodes position pb + lane/2, dims 64*(lane&1) .. +63 into fp16 ----
         {
-            const int half = lane & 1;
-            uint8_t* dst = vblk + (lane >> 1) * kVPitch + 128 * half;
+            uint8_t* dst = vblk + (lane >> 1) * kVPitch + 128 * (lane & 1);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                const uint32_t bw[4] = {cur.vb[c].x, cur.vb[c].y, cur.vb[c].z, cur.vb[c].w};
-                const uint32_t rw[4] = {cur.vr[c].x, cur.vr[c].y, cur.vr[c].z, cur.vr[c].w};
+                const uint32_t bw[4] = {buf.vb[c].x, buf.vb[c].y, buf.vb[c].z, buf.vb[c].w};
+                const uint32_t rw[4] = {buf.vr[c].x, buf.vr[c].y, buf.vr[c].z, buf.vr[c].w};
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     uint32_t cv[4];
-                    codes8(bw[w], rw[w], cv);
+                    if (kv8) dec8(bw[w], rw[w], cv);
+                    else dec4(bw[w], cv);
                     *reinterpret_cast<uint4*>(dst + 64 * c + 16 * w) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
                 }
             }
         }
+        if (pn < p1) load_v(pn, buf);
         __syncwarp();
 
-        // ---- scores S[pos][row] ----
-        uint32_t ka[8][4];                    // A fragments: rows g (a0, a2), g + 8 (a1, a3) per k-step
-        {
-            const uint32_t b0w[4] = {kb[0].x, kb[0].y, kb[0].z, kb[0].w};
-            const uint32_t r0w[4] = {kr[0].x, kr[0].y, kr[0].z, kr[0].w};
-            const uint32_t b1w[4] = {kb[1].x, kb[1].y, kb[1].z, kb[1].w};
-            const uint32_t r1w[4] = {kr[1].x, kr[1].y, kr[1].z, kr[1].w};
+        // ---- scores S[pos][row]: each key word is decoded right before its two k-steps ----
+        // A fragments: rows g (a0, a2), g + 8 (a1, a3); word w holds dims 32q + 8w .. +7
+        float scs[NRT][2][4];                 // two independent accumulation chains per n-tile
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {     // word w: dims 32q + 8w .. +7 = k-steps 2w, 2w+1
+        for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) scs[nt][0][e] = scs[nt][1][e] = 0.0f;
+        {
+            const uint32_t b0w[4] = {buf.kb[0].x, buf.kb[0].y, buf.kb[0].z, buf.kb[0].w};
+            const uint32_t r0w[4] = {buf.kr[0].x, buf.kr[0].y, buf.kr[0].z, buf.kr[0].w};
+            const uint32_t b1w[4] = {buf.kb[1].x, buf.kb[1].y, buf.kb[1].z, buf.kb[1].w};
+            const uint32_t r1w[4] = {buf.kr[1].x, buf.kr[1].y, buf.kr[1].z, buf.kr[1].w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
                 uint32_t c0[4], c1[4];
-                codes8(b0w[w], r0w[w], c0);
-                codes8(b1w[w], r1w[w], c1);
-                ka[2 * w][0] = c0[0]; ka[2 * w][2] = c0[1]; ka[2 * w][1] = c1[0]; ka[2 * w][3] = c1[1];
-                ka[2 * w + 1][0] = c0[2]; ka[2 * w + 1][2] = c0[3]; ka[2 * w + 1][1] = c1[2]; ka[2 * w + 1][3] = c1[3];
+                if (kv8) {
+                    dec8(b0w[w], r0w[w], c0);
+                    dec8(b1w[w], r1w[w], c1);
+                } else {
+                    dec4(b0w[w], c0);
+                    dec4(b1w[w], c1);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NRT; ++nt) {
+                    mma16816f(scs[nt][0], c0[0], c1[0], c0[1], c1[1], qb[nt][2 * w][0], qb[nt][2 * w][1]);
+                    mma16816f(scs[nt][1], c0[2], c1[2], c0[3], c1[3], qb[nt][2 * w + 1][0],
+                              qb[nt][2 * w + 1][1]);
+                }
             }
         }
-        float vsc[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int p = pb + g + 8 * e;
-            vsc[e] = p < p1 ? __half2float(__ushort_as_half(a.vscale[hrow + p])) * 0.0625f : 0.0f;
-        }
+        if (pn < p1) load_k(pn, buf);
 #pragma unroll
         for (int nt = 0; nt < NRT; ++nt) {
-            float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            // sc: (pos g, rows 2q, 2q+1), (pos g+8, rows 2q, 2q+1)
+            float sc[4], pr[4];
 #pragma unroll
-            for (int s = 0; s < 8; s += 2) {      // two independent accumulation chains
-                mma16816f(sc, ka[s][0], ka[s][1], ka[s][2], ka[s][3], qb[nt][s][0], qb[nt][s][1]);
-                mma16816f(sc2, ka[s + 1][0], ka[s + 1][1], ka[s + 1][2], ka[s + 1][3], qb[nt][s + 1][0],
-                          qb[nt][s + 1][1]);
-            }
+            for (int e = 0; e < 4; ++e) sc[e] = (scs[nt][0][e] + scs[nt][1][e]) * ks[e >> 1];
+            if constexpr (!MASK) {
+                float mx[2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
-            // sc: (pos g, rows 2q, 2q+1), (pos g+8, rows 2q, 2q+1); scale, mask
+                for (int re = 0; re < 2; ++re) {
+                    mx[re] = fmaxf(sc[re], sc[2 + re]);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int pe = pb + g + 8 * (e >> 1), re = e & 1;
-                sc[e] = (pe < p1 && pe < vis[nt][re]) ? sc[e] * ks[e >> 1] : -INFINITY;
-            }
-            float pr[4];
+                    for (int off = 4; off < 32; off <<= 1)
+                        mx[re] = fmaxf(mx[re], __shfl_xor_sync(0xffffffffu, mx[re], off));
+                }
+                // the outputs are rescaled only when some row's running max grows
+                if (__any_sync(0xffffffffu, mx[0] > m[nt][0] || mx[1] > m[nt][1])) {
 #pragma unroll
-            for (int re = 0; re < 2; ++re) {
-                float mx = fmaxf(sc[re], sc[2 + re]);
+                    for (int re = 0; re < 2; ++re) {
+                        const float mn = fmaxf(m[nt][re], mx[re]);
+                        const float corr = ex2(m[nt][re] - mn);  // m = -inf before the first block: 0
+                        l[nt][re] *= corr;
+                        m[nt][re] = mn;
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                const float mn = fmaxf(m[nt][re], mx);
-                const float corr = mn == -INFINITY ? 1.0f : exp2f(m[nt][re] - mn);
-                const float e0 = sc[re] == -INFINITY ? 0.0f : exp2f(sc[re] - mn);
-                const float e1 = sc[2 + re] == -INFINITY ? 0.0f : exp2f(sc[2 + re] - mn);
-                float sum = e0 + e1;
+                        for (int dt = 0; dt < 8; ++dt) { o[nt][dt][re] *= corr; o[nt][dt][2 + re] *= corr; }
+                    }
+                }
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                l[nt][re] = l[nt][re] * corr + sum;
-                m[nt][re] = mn;
+                for (int re = 0; re < 2; ++re) {
+                    const float e0 = ex2(sc[re] - m[nt][re]), e1 = ex2(sc[2 + re] - m[nt][re]);
+                    // per-lane partial sum under the row's common max; lanes are summed at the end
+                    l[nt][re] += e0 + e1;
+                    pr[re] = e0 * vsc[0];
+                    pr[2 + re] = e1 * vsc[1];
+                }
+            } else {
 #pragma unroll
-                for (int dt = 0; dt < 8; ++dt) { o[nt][dt][re] *= corr; o[nt][dt][2 + re] *= corr; }
-                pr[re] = e0 * vsc[0];
-                pr[2 + re] = e1 * vsc[1];
+                for (int e = 0; e < 4; ++e) {
+                    const int pe = pb + g + 8 * (e >> 1), re = e & 1;
+                    if (!(pe < p1 && pe < vis[nt][re])) sc[e] = -INFINITY;
+                }
+#pragma unroll
+                for (int re = 0; re < 2; ++re) {
+                    float mx = fmaxf(sc[re], sc[2 + re]);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    const float mn = fmaxf(m[nt][re], mx);
+                    const float corr = mn == -INFINITY ? 1.0f : ex2(m[nt][re] - mn);
+                    const float e0 = sc[re] == -INFINITY ? 0.0f : ex2(sc[re] - mn);
+                    const float e1 = sc[2 + re] == -INFINITY ? 0.0f : ex2(sc[2 + re] - mn);
+                    l[nt][re] = l[nt][re] * corr + (e0 + e1);
+                    m[nt][re] = mn;
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) { o[nt][dt][re] *= corr; o[nt][dt][2 + re] *= corr; }
+                    pr[re] = e0 * vsc[0];
+                    pr[2 + re] = e1 * vsc[1];
+                }
             }
             // B fragments of P^T: b0 = positions 2q, 2q+1 of row g; b1 = positions 2q+8, 2q+9
             const uint32_t pb0 = movmatrix_trans(pack_h2(pr[0], pr[1]));
@@ -539,9 +653,27 @@ k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
             }
         }
         __syncwarp();
+        pb = pn;
+    };
+    using Dec4 = std::integral_constant<int, 0>;
+    using Dec8 = std::integral_constant<int, 1>;
+    using DecAny = std::integral_constant<int, 2>;
+    // interior blocks (inside the split, visible to every row): first those wholly before
+    // a KV4 read's Recent-N window, then the rest; the last few blocks take the masked step
+    if (!view8) {
+        const int lim = vis_all < recent0 ? vis_all : recent0;
+        while (pb + 16 <= lim) step(Dec4{}, std::false_type{});
     }
+    while (pb + 16 <= vis_all) step(Dec8{}, std::false_type{});
+    while (pb < p1) step(DecAny{}, std::true_type{});
 
     // o[nt][dt]: (dim 16dt + g, rows 2q, 2q+1), (dim 16dt + g + 8, rows 2q, 2q+1) of the n-tile
+#pragma unroll
+    for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+        for (int re = 0; re < 2; ++re)
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) l[nt][re] += __shfl_xor_sync(0xffffffffu, l[nt][re], off);
     __syncthreads();                          // every warp is done with its value block (aliased below)
 #pragma unroll
     for (int nt = 0; nt < NRT; ++nt) {
@@ -551,8 +683,8 @@ k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
             if (g == 0) { sm[warp][rr] = m[nt][re]; sl[warp][rr] = l[nt][re]; }
 #pragma unroll
             for (int dt = 0; dt < 8; ++dt) {
-                so[warp][rr][16 * dt + g] = o[nt][dt][re];
-                so[warp][rr][16 * dt + g + 8] = o[nt][dt][2 + re];
+                so[warp][rr][slot_dim(16 * dt + g)] = o[nt][dt][re];
+                so[warp][rr][slot_dim(16 * dt + g + 8)] = o[nt][dt][2 + re];
             }
         }
     }
@@ -634,16 +766,41 @@ cudaError_t launch_kv_write(const void* x, int bf16, int T, int H, int pos0, int
 
 int kv_rows_per_tile() { return kRowsPerTile; }
 
-// Position splits: enough CTAs for eight per SM (many loads in flight), at least 128
-// positions per split, at most kMaxSplits.
+// Resident CTAs per SM of the tensor-core kernel for 8 (nrt 1) or 16 (nrt 2) query rows.
+int tc_resident(int nrt) {
+    static int cached[3] = {0, 0, 0};
+    if (cached[nrt] == 0) {
+        int n = 0;
+        const cudaError_t e =
+            nrt == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_kv_attn_tc<1>, kTcThreads, kv_tc_smem<1>())
+                     : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_kv_attn_tc<2>, kTcThreads, kv_tc_smem<2>());
+        if (e != cudaSuccess) (void)cudaGetLastError();
+        cached[nrt] = (e == cudaSuccess && n > 0) ? n : 1;
+    }
+    return cached[nrt];
+}
+
+// Position splits: the smallest count whose CTAs fill the resident slots (SMs x CTAs per
+// SM) to 95 % over whole waves, else the best fill up to four waves; at least 128
+// positions per split and at most kMaxSplits splits.
 int kv_splits(int T, int G, int Hkv, int L, int sms) {
-    const int tiles = (T * G + kRowsPerTile - 1) / kRowsPerTile;
-    const int base = Hkv * tiles;
-    int ns = (8 * sms + base - 1) / base;
-    const int by_len = (L + 127) / 128;
-    ns = ns < by_len ? ns : by_len;
-    ns = ns < kMaxSplits ? ns : kMaxSplits;     // the combine holds one weight per split in shared memory
-    return ns < 1 ? 1 : ns;
+    const int R = T * G;
+    const int nrt = R <= 8 ? 1 : 2;
+    const long long base = (long long)Hkv * ((R + 8 * nrt - 1) / (8 * nrt));
+    const long long slots = (long long)tc_resident(nrt) * (sms > 0 ? sms : 1);
+    long long cap = (L + 127) / 128;
+    cap = cap < kMaxSplits ? cap : kMaxSplits;
+    const long long by_waves = (4 * slots + base - 1) / base;
+    cap = cap < by_waves ? cap : by_waves;
+    int best = 1;
+    double best_eff = -1.0;
+    for (int n = 1; n <= cap; ++n) {
+        const long long ctas = base * n, waves = (ctas + slots - 1) / slots;
+        const double eff = (double)ctas / (double)(waves * slots);
+        if (eff >= 0.95) return n;
+        if (eff > best_eff + 1e-9) { best_eff = eff; best = n; }
+    }
+    return best;
 }
 
 cudaError_t launch_kv_attention(KvAttnArgs& a, int sms, cudaStream_t stream) {

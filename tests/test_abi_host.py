@@ -194,6 +194,8 @@ def test_kv_cache_validation(lib):
     assert w(ctypes.c_void_p(0x50002), 0, 8, ctypes.byref(C), 0, None) == 3
     bad = nest._KvCache(0x50008, 0x60000, 0x70000, 4, 64)
     assert w(ok, 0, 8, ctypes.byref(bad), 0, None) == 3
+    huge = nest._KvCache(0x50000, 0x60000, 0x70000, 64, 1 << 20)         # a plane of 4 GiB
+    assert w(ok, 0, 8, ctypes.byref(huge), 0, None) == 2
     a = lib.nest_kv_attention
     V = nest._KvCache(0x50000, 0x60000, 0x70000, 4, 64)
     assert a(ok, 0, 2, 6, ctypes.byref(C), ctypes.byref(V), 32, 8, 0, ok, ok, None) == 1   # Hq % Hkv

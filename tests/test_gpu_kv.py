@@ -117,3 +117,25 @@ def test_kv_attention_both_kernels(dev, impl, monkeypatch):
             parity(got.reshape(-1, 128), O.kv_attention(q, k, v, L, view, rn).reshape(-1, 128))
     monkeypatch.delenv("NEST_KV_IMPL")
     nest.error_check()
+
+
+@pytest.mark.parametrize("view", [4, 8])
+def test_kv_attention_growing_and_falling_scores(dev, view):
+    """Key norms that ramp up over the context (the running max grows at every block) and
+    then down again (it never grows): both branches of the online-softmax rescale."""
+    rng = np.random.default_rng(31 + view)
+    T, Hq, Hkv, L = 4, 8, 2, 3000
+    ramp = np.concatenate([np.linspace(0.2, 3.0, L // 2), np.linspace(3.0, 0.2, L - L // 2)])
+    direction = rng.normal(size=(Hkv, 128))
+    kx = (ramp[:, None, None] * (direction[None] + 0.3 * rng.normal(size=(L, Hkv, 128)))).astype(np.float32)
+    vx = rng.normal(size=(L, Hkv, 128)).astype(np.float32)
+    kc, vc = nest.KVCache(Hkv, L, dev), nest.KVCache(Hkv, L, dev)
+    nest.kv_write(kc, torch.from_numpy(kx).to(dev), 0)
+    nest.kv_write(vc, torch.from_numpy(vx).to(dev), 0)
+    k = O.kv_quantize(np.transpose(kx, (1, 0, 2)))
+    v = O.kv_quantize(np.transpose(vx, (1, 0, 2)))
+    G = Hq // Hkv
+    q = (np.repeat(direction, G, axis=0)[None] * 0.4 + 0.1 * rng.normal(size=(T, Hq, 128))).astype(np.float32)
+    got = nest.kv_attention(torch.from_numpy(q).to(dev), kc, vc, L, view, 0).cpu().numpy()
+    parity(got.reshape(-1, 128), O.kv_attention(q, k, v, L, view, 0).reshape(-1, 128))
+    nest.error_check()
