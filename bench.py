@@ -624,8 +624,11 @@ def run_kv(args):
     stream = torch.cuda.Stream(device=dev)
     hbm, _ = peaks()
     recs = []
-    for name, T, view, rn in (("draft KV4", 1, 4, 0), ("draft KV4 + Recent-1024", 1, 4, 1024),
-                              ("verify KV8", 16, 8, 0), ("draft KV8", 1, 8, 0)):
+    cases = (("draft KV4", 1, 4, 0), ("draft KV4 + Recent-1024", 1, 4, 1024),
+             ("verify KV8", 16, 8, 0), ("draft KV8", 1, 8, 0))
+    if args.kv_case is not None:
+        cases = (cases[args.kv_case],)
+    for name, T, view, rn in cases:
         q = torch.randn((T, Hq, d), generator=g, device=dev).to(torch.bfloat16)
         out = torch.empty((T, Hq, d), dtype=torch.float32, device=dev)
         work = torch.empty(int(nest.load().nest_kv_attention_work_bytes(T, Hq, Hkv, L)) // 4 + 1,
@@ -681,6 +684,9 @@ def main():
                     help="weight codec of the default workload: l2 (2-bit base + 7-bit residual, the metric's) "
                          "or w4w8 (BitNest W4 base + 4-bit refinement)")
     ap.add_argument("--context", type=int, default=32768, help="context length of --workload kv_31b")
+    ap.add_argument("--kv-case", type=int, default=None, choices=[0, 1, 2, 3],
+                    help="--workload kv_31b: one case only (0 KV4 draft, 1 KV4 + Recent-1024, 2 KV8 verify "
+                         "T=16, 3 KV8 draft)")
     ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "decoder_31b", "stack_31b", "kv_31b"],
                     help="mlp_triplet_4b (default, the metric's workload), one chained 31B-class layer, "
                          "or the 60-layer 31B-class speculative cycle")

@@ -3,6 +3,7 @@
 // point allocates memory or synchronises (except nest_error_check).
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 #include <cuda_runtime.h>
 
 #include "../../include/nest.h"
@@ -477,8 +478,9 @@ nest_status nest_kv_attention(const void* q, int32_t q_dtype, int32_t T, int32_t
     a.Lmax = k->Lmax;
     a.view = view;
     a.recent_n = recent_n;
-    const char* impl = getenv("NEST_KV_IMPL");            // "cuda": the CUDA-core kernel, for measurement
-    a.impl = (impl && impl[0] == 'c') ? 1 : 0;
+    // for measurement: "cuda" the CUDA-core kernel, "tc16" tensor-core CTAs of at most 16 rows
+    const char* impl = getenv("NEST_KV_IMPL");
+    a.impl = (impl && impl[0] == 'c') ? 1 : (impl && strncmp(impl, "tc16", 4) == 0) ? 2 : 0;
     return from_cuda(launch_kv_attention(a, sms, as_stream(stream)));
 }
 

@@ -711,6 +711,313 @@ k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Paired variant for more than 16 query rows per KV head (the verify's T tokens x G heads):
+// a CTA of four warps in two pairs takes 32 rows.  Both warps of a pair walk the same
+// 16-position blocks; warp 0 decodes the block's keys and warp 1 its values into fp16 tiles
+// in shared memory (slot order as above), and each warp then computes the scores, softmax
+// and PV of its own 16 rows from the two tiles (ldmatrix for the keys as A, ldmatrix.trans
+// for the values).  The cache is read and decoded once per 32 rows instead of once per 16.
+// A pair alternates between two tile buffers, so one pair barrier per block orders the
+// writes of a block after the partner's reads of the block two steps back.
+// ---------------------------------------------------------------------------
+constexpr int kPairWarps = 4;
+constexpr int kPairThreads = 32 * kPairWarps;
+constexpr int kPairRows = 32;
+constexpr int kPairTile = 16 * kVPitch;                          // one decoded 16-position tile
+constexpr int kPairBuf = 2 * kPairTile + 2 * 16 * 4;             // key tile, value tile, their scales
+constexpr int kPairFront = (kPairWarps / 2) * 2 * kPairBuf;      // two pairs, two buffers each
+constexpr int kPairMerge = kPairWarps * 16 * (kD + 1) * 4;
+constexpr int kPairFrontMax = kPairFront > kPairMerge ? kPairFront : kPairMerge;
+constexpr int kPairSmem = kPairFrontMax + 2 * kPairWarps * 16 * 4;
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__global__ void __launch_bounds__(kPairThreads, 3)
+k_kv_attn_pair(const __grid_constant__ KvAttnArgs a) {
+    // dynamic shared memory: the pairs' tile buffers, later reused for the merge of the
+    // warps' outputs; the warps' softmax states after the larger of the two
+    extern __shared__ __align__(16) uint8_t dsm[];
+    float (*so)[16][kD + 1] = reinterpret_cast<float (*)[16][kD + 1]>(dsm);
+    float (*sm)[16] = reinterpret_cast<float (*)[16]>(dsm + kPairFrontMax);
+    float (*sl)[16] = reinterpret_cast<float (*)[16]>(dsm + kPairFrontMax + kPairWarps * 16 * 4);
+    grid_dep_launch_dependents();
+    const int h = blockIdx.x, split = blockIdx.y, tile = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pair = warp >> 1, role = warp & 1;       // role 0 decodes the keys, 1 the values
+    const int g = lane >> 2, q = lane & 3;
+    const int R = a.T * a.G;
+    const int r0 = tile * kPairRows + 16 * role;       // the warp's first row
+    const int per = (a.L + a.nsplit - 1) / a.nsplit;
+    const int p0 = split * per, p1 = p0 + per < a.L ? p0 + per : a.L;
+    const size_t hrow = (size_t)h * a.Lmax;
+    const int recent0 = a.L - a.recent_n;
+    const bool view8 = a.view == 8;
+    uint8_t* pbuf = dsm + pair * 2 * kPairBuf;
+    grid_dep_wait();
+
+    // B fragments of the queries in the tiles' slot order: in k-step s, slots 16s + 2q + e
+    // and 16s + 8 + 2q + e hold dims 16s + q + 4e and 16s + 8 + q + 4e
+    uint32_t qb[2][8][2];
+    const float qscale = 1.4426950408889634f / sqrtf((float)kD);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int row = r0 + 8 * nt + g;
+        const bool ok = row < R;
+        const int t = ok ? row / a.G : 0, gg = ok ? row % a.G : 0;
+        const size_t qi = ((size_t)t * a.Hq + (size_t)h * a.G + gg) * kD;
+        auto qv = [&](int dd) {
+            float x = 0.0f;
+            if (ok) x = a.q_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.q)[qi + dd])
+                                 : reinterpret_cast<const float*>(a.q)[qi + dd];
+            return x * qscale;
+        };
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+            qb[nt][st][0] = pack_h2(qv(16 * st + q), qv(16 * st + q + 4));
+            qb[nt][st][1] = pack_h2(qv(16 * st + 8 + q), qv(16 * st + 12 + q));
+        }
+    }
+    int vis[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int row = r0 + 8 * nt + 2 * q + e;
+            vis[nt][e] = row < R ? a.L - a.T + row / a.G + 1 : 0;
+        }
+    const int vis_r0 = a.L - a.T + r0 / a.G + 1;
+    const int vis_all = vis_r0 < p1 ? vis_r0 : p1;
+
+    float m[2][2], l[2][2], o[2][8][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.0f;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) o[nt][dt][0] = o[nt][dt][1] = o[nt][dt][2] = o[nt][dt][3] = 0.0f;
+    }
+
+    // The warp's loads: role 0 the key rows, role 1 the value rows of a block; lane reads
+    // position pb + lane/2, bytes 32 (lane & 1) .. +31 of the base and refinement rows, and
+    // the scale of position pb + (lane & 15).
+    const uint8_t* bplane = role ? a.vbase : a.kbase;
+    const uint8_t* rplane = role ? a.vref : a.kref;
+    const uint16_t* splane = role ? a.vscale : a.kscale;
+    const uint32_t wrow = (uint32_t)((hrow + (lane >> 1)) * (kD / 2)) + 32u * (lane & 1);
+    const uint32_t srow = (uint32_t)hrow;
+    const uint4 z8 = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+    auto ld16 = [](const uint8_t* ptr) { return *reinterpret_cast<const uint4*>(ptr); };
+    struct Blk {
+        uint4 b[2], r[2];
+        uint16_t sc;
+    };
+    auto load = [&](int pb, Blk& B) {
+        const int p = pb + (lane >> 1), ps = pb + (lane & 15);
+        const uint32_t o_ = wrow + (uint32_t)pb * (kD / 2);
+        const bool need_ref = view8 || pb + 15 >= recent0;
+        B.sc = ps < p1 ? splane[srow + ps] : (uint16_t)0;
+        if (pb + 16 <= p1) {
+            B.b[0] = ld16(bplane + o_);
+            B.b[1] = ld16(bplane + o_ + 16);
+            if (need_ref) {
+                const bool use = view8 || p >= recent0;
+                B.r[0] = use ? ld16(rplane + o_) : z8;
+                B.r[1] = use ? ld16(rplane + o_ + 16) : z8;
+            }
+            return;
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            B.b[c] = z8;
+            B.r[c] = z8;
+            if (p < p1) {
+                B.b[c] = ld16(bplane + o_ + 16 * c);
+                if (view8 || p >= recent0) B.r[c] = ld16(rplane + o_ + 16 * c);
+            }
+        }
+    };
+    // ldmatrix row addresses inside a tile: keys (A, rows = positions) and values (A = V^T)
+    const uint32_t koff = (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * kVPitch + 16 * (lane >> 4));
+    const int lm = lane >> 3, lr = lane & 7;
+    const uint32_t voff = (uint32_t)((lr + 8 * (lm >> 1)) * kVPitch + 16 * (lm & 1));
+
+    int pb = p0 + 16 * pair, it = 0;
+    Blk buf;
+    if (pb < p1) load(pb, buf);
+
+    auto step = [&](auto dec_c, auto mask_c) {
+        constexpr int DEC = decltype(dec_c)::value;
+        constexpr bool MASK = decltype(mask_c)::value;
+        const int pn = pb + 16 * (kPairWarps / 2);
+        const bool kv8 = DEC == 1 || (DEC == 2 && (view8 || pb + 15 >= recent0));
+        uint8_t* bt = pbuf + (it & 1) * kPairBuf;
+        float* ssc = reinterpret_cast<float*>(bt + 2 * kPairTile);     // 16 key scales, 16 value scales
+        {
+            uint8_t* dst = bt + role * kPairTile + (lane >> 1) * kVPitch + 128 * (lane & 1);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t bw[4] = {buf.b[c].x, buf.b[c].y, buf.b[c].z, buf.b[c].w};
+                const uint32_t rw[4] = {buf.r[c].x, buf.r[c].y, buf.r[c].z, buf.r[c].w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t cv[4];
+                    if (kv8) dec8(bw[w], rw[w], cv);
+                    else dec4(bw[w], cv);
+                    *reinterpret_cast<uint4*>(dst + 64 * c + 16 * w) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
+                }
+            }
+            if (lane < 16) ssc[16 * role + lane] = __half2float(__ushort_as_half(buf.sc)) * 0.0625f;
+        }
+        if (pn < p1) load(pn, buf);
+        named_sync(1 + pair, 64);             // both tiles of the block are in place
+
+        const uint32_t kt = smem_u32(bt), vt = kt + kPairTile;
+        float scs[2][2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) scs[nt][0][e] = scs[nt][1][e] = 0.0f;
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4(kt + koff + 32 * st, a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) mma16816f(scs[nt][st & 1], a0, a1, a2, a3, qb[nt][st][0], qb[nt][st][1]);
+        }
+        float ks[2], vsc[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            ks[e] = ssc[g + 8 * e];
+            vsc[e] = ssc[16 + g + 8 * e];
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float sc[4], pr[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[e] = (scs[nt][0][e] + scs[nt][1][e]) * ks[e >> 1];
+            if constexpr (!MASK) {
+                float mx[2];
+#pragma unroll
+                for (int re = 0; re < 2; ++re) {
+                    mx[re] = fmaxf(sc[re], sc[2 + re]);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1)
+                        mx[re] = fmaxf(mx[re], __shfl_xor_sync(0xffffffffu, mx[re], off));
+                }
+                if (__any_sync(0xffffffffu, mx[0] > m[nt][0] || mx[1] > m[nt][1])) {
+#pragma unroll
+                    for (int re = 0; re < 2; ++re) {
+                        const float mn = fmaxf(m[nt][re], mx[re]);
+                        const float corr = ex2(m[nt][re] - mn);
+                        l[nt][re] *= corr;
+                        m[nt][re] = mn;
+#pragma unroll
+                        for (int dt = 0; dt < 8; ++dt) { o[nt][dt][re] *= corr; o[nt][dt][2 + re] *= corr; }
+                    }
+                }
+#pragma unroll
+                for (int re = 0; re < 2; ++re) {
+                    const float e0 = ex2(sc[re] - m[nt][re]), e1 = ex2(sc[2 + re] - m[nt][re]);
+                    l[nt][re] += e0 + e1;
+                    pr[re] = e0 * vsc[0];
+                    pr[2 + re] = e1 * vsc[1];
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int pe = pb + g + 8 * (e >> 1), re = e & 1;
+                    if (!(pe < p1 && pe < vis[nt][re])) sc[e] = -INFINITY;
+                }
+#pragma unroll
+                for (int re = 0; re < 2; ++re) {
+                    float mx = fmaxf(sc[re], sc[2 + re]);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    const float mn = fmaxf(m[nt][re], mx);
+                    const float corr = mn == -INFINITY ? 1.0f : ex2(m[nt][re] - mn);
+                    const float e0 = sc[re] == -INFINITY ? 0.0f : ex2(sc[re] - mn);
+                    const float e1 = sc[2 + re] == -INFINITY ? 0.0f : ex2(sc[2 + re] - mn);
+                    l[nt][re] = l[nt][re] * corr + (e0 + e1);
+                    m[nt][re] = mn;
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) { o[nt][dt][re] *= corr; o[nt][dt][2 + re] *= corr; }
+                    pr[re] = e0 * vsc[0];
+                    pr[2 + re] = e1 * vsc[1];
+                }
+            }
+            const uint32_t pb0 = movmatrix_trans(pack_h2(pr[0], pr[1]));
+            const uint32_t pb1 = movmatrix_trans(pack_h2(pr[2], pr[3]));
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(vt + voff + 32 * dt, v0, v1, v2, v3);
+                mma16816f(o[nt][dt], v0, v1, v2, v3, pb0, pb1);
+            }
+        }
+        pb = pn;
+        ++it;
+    };
+    using Dec4 = std::integral_constant<int, 0>;
+    using Dec8 = std::integral_constant<int, 1>;
+    using DecAny = std::integral_constant<int, 2>;
+    // Both warps of a pair take every block of the pair in the same order (one pair barrier
+    // each); the specialised steps only change what a warp does inside a block.
+    if (!view8) {
+        const int lim = vis_all < recent0 ? vis_all : recent0;
+        while (pb + 16 <= lim) step(Dec4{}, std::false_type{});
+    }
+    while (pb + 16 <= vis_all) step(Dec8{}, std::false_type{});
+    while (pb < p1) step(DecAny{}, std::true_type{});
+
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int re = 0; re < 2; ++re)
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) l[nt][re] += __shfl_xor_sync(0xffffffffu, l[nt][re], off);
+    __syncthreads();                          // every warp is done with the tiles (aliased below)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int re = 0; re < 2; ++re) {
+            const int rr = 8 * nt + 2 * q + re;
+            if (g == 0) { sm[warp][rr] = m[nt][re]; sl[warp][rr] = l[nt][re]; }
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+                so[warp][rr][slot_dim(16 * dt + g)] = o[nt][dt][re];
+                so[warp][rr][slot_dim(16 * dt + g + 8)] = o[nt][dt][2 + re];
+            }
+        }
+    }
+    __syncthreads();
+    const int rbase = tile * kPairRows;
+    const int nr = R - rbase < kPairRows ? R - rbase : kPairRows;
+    for (int i = threadIdx.x; i < nr * kD; i += kPairThreads) {
+        const int rr = i / kD, dd = i % kD;
+        const int rl = rr & 15, w0 = rr >> 4;     // the row's warps: w0 (pair 0), w0 + 2 (pair 1)
+        float M = -INFINITY;
+        for (int w2 = w0; w2 < kPairWarps; w2 += 2) M = fmaxf(M, sm[w2][rl]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+            for (int w2 = w0; w2 < kPairWarps; w2 += 2) {
+                const float f = sm[w2][rl] == -INFINITY ? 0.0f : exp2f(sm[w2][rl] - M);
+                L += f * sl[w2][rl];
+                O += f * so[w2][rl][dd];
+            }
+        }
+        const int rg = rbase + rr;
+        const int tile16 = rg / kRowsPerTile, r16 = rg % kRowsPerTile;
+        const size_t slot = (((size_t)h * a.ntiles + tile16) * a.nsplit + split) * kRowsPerTile + r16;
+        float* wp = a.work + slot * (kD + 2);
+        wp[2 + dd] = O;
+        if (dd == 0) { wp[0] = M; wp[1] = L; }
+    }
+}
+
 // out[t][h*G+g][:] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits.
 // The splits' (max, sum) pairs are read in parallel into shared memory first, so the
 // per-dim pass below issues independent loads.
@@ -766,28 +1073,33 @@ cudaError_t launch_kv_write(const void* x, int bf16, int T, int H, int pos0, int
 
 int kv_rows_per_tile() { return kRowsPerTile; }
 
-// Resident CTAs per SM of the tensor-core kernel for 8 (nrt 1) or 16 (nrt 2) query rows.
-int tc_resident(int nrt) {
-    static int cached[3] = {0, 0, 0};
-    if (cached[nrt] == 0) {
+// Resident CTAs per SM of the tensor-core kernel for 8 (kind 1) or 16 (kind 2) query rows,
+// or of the paired kernel for 32 (kind 3).
+int tc_resident(int kind) {
+    static int cached[4] = {0, 0, 0, 0};
+    if (cached[kind] == 0) {
         int n = 0;
         const cudaError_t e =
-            nrt == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_kv_attn_tc<1>, kTcThreads, kv_tc_smem<1>())
-                     : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_kv_attn_tc<2>, kTcThreads, kv_tc_smem<2>());
+            kind == 1   ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_kv_attn_tc<1>, kTcThreads, kv_tc_smem<1>())
+            : kind == 2 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_kv_attn_tc<2>, kTcThreads, kv_tc_smem<2>())
+                        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_kv_attn_pair, kPairThreads, kPairSmem);
         if (e != cudaSuccess) (void)cudaGetLastError();
-        cached[nrt] = (e == cudaSuccess && n > 0) ? n : 1;
+        cached[kind] = (e == cudaSuccess && n > 0) ? n : 1;
     }
-    return cached[nrt];
+    return cached[kind];
 }
 
 // Position splits: the smallest count whose CTAs fill the resident slots (SMs x CTAs per
 // SM) to 95 % over whole waves, else the best fill up to four waves; at least 128
 // positions per split and at most kMaxSplits splits.
+int kv_kind(int R) { return R <= 8 ? 1 : R <= 16 ? 2 : 3; }
+int kv_rows_per_cta(int kind) { return kind == 1 ? 8 : kind == 2 ? 16 : kPairRows; }
+
 int kv_splits(int T, int G, int Hkv, int L, int sms) {
     const int R = T * G;
-    const int nrt = R <= 8 ? 1 : 2;
-    const long long base = (long long)Hkv * ((R + 8 * nrt - 1) / (8 * nrt));
-    const long long slots = (long long)tc_resident(nrt) * (sms > 0 ? sms : 1);
+    const int kind = kv_kind(R), rows = kv_rows_per_cta(kind);
+    const long long base = (long long)Hkv * ((R + rows - 1) / rows);
+    const long long slots = (long long)tc_resident(kind) * (sms > 0 ? sms : 1);
     long long cap = (L + 127) / 128;
     cap = cap < kMaxSplits ? cap : kMaxSplits;
     const long long by_waves = (4 * slots + base - 1) / base;
@@ -815,13 +1127,17 @@ cudaError_t launch_kv_attention(KvAttnArgs& a, int sms, cudaStream_t stream) {
             : rows <= 4 ? launch_pdl(k_kv_attn<4>, grid, blk, 0, stream, a)
             : rows <= 8 ? launch_pdl(k_kv_attn<8>, grid, blk, 0, stream, a)
                         : launch_pdl(k_kv_attn<16>, grid, blk, 0, stream, a);
-    } else {                                  // tensor cores: 8 or 16 rows per CTA
-        if (rows <= 8) {
+    } else {                                  // tensor cores: 8, 16 or (paired) 32 rows per CTA
+        const int kind = kv_kind(R);
+        if (kind == 1) {
             const dim3 grid(a.Hkv, a.nsplit, (R + 7) / 8), blk(kTcThreads);
             e = launch_pdl(k_kv_attn_tc<1>, grid, blk, kv_tc_smem<1>(), stream, a);
-        } else {
+        } else if (kind == 2 || a.impl == 2) {  // impl 2: 16-row CTAs only (kept for measurement)
             const dim3 grid(a.Hkv, a.nsplit, a.ntiles), blk(kTcThreads);
             e = launch_pdl(k_kv_attn_tc<2>, grid, blk, kv_tc_smem<2>(), stream, a);
+        } else {
+            const dim3 grid(a.Hkv, a.nsplit, (R + kPairRows - 1) / kPairRows), blk(kPairThreads);
+            e = launch_pdl(k_kv_attn_pair, grid, blk, kPairSmem, stream, a);
         }
     }
     if (e != cudaSuccess) return e;

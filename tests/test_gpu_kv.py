@@ -96,10 +96,11 @@ def test_kv_attention_bf16_queries_and_long_context(dev):
     nest.error_check()
 
 
-@pytest.mark.parametrize("impl", ["cuda", "tc"])
+@pytest.mark.parametrize("impl", ["cuda", "tc", "tc16"])
 def test_kv_attention_both_kernels(dev, impl, monkeypatch):
-    """The tensor-core kernel (default) and the CUDA-core kernel on the same cache, rows
-    per KV head from 1 to 40 (one and several 8- and 16-row tiles)."""
+    """The tensor-core kernels (default: 8- and 16-row CTAs, paired 32-row CTAs above 16
+    rows), the tensor-core kernel with 16-row CTAs only, and the CUDA-core kernel on the
+    same cache, rows per KV head from 1 to 40 (one and several tiles)."""
     monkeypatch.setenv("NEST_KV_IMPL", impl)
     rng = np.random.default_rng(21)
     Hkv, L = 3, 500
@@ -110,7 +111,7 @@ def test_kv_attention_both_kernels(dev, impl, monkeypatch):
     nest.kv_write(vc, torch.from_numpy(vx).to(dev), 0)
     k = O.kv_quantize(np.transpose(kx, (1, 0, 2)))
     v = O.kv_quantize(np.transpose(vx, (1, 0, 2)))
-    for T, G in ((1, 1), (3, 3), (9, 1), (5, 8)):
+    for T, G in ((1, 1), (3, 3), (9, 1), (5, 8), (17, 2), (16, 3)):
         q = rng.normal(size=(T, Hkv * G, 128)).astype(np.float32)
         for view, rn in ((8, 0), (4, 17)):
             got = nest.kv_attention(torch.from_numpy(q).to(dev), kc, vc, L, view, rn).cpu().numpy()
