@@ -99,13 +99,15 @@ struct Cfg {
     static constexpr int kNumD = NP >= 256 ? 1 : 2;          // accumulator buffers
     static constexpr int kColA = kNumD * NP;                 // A buffers after the D buffers
     static constexpr int kNumARaw = (kTmemCols - kColA) / 64;
-    static constexpr int kMaxA = NP >= 256 ? 2 : (NP >= 128 ? 3 : 8);   // activation slots the smem holds
+    static constexpr int kMaxA = NP >= 256 ? 2 : (NP >= 128 ? 4 : 8);   // activation slots the smem holds
     static constexpr int kNumA = kNumARaw < kMaxA ? kNumARaw : kMaxA;   // A buffers (64 columns) = activation slots
     static constexpr int kXRing = kNumA * kXBytes;
     static constexpr int kSmemBudget = kCtasPerSm == 1 ? 220 * 1024 : 110 * 1024;
     static constexpr int kStagesRaw = (kSmemBudget - 512 - kXRing) / kWStage;
     static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
-    static constexpr int kDeqWG = 2;                         // dequantising warpgroups
+    // dequantising warpgroups: a CTA that has the SM to itself at 128 tokens runs four, one
+    // per activation slot, so that the decode keeps up with the longer MMAs
+    static constexpr int kDeqWG = NP == 128 ? 4 : 2;
     static constexpr int kProducerWarp = 4 * kDeqWG;
     static constexpr int kMmaWarp = 4 * kDeqWG + 1;
     static constexpr int kThreads = 32 * (4 * kDeqWG + 2);
