@@ -585,8 +585,9 @@ struct RfCfg {
     static constexpr int kNB = NT < 2 ? 2 : NT;              // operand token blocks (n_pad / 8)
     static constexpr bool kStageX = NT >= 2;                 // T <= 8 reads its B fragments from global memory
     static constexpr int kXBytes = kStageX ? 2048 * kNB : 0; // one group of the operand
-    static constexpr int kResUnit = resid_unit_bytes(BITS);
-    static constexpr int kUnit = kBaseUnit + kResUnit + kXBytes;
+    static constexpr int kBaseBytes = base_unit_bytes(BITS);
+    static constexpr int kResUnit = second_unit_bytes(BITS);
+    static constexpr int kUnit = kBaseBytes + kResUnit + kXBytes;
     static constexpr int kSmemBudget = kCtasPerSm == 1 ? 220 * 1024 : 110 * 1024;
     static constexpr int kAvail = kSmemBudget - 512;
     static constexpr int kKURaw = kAvail / (4 * kUnit);      // room for two stages per team
@@ -594,7 +595,7 @@ struct RfCfg {
     static constexpr int kStageBytes = kKU * kUnit;
     static constexpr int kStagesRaw = kAvail / kStageBytes;
     static constexpr int kStages = (kStagesRaw > 8 ? 8 : kStagesRaw) & ~1;   // even: a stage keeps its team
-    static constexpr int kResOff = kKU * kBaseUnit;          // parts of a stage: bases, residuals, operand
+    static constexpr int kResOff = kKU * kBaseBytes;         // parts of a stage: bases, residuals, operand
     static constexpr int kXOff = kResOff + kKU * kResUnit;
     static constexpr int kTeams = 2;
     static constexpr int kWarpsPerTeam = 4;
@@ -697,8 +698,8 @@ k_nest_rf(const __grid_constant__ GemmArgs p) {
             const GemmTask& t = p.task[c.k];
             const long long lu = c.local(p);
             mbar_arrive_expect_tx(full(s), kc * C::kUnit);
-            bulk_g2s(smem_u32(stage(s)), t.base + lu * kBaseUnit, kc * kBaseUnit, full(s));
-            if constexpr (BITS != 0)
+            bulk_g2s(smem_u32(stage(s)), t.base + lu * C::kBaseBytes, kc * C::kBaseBytes, full(s));
+            if constexpr (C::kResUnit != 0)
                 bulk_g2s(smem_u32(stage(s) + C::kResOff), t.resid + lu * C::kResUnit, kc * C::kResUnit, full(s));
         };
         auto issue_x = [&](int j, const UnitCursor& c, int kc) {
@@ -763,7 +764,8 @@ k_nest_rf(const __grid_constant__ GemmArgs p) {
         lut_lo = (hv[0] & 0xFFu) | ((hv[1] & 0xFFu) << 8) | ((hv[2] & 0xFFu) << 16) | ((hv[3] & 0xFFu) << 24);
         lut_hi = (hv[0] >> 8) | ((hv[1] >> 8) << 8) | ((hv[2] >> 8) << 16) | ((hv[3] >> 8) << 24);
     }
-    const __half2 off2 = __float2half2_rn(1024.0f + (BITS ? (float)(1 << (BITS - 1)) : 0.0f));
+    const __half2 off2 = __float2half2_rn(1024.0f + ((BITS && !is_w4(BITS)) ? (float)(1 << (BITS - 1)) : 0.0f));
+    const __half2 off4 = __float2half2_rn(1024.0f + 8.0f);   // W4: 1024 + the nibble offset
     float zacc[2][NT][4];
 #pragma unroll
     for (int sl = 0; sl < 2; ++sl)
@@ -818,22 +820,32 @@ k_nest_rf(const __grid_constant__ GemmArgs p) {
                     if (u + 1 < kc) load_bx(task.xop, cj.g + u + 1, bxn);
                     else if (has_next) load_bx(p.task[c2.k].xop, c2.g, bxn);
                 }
-                const uint8_t* sb = stage(s_) + u * kBaseUnit;
+                const uint8_t* sb = stage(s_) + u * C::kBaseBytes;
                 const uint8_t* sr = stage(s_) + C::kResOff + u * C::kResUnit;
                 const uint8_t* sx = stage(s_) + C::kXOff + u * C::kXBytes;
 #pragma unroll
                 for (int sl = 0; sl < 2; ++sl) {
                     const int r0 = 32 * wq + 16 * sl + g, r1 = r0 + 8;
-                    uint32_t bw0[2], bw1[2];
+                    // 2-bit base: one word per row and half (codes of columns 4Q.., Q = 16h + 4q + s,
+                    // in bits 2s of each byte).  W4: the row's nibble words 8h + 2q and 8h + 2q + 1
+                    // (column 8w + 4k + j in bits 8j + 4k of word w).
+                    uint32_t bw0[2][2], bw1[2][2];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        bw0[h] = *reinterpret_cast<const uint32_t*>(sb + (h * kRows + r0) * 16 + 4 * q);
-                        bw1[h] = *reinterpret_cast<const uint32_t*>(sb + (h * kRows + r1) * 16 + 4 * q);
+                        if constexpr (is_w4(BITS)) {
+                            const uint2 v0 = *reinterpret_cast<const uint2*>(sb + ((2 * h + (q >> 1)) * kRows + r0) * 16 + 8 * (q & 1));
+                            const uint2 v1 = *reinterpret_cast<const uint2*>(sb + ((2 * h + (q >> 1)) * kRows + r1) * 16 + 8 * (q & 1));
+                            bw0[h][0] = v0.x; bw0[h][1] = v0.y; bw1[h][0] = v1.x; bw1[h][1] = v1.y;
+                        } else {
+                            bw0[h][0] = *reinterpret_cast<const uint32_t*>(sb + (h * kRows + r0) * 16 + 4 * q);
+                            bw1[h][0] = *reinterpret_cast<const uint32_t*>(sb + (h * kRows + r1) * 16 + 4 * q);
+                        }
                     }
-                    const float sb0 = __half2float(*reinterpret_cast<const __half*>(sb + 4096 + 2 * r0));
-                    const float sb1 = __half2float(*reinterpret_cast<const __half*>(sb + 4096 + 2 * r1));
+                    constexpr int kScaleOff = is_w4(BITS) ? 8192 : 4096;   // s4 (W4) or s_b
+                    const float sb0 = __half2float(*reinterpret_cast<const __half*>(sb + kScaleOff + 2 * r0));
+                    const float sb1 = __half2float(*reinterpret_cast<const __half*>(sb + kScaleOff + 2 * r1));
                     float sr0 = 0.0f, sr1 = 0.0f;
-                    if constexpr (BITS != 0) {
+                    if constexpr (C::kResUnit != 0) {
                         sr0 = __half2float(*reinterpret_cast<const __half*>(sr + 2048 * BITS + 2 * r0));
                         sr1 = __half2float(*reinterpret_cast<const __half*>(sr + 2048 * BITS + 2 * r1));
                     }
@@ -844,8 +856,8 @@ k_nest_rf(const __grid_constant__ GemmArgs p) {
                         for (int e = 0; e < 4; ++e) { db[nt][e] = 0.0f; dr[nt][e] = 0.0f; }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        ResidWords<BITS> rw0, rw1;
-                        if constexpr (BITS != 0) { rw0.load(sr, r0, h, q); rw1.load(sr, r1, h, q); }
+                        ResidWords<is_w4(BITS) ? 0 : BITS> rw0, rw1;
+                        if constexpr (C::kResUnit != 0) { rw0.load(sr, r0, h, q); rw1.load(sr, r1, h, q); }
 #pragma unroll
                         for (int pp = 0; pp < 2; ++pp) {
                             // B fragments of k-steps 2pp and 2pp+1: x'[8nt + g][4Q .. 4Q+7], Q = 16h + 4q + 2pp
@@ -861,15 +873,28 @@ k_nest_rf(const __grid_constant__ GemmArgs p) {
 #pragma unroll
                             for (int s2 = 0; s2 < 2; ++s2) {
                                 const int s = 2 * pp + s2;
-                                const uint32_t v0 = (bw0[h] >> (2 * s)) & 0x03030303u;
-                                const uint32_t v1 = (bw1[h] >> (2 * s)) & 0x03030303u;
-                                const uint32_t sel0 = v0 * 0x11u + 0x40404040u, sel1 = v1 * 0x11u + 0x40404040u;
-                                const uint32_t a0 = prmt(lut_lo, lut_hi, sel0), a2 = prmt(lut_lo, lut_hi, sel0 >> 16);
-                                const uint32_t a1 = prmt(lut_lo, lut_hi, sel1), a3 = prmt(lut_lo, lut_hi, sel1 >> 16);
+                                uint32_t a0, a1, a2, a3;
+                                if constexpr (is_w4(BITS)) {
+                                    // u4 = q4 + 8 of columns 4Q .. 4Q+3, one per byte, as fp16 q4
+                                    const uint32_t b0 = (bw0[h][s >> 1] >> (4 * (s & 1))) & 0x0F0F0F0Fu;
+                                    const uint32_t b1 = (bw1[h][s >> 1] >> (4 * (s & 1))) & 0x0F0F0F0Fu;
+                                    a0 = h2_as_u32(__hsub2(u32_as_h2(prmt(b0, 0x64646464u, 0x5140u)), off4));
+                                    a2 = h2_as_u32(__hsub2(u32_as_h2(prmt(b0, 0x64646464u, 0x7362u)), off4));
+                                    a1 = h2_as_u32(__hsub2(u32_as_h2(prmt(b1, 0x64646464u, 0x5140u)), off4));
+                                    a3 = h2_as_u32(__hsub2(u32_as_h2(prmt(b1, 0x64646464u, 0x7362u)), off4));
+                                } else {
+                                    const uint32_t v0 = (bw0[h][0] >> (2 * s)) & 0x03030303u;
+                                    const uint32_t v1 = (bw1[h][0] >> (2 * s)) & 0x03030303u;
+                                    const uint32_t sel0 = v0 * 0x11u + 0x40404040u, sel1 = v1 * 0x11u + 0x40404040u;
+                                    a0 = prmt(lut_lo, lut_hi, sel0);
+                                    a2 = prmt(lut_lo, lut_hi, sel0 >> 16);
+                                    a1 = prmt(lut_lo, lut_hi, sel1);
+                                    a3 = prmt(lut_lo, lut_hi, sel1 >> 16);
+                                }
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt)
                                     mma16816(db[nt], a0, a1, a2, a3, s2 ? bx[nt].z : bx[nt].x, s2 ? bx[nt].w : bx[nt].y);
-                                if constexpr (BITS != 0) {
+                                if constexpr (C::kResUnit != 0) {
                                     const uint32_t u0 = rw0.codes(s, q), u1 = rw1.codes(s, q);
                                     const uint32_t q0 = h2_as_u32(__hsub2(u32_as_h2(prmt(u0, 0x64646464u, 0x5140u)), off2));
                                     const uint32_t q2 = h2_as_u32(__hsub2(u32_as_h2(prmt(u0, 0x64646464u, 0x7362u)), off2));
@@ -955,11 +980,11 @@ cudaError_t launch_t(const GemmArgs& a, int grid, cudaStream_t stream) {
 
 // Kernel choice, from measurements on GB300 (a 128 x N x 16 tcgen05.mma costs a
 // fixed ~50 cycles to issue whatever N is; mma.sync m16n8k16 runs ~0.47 per cycle
-// per SM): the draft (base only) at T <= 8 on the register-fragment kernel, where
-// the 2-bit decode and not the MMA issue bounds it; everything else on tcgen05,
-// which is faster for the verify at every T.  NEST_GEMM_PATH=tc or =rf in the
-// environment forces one kernel (rf up to 32 tokens), for measuring one against
-// the other.
+// per SM): the drafts (2-bit base or W4 alone) at T <= 8 on the register-fragment
+// kernel, where the decode and not the MMA issue bounds them; everything else on
+// tcgen05, which is faster for the verify at every T (and the only kernel with the
+// W8 decode).  NEST_GEMM_PATH=tc or =rf in the environment forces one kernel (rf up
+// to 32 tokens, not for W8), for measuring one against the other.
 int path_override() {
     const char* e = getenv("NEST_GEMM_PATH");
     return (e && e[0] == 't') ? 1 : (e && e[0] == 'r') ? 2 : 0;
@@ -967,9 +992,9 @@ int path_override() {
 
 template <int BITS>
 cudaError_t launch_bits(const GemmArgs& a, int grid, cudaStream_t stream) {
-    if constexpr (!is_w4(BITS)) {
+    if constexpr (BITS != 48) {               // the register-fragment kernel has no W8 decode
         const int ov = path_override();
-        const bool rf = ov == 2 ? a.T <= 32 : (ov == 0 && BITS == 0 && a.T <= 8);
+        const bool rf = ov == 2 ? a.T <= 32 : (ov == 0 && (BITS == 0 || BITS == 40) && a.T <= 8);
         if (rf) {
             if (a.T <= 8) return launch_rf<BITS, 1>(a, grid, stream);
             if (a.T <= 16) return launch_rf<BITS, 2>(a, grid, stream);

@@ -122,6 +122,28 @@ def test_edge_codes_and_linear(dev):
     nest.error_check()
 
 
+def test_draft_register_fragment_and_tcgen05_paths(dev, monkeypatch):
+    """The W4 draft on both GEMM kernels: the register-fragment (mma.sync) kernel that
+    serves T <= 8 by default, forced up to T = 32, and the tcgen05 kernel forced down to
+    T = 1; random admissible codes (every q4 value), each against the oracle."""
+    M, K = 1280, 2560
+    q4, s4, qr = _codes(M, K, 90)
+    s_o, s_i = synth.sign_pair(M, K, 91)
+    L = _layer(q4, s4, qr, s_o, s_i, dev)
+    lay = {"q4": q4, "s4": s4, "qr": qr}
+    for T in (1, 3, 8, 9, 16, 17, 32):
+        xb, xv = synth.activations(T, K, 92 + T)
+        x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+        xop = nest.new_xop(K, T, dev)
+        nest.rotate(x, L.sign_in, 0, x_op=xop)
+        ref = O.forward_w4w8(lay, s_o, s_i, xv, False)["z"]
+        for path in ("rf", "tc"):
+            monkeypatch.setenv("NEST_GEMM_PATH", path)
+            parity(nest.gemm(L, xop, T, False).cpu().numpy(), ref)
+    monkeypatch.delenv("NEST_GEMM_PATH")
+    nest.error_check()
+
+
 def test_draft_is_exact_subset(dev):
     """With a zero refinement the W8 target decodes to 16 q4 s4 / 16: the draft's values."""
     M, K = 512, 1024
