@@ -205,6 +205,33 @@ def test_register_fragment_and_tcgen05_paths(dev, bits, monkeypatch):
     nest.error_check()
 
 
+def test_draft_grouped_many_units(dev):
+    """The draft with several stages per CTA and stages that meet the boundary of two
+    linears: gate and up of the MLP triplet's shape (2 x 9728x2560, 3040 units) in one
+    grouped launch, random 2-bit codes and scales, T from 1 to 8."""
+    M, K, G = 9728, 2560, 2560 // 128
+    rng = np.random.default_rng(77)
+    layers, refs = [], []
+    for i in range(2):
+        q = {"base_codes": rng.integers(0, 4, size=(M, K)).astype(np.uint8),
+             "base_scales": np.exp(rng.uniform(np.log(1e-3), np.log(3e-2), size=(M, G))).astype(np.float16),
+             "resid_codes": np.zeros((M, K), np.int8), "resid_scales": np.zeros((M, G), np.float16)}
+        s_o, s_i = synth.sign_pair(M, K, 78 + i)
+        layers.append(dev_layer(q, 0, s_o, s_i, dev))
+        refs.append((q, s_o, s_i))
+    for T in (1, 5, 8):
+        x, xv = bf16_x(T, K, 80 + T, dev)
+        xops = []
+        for L in layers:
+            xop = nest.new_xop(K, T, dev)
+            nest.rotate(x, L.sign_in, 0, x_op=xop)
+            xops.append(xop)
+        zs = nest.gemm_group(layers, xops, T, False)
+        for (q, s_o, s_i), z in zip(refs, zs):
+            parity(z.cpu().numpy(), O.forward(q, s_o, s_i, xv, False)["z"])
+    nest.error_check()
+
+
 def _close(a, b, rel=1e-6):
     """Equal up to the order of the fp32 additions of the split K range."""
     scale = np.sqrt(np.mean(np.asarray(b, np.float64) ** 2))
