@@ -42,8 +42,8 @@ PREFILL_T = (128, 256)
 # dram__bytes_write.sum of a grouped gate+up verify launch at T=16, divided by its two
 # linears).  Valid only for the kernel source it was taken on: reported as null otherwise.
 NCU_TRAFFIC = {"src": "nested_bit_quantized_gb300/csrc/nest_gemm.cu",
-               "sha256": "784958d7d9b7cb6e1be09f322d22198a82bc622d839635a2e4107a8e3af9f951",
-               "bytes_per_linear": (59.045376e6 + 0.057344e6) / 2}
+               "sha256": "9518113b720a93ed86254df83bb14aee75eab28625c2f445acc59aa0b4a7028a",
+               "bytes_per_linear": (59.045120e6 + 0.047104e6) / 2}
 
 
 def ncu_traffic():
