@@ -316,29 +316,56 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, u
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
+// Logic helpers with one immediate each.  A single lop3 takes one 32-bit immediate, so
+// an expression with two constants (a mask and the fp16 exponent bytes) costs two; the
+// kernels keep the second constant in a register (see kv_consts) and use these.
+template <uint32_t M>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {      // (a & M) | c
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(M), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t select_bits(uint32_t a, uint32_t b, uint32_t m) {   // (a & m) | (b & ~m)
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(d) : "r"(a), "r"(b), "r"(m));
+    return d;
+}
+
+// Constants of the decode, held in registers: the fp16 exponent bytes 0x64 of a pair
+// (e64), of four bytes (e6464) and the high-nibble mask (mhi).  They are built from a
+// kernel parameter (x >> 31 of a non-negative count is 0) so that they are not folded
+// back into immediates.
+struct KvConsts {
+    uint32_t e64, e6464, mhi;
+};
+__device__ __forceinline__ KvConsts kv_consts(int nonneg) {
+    const uint32_t z = (uint32_t)nonneg >> 31;
+    return {0x64006400u | z, 0x64646464u | z, 0xF0F0F0F0u | z};
+}
+
 // One 32-bit base word b and refinement word r (dims 8w .. 8w+7 of a row, byte i = dims
 // 2i | 2i+1) as the fp16 codes 16 u4 + u_r - 136 in pairs out[j] = (dim j, dim j + 4).
-__device__ __forceinline__ void dec8(uint32_t b, uint32_t r, uint32_t (&out)[4]) {
-    const uint32_t ev = ((b << 4) & 0xF0F0F0F0u) | (r & 0x0F0F0F0Fu);          // byte i: dim 2i
-    const uint32_t od = (b & 0xF0F0F0F0u) | ((r >> 4) & 0x0F0F0F0Fu);          // byte i: dim 2i + 1
+__device__ __forceinline__ void dec8(uint32_t b, uint32_t r, const KvConsts& k, uint32_t (&out)[4]) {
+    const uint32_t ev = select_bits(b << 4, r, k.mhi);          // byte i: dim 2i
+    const uint32_t od = select_bits(b, r >> 4, k.mhi);          // byte i: dim 2i + 1
     const __half2 off = __float2half2_rn(1024.0f + 136.0f);
-    out[0] = h2_as_u32(__hsub2(u32_as_h2(prmt(ev, 0x64646464u, 0x4240u)), off));   // dims 0, 4
-    out[1] = h2_as_u32(__hsub2(u32_as_h2(prmt(od, 0x64646464u, 0x4240u)), off));   // dims 1, 5
-    out[2] = h2_as_u32(__hsub2(u32_as_h2(prmt(ev, 0x64646464u, 0x4341u)), off));   // dims 2, 6
-    out[3] = h2_as_u32(__hsub2(u32_as_h2(prmt(od, 0x64646464u, 0x4341u)), off));   // dims 3, 7
+    out[0] = h2_as_u32(__hsub2(u32_as_h2(prmt(ev, k.e6464, 0x4240u)), off));   // dims 0, 4
+    out[1] = h2_as_u32(__hsub2(u32_as_h2(prmt(od, k.e6464, 0x4240u)), off));   // dims 1, 5
+    out[2] = h2_as_u32(__hsub2(u32_as_h2(prmt(ev, k.e6464, 0x4341u)), off));   // dims 2, 6
+    out[3] = h2_as_u32(__hsub2(u32_as_h2(prmt(od, k.e6464, 0x4341u)), off));   // dims 3, 7
 }
 
 // The same word read at KV4 (u_r = 8): 16 u4 - 128 in the same pair order.  A nibble in
 // bits 0-3 of an fp16 with exponent field 0x64 reads as 1024 + u4, one in bits 4-7 as
 // 1024 + 16 u4; both are mapped to 16 u4 - 128 exactly by one fp16 operation.
-__device__ __forceinline__ void dec4(uint32_t b, uint32_t (&out)[4]) {
+__device__ __forceinline__ void dec4(uint32_t b, const KvConsts& k, uint32_t (&out)[4]) {
     const uint32_t b8 = b >> 8;
     const __half2 x16 = __float2half2_rn(16.0f), o16 = __float2half2_rn(-16.0f * 1024.0f - 128.0f);
     const __half2 o1 = __float2half2_rn(1024.0f + 128.0f);
-    out[0] = h2_as_u32(__hfma2(u32_as_h2((b & 0x000F000Fu) | 0x64006400u), x16, o16));    // dims 0, 4
-    out[1] = h2_as_u32(__hsub2(u32_as_h2((b & 0x00F000F0u) | 0x64006400u), o1));          // dims 1, 5
-    out[2] = h2_as_u32(__hfma2(u32_as_h2((b8 & 0x000F000Fu) | 0x64006400u), x16, o16));   // dims 2, 6
-    out[3] = h2_as_u32(__hsub2(u32_as_h2((b8 & 0x00F000F0u) | 0x64006400u), o1));         // dims 3, 7
+    out[0] = h2_as_u32(__hfma2(u32_as_h2(and_or<0x000F000Fu>(b, k.e64)), x16, o16));    // dims 0, 4
+    out[1] = h2_as_u32(__hsub2(u32_as_h2(and_or<0x00F000F0u>(b, k.e64)), o1));          // dims 1, 5
+    out[2] = h2_as_u32(__hfma2(u32_as_h2(and_or<0x000F000Fu>(b8, k.e64)), x16, o16));   // dims 2, 6
+    out[3] = h2_as_u32(__hsub2(u32_as_h2(and_or<0x00F000F0u>(b8, k.e64)), o1));         // dims 3, 7
 }
 
 // Dim of slot x of the decoded order (pairs (j, j + 4) inside each group of 8).
@@ -448,6 +475,7 @@ k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
     // per-lane 32-bit offsets of position 0 of the head (a plane holds fewer than 2^32
     // bytes); a block at pb adds pb rows.  The plane pointers stay kernel parameters.
     const bool view8 = a.view == 8;
+    const KvConsts kc = kv_consts(a.T);
     const uint32_t krow = (uint32_t)((hrow + g) * (kD / 2)) + 16u * q;
     const uint32_t vrow = (uint32_t)((hrow + (lane >> 1)) * (kD / 2)) + 32u * (lane & 1);
     const uint32_t srow = (uint32_t)(hrow + g);
@@ -544,8 +572,8 @@ k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     uint32_t cv[4];
-                    if (kv8) dec8(bw[w], rw[w], cv);
-                    else dec4(bw[w], cv);
+                    if (kv8) dec8(bw[w], rw[w], kc, cv);
+                    else dec4(bw[w], kc, cv);
                     *reinterpret_cast<uint4*>(dst + 64 * c + 16 * w) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
                 }
             }
@@ -569,11 +597,11 @@ k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
             for (int w = 0; w < 4; ++w) {
                 uint32_t c0[4], c1[4];
                 if (kv8) {
-                    dec8(b0w[w], r0w[w], c0);
-                    dec8(b1w[w], r1w[w], c1);
+                    dec8(b0w[w], r0w[w], kc, c0);
+                    dec8(b1w[w], r1w[w], kc, c1);
                 } else {
-                    dec4(b0w[w], c0);
-                    dec4(b1w[w], c1);
+                    dec4(b0w[w], kc, c0);
+                    dec4(b1w[w], kc, c1);
                 }
 #pragma unroll
                 for (int nt = 0; nt < NRT; ++nt) {
@@ -756,6 +784,7 @@ k_kv_attn_pair(const __grid_constant__ KvAttnArgs a) {
     const size_t hrow = (size_t)h * a.Lmax;
     const int recent0 = a.L - a.recent_n;
     const bool view8 = a.view == 8;
+    const KvConsts kc = kv_consts(a.T);
     uint8_t* pbuf = dsm + pair * 2 * kPairBuf;
     grid_dep_wait();
 
@@ -865,8 +894,8 @@ k_kv_attn_pair(const __grid_constant__ KvAttnArgs a) {
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     uint32_t cv[4];
-                    if (kv8) dec8(bw[w], rw[w], cv);
-                    else dec4(bw[w], cv);
+                    if (kv8) dec8(bw[w], rw[w], kc, cv);
+                    else dec4(bw[w], kc, cv);
                     *reinterpret_cast<uint4*>(dst + 64 * c + 16 * w) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
                 }
             }
