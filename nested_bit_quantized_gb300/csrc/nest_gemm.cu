@@ -19,7 +19,9 @@
 //                    memory (128 x 16 per instruction), B = the activation block
 //                    in shared memory (Np x 16), D = fp32 accumulators in tensor
 //                    memory (128 lanes x Np columns).
-//   epilogue       : warpgroup 0 reads D with tcgen05.ld and writes z.
+//   epilogue       : warpgroup 0 (at 128 tokens and more every warpgroup, each
+//                    for its share of the columns) reads D with tcgen05.ld and
+//                    adds it into z.
 // Work split: the (tile, group) units, tile-major, are cut into equal
 // contiguous ranges, one per CTA ("stream-K").  Every CTA adds the sums of
 // each row-tile segment it covers into z with fp32 reductions (z += ...), so a
@@ -108,6 +110,9 @@ struct Cfg {
     // dequantising warpgroups: a CTA that has the SM to itself at 128 tokens runs four, one
     // per activation slot, so that the decode keeps up with the longer MMAs
     static constexpr int kDeqWG = NP == 128 ? 4 : 2;
+    // warpgroups that run the epilogues: all of them at 128 tokens and more (each reads
+    // and reduces its share of the accumulator columns), warpgroup 0 alone below
+    static constexpr int kEpiWG = NP >= 128 ? kDeqWG : 1;
     static constexpr int kProducerWarp = 4 * kDeqWG;
     static constexpr int kMmaWarp = 4 * kDeqWG + 1;
     static constexpr int kThreads = 32 * (4 * kDeqWG + 2);
@@ -119,6 +124,7 @@ struct Cfg {
     static_assert(kStages % kDeqWG == 0 || kStages >= kNumA, "weight-stage phase order needs S >= NA when S is odd");
     static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
     static_assert(kWStage % 128 == 0 && kXBytes % 128 == 0, "stage alignment");
+    static_assert(NP < 128 || (NP / kEpiWG) % 32 == 0, "epilogue columns per warpgroup");
 };
 
 // W4/W8: decode 64 columns (half h) of row r into 32 fp16x2 registers, w = c * s4 with
@@ -303,7 +309,7 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) { mbar_init(full_w(s), 1); mbar_init(empty_w(s), kRows); }
         for (int a = 0; a < NA; ++a) { mbar_init(full_x(a), 1); mbar_init(a_full(a), kRows); mbar_init(done(a), 1); }
-        for (int d = 0; d < ND; ++d) { mbar_init(d_full(d), 1); mbar_init(d_empty(d), kRows); }
+        for (int d = 0; d < ND; ++d) { mbar_init(d_full(d), 1); mbar_init(d_empty(d), C::kEpiWG * kRows); }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -431,7 +437,7 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
             warp_wait(drain_bar, 0, abort_flag, false);
         }
     } else {
-        // dequantisation warpgroups; warpgroup 0 also runs the epilogues
+        // dequantisation warpgroups; they (warpgroup 0 alone below 128 tokens) also run the epilogues
         const int wg = warp >> 2;
         const int r = 32 * (warp & 3) + lane;               // row of the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -492,7 +498,7 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
                 if (!warp_wait(full_x(a), (i / NA) & 1, abort_flag)) break;
                 mbar_arrive(a_full(a));
             }
-            if (wg == 0 && last) {
+            if (wg < C::kEpiWG && last) {
                 const int d = seg % ND;
                 if (!warp_wait(d_full(d), (seg / ND) & 1, abort_flag)) break;
                 tc_fence_after();
@@ -512,12 +518,14 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
                             if (t < T) atomicAdd(zp + (size_t)t * M, v[t] * kOutScale);   // fire-and-forget reduction
                     }
                 } else {
-                    // 32 accumulator columns at a time; the buffer is released after the last load
+                    // warpgroup wg takes its kEpiCols accumulator columns, 32 at a time; it
+                    // releases the buffer after its last load
+                    constexpr int kEpiCols = NP / C::kEpiWG;
                     if (!dep_done) { grid_dep_wait(); dep_done = true; }
-                    for (int c0 = 0; c0 < NP; c0 += 32) {
+                    for (int c0 = wg * kEpiCols; c0 < (wg + 1) * kEpiCols; c0 += 32) {
                         float v[32];
                         tmem_ld_cols<32>(tmem + lane_base + d * NP + c0, v);
-                        if (c0 + 32 == NP) {
+                        if (c0 + 32 == (wg + 1) * kEpiCols) {
                             tc_fence_before();
                             mbar_arrive(d_empty(d));
                         }
