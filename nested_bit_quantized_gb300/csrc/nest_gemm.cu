@@ -107,9 +107,12 @@ struct Cfg {
     static constexpr int kSmemBudget = kCtasPerSm == 1 ? 220 * 1024 : 110 * 1024;
     static constexpr int kStagesRaw = (kSmemBudget - 512 - kXRing) / kWStage;
     static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
-    // dequantising warpgroups: a CTA that has the SM to itself at 128 tokens runs four, one
-    // per activation slot, so that the decode keeps up with the longer MMAs
-    static constexpr int kDeqWG = NP == 128 ? 4 : 2;
+    // dequantising warpgroups: a CTA that has the SM to itself (128 and 256 tokens) runs
+    // four, so that the decode keeps up with the longer MMAs.  At 128 tokens each takes
+    // whole units (one per activation slot); at 256 the smem holds only two activation
+    // slots, so two warpgroups share each unit, one 64-column half each.
+    static constexpr int kDeqWG = NP >= 128 ? 4 : 2;
+    static constexpr int kUnitWG = NP >= 256 ? 2 : 1;        // warpgroups per unit
     // warpgroups that run the epilogues: all of them at 128 tokens and more (each reads
     // and reduces its share of the accumulator columns), warpgroup 0 alone below
     static constexpr int kEpiWG = NP >= 128 ? kDeqWG : 1;
@@ -122,6 +125,7 @@ struct Cfg {
     static_assert(kNumA >= 2, "tensor memory budget");
     static_assert(kStages >= 2, "stage too large");
     static_assert(kStages % kDeqWG == 0 || kStages >= kNumA, "weight-stage phase order needs S >= NA when S is odd");
+    static_assert(kDeqWG % kUnitWG == 0 && (kUnitWG == 1 || kUnitWG == 2), "warpgroups per unit");
     static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
     static_assert(kWStage % 128 == 0 && kXBytes % 128 == 0, "stage alignment");
     static_assert(NP < 128 || (NP / kEpiWG) % 32 == 0, "epilogue columns per warpgroup");
@@ -307,8 +311,12 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) { mbar_init(full_w(s), 1); mbar_init(empty_w(s), kRows); }
-        for (int a = 0; a < NA; ++a) { mbar_init(full_x(a), 1); mbar_init(a_full(a), kRows); mbar_init(done(a), 1); }
+        for (int s = 0; s < S; ++s) { mbar_init(full_w(s), 1); mbar_init(empty_w(s), C::kUnitWG * kRows); }
+        for (int a = 0; a < NA; ++a) {
+            mbar_init(full_x(a), 1);
+            mbar_init(a_full(a), C::kUnitWG * kRows);
+            mbar_init(done(a), 1);
+        }
         for (int d = 0; d < ND; ++d) { mbar_init(d_full(d), 1); mbar_init(d_empty(d), C::kEpiWG * kRows); }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -452,7 +460,7 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
             const bool first = (i == 0) || cu.g == 0;
             const bool last = (i == n - 1) || cu.group_end(p);
             if (first) ++seg;
-            if (i % C::kDeqWG == wg) {
+            if (i % (C::kDeqWG / C::kUnitWG) == wg / C::kUnitWG) {
                 const int s = i % S, a = i % NA;
                 // Order matters when S is odd: stage s then alternates between the two
                 // warpgroups, and a parity wait cannot tell phase k+1 from phase k-1.  The
@@ -466,10 +474,13 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
                 tc_fence_after();
                 const uint8_t* sb = st_base(s);
                 const uint8_t* sr = st_res(s);
+                constexpr int kHalves = 2 / C::kUnitWG;          // the 64-column halves this warpgroup decodes
+                const int h_first = (wg % C::kUnitWG) * kHalves;
                 if constexpr (is_w4(BITS)) {
                     const __half2 s2 = __half2half2(*reinterpret_cast<const __half*>(sb + 8192 + 2 * r));
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int j = 0; j < kHalves; ++j) {
+                        const int hh = h_first + j;
                         uint32_t w[32];
                         dequant_half_w4<BITS>(sb, sr, r, hh, s2, off2, w);
                         tmem_st32_wait(tmem + lane_base + C::kColA + 64 * a + 32 * hh, w);
@@ -486,7 +497,8 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
                     if constexpr (BITS != 0)
                         sr2 = __half2half2(*reinterpret_cast<const __half*>(sr + 2048 * BITS + 2 * r));
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int j = 0; j < kHalves; ++j) {
+                        const int hh = h_first + j;
                         uint32_t w[32];
                         dequant_half<BITS>(sb, sr, r, hh, lut_lo, lut_hi, sr2, off2, w);
                         tmem_st32_wait(tmem + lane_base + C::kColA + 64 * a + 32 * hh, w);
