@@ -176,6 +176,17 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def max_over_ranks(value, dist, device):
+    """The largest value over the ranks of the process group (the slowest rank's time),
+    or value itself without a process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -311,12 +322,7 @@ def run_gpu(args, rank, world):
                 g.replay()
             e.record(stream)
         torch.cuda.synchronize()
-        ms = s.elapsed_time(e)
-        if dist is not None:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(s.elapsed_time(e), dist, dev)
 
     n_lin = 3 * C
     step_bytes = sum(lin_bytes(L.M, L.K, T_DRAFT, DC) + lin_bytes(L.M, L.K, T_VERIFY, VC)
@@ -430,11 +436,7 @@ def run_gpu(args, rank, world):
         e2e_once()
     e.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = s.elapsed_time(e) / args.steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(s.elapsed_time(e) / args.steps, dist, dev)
     nest.error_check()
 
     cpu = None
