@@ -289,6 +289,7 @@ k_kv_attn(const __grid_constant__ KvAttnArgs a) {
 // ---------------------------------------------------------------------------
 
 constexpr int kTcWarps = 4;
+constexpr float kLazy = 8.0f;             // log2 headroom before the outputs are rescaled
 constexpr int kTcThreads = 32 * kTcWarps;
 constexpr int kVPitch = 272;              // bytes per position row of a warp's fp16 value block (bank-conflict free)
 
@@ -627,8 +628,11 @@ k_kv_attn_tc(const __grid_constant__ KvAttnArgs a) {
                     for (int off = 4; off < 32; off <<= 1)
                         mx[re] = fmaxf(mx[re], __shfl_xor_sync(0xffffffffu, mx[re], off));
                 }
-                // the outputs are rescaled only when some row's running max grows
-                if (__any_sync(0xffffffffu, mx[0] > m[nt][0] || mx[1] > m[nt][1])) {
+                // The outputs are rescaled only when some row's block max exceeds its running
+                // max by more than kLazy (log2 units): in between, the probabilities against the
+                // kept max stay below 2^kLazy, which fp16 P and the fp32 sums hold without loss,
+                // and the final merge divides by the sum taken against the same max.
+                if (__any_sync(0xffffffffu, mx[0] > m[nt][0] + kLazy || mx[1] > m[nt][1] + kLazy)) {
 #pragma unroll
                     for (int re = 0; re < 2; ++re) {
                         const float mn = fmaxf(m[nt][re], mx[re]);
@@ -937,7 +941,7 @@ k_kv_attn_pair(const __grid_constant__ KvAttnArgs a) {
                     for (int off = 4; off < 32; off <<= 1)
                         mx[re] = fmaxf(mx[re], __shfl_xor_sync(0xffffffffu, mx[re], off));
                 }
-                if (__any_sync(0xffffffffu, mx[0] > m[nt][0] || mx[1] > m[nt][1])) {
+                if (__any_sync(0xffffffffu, mx[0] > m[nt][0] + kLazy || mx[1] > m[nt][1] + kLazy)) {   // see k_kv_attn_tc
 #pragma unroll
                     for (int re = 0; re < 2; ++re) {
                         const float mn = fmaxf(m[nt][re], mx[re]);
