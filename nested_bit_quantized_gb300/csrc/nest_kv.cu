@@ -20,8 +20,8 @@ namespace {
 constexpr int kD = 128;
 
 // One warp per (token, head): lane l owns dims 4l .. 4l+3.  Decisions in fp32 with
-// each operation rounded on its own (no contraction), so that they match the
-// reference bit for bit:  s = fp16(max|x| / 7);  q4 = clip(rint(x / s), -8, 7);
+// each operation rounded on its own (no contraction), so that the codes are those of
+// the definition, bit for bit:  s = fp16(max|x| / 7);  q4 = clip(rint(x / s), -8, 7);
 // q_r = clip(rint((x - q4 s) / (s / 16)), -8, 7).
 template <bool BF16>
 __global__ void k_kv_write(const void* __restrict__ x, int T, int H, int pos0, int Lmax,

@@ -27,7 +27,7 @@ time, with no blocking or fusion beyond what the definitions themselves say:
   same but without y_r").  The split between GPU and CPU in that step is
   prior art; the oracle computes the plain sum.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 * nearest-level ties: |u| exactly at the midpoint of the inner and outer
   level goes to the inner level; u == 0 takes the positive inner level.
 * zero groups: scale 0 gives code 2 (+inner level) and a zero base; a zero
