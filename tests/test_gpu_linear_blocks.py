@@ -1,14 +1,15 @@
-"""Whole linears across the shapes of the output rotation's blocks.
+"""Whole linears across the shapes of the rotations' blocks.
 
-nest_linear and nest_linear_group rotate the GEMM's accumulator back with
-y = S_o H_o z (feedman.me/posts/wZBTJ, POC recipe step 4), H_o block-diagonal
-with blocks of b_out = the largest power of two dividing M, at most 4096.
-These cases cover b_out from 1 to 4096 (ragged last tiles, a block spanning
-32 row tiles), both GEMM kernels and every epilogue split, scratch that starts
-as garbage, the same scratch used again by calls of other T, outputs that
-start as NaN (every element written), and grouped calls of many row tiles
-with one 128-column group each.  Each output is checked against the oracle
-with the workload's parity gate.
+nest_linear and nest_linear_group compute y = S_o H_o (Q (H_i S_i x))
+(feedman.me/posts/wZBTJ, POC recipe steps 1 and 4), H_i and H_o block-diagonal
+with blocks of b = the largest power of two dividing K (or M), at most 4096.
+These cases cover b_in from 128 to 4096 and b_out from 1 to 4096 (ragged last
+tiles, a block spanning 32 row tiles), fp32 and bf16 inputs, a bf16 input off
+a 16-byte boundary, both GEMM kernels and every epilogue split, scratch that
+starts as garbage and is reused by calls of other T, outputs that start as NaN
+(every element written), and grouped calls of many row tiles with one
+128-column group each.  Each output is checked against the oracle with the
+workload's parity gate.
 """
 import numpy as np
 import pytest
@@ -50,28 +51,50 @@ def _random_codes(M, K, bits, seed):
             "resid_scales": rs.view(np.float16)}
 
 
-# (M, K): b_out = 4096 (one segment of 32 row tiles), 1024, 512, 128, 8 with a ragged
-# last tile, 32 inside one partial tile, and M = 1 (b_out = 1)
-SHAPES = [(4096, 256), (1024, 384), (1536, 256), (640, 256), (200, 128), (96, 256), (1, 128)]
+# (M, K): b_out / b_in = 4096 / 256 (a block of 32 row tiles), 1024 / 128, 512 / 256,
+# 128 / 512, 8 / 128 with a ragged last tile, 32 / 256 inside one partial tile, 1 / 128
+# (M = 1), 128 / 1024 and 256 / 4096
+SHAPES = [(4096, 256), (1024, 384), (1536, 256), (640, 512), (200, 128), (96, 256), (1, 128), (384, 1024),
+          (256, 4096)]
 
 
 @pytest.mark.parametrize("M,K", SHAPES)
-def test_linear_rotates_every_segment(dev, M, K):
+def test_linear_rotates_every_block(dev, M, K):
     bits = 7
     W = synth.weights(M, K, 5 + M, "entries")
     s_o, s_i = synth.sign_pair(M, K, 6 + M)
     q = O.quantize_layer(W, s_o, s_i, bits)
     layer = _layer(q, bits, s_o, s_i, dev)
-    for T in (1, 3, 16, 17, 64, 130):
+    # one scratch of garbage bytes for every T (each call clears what it needs)
+    scratch = torch.full((nest.linear_scratch_bytes(M, K, 130),), 0xFF, dtype=torch.uint8, device=dev)
+    for T in (1, 3, 16, 17, 32, 33, 64, 130, 2):
         x, xv = _bf16_x(T, K, 40 + T, dev)
-        # scratch of garbage bytes (the call clears what it needs), y of NaNs (every element written)
-        scratch = torch.full((nest.linear_scratch_bytes(M, K, T),), 0xFF, dtype=torch.uint8, device=dev)
         for verify in (False, True):
             ref = O.forward(q, s_o, s_i, xv, verify)["y"]
-            for _ in range(2):                       # the second call finds the scratch as the first left it
-                y = torch.full((T, M), float("nan"), dtype=torch.float32, device=dev)
-                nest.linear(layer, x, verify, y=y, scratch=scratch)
-                parity(y.cpu().numpy(), ref)
+            y = torch.full((T, M), float("nan"), dtype=torch.float32, device=dev)
+            nest.linear(layer, x, verify, y=y, scratch=scratch)
+            parity(y.cpu().numpy(), ref)
+    nest.error_check()
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_linear_fp32_and_misaligned_inputs(dev, T):
+    """fp32 activations, and a bf16 input 2 bytes off a 16-byte boundary."""
+    M, K, bits = 640, 1536, 8
+    W = synth.weights(M, K, 31, "entries")
+    s_o, s_i = synth.sign_pair(M, K, 32)
+    q = O.quantize_layer(W, s_o, s_i, bits)
+    layer = _layer(q, bits, s_o, s_i, dev)
+    xb, xv = synth.activations(T, K, 33)
+    x32 = torch.from_numpy(xv.astype(np.float32)).to(dev)
+    raw = torch.zeros(T * K + 1, dtype=torch.int16, device=dev)
+    raw[1:] = torch.from_numpy(xb.view(np.int16).ravel()).to(dev)
+    x_off = raw[1:].view(T, K).view(torch.bfloat16)
+    assert x_off.data_ptr() % 16 == 2
+    for verify in (False, True):
+        ref = O.forward(q, s_o, s_i, xv, verify)["y"]
+        parity(nest.linear(layer, x32, verify).cpu().numpy(), ref)
+        parity(nest.linear(layer, x_off, verify).cpu().numpy(), ref)
     nest.error_check()
 
 
