@@ -38,6 +38,7 @@ struct RotTask {
     unsigned n, total;        // vector length, T * n
     int L, NB, cta_begin;     // log2 block size, operand token blocks, first CTA of the task
     float scale;
+    int reg;                  // 1: the register path (b <= 512, see nest_rotate.cu)
 };
 
 struct RotArgs {

@@ -5,11 +5,14 @@
 // with blocks of size b = largest power of two dividing n (at most 4096), each
 // scaled by 1/sqrt(b).
 //
-// A CTA takes 4096 consecutive elements of the token-major [T][n] array (a
-// whole number of blocks, since b divides both n and 4096), views them as a
-// 64 x 64 tile in shared memory, and runs the butterflies in two phases with
-// warp shuffles: phase 1 along rows (index bits 0..5), phase 2 along columns
-// (index bits 6..11).  Each warp holds 64 elements, two per lane.
+// Two ways, chosen per vector set of a launch:
+// - blocks of at most 512 (and n % 8 == 0, 16-byte aligned vectors, 8-byte aligned
+//   signs): each warp takes one (token, chunk of max(b, 256) elements) and runs the
+//   butterflies in registers and warp shuffles, with no shared memory and no barrier;
+// - otherwise a CTA takes 4096 consecutive elements of the token-major [T][n] array (a
+//   whole number of blocks, since b divides both n and 4096), views them as a 64 x 64
+//   tile in shared memory, and runs the butterflies in two phases with warp shuffles:
+//   phase 1 along rows (index bits 0..5), phase 2 along columns (index bits 6..11).
 #include "nest_device.cuh"
 #include "nest_internal.h"
 
@@ -18,6 +21,123 @@ namespace {
 
 constexpr int kSeg = 4096;
 constexpr int kThreads = 512;
+constexpr int kRegWarps = kThreads / 32;
+
+__host__ __device__ constexpr int reg_chunk(int L) { return L <= 8 ? 256 : 512; }
+
+// Register path: one warp per (token, chunk of W = max(b, 256) consecutive elements).
+// Lane l holds elements 256 h + 8 l + i of the chunk (i < 8, h < W / 256): index bits 0-2
+// in registers, bits 3-7 across lanes, bit 8 in registers again, so each lane's loads and
+// stores are 16- or 32-byte pieces.  The signs are constants of the layer, not outputs of
+// the previous kernel, so they are loaded before waiting for it; the clearing stores are
+// issued after the loads.
+template <int MODE, bool BF16>
+__device__ __forceinline__ void rotate_reg(const RotTask& tk, unsigned cta) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned n = tk.n, T = tk.total / tk.n;
+    const int L = tk.L, W = reg_chunk(L);
+    const unsigned nchunk = (n + W - 1) / W;
+    const unsigned nctas = (T * nchunk + kRegWarps - 1) / kRegWarps;
+    const unsigned item = cta * kRegWarps + warp;
+    const bool active = item < T * nchunk;             // the same for the whole warp
+    const unsigned tok = active ? item / nchunk : 0, c0 = active ? (item - tok * nchunk) * W : 0;
+    bool have[2];
+    uint2 sg[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const unsigned col = c0 + 256 * h + 8 * lane;
+        have[h] = active && 256 * h < W && col < n;
+        sg[h] = have[h] ? *reinterpret_cast<const uint2*>(tk.signs + col) : make_uint2(0u, 0u);
+    }
+    grid_dep_wait();                      // x may be the previous kernel's output; y may be its input
+    float v[16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const size_t idx = (size_t)tok * n + c0 + 256 * h + 8 * lane;
+        if (have[h]) {
+            if constexpr (BF16) {
+                const uint4 u = __ldcg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(tk.x) + idx));
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[8 * h + 2 * e] = __uint_as_float(w[e] << 16);
+                    v[8 * h + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+                }
+            } else {
+                const float4* xp = reinterpret_cast<const float4*>(static_cast<const float*>(tk.x) + idx);
+                const float4 a = __ldcg(xp), b = __ldcg(xp + 1);
+                v[8 * h + 0] = a.x; v[8 * h + 1] = a.y; v[8 * h + 2] = a.z; v[8 * h + 3] = a.w;
+                v[8 * h + 4] = b.x; v[8 * h + 5] = b.y; v[8 * h + 6] = b.z; v[8 * h + 7] = b.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[8 * h + i] = 0.0f;
+        }
+    }
+    if (tk.zero_out != nullptr) {         // clear the accumulator of the GEMM that follows
+        const long long per = (tk.zero_count + nctas - 1) / nctas;
+        const long long lo = per * cta, hi = lo + per < tk.zero_count ? lo + per : tk.zero_count;
+        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) tk.zero_out[i] = 0.0f;
+    }
+    if (!active) return;
+    auto sign = [&](int j) { return (float)(int8_t)((((j & 7) < 4 ? sg[j >> 3].x : sg[j >> 3].y) >> (8 * (j & 3))) & 0xFFu); };
+    if constexpr (MODE == 0) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] *= sign(j);
+    }
+    // butterflies over index bits 0 .. L-1 (unnormalised Sylvester order)
+#pragma unroll
+    for (int b = 0; b < 3; ++b) {
+        if (b < L) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (j & (1 << b)) continue;
+                const float a = v[j], d = v[j + (1 << b)];
+                v[j] = a + d;
+                v[j + (1 << b)] = a - d;
+            }
+        }
+    }
+    const bool two = L > 8;                 // 512-element chunks: registers 8..15 hold h = 1
+    for (int b = 3; b < 8 && b < L; ++b) {
+        const int m = 1 << (b - 3);
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j >= 8 && !two) break;
+            const float o = __shfl_xor_sync(0xffffffffu, v[j], m);
+            v[j] = upper ? o - v[j] : v[j] + o;
+        }
+    }
+    if (two) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float a = v[j], d = v[j + 8];
+            v[j] = a + d;
+            v[j + 8] = a - d;
+        }
+    }
+    const float scale = tk.scale;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] *= MODE == 1 ? scale * sign(j) : scale;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (!have[h]) continue;
+        const unsigned col = c0 + 256 * h + 8 * lane;
+        if (tk.y != nullptr) {
+            float4* yp = reinterpret_cast<float4*>(tk.y + (size_t)tok * n + col);
+            yp[0] = make_float4(v[8 * h + 0], v[8 * h + 1], v[8 * h + 2], v[8 * h + 3]);
+            yp[1] = make_float4(v[8 * h + 4], v[8 * h + 5], v[8 * h + 6], v[8 * h + 7]);
+        }
+        if (MODE == 0 && tk.xop != nullptr) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = h2_as_u32(__floats2half2_rn(v[8 * h + 2 * e], v[8 * h + 2 * e + 1]));
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(tk.xop) + xop_offset((int)col, (int)tok, tk.NB)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
 
 template <int MODE, bool BF16>
 __global__ void __launch_bounds__(kThreads)
@@ -27,6 +147,10 @@ k_rotate(const __grid_constant__ RotArgs args) {
     int k = 0;                            // the vector set this CTA works on
     while (k + 1 < args.ntasks && args.task[k + 1].cta_begin <= (int)blockIdx.x) ++k;
     const RotTask& tk = args.task[k];
+    if (tk.reg) {                         // the same for every thread of the CTA
+        rotate_reg<MODE, BF16>(tk, blockIdx.x - tk.cta_begin);
+        return;
+    }
     const void* __restrict__ x = tk.x;
     const int8_t* __restrict__ signs = tk.signs;
     const unsigned n = tk.n, total = tk.total;
@@ -37,11 +161,6 @@ k_rotate(const __grid_constant__ RotArgs args) {
     const unsigned cta = blockIdx.x - tk.cta_begin;
     const unsigned nctas = (total + kSeg - 1) / kSeg;
     grid_dep_wait();                      // x may be the previous kernel's output; y may be its input
-    if (tk.zero_out != nullptr) {         // clear the accumulator of the GEMM that follows
-        const long long per = (tk.zero_count + nctas - 1) / nctas;
-        const long long lo = per * cta, hi = lo + per < tk.zero_count ? lo + per : tk.zero_count;
-        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) tk.zero_out[i] = 0.0f;
-    }
     const unsigned seg0 = cta * (unsigned)kSeg;
     const unsigned rem = total - seg0;
     const int count = rem < (unsigned)kSeg ? (int)rem : kSeg;
@@ -59,6 +178,11 @@ k_rotate(const __grid_constant__ RotArgs args) {
             else v[j] = reinterpret_cast<const float*>(x)[idx];
             if constexpr (MODE == 0) v[j] *= (float)signs[idx % n];
         }
+    }
+    if (tk.zero_out != nullptr) {         // clear the accumulator of the GEMM that follows (after the loads)
+        const long long per = (tk.zero_count + nctas - 1) / nctas;
+        const long long lo = per * cta, hi = lo + per < tk.zero_count ? lo + per : tk.zero_count;
+        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) tk.zero_out[i] = 0.0f;
     }
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -110,6 +234,8 @@ int hadamard_block(int n) {
     return b;
 }
 
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
 cudaError_t launch_rotate_group(RotArgs& a, int x_dtype, int mode, int T, cudaStream_t stream) {
     int ctas = 0;
     for (int k = 0; k < a.ntasks; ++k) {
@@ -121,8 +247,14 @@ cudaError_t launch_rotate_group(RotArgs& a, int x_dtype, int mode, int T, cudaSt
         t.scale = (float)(1.0 / sqrt((double)b));
         t.total = (unsigned)T * t.n;                     // the entry points keep T * n < 2^31
         t.NB = n_pad(T) / 8;
+        t.reg = b <= 512 && t.n % 8 == 0 && aligned(t.x, 16) && aligned(t.y, 16) && aligned(t.signs, 8);
         t.cta_begin = ctas;
-        ctas += (int)((t.total + kSeg - 1) / kSeg);
+        if (t.reg) {
+            const long long items = (long long)T * ((t.n + reg_chunk(L) - 1) / reg_chunk(L));
+            ctas += (int)((items + kRegWarps - 1) / kRegWarps);
+        } else {
+            ctas += (int)((t.total + kSeg - 1) / kSeg);
+        }
     }
     const dim3 g(ctas), blk(kThreads);
     if (mode == 0)

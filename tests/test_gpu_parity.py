@@ -111,7 +111,7 @@ def test_quantize_matches_oracle(dev, M, K, bits, outl):
 # ----------------------------------------------------------------------------
 
 @pytest.mark.parametrize("n,T", [(128, 1), (384, 3), (2560, 16), (4096, 17), (5376, 5), (8192, 2), (96, 4),
-                                 (200, 3), (7, 2), (15360, 1), (1024, 64)])
+                                 (200, 3), (7, 2), (15360, 1), (1024, 64), (1000, 3), (12, 5), (9728, 16)])
 def test_rotate_matches_oracle(dev, n, T):
     s = synth.signs(n, 31)
     xb, xv = synth.activations(T, n, 32)
@@ -131,6 +131,11 @@ def test_rotate_matches_oracle(dev, n, T):
     nest.rotate(torch.from_numpy(z).to(dev), to_dev(s, torch, dev), 1, y=yo)
     refo = O.unrotate_outputs(z, s)
     assert np.max(np.abs(yo.cpu().numpy() - refo)) <= 1e-5 * max(1.0, np.max(np.abs(refo)))
+    # input side from fp32 input
+    yi = torch.empty((T, n), dtype=torch.float32, device=dev)
+    nest.rotate(torch.from_numpy(z).to(dev), to_dev(s, torch, dev), 0, y=yi)
+    refi = O.rotate_activations(z, s)
+    assert np.max(np.abs(yi.cpu().numpy() - refi)) <= 1e-5 * max(1.0, np.max(np.abs(refi)))
 
 
 # ----------------------------------------------------------------------------
