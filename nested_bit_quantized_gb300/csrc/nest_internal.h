@@ -39,6 +39,7 @@ struct RotTask {
     int L, NB, cta_begin;     // log2 block size, operand token blocks, first CTA of the task
     float scale;
     int reg;                  // 1: the register path (b <= 512, see nest_rotate.cu)
+    unsigned nctas;           // CTAs of the task
 };
 
 struct RotArgs {

@@ -24,6 +24,22 @@ constexpr int kThreads = 512;
 constexpr int kRegWarps = kThreads / 32;
 
 __host__ __device__ constexpr int reg_chunk(int L) { return L <= 8 ? 256 : 512; }
+constexpr long long kClearPerCta = 8192;     // floats a register-path CTA clears at most
+
+// This CTA's share (of nctas) of clearing `count` floats at p: 16-byte stores when p and
+// count allow them.
+__device__ __forceinline__ void clear_share(float* p, long long count, unsigned cta, unsigned nctas) {
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0 && (count & 3) == 0) {
+        float4* q = reinterpret_cast<float4*>(p);
+        const long long c4 = count >> 2, per = (c4 + nctas - 1) / nctas;
+        const long long lo = per * cta, hi = lo + per < c4 ? lo + per : c4;
+        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) q[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    } else {
+        const long long per = (count + nctas - 1) / nctas;
+        const long long lo = per * cta, hi = lo + per < count ? lo + per : count;
+        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) p[i] = 0.0f;
+    }
+}
 
 // Register path: one warp per (token, chunk of W = max(b, 256) consecutive elements).
 // Lane l holds elements 256 h + 8 l + i of the chunk (i < 8, h < W / 256): index bits 0-2
@@ -37,7 +53,6 @@ __device__ __forceinline__ void rotate_reg(const RotTask& tk, unsigned cta) {
     const unsigned n = tk.n, T = tk.total / tk.n;
     const int L = tk.L, W = reg_chunk(L);
     const unsigned nchunk = (n + W - 1) / W;
-    const unsigned nctas = (T * nchunk + kRegWarps - 1) / kRegWarps;
     const unsigned item = cta * kRegWarps + warp;
     const bool active = item < T * nchunk;             // the same for the whole warp
     const unsigned tok = active ? item / nchunk : 0, c0 = active ? (item - tok * nchunk) * W : 0;
@@ -74,11 +89,8 @@ __device__ __forceinline__ void rotate_reg(const RotTask& tk, unsigned cta) {
             for (int i = 0; i < 8; ++i) v[8 * h + i] = 0.0f;
         }
     }
-    if (tk.zero_out != nullptr) {         // clear the accumulator of the GEMM that follows
-        const long long per = (tk.zero_count + nctas - 1) / nctas;
-        const long long lo = per * cta, hi = lo + per < tk.zero_count ? lo + per : tk.zero_count;
-        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) tk.zero_out[i] = 0.0f;
-    }
+    // clear the accumulator of the GEMM that follows (the task may have CTAs for this alone)
+    if (tk.zero_out != nullptr) clear_share(tk.zero_out, tk.zero_count, cta, tk.nctas);
     if (!active) return;
     auto sign = [&](int j) { return (float)(int8_t)((((j & 7) < 4 ? sg[j >> 3].x : sg[j >> 3].y) >> (8 * (j & 3))) & 0xFFu); };
     if constexpr (MODE == 0) {
@@ -179,11 +191,8 @@ k_rotate(const __grid_constant__ RotArgs args) {
             if constexpr (MODE == 0) v[j] *= (float)signs[idx % n];
         }
     }
-    if (tk.zero_out != nullptr) {         // clear the accumulator of the GEMM that follows (after the loads)
-        const long long per = (tk.zero_count + nctas - 1) / nctas;
-        const long long lo = per * cta, hi = lo + per < tk.zero_count ? lo + per : tk.zero_count;
-        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) tk.zero_out[i] = 0.0f;
-    }
+    // clear the accumulator of the GEMM that follows (after the loads)
+    if (tk.zero_out != nullptr) clear_share(tk.zero_out, tk.zero_count, cta, nctas);
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int f = threadIdx.x + j * kThreads;
@@ -249,12 +258,17 @@ cudaError_t launch_rotate_group(RotArgs& a, int x_dtype, int mode, int T, cudaSt
         t.NB = n_pad(T) / 8;
         t.reg = b <= 512 && t.n % 8 == 0 && aligned(t.x, 16) && aligned(t.y, 16) && aligned(t.signs, 8);
         t.cta_begin = ctas;
+        long long c;
         if (t.reg) {
             const long long items = (long long)T * ((t.n + reg_chunk(L) - 1) / reg_chunk(L));
-            ctas += (int)((items + kRegWarps - 1) / kRegWarps);
+            c = (items + kRegWarps - 1) / kRegWarps;
+            const long long cz = t.zero_out != nullptr ? (t.zero_count + kClearPerCta - 1) / kClearPerCta : 0;
+            if (cz > c) c = cz;
         } else {
-            ctas += (int)((t.total + kSeg - 1) / kSeg);
+            c = (t.total + kSeg - 1) / kSeg;
         }
+        t.nctas = (unsigned)c;
+        ctas += (int)c;
     }
     const dim3 g(ctas), blk(kThreads);
     if (mode == 0)
