@@ -11,7 +11,9 @@
 // reading used by the chained-layer workload.
 //
 // Two launches, both spread over every (token, 4096-element segment) pair so that
-// a single token still occupies many SMs:
+// a single token still occupies many SMs.  For blocks of up to 1024 elements the
+// butterflies of a segment run in registers, one warp per chunk of max(b, 256)
+// elements (the register path below); otherwise:
 //   k_glue_out: one CTA per (t, segment) rotates its segment of z_a (and z_b) in a
 //               64 x 64 shared-memory tile, writes h and the segment's sum of
 //               squares.  A segment is a whole number of Hadamard blocks (the block
@@ -30,6 +32,125 @@ namespace {
 constexpr int kSeg = 4096;
 constexpr int kThreads = 512;
 constexpr int kPer = kSeg / kThreads;
+constexpr int kWarps = kThreads / 32;
+
+// Register path (GlueArgs::reg: b <= 1024, M % 8 == 0, 16-byte aligned vectors, 8-byte
+// aligned signs).  The CTA's 4096-element segment is cut into chunks of W = max(b, 256)
+// elements, one per warp; a warp keeps its chunk in registers (chunk_fwht: lane l holds
+// elements 256 h + 8 l + i) and needs no shared memory or barrier for the butterflies.
+// The signs are layer constants and are loaded before waiting for the previous kernel.
+
+// Load the 8 H fp32 values of a warp's chunk that starts at element c0 of row `row`.
+template <int H>
+__device__ __forceinline__ void load_chunk(const float* base, const bool (&have)[H], int lane, float (&v)[8 * H]) {
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        if (have[h]) {
+            const float4* p = reinterpret_cast<const float4*>(base + 256 * h + 8 * lane);
+            const float4 x = __ldcg(p), y = __ldcg(p + 1);
+            v[8 * h + 0] = x.x; v[8 * h + 1] = x.y; v[8 * h + 2] = x.z; v[8 * h + 3] = x.w;
+            v[8 * h + 4] = y.x; v[8 * h + 5] = y.y; v[8 * h + 6] = y.z; v[8 * h + 7] = y.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[8 * h + i] = 0.0f;
+        }
+    }
+}
+
+template <bool PROD, int H>
+__device__ __forceinline__ void glue_out_reg(const GlueArgs& a, int t, int seg0, float* red) {
+    constexpr int W = 256 * H, NR = 8 * H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c0 = seg0 + warp * W;                    // this warp's chunk
+    const bool active = warp * W < kSeg && c0 < a.M;
+    bool have[H];
+    uint2 sa[H], sb[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const int col = c0 + 256 * h + 8 * lane;
+        have[h] = active && col < a.M;
+        sa[h] = have[h] ? *reinterpret_cast<const uint2*>(a.sa + col) : make_uint2(0u, 0u);
+        sb[h] = (PROD && have[h]) ? *reinterpret_cast<const uint2*>(a.sb + col) : make_uint2(0u, 0u);
+    }
+    grid_dep_wait();                 // z_a, z_b come from the GEMM before this launch
+    const size_t row = (size_t)t * a.M + c0;
+    float ss = 0.0f;
+    if (active) {
+        float v[NR], w[NR];
+        load_chunk<H>(a.za + row, have, lane, v);
+        if constexpr (PROD) load_chunk<H>(a.zb + row, have, lane, w);
+        chunk_fwht<H>(v, a.L, lane);
+        if constexpr (PROD) chunk_fwht<H>(w, a.L, lane);
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+            v[j] *= a.scale * chunk_sign<H>(sa, j);
+            if constexpr (PROD) v[j] *= w[j] * a.scale * chunk_sign<H>(sb, j);
+            ss += v[j] * v[j];
+        }
+        // h may overwrite z_a: this warp read its whole chunk above
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            if (!have[h]) continue;
+            float4* hp = reinterpret_cast<float4*>(a.h + row + 256 * h + 8 * lane);
+            hp[0] = make_float4(v[8 * h + 0], v[8 * h + 1], v[8 * h + 2], v[8 * h + 3]);
+            hp[1] = make_float4(v[8 * h + 4], v[8 * h + 5], v[8 * h + 6], v[8 * h + 7]);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {                            // the warps' sums in a fixed order
+        float tot = 0.0f;
+        for (int i = 0; i < kWarps; ++i) tot += red[i];
+        a.work[blockIdx.x] = tot;
+    }
+}
+
+template <int H>
+__device__ __forceinline__ void glue_in_reg(const GlueArgs& a, const GlueNext& nx, int t, int seg0, int rem,
+                                            int per_next) {
+    constexpr int W = 256 * H, NR = 8 * H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c0 = seg0 + warp * W;
+    const bool active = warp * W < kSeg && c0 < a.M;
+    bool have[H];
+    uint2 sg[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const int col = c0 + 256 * h + 8 * lane;
+        have[h] = active && col < a.M;
+        sg[h] = have[h] ? *reinterpret_cast<const uint2*>(nx.sign_in + col) : make_uint2(0u, 0u);
+    }
+    grid_dep_wait();                 // h and the segment sums come from k_glue_out
+    float v[NR];
+    if (active) load_chunk<H>(a.h + (size_t)t * a.M + c0, have, lane, v);
+    // this CTA's share of the next GEMM's accumulator, after the loads
+    if (nx.zero_out != nullptr) clear_share<kThreads>(nx.zero_out, nx.zero_count, rem, per_next);
+    if (!active) return;
+    // the token's sum of squares: every warp adds the segment sums in the same tree order
+    float ss = 0.0f;
+    for (int i = lane; i < a.nseg; i += 32) ss += __ldcg(a.work + t * a.nseg + i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rms = sqrtf(ss / (float)a.M);
+    const float inv = rms > 0.0f ? 1.0f / rms : 0.0f;
+#pragma unroll
+    for (int j = 0; j < NR; ++j)
+        v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * inv)) * chunk_sign<H>(sg, j);
+    chunk_fwht<H>(v, a.L, lane);
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        if (!have[h]) continue;
+        const int col = c0 + 256 * h + 8 * lane;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            w[e] = h2_as_u32(__floats2half2_rn(v[8 * h + 2 * e] * a.scale, v[8 * h + 2 * e + 1] * a.scale));
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(nx.xop) + xop_offset(col, t, a.NB)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
 
 template <bool PROD>
 __global__ void __launch_bounds__(kThreads) k_glue_out(const __grid_constant__ GlueArgs a) {
@@ -39,6 +160,12 @@ __global__ void __launch_bounds__(kThreads) k_glue_out(const __grid_constant__ G
     grid_dep_launch_dependents();
     const int t = blockIdx.x / a.nseg, s = blockIdx.x - t * a.nseg;
     const int seg0 = s * kSeg;
+    if (a.reg) {
+        if (a.L <= 8) glue_out_reg<PROD, 1>(a, t, seg0, red);
+        else if (a.L == 9) glue_out_reg<PROD, 2>(a, t, seg0, red);
+        else glue_out_reg<PROD, 4>(a, t, seg0, red);
+        return;
+    }
     const int count = a.M - seg0 < kSeg ? a.M - seg0 : kSeg;
     const size_t row = (size_t)t * a.M + seg0;
     grid_dep_wait();                 // z_a, z_b come from the GEMM before this launch
@@ -85,9 +212,15 @@ __global__ void __launch_bounds__(kThreads) k_glue_in(const __grid_constant__ Gl
     const int rem = blockIdx.x - jn * per_next;
     const int t = rem / a.nseg, s = rem - t * a.nseg;
     const int seg0 = s * kSeg;
+    const GlueNext& nx = a.next[jn];
+    if (a.reg) {
+        if (a.L <= 8) glue_in_reg<1>(a, nx, t, seg0, rem, per_next);
+        else if (a.L == 9) glue_in_reg<2>(a, nx, t, seg0, rem, per_next);
+        else glue_in_reg<4>(a, nx, t, seg0, rem, per_next);
+        return;
+    }
     const int count = a.M - seg0 < kSeg ? a.M - seg0 : kSeg;
     const size_t row = (size_t)t * a.M + seg0;
-    const GlueNext& nx = a.next[jn];
     grid_dep_wait();                 // h and the segment sums come from k_glue_out
 
     if (nx.zero_out != nullptr) {    // this CTA's share of the next GEMM's accumulator
@@ -145,6 +278,10 @@ cudaError_t launch_glue(GlueArgs& a, cudaStream_t stream) {
     a.scale = (float)(1.0 / sqrt((double)b));
     a.NB = n_pad(a.T) / 8;
     a.nseg = glue_segments(a.M);
+    auto al = [](const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; };
+    bool reg = b <= 1024 && a.M % 8 == 0 && al(a.za, 16) && al(a.zb, 16) && al(a.h, 16) && al(a.sa, 8) && al(a.sb, 8);
+    for (int j = 0; j < a.nnext; ++j) reg = reg && al(a.next[j].sign_in, 8);
+    a.reg = reg ? 1 : 0;
     const dim3 blk(kThreads);
     cudaError_t e = a.zb != nullptr ? launch_pdl(k_glue_out<true>, dim3(a.T * a.nseg), blk, 0, stream, a)
                                     : launch_pdl(k_glue_out<false>, dim3(a.T * a.nseg), blk, 0, stream, a);

@@ -190,6 +190,73 @@ __device__ __forceinline__ void warp_fwht(float& v0, float& v1, int nbits, int l
     }
 }
 
+// This CTA's share (of nctas CTAs of THREADS threads) of clearing `count` floats at p:
+// 16-byte stores when p and count allow them.
+template <int THREADS>
+__device__ __forceinline__ void clear_share(float* p, long long count, unsigned cta, unsigned nctas) {
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0 && (count & 3) == 0) {
+        float4* q = reinterpret_cast<float4*>(p);
+        const long long c4 = count >> 2, per = (c4 + nctas - 1) / nctas;
+        const long long lo = per * cta, hi = lo + per < c4 ? lo + per : c4;
+        for (long long i = lo + threadIdx.x; i < hi; i += THREADS) q[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    } else {
+        const long long per = (count + nctas - 1) / nctas;
+        const long long lo = per * cta, hi = lo + per < count ? lo + per : count;
+        for (long long i = lo + threadIdx.x; i < hi; i += THREADS) p[i] = 0.0f;
+    }
+}
+
+// Sign j (0 <= j < 8 H) of a register chunk whose lane holds 8 signs per h in sg[h].
+template <int H>
+__device__ __forceinline__ float chunk_sign(const uint2 (&sg)[H], int j) {
+    return (float)(int8_t)((((j & 7) < 4 ? sg[j >> 3].x : sg[j >> 3].y) >> (8 * (j & 3))) & 0xFFu);
+}
+
+// Block-diagonal FWHT (unnormalised Sylvester order, blocks of 2^L <= 256 H elements) of
+// one warp's chunk of 256 H consecutive elements held in registers: element 256 h + 8 l + i
+// of the chunk in v[8 h + i] of lane l (i < 8, h < H).  Index bits 0-2 and 8-9 are
+// butterflies inside the lane, bits 3-7 warp shuffles.  All 32 lanes call it.
+template <int H>
+__device__ __forceinline__ void chunk_fwht(float (&v)[8 * H], int L, int lane) {
+    constexpr int NR = 8 * H;
+#pragma unroll
+    for (int b = 0; b < 3; ++b) {
+        if (b < L) {
+#pragma unroll
+            for (int j = 0; j < NR; ++j) {
+                if (j & (1 << b)) continue;
+                const float a = v[j], d = v[j + (1 << b)];
+                v[j] = a + d;
+                v[j + (1 << b)] = a - d;
+            }
+        }
+    }
+    for (int b = 3; b < 8 && b < L; ++b) {
+        const int m = 1 << (b - 3);
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[j], m);
+            v[j] = upper ? o - v[j] : v[j] + o;
+        }
+    }
+#pragma unroll
+    for (int q = 0; (8 << q) < NR; ++q) {
+        if (8 + q < L) {
+#pragma unroll
+            for (int j = 0; j < NR; ++j) {
+                if (j & (8 << q)) continue;
+                const float a = v[j], d = v[j + (8 << q)];
+                v[j] = a + d;
+                v[j + (8 << q)] = a - d;
+            }
+        }
+    }
+}
+
+// Chunk of the register-path FWHT for blocks of 2^L (L <= 10): 256, 512 or 1024 elements.
+__host__ __device__ constexpr int reg_chunk(int L) { return L <= 8 ? 256 : (L == 9 ? 512 : 1024); }
+
 // Block-diagonal FWHT (unnormalised, blocks of 2^L, 0 <= L <= 12) of the 4096 values
 // of a 64 x 64 shared-memory tile, value f at tile[f / 64][f % 64]: butterflies over
 // index bits 0..5 along rows, then bits 6..11 along columns (the padding column keeps

@@ -6,7 +6,7 @@
 // scaled by 1/sqrt(b).
 //
 // Two ways, chosen per vector set of a launch:
-// - blocks of at most 512 (and n % 8 == 0, 16-byte aligned vectors, 8-byte aligned
+// - blocks of at most 1024 (and n % 8 == 0, 16-byte aligned vectors, 8-byte aligned
 //   signs): each warp takes one (token, chunk of max(b, 256) elements) and runs the
 //   butterflies in registers and warp shuffles, with no shared memory and no barrier;
 // - otherwise a CTA takes 4096 consecutive elements of the token-major [T][n] array (a
@@ -23,51 +23,34 @@ constexpr int kSeg = 4096;
 constexpr int kThreads = 512;
 constexpr int kRegWarps = kThreads / 32;
 
-__host__ __device__ constexpr int reg_chunk(int L) { return L <= 8 ? 256 : 512; }
 constexpr long long kClearPerCta = 8192;     // floats a register-path CTA clears at most
 
-// This CTA's share (of nctas) of clearing `count` floats at p: 16-byte stores when p and
-// count allow them.
-__device__ __forceinline__ void clear_share(float* p, long long count, unsigned cta, unsigned nctas) {
-    if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0 && (count & 3) == 0) {
-        float4* q = reinterpret_cast<float4*>(p);
-        const long long c4 = count >> 2, per = (c4 + nctas - 1) / nctas;
-        const long long lo = per * cta, hi = lo + per < c4 ? lo + per : c4;
-        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) q[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    } else {
-        const long long per = (count + nctas - 1) / nctas;
-        const long long lo = per * cta, hi = lo + per < count ? lo + per : count;
-        for (long long i = lo + threadIdx.x; i < hi; i += kThreads) p[i] = 0.0f;
-    }
-}
-
-// Register path: one warp per (token, chunk of W = max(b, 256) consecutive elements).
-// Lane l holds elements 256 h + 8 l + i of the chunk (i < 8, h < W / 256): index bits 0-2
-// in registers, bits 3-7 across lanes, bit 8 in registers again, so each lane's loads and
-// stores are 16- or 32-byte pieces.  The signs are constants of the layer, not outputs of
-// the previous kernel, so they are loaded before waiting for it; the clearing stores are
-// issued after the loads.
-template <int MODE, bool BF16>
+// Register path: one warp per (token, chunk of W = max(b, 256) consecutive elements, b <=
+// 1024).  Lane l holds elements 256 h + 8 l + i of the chunk (i < 8, h < W / 256), so each
+// lane's loads and stores are 16- or 32-byte pieces (chunk_fwht).  The signs are constants
+// of the layer, not outputs of the previous kernel, so they are loaded before waiting for
+// it; the clearing stores are issued after the loads.
+template <int MODE, bool BF16, int H>
 __device__ __forceinline__ void rotate_reg(const RotTask& tk, unsigned cta) {
+    constexpr int W = 256 * H, NR = 8 * H;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned n = tk.n, T = tk.total / tk.n;
-    const int L = tk.L, W = reg_chunk(L);
     const unsigned nchunk = (n + W - 1) / W;
     const unsigned item = cta * kRegWarps + warp;
     const bool active = item < T * nchunk;             // the same for the whole warp
     const unsigned tok = active ? item / nchunk : 0, c0 = active ? (item - tok * nchunk) * W : 0;
-    bool have[2];
-    uint2 sg[2];
+    bool have[H];
+    uint2 sg[H];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < H; ++h) {
         const unsigned col = c0 + 256 * h + 8 * lane;
-        have[h] = active && 256 * h < W && col < n;
+        have[h] = active && col < n;
         sg[h] = have[h] ? *reinterpret_cast<const uint2*>(tk.signs + col) : make_uint2(0u, 0u);
     }
     grid_dep_wait();                      // x may be the previous kernel's output; y may be its input
-    float v[16];
+    float v[NR];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < H; ++h) {
         const size_t idx = (size_t)tok * n + c0 + 256 * h + 8 * lane;
         if (have[h]) {
             if constexpr (BF16) {
@@ -90,50 +73,19 @@ __device__ __forceinline__ void rotate_reg(const RotTask& tk, unsigned cta) {
         }
     }
     // clear the accumulator of the GEMM that follows (the task may have CTAs for this alone)
-    if (tk.zero_out != nullptr) clear_share(tk.zero_out, tk.zero_count, cta, tk.nctas);
+    if (tk.zero_out != nullptr) clear_share<kThreads>(tk.zero_out, tk.zero_count, cta, tk.nctas);
     if (!active) return;
     auto sign = [&](int j) { return (float)(int8_t)((((j & 7) < 4 ? sg[j >> 3].x : sg[j >> 3].y) >> (8 * (j & 3))) & 0xFFu); };
     if constexpr (MODE == 0) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] *= sign(j);
+        for (int j = 0; j < NR; ++j) v[j] *= sign(j);
     }
-    // butterflies over index bits 0 .. L-1 (unnormalised Sylvester order)
-#pragma unroll
-    for (int b = 0; b < 3; ++b) {
-        if (b < L) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                if (j & (1 << b)) continue;
-                const float a = v[j], d = v[j + (1 << b)];
-                v[j] = a + d;
-                v[j + (1 << b)] = a - d;
-            }
-        }
-    }
-    const bool two = L > 8;                 // 512-element chunks: registers 8..15 hold h = 1
-    for (int b = 3; b < 8 && b < L; ++b) {
-        const int m = 1 << (b - 3);
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if (j >= 8 && !two) break;
-            const float o = __shfl_xor_sync(0xffffffffu, v[j], m);
-            v[j] = upper ? o - v[j] : v[j] + o;
-        }
-    }
-    if (two) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float a = v[j], d = v[j + 8];
-            v[j] = a + d;
-            v[j + 8] = a - d;
-        }
-    }
+    chunk_fwht<H>(v, tk.L, lane);
     const float scale = tk.scale;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] *= MODE == 1 ? scale * sign(j) : scale;
+    for (int j = 0; j < NR; ++j) v[j] *= MODE == 1 ? scale * sign(j) : scale;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < H; ++h) {
         if (!have[h]) continue;
         const unsigned col = c0 + 256 * h + 8 * lane;
         if (tk.y != nullptr) {
@@ -160,7 +112,10 @@ k_rotate(const __grid_constant__ RotArgs args) {
     while (k + 1 < args.ntasks && args.task[k + 1].cta_begin <= (int)blockIdx.x) ++k;
     const RotTask& tk = args.task[k];
     if (tk.reg) {                         // the same for every thread of the CTA
-        rotate_reg<MODE, BF16>(tk, blockIdx.x - tk.cta_begin);
+        const unsigned cta = blockIdx.x - tk.cta_begin;
+        if (tk.L <= 8) rotate_reg<MODE, BF16, 1>(tk, cta);
+        else if (tk.L == 9) rotate_reg<MODE, BF16, 2>(tk, cta);
+        else rotate_reg<MODE, BF16, 4>(tk, cta);
         return;
     }
     const void* __restrict__ x = tk.x;
@@ -192,7 +147,7 @@ k_rotate(const __grid_constant__ RotArgs args) {
         }
     }
     // clear the accumulator of the GEMM that follows (after the loads)
-    if (tk.zero_out != nullptr) clear_share(tk.zero_out, tk.zero_count, cta, nctas);
+    if (tk.zero_out != nullptr) clear_share<kThreads>(tk.zero_out, tk.zero_count, cta, nctas);
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int f = threadIdx.x + j * kThreads;
@@ -256,7 +211,7 @@ cudaError_t launch_rotate_group(RotArgs& a, int x_dtype, int mode, int T, cudaSt
         t.scale = (float)(1.0 / sqrt((double)b));
         t.total = (unsigned)T * t.n;                     // the entry points keep T * n < 2^31
         t.NB = n_pad(T) / 8;
-        t.reg = b <= 512 && t.n % 8 == 0 && aligned(t.x, 16) && aligned(t.y, 16) && aligned(t.signs, 8);
+        t.reg = b <= 1024 && t.n % 8 == 0 && aligned(t.x, 16) && aligned(t.y, 16) && aligned(t.signs, 8);
         t.cta_begin = ctas;
         long long c;
         if (t.reg) {
