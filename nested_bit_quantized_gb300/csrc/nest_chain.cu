@@ -11,9 +11,11 @@
 // reading used by the chained-layer workload.
 //
 // Two launches, both spread over every (token, 4096-element segment) pair so that
-// a single token still occupies many SMs.  For blocks of up to 1024 elements the
+// a single token still occupies many SMs.  For blocks of up to 512 elements the
 // butterflies of a segment run in registers, one warp per chunk of max(b, 256)
-// elements (the register path below); otherwise:
+// elements (the register path below); for blocks of 1024 to 4096 a segment is
+// 16 rows x 256 columns with one pass through shared memory (the segment path);
+// otherwise:
 //   k_glue_out: one CTA per (t, segment) rotates its segment of z_a (and z_b) in a
 //               64 x 64 shared-memory tile, writes h and the segment's sum of
 //               squares.  A segment is a whole number of Hadamard blocks (the block
@@ -34,7 +36,7 @@ constexpr int kThreads = 512;
 constexpr int kPer = kSeg / kThreads;
 constexpr int kWarps = kThreads / 32;
 
-// Register path (GlueArgs::reg: b <= 1024, M % 8 == 0, 16-byte aligned vectors, 8-byte
+// Register path (GlueArgs::path 1: b <= 512, M % 8 == 0, 16-byte aligned vectors, 8-byte
 // aligned signs).  The CTA's 4096-element segment is cut into chunks of W = max(b, 256)
 // elements, one per warp; a warp keeps its chunk in registers (chunk_fwht: lane l holds
 // elements 256 h + 8 l + i) and needs no shared memory or barrier for the butterflies.
@@ -152,18 +154,128 @@ __device__ __forceinline__ void glue_in_reg(const GlueArgs& a, const GlueNext& n
     }
 }
 
+// Segment path (GlueArgs::path 2: b = 1024 .. 4096, 16-byte aligned h, 8-byte aligned
+// signs): the CTA's (token, 4096-element segment) as 16 rows x 256 columns (seg_col in
+// nest_device.cuh): coalesced column loads and the butterflies over the high index bits,
+// one pass through shared memory, then the low 8 bits along the rows, one row per warp.
+template <bool PROD>
+__device__ __forceinline__ void glue_out_seg(const GlueArgs& a, int t, int seg0, float* sm, float* sm2, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int L = a.L, M = a.M;
+    const SegCol sc = seg_col(L);
+    const int eB = seg0 + 256 * warp + 8 * lane;       // phase B: this lane's 8 elements
+    uint2 sa[1] = {make_uint2(0u, 0u)}, sb[1] = {make_uint2(0u, 0u)};
+    if (eB < M) {
+        sa[0] = *reinterpret_cast<const uint2*>(a.sa + eB);
+        if constexpr (PROD) sb[0] = *reinterpret_cast<const uint2*>(a.sb + eB);
+    }
+    grid_dep_wait();                 // z_a, z_b come from the GEMM before this launch
+    const size_t row = (size_t)t * M;
+    float v[16], w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int e = seg0 + 256 * (sc.r0 + k) + sc.c;
+        const bool in = k < sc.nr && e < M;
+        v[k] = in ? __ldcg(a.za + row + e) : 0.0f;
+        w[k] = (PROD && in) ? __ldcg(a.zb + row + e) : 0.0f;
+    }
+    seg_rows_fwht(v, L);
+    seg_col_store(sm, sc, v);
+    if constexpr (PROD) {
+        seg_rows_fwht(w, L);
+        seg_col_store(sm2, sc, w);
+    }
+    __syncthreads();                 // every load of the segment is done: h may overwrite z_a
+    float hv[8], wb[8];
+    seg_row_load(sm, warp, lane, hv);
+    chunk_fwht<1>(hv, 8, lane);
+    if constexpr (PROD) {
+        seg_row_load(sm2, warp, lane, wb);
+        chunk_fwht<1>(wb, 8, lane);
+    }
+    float ss = 0.0f;
+    if (eB < M) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            hv[i] *= a.scale * chunk_sign<1>(sa, i);
+            if constexpr (PROD) hv[i] *= wb[i] * a.scale * chunk_sign<1>(sb, i);
+            ss += hv[i] * hv[i];
+        }
+        float4* hp = reinterpret_cast<float4*>(a.h + row + eB);
+        hp[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+        hp[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {                            // the warps' sums in a fixed order
+        float tot = 0.0f;
+        for (int i = 0; i < kWarps; ++i) tot += red[i];
+        a.work[blockIdx.x] = tot;
+    }
+}
+
+__device__ __forceinline__ void glue_in_seg(const GlueArgs& a, const GlueNext& nx, int t, int seg0, int rem,
+                                            int per_next, float* sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int L = a.L, M = a.M;
+    const SegCol sc = seg_col(L);
+    float sg[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int e = seg0 + 256 * (sc.r0 + k) + sc.c;
+        sg[k] = (k < sc.nr && e < M) ? (float)nx.sign_in[e] : 0.0f;
+    }
+    grid_dep_wait();                 // h and the segment sums come from k_glue_out
+    const size_t row = (size_t)t * M;
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int e = seg0 + 256 * (sc.r0 + k) + sc.c;
+        v[k] = (k < sc.nr && e < M) ? __ldcg(a.h + row + e) : 0.0f;
+    }
+    // this CTA's share of the next GEMM's accumulator, after the loads
+    if (nx.zero_out != nullptr) clear_share<kThreads>(nx.zero_out, nx.zero_count, rem, per_next);
+    // the token's sum of squares: every warp adds the segment sums in the same tree order
+    float ss = 0.0f;
+    for (int i = lane; i < a.nseg; i += 32) ss += __ldcg(a.work + t * a.nseg + i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rms = sqrtf(ss / (float)M);
+    const float inv = rms > 0.0f ? 1.0f / rms : 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = __bfloat162float(__float2bfloat16_rn(v[k] * inv)) * sg[k];
+    seg_rows_fwht(v, L);
+    seg_col_store(sm, sc, v);
+    __syncthreads();
+    float w[8];
+    seg_row_load(sm, warp, lane, w);
+    chunk_fwht<1>(w, 8, lane);
+    const int eB = seg0 + 256 * warp + 8 * lane;
+    if (eB >= M) return;
+    uint32_t q[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) q[e] = h2_as_u32(__floats2half2_rn(w[2 * e] * a.scale, w[2 * e + 1] * a.scale));
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(nx.xop) + xop_offset(eB, t, a.NB)) =
+        make_uint4(q[0], q[1], q[2], q[3]);
+}
+
 template <bool PROD>
 __global__ void __launch_bounds__(kThreads) k_glue_out(const __grid_constant__ GlueArgs a) {
-    __shared__ float buf[64][65];
-    __shared__ float buf2[PROD ? 64 : 1][65];
+    __shared__ __align__(16) float buf[64][65];
+    __shared__ __align__(16) float buf2[PROD ? 64 : 1][65];
     __shared__ float red[32];
     grid_dep_launch_dependents();
     const int t = blockIdx.x / a.nseg, s = blockIdx.x - t * a.nseg;
     const int seg0 = s * kSeg;
-    if (a.reg) {
+    if (a.path == 2) {
+        glue_out_seg<PROD>(a, t, seg0, &buf[0][0], &buf2[0][0], red);
+        return;
+    }
+    if (a.path == 1) {
         if (a.L <= 8) glue_out_reg<PROD, 1>(a, t, seg0, red);
-        else if (a.L == 9) glue_out_reg<PROD, 2>(a, t, seg0, red);
-        else glue_out_reg<PROD, 4>(a, t, seg0, red);
+        else glue_out_reg<PROD, 2>(a, t, seg0, red);
         return;
     }
     const int count = a.M - seg0 < kSeg ? a.M - seg0 : kSeg;
@@ -204,7 +316,7 @@ __global__ void __launch_bounds__(kThreads) k_glue_out(const __grid_constant__ G
 }
 
 __global__ void __launch_bounds__(kThreads) k_glue_in(const __grid_constant__ GlueArgs a) {
-    __shared__ float buf[64][65];
+    __shared__ __align__(16) float buf[64][65];
     __shared__ float s_inv;
     grid_dep_launch_dependents();
     const int per_next = a.T * a.nseg;
@@ -213,10 +325,13 @@ __global__ void __launch_bounds__(kThreads) k_glue_in(const __grid_constant__ Gl
     const int t = rem / a.nseg, s = rem - t * a.nseg;
     const int seg0 = s * kSeg;
     const GlueNext& nx = a.next[jn];
-    if (a.reg) {
+    if (a.path == 2) {
+        glue_in_seg(a, nx, t, seg0, rem, per_next, &buf[0][0]);
+        return;
+    }
+    if (a.path == 1) {
         if (a.L <= 8) glue_in_reg<1>(a, nx, t, seg0, rem, per_next);
-        else if (a.L == 9) glue_in_reg<2>(a, nx, t, seg0, rem, per_next);
-        else glue_in_reg<4>(a, nx, t, seg0, rem, per_next);
+        else glue_in_reg<2>(a, nx, t, seg0, rem, per_next);
         return;
     }
     const int count = a.M - seg0 < kSeg ? a.M - seg0 : kSeg;
@@ -279,9 +394,10 @@ cudaError_t launch_glue(GlueArgs& a, cudaStream_t stream) {
     a.NB = n_pad(a.T) / 8;
     a.nseg = glue_segments(a.M);
     auto al = [](const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; };
-    bool reg = b <= 1024 && a.M % 8 == 0 && al(a.za, 16) && al(a.zb, 16) && al(a.h, 16) && al(a.sa, 8) && al(a.sb, 8);
+    bool reg = b <= 512 && a.M % 8 == 0 && al(a.za, 16) && al(a.zb, 16) && al(a.h, 16) && al(a.sa, 8) && al(a.sb, 8);
     for (int j = 0; j < a.nnext; ++j) reg = reg && al(a.next[j].sign_in, 8);
-    a.reg = reg ? 1 : 0;
+    const bool seg = b >= 1024 && al(a.h, 16) && al(a.sa, 8) && al(a.sb, 8);
+    a.path = reg ? 1 : (seg ? 2 : 0);
     const dim3 blk(kThreads);
     cudaError_t e = a.zb != nullptr ? launch_pdl(k_glue_out<true>, dim3(a.T * a.nseg), blk, 0, stream, a)
                                     : launch_pdl(k_glue_out<false>, dim3(a.T * a.nseg), blk, 0, stream, a);

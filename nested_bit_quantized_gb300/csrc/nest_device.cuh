@@ -254,6 +254,47 @@ __device__ __forceinline__ void chunk_fwht(float (&v)[8 * H], int L, int lane) {
     }
 }
 
+// Segment path of the FWHT for blocks of 2^L, 10 <= L <= 12: one CTA of 512 threads per
+// 4096-element segment, seen as 16 rows x 256 columns (element 256 r + c).  The butterflies
+// over index bits 8 .. L-1 run first, each thread holding rows of one column in registers
+// (phase A, seg_col and seg_rows_fwht); one pass through shared memory; then bits 0 .. 7
+// along the rows, warp w holding row w in the chunk layout (phase B, seg_row_load and
+// chunk_fwht<1>).  The stage order does not change the transform.
+struct SegCol {
+    int c, r0, nr;            // column, first row, rows held (0: idle in phase A)
+};
+__device__ __forceinline__ SegCol seg_col(int L) {
+    const int t = threadIdx.x;
+    if (L >= 12) return SegCol{t & 255, 0, t < 256 ? 16 : 0};
+    return SegCol{t & 255, 8 * (t >> 8), 8};
+}
+// v[k] holds row r0 + k of the thread's column; butterflies over row bits 0 .. L-9.
+__device__ __forceinline__ void seg_rows_fwht(float (&v)[16], int L) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (q < L - 8) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                if (k & (1 << q)) continue;
+                const float a = v[k], d = v[k + (1 << q)];
+                v[k] = a + d;
+                v[k + (1 << q)] = a - d;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void seg_col_store(float* sm, const SegCol& sc, const float (&v)[16]) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        if (k < sc.nr) sm[(sc.r0 + k) * 256 + sc.c] = v[k];
+}
+// Phase B input of warp w: row w, lane l's elements 8 l .. 8 l + 7.
+__device__ __forceinline__ void seg_row_load(const float* sm, int w, int lane, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(sm + w * 256 + 8 * lane);
+    const float4 b = *reinterpret_cast<const float4*>(sm + w * 256 + 8 * lane + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
 // Chunk of the register-path FWHT for blocks of 2^L (L <= 10): 256, 512 or 1024 elements.
 __host__ __device__ constexpr int reg_chunk(int L) { return L <= 8 ? 256 : (L == 9 ? 512 : 1024); }
 

@@ -38,7 +38,7 @@ struct RotTask {
     unsigned n, total;        // vector length, T * n
     int L, NB, cta_begin;     // log2 block size, operand token blocks, first CTA of the task
     float scale;
-    int reg;                  // 1: the register path (b <= 1024, see nest_rotate.cu)
+    int path;                 // 0 shared-memory tile, 1 register (b <= 512), 2 segment (b >= 1024)
     unsigned nctas;           // CTAs of the task
 };
 
@@ -104,7 +104,7 @@ struct GlueArgs {
     GlueNext next[kMaxChainNext];
     int nnext, M, T, L, NB, nseg;
     float scale;
-    int reg;                  // 1: the register path (b <= 1024, see nest_chain.cu)
+    int path;                 // 0 shared-memory tile, 1 register (b <= 512), 2 segment (b >= 1024)
 };
 int glue_segments(int M);     // 4096-element segments per token
 cudaError_t launch_glue(GlueArgs& a, cudaStream_t stream);

@@ -5,10 +5,13 @@
 // with blocks of size b = largest power of two dividing n (at most 4096), each
 // scaled by 1/sqrt(b).
 //
-// Two ways, chosen per vector set of a launch:
-// - blocks of at most 1024 (and n % 8 == 0, 16-byte aligned vectors, 8-byte aligned
+// Three ways, chosen per vector set of a launch:
+// - blocks of at most 512 (and n % 8 == 0, 16-byte aligned vectors, 8-byte aligned
 //   signs): each warp takes one (token, chunk of max(b, 256) elements) and runs the
 //   butterflies in registers and warp shuffles, with no shared memory and no barrier;
+// - blocks of 1024 to 4096 (aligned output and signs): one CTA per (token, 4096-element
+//   segment), butterflies over the high index bits per column, one pass through shared
+//   memory, then the low 8 bits along rows (rotate_seg);
 // - otherwise a CTA takes 4096 consecutive elements of the token-major [T][n] array (a
 //   whole number of blocks, since b divides both n and 4096), views them as a 64 x 64
 //   tile in shared memory, and runs the butterflies in two phases with warp shuffles:
@@ -26,7 +29,7 @@ constexpr int kRegWarps = kThreads / 32;
 constexpr long long kClearPerCta = 8192;     // floats a register-path CTA clears at most
 
 // Register path: one warp per (token, chunk of W = max(b, 256) consecutive elements, b <=
-// 1024).  Lane l holds elements 256 h + 8 l + i of the chunk (i < 8, h < W / 256), so each
+// 512).  Lane l holds elements 256 h + 8 l + i of the chunk (i < 8, h < W / 256), so each
 // lane's loads and stores are 16- or 32-byte pieces (chunk_fwht).  The signs are constants
 // of the layer, not outputs of the previous kernel, so they are loaded before waiting for
 // it; the clearing stores are issued after the loads.
@@ -103,19 +106,87 @@ __device__ __forceinline__ void rotate_reg(const RotTask& tk, unsigned cta) {
     }
 }
 
+// Segment path (blocks of 1024 .. 4096, 16-byte aligned y, 8-byte aligned signs): one CTA
+// per (token, 4096-element segment of the vector), see seg_col in nest_device.cuh.  Phase A
+// loads each thread's rows of one column (coalesced scalar loads; input-side signs applied
+// there), phase B stores each warp's row as 16- or 32-byte pieces.  One barrier.
+template <int MODE, bool BF16>
+__device__ __forceinline__ void rotate_seg(const RotTask& tk, unsigned cta, float* sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned n = tk.n, T = tk.total / tk.n;
+    const unsigned nseg = (n + 4095) / 4096;
+    const bool work = cta < T * nseg;                  // the same for the whole CTA
+    const unsigned tok = work ? cta / nseg : 0, s0 = work ? (cta - tok * nseg) * 4096 : 0;
+    const int L = tk.L;
+    const SegCol sc = seg_col(L);
+    float sgA[16];
+    uint2 sgB = make_uint2(0u, 0u);
+    const unsigned eB = s0 + 256 * warp + 8 * lane;    // phase B: this lane's 8 elements
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const unsigned e = s0 + 256 * (sc.r0 + k) + sc.c;
+        sgA[k] = (MODE == 0 && work && k < sc.nr && e < n) ? (float)tk.signs[e] : 0.0f;
+    }
+    if (MODE == 1 && work && eB < n) sgB = *reinterpret_cast<const uint2*>(tk.signs + eB);
+    grid_dep_wait();                      // x may be the previous kernel's output; y may be its input
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const unsigned e = s0 + 256 * (sc.r0 + k) + sc.c;
+        float x = 0.0f;
+        if (work && k < sc.nr && e < n) {
+            const size_t idx = (size_t)tok * n + e;
+            if constexpr (BF16) x = __bfloat162float(__ldcg(static_cast<const __nv_bfloat16*>(tk.x) + idx));
+            else x = __ldcg(static_cast<const float*>(tk.x) + idx);
+        }
+        v[k] = MODE == 0 ? x * sgA[k] : x;
+    }
+    // clear the accumulator of the GEMM that follows (the task may have CTAs for this alone)
+    if (tk.zero_out != nullptr) clear_share<kThreads>(tk.zero_out, tk.zero_count, cta, tk.nctas);
+    if (!work) return;
+    seg_rows_fwht(v, L);
+    seg_col_store(sm, sc, v);
+    __syncthreads();
+    float w[8];
+    seg_row_load(sm, warp, lane, w);
+    chunk_fwht<1>(w, 8, lane);
+    if (eB >= n) return;                  // n is a multiple of 1024: whole groups of 8
+    const float scale = tk.scale;
+    if constexpr (MODE == 1) {
+        const uint2 sg[1] = {sgB};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] *= scale * chunk_sign<1>(sg, i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] *= scale;
+    }
+    if (tk.y != nullptr) {
+        float4* yp = reinterpret_cast<float4*>(tk.y + (size_t)tok * n + eB);
+        yp[0] = make_float4(w[0], w[1], w[2], w[3]);
+        yp[1] = make_float4(w[4], w[5], w[6], w[7]);
+    }
+    if (MODE == 0 && tk.xop != nullptr) {
+        uint32_t q[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) q[e] = h2_as_u32(__floats2half2_rn(w[2 * e], w[2 * e + 1]));
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(tk.xop) + xop_offset((int)eB, (int)tok, tk.NB)) =
+            make_uint4(q[0], q[1], q[2], q[3]);
+    }
+}
+
 template <int MODE, bool BF16>
 __global__ void __launch_bounds__(kThreads)
 k_rotate(const __grid_constant__ RotArgs args) {
-    __shared__ float buf[64][65];
+    __shared__ __align__(16) float buf[64][65];
     grid_dep_launch_dependents();
     int k = 0;                            // the vector set this CTA works on
     while (k + 1 < args.ntasks && args.task[k + 1].cta_begin <= (int)blockIdx.x) ++k;
     const RotTask& tk = args.task[k];
-    if (tk.reg) {                         // the same for every thread of the CTA
+    if (tk.path != 0) {                   // the same for every thread of the CTA
         const unsigned cta = blockIdx.x - tk.cta_begin;
-        if (tk.L <= 8) rotate_reg<MODE, BF16, 1>(tk, cta);
-        else if (tk.L == 9) rotate_reg<MODE, BF16, 2>(tk, cta);
-        else rotate_reg<MODE, BF16, 4>(tk, cta);
+        if (tk.path == 2) rotate_seg<MODE, BF16>(tk, cta, &buf[0][0]);
+        else if (tk.L <= 8) rotate_reg<MODE, BF16, 1>(tk, cta);
+        else rotate_reg<MODE, BF16, 2>(tk, cta);
         return;
     }
     const void* __restrict__ x = tk.x;
@@ -211,12 +282,14 @@ cudaError_t launch_rotate_group(RotArgs& a, int x_dtype, int mode, int T, cudaSt
         t.scale = (float)(1.0 / sqrt((double)b));
         t.total = (unsigned)T * t.n;                     // the entry points keep T * n < 2^31
         t.NB = n_pad(T) / 8;
-        t.reg = b <= 1024 && t.n % 8 == 0 && aligned(t.x, 16) && aligned(t.y, 16) && aligned(t.signs, 8);
+        if (b <= 512 && t.n % 8 == 0 && aligned(t.x, 16) && aligned(t.y, 16) && aligned(t.signs, 8)) t.path = 1;
+        else if (b >= 1024 && aligned(t.y, 16) && aligned(t.signs, 8)) t.path = 2;
+        else t.path = 0;
         t.cta_begin = ctas;
         long long c;
-        if (t.reg) {
-            const long long items = (long long)T * ((t.n + reg_chunk(L) - 1) / reg_chunk(L));
-            c = (items + kRegWarps - 1) / kRegWarps;
+        if (t.path != 0) {
+            const long long items = t.path == 1 ? (long long)T * ((t.n + reg_chunk(L) - 1) / reg_chunk(L)) : 0;
+            c = t.path == 1 ? (items + kRegWarps - 1) / kRegWarps : (long long)T * ((t.n + 4095) / 4096);
             const long long cz = t.zero_out != nullptr ? (t.zero_count + kClearPerCta - 1) / kClearPerCta : 0;
             if (cz > c) c = cz;
         } else {
