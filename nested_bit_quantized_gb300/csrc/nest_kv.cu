@@ -927,6 +927,7 @@ k_kv_attn_pair(const __grid_constant__ KvAttnArgs a) {
             ks[e] = ssc[g + 8 * e];
             vsc[e] = ssc[16 + g + 8 * e];
         }
+        uint32_t pf[2][2];                    // P^T fragments of both row groups
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             float sc[4], pr[4];
@@ -982,14 +983,16 @@ k_kv_attn_pair(const __grid_constant__ KvAttnArgs a) {
                     pr[2 + re] = e1 * vsc[1];
                 }
             }
-            const uint32_t pb0 = movmatrix_trans(pack_h2(pr[0], pr[1]));
-            const uint32_t pb1 = movmatrix_trans(pack_h2(pr[2], pr[3]));
+            pf[nt][0] = movmatrix_trans(pack_h2(pr[0], pr[1]));
+            pf[nt][1] = movmatrix_trans(pack_h2(pr[2], pr[3]));
+        }
+        // each value fragment is read from the tile once, for both row groups
 #pragma unroll
-            for (int dt = 0; dt < 8; ++dt) {
-                uint32_t v0, v1, v2, v3;
-                ldmatrix_x4_trans(vt + voff + 32 * dt, v0, v1, v2, v3);
-                mma16816f(o[nt][dt], v0, v1, v2, v3, pb0, pb1);
-            }
+        for (int dt = 0; dt < 8; ++dt) {
+            uint32_t v0, v1, v2, v3;
+            ldmatrix_x4_trans(vt + voff + 32 * dt, v0, v1, v2, v3);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) mma16816f(o[nt][dt], v0, v1, v2, v3, pf[nt][0], pf[nt][1]);
         }
         pb = pn;
         ++it;
