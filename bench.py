@@ -105,7 +105,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -143,18 +143,30 @@ class ClockSampler:
 # CPU oracle timing (cpu_baseline and --impl reference)
 # ----------------------------------------------------------------------------
 
+_ORACLE_LAYERS = {}
+
+
+def _oracle_layer(lin):
+    """The oracle's quantised layer, computed once per linear (offline work, not timed)."""
+    if lin.name not in _ORACLE_LAYERS:
+        from nested_bit_quantized_gb300 import synth
+        from oracle import nest_oracle as O
+        W = synth.weights(lin.M, lin.K, lin.w_seed, lin.outliers)
+        s_o, s_i = synth.sign_pair(lin.M, lin.K, lin.sign_seed)
+        _ORACLE_LAYERS[lin.name] = (O.quantize_layer(W, s_o, s_i, BITS), s_o, s_i)
+    return _ORACLE_LAYERS[lin.name]
+
+
 def oracle_sample(n_linears=3, seconds_cap=25.0):
     """Times the oracle's draft (T=1) and verify (T=16) forward passes on the
-    workload's linears (offline quantisation excluded).  Returns bytes, seconds, what."""
-    import numpy as np
+    workload's linears (offline quantisation excluded, done once per linear).
+    Returns bytes, seconds, what."""
     from nested_bit_quantized_gb300 import synth
     from oracle import nest_oracle as O
     wl = synth.WORKLOADS[WORKLOAD]
     tot_b, tot_s, done = 0.0, 0.0, []
     for lin in wl.linears[:n_linears]:
-        W = synth.weights(lin.M, lin.K, lin.w_seed, lin.outliers)
-        s_o, s_i = synth.sign_pair(lin.M, lin.K, lin.sign_seed)
-        q = O.quantize_layer(W, s_o, s_i, BITS)
+        q, s_o, s_i = _oracle_layer(lin)
         for T, verify in ((T_DRAFT, False), (T_VERIFY, True)):
             _, x = synth.activations(T, lin.K, wl.x_seed)
             t0 = time.perf_counter()
@@ -676,7 +688,7 @@ def run_kv(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="nest", choices=["nest", "reference"])
     ap.add_argument("--copies", type=int, default=12)

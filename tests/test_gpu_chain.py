@@ -40,17 +40,25 @@ def dev():
 
 @pytest.mark.parametrize("M,T,product,in_place,n_next", [
     (512, 1, False, False, 2), (5376, 17, True, False, 2), (3840, 64, False, True, 2), (8192, 5, True, True, 1),
-    (21504, 3, True, False, 1), (300, 4, True, False, 0), (4096, 2, False, True, 3), (5376, 160, True, False, 2)])
+    (21504, 3, True, False, 1), (300, 4, True, False, 0), (4096, 2, False, True, 3), (5376, 160, True, False, 2),
+    (8192, 3, True, "odd", 2), (21504, 2, False, "odd", 1), (2560, 4, True, "odd", 1)])
 def test_chain_kernel(dev, M, T, product, in_place, n_next):
     """Out-rotation (+ product), RMS rescale, bf16 cast and next in-rotations; ragged last
-    4096-element segments (5376, 21504), a segment shorter than one (300, 3840), h in place."""
+    4096-element segments (5376, 21504), a segment shorter than one (300, 3840), h in place,
+    and h written to a y 4 bytes off a 16-byte boundary ("odd": the shared-memory tile path
+    instead of the register path for b <= 512 or the segment path for b >= 1024)."""
     rng = np.random.default_rng(M + T)
     za = rng.normal(size=(T, M)).astype(np.float32)
     zb = rng.normal(size=(T, M)).astype(np.float32) if product else None
     sa, sb = synth.signs(M, 1), synth.signs(M, 2)
     nxt = [synth.signs(M, 3 + j) for j in range(n_next)]
     za_d = to_dev(za, torch, dev)
-    y = None if in_place else torch.empty((T, M), dtype=torch.float32, device=dev)
+    if in_place == "odd":
+        y = torch.empty(T * M + 4, dtype=torch.float32, device=dev)[1:1 + T * M].view(T, M)
+        assert y.data_ptr() % 16 == 4
+        in_place = False
+    else:
+        y = None if in_place else torch.empty((T, M), dtype=torch.float32, device=dev)
     # next linears reading h (their descriptors only need K == M and S_i)
     dummy = torch.zeros(16, dtype=torch.uint8, device=dev)
     layers = [nest.Layer(1000 + 24 * j, M, 0, dummy, None, to_dev(sa, torch, dev), to_dev(s, torch, dev))
