@@ -214,7 +214,7 @@ __device__ __forceinline__ float chunk_sign(const uint2 (&sg)[H], int j) {
 
 // Block-diagonal FWHT (unnormalised Sylvester order, blocks of 2^L <= 256 H elements) of
 // one warp's chunk of 256 H consecutive elements held in registers: element 256 h + 8 l + i
-// of the chunk in v[8 h + i] of lane l (i < 8, h < H).  Index bits 0-2 and 8-9 are
+// of the chunk in v[8 h + i] of lane l (i < 8, h < H).  Index bits 0-2 and 8 and up are
 // butterflies inside the lane, bits 3-7 warp shuffles.  All 32 lanes call it.
 template <int H>
 __device__ __forceinline__ void chunk_fwht(float (&v)[8 * H], int L, int lane) {
@@ -295,8 +295,8 @@ __device__ __forceinline__ void seg_row_load(const float* sm, int w, int lane, f
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// Chunk of the register-path FWHT for blocks of 2^L (L <= 10): 256, 512 or 1024 elements.
-__host__ __device__ constexpr int reg_chunk(int L) { return L <= 8 ? 256 : (L == 9 ? 512 : 1024); }
+// Chunk of the register-path FWHT for blocks of 2^L (L <= 9): 256 or 512 elements.
+__host__ __device__ constexpr int reg_chunk(int L) { return L <= 8 ? 256 : 512; }
 
 // Block-diagonal FWHT (unnormalised, blocks of 2^L, 0 <= L <= 12) of the 4096 values
 // of a 64 x 64 shared-memory tile, value f at tile[f / 64][f % 64]: butterflies over
