@@ -397,8 +397,8 @@ nest_status nest_rotate_group(const nest_rotate_task* tasks, int32_t count, int3
             return NEST_ERR_MISALIGNED;
         if (r.zero_count < 0 || (r.zero_count > 0 && r.zero_out == nullptr)) return NEST_ERR_INVALID_ARG;
         if (r.zero_out && (reinterpret_cast<uintptr_t>(r.zero_out) & 3u)) return NEST_ERR_MISALIGNED;
-        // at most one CTA per 4096 elements, or per 8192 floats to clear (the launch's bound)
-        const long long c_rot = ((long long)r.n * T + 4095) / 4096, c_clr = (r.zero_count + 8191) / 8192;
+        // at most one CTA per 512 elements, or per 2048 floats to clear (the launch's bound)
+        const long long c_rot = ((long long)r.n * T + 511) / 512, c_clr = (r.zero_count + 2047) / 2048;
         ctas += c_rot > c_clr ? c_rot : c_clr;
         a.task[k].x = r.x;
         a.task[k].signs = r.signs;

@@ -33,13 +33,13 @@ constexpr long long kClearPerCta = 8192;     // floats a register-path CTA clear
 // lane's loads and stores are 16- or 32-byte pieces (chunk_fwht).  The signs are constants
 // of the layer, not outputs of the previous kernel, so they are loaded before waiting for
 // it; the clearing stores are issued after the loads.
-template <int MODE, bool BF16, int H>
+template <int MODE, bool BF16, int H, int WARPS = kRegWarps>
 __device__ __forceinline__ void rotate_reg(const RotTask& tk, unsigned cta) {
     constexpr int W = 256 * H, NR = 8 * H;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned n = tk.n, T = tk.total / tk.n;
     const unsigned nchunk = (n + W - 1) / W;
-    const unsigned item = cta * kRegWarps + warp;
+    const unsigned item = cta * WARPS + warp;
     const bool active = item < T * nchunk;             // the same for the whole warp
     const unsigned tok = active ? item / nchunk : 0, c0 = active ? (item - tok * nchunk) * W : 0;
     bool have[H];
@@ -76,7 +76,7 @@ __device__ __forceinline__ void rotate_reg(const RotTask& tk, unsigned cta) {
         }
     }
     // clear the accumulator of the GEMM that follows (the task may have CTAs for this alone)
-    if (tk.zero_out != nullptr) clear_share<kThreads>(tk.zero_out, tk.zero_count, cta, tk.nctas);
+    if (tk.zero_out != nullptr) clear_share<32 * WARPS>(tk.zero_out, tk.zero_count, cta, tk.nctas);
     if (!active) return;
     auto sign = [&](int j) { return (float)(int8_t)((((j & 7) < 4 ? sg[j >> 3].x : sg[j >> 3].y) >> (8 * (j & 3))) & 0xFFu); };
     if constexpr (MODE == 0) {
@@ -172,6 +172,25 @@ __device__ __forceinline__ void rotate_seg(const RotTask& tk, unsigned cta, floa
         *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(tk.xop) + xop_offset((int)eB, (int)tok, tk.NB)) =
             make_uint4(q[0], q[1], q[2], q[3]);
     }
+}
+
+// Launches whose vector sets all take the register path: CTAs of two warps with no shared
+// memory, small enough to become resident on an SM beside the GEMM's two CTAs, so that
+// the launch's CTAs are in place, signs loaded, when the GEMM before them completes (and
+// leave the GEMM after them every SM).
+constexpr int kSmallWarps = 2;
+constexpr long long kSmallClear = 2048;      // floats a small CTA clears at most
+
+template <int MODE, bool BF16>
+__global__ void __launch_bounds__(32 * kSmallWarps)
+k_rotate_small(const __grid_constant__ RotArgs args) {
+    grid_dep_launch_dependents();
+    int k = 0;
+    while (k + 1 < args.ntasks && args.task[k + 1].cta_begin <= (int)blockIdx.x) ++k;
+    const RotTask& tk = args.task[k];
+    const unsigned cta = blockIdx.x - tk.cta_begin;
+    if (tk.L <= 8) rotate_reg<MODE, BF16, 1, kSmallWarps>(tk, cta);
+    else rotate_reg<MODE, BF16, 2, kSmallWarps>(tk, cta);
 }
 
 template <int MODE, bool BF16>
@@ -272,6 +291,14 @@ int hadamard_block(int n) {
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 cudaError_t launch_rotate_group(RotArgs& a, int x_dtype, int mode, int T, cudaStream_t stream) {
+    bool small = true;                                   // every set takes the register path
+    for (int k = 0; k < a.ntasks; ++k) {
+        const RotTask& t = a.task[k];
+        const int b = hadamard_block((int)t.n);
+        small = small && b <= 512 && t.n % 8 == 0 && aligned(t.x, 16) && aligned(t.y, 16) && aligned(t.signs, 8);
+    }
+    const int warps = small ? kSmallWarps : kRegWarps;
+    const long long clear_per = small ? kSmallClear : kClearPerCta;
     int ctas = 0;
     for (int k = 0; k < a.ntasks; ++k) {
         RotTask& t = a.task[k];
@@ -289,14 +316,22 @@ cudaError_t launch_rotate_group(RotArgs& a, int x_dtype, int mode, int T, cudaSt
         long long c;
         if (t.path != 0) {
             const long long items = t.path == 1 ? (long long)T * ((t.n + reg_chunk(L) - 1) / reg_chunk(L)) : 0;
-            c = t.path == 1 ? (items + kRegWarps - 1) / kRegWarps : (long long)T * ((t.n + 4095) / 4096);
-            const long long cz = t.zero_out != nullptr ? (t.zero_count + kClearPerCta - 1) / kClearPerCta : 0;
+            c = t.path == 1 ? (items + warps - 1) / warps : (long long)T * ((t.n + 4095) / 4096);
+            const long long cz = t.zero_out != nullptr ? (t.zero_count + clear_per - 1) / clear_per : 0;
             if (cz > c) c = cz;
         } else {
             c = (t.total + kSeg - 1) / kSeg;
         }
         t.nctas = (unsigned)c;
         ctas += (int)c;
+    }
+    if (small) {
+        const dim3 g(ctas), blk(32 * kSmallWarps);
+        if (mode == 0)
+            return x_dtype == 1 ? launch_pdl(k_rotate_small<0, true>, g, blk, 0, stream, a)
+                                : launch_pdl(k_rotate_small<0, false>, g, blk, 0, stream, a);
+        return x_dtype == 1 ? launch_pdl(k_rotate_small<1, true>, g, blk, 0, stream, a)
+                            : launch_pdl(k_rotate_small<1, false>, g, blk, 0, stream, a);
     }
     const dim3 g(ctas), blk(kThreads);
     if (mode == 0)
