@@ -337,7 +337,7 @@ nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, 
 
 size_t nest_chain_work_bytes(int32_t M, int32_t T) {
     if (M < 1 || T < 1 || T > kMaxT) return 0;
-    return round256((size_t)T * glue_segments(M) * sizeof(float));
+    return round256((size_t)glue_work_floats(M, T) * sizeof(float));
 }
 
 nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,

@@ -12,8 +12,8 @@
 //
 // Two launches, both spread over every (token, 4096-element segment) pair so that
 // a single token still occupies many SMs.  For blocks of up to 512 elements the
-// butterflies of a segment run in registers, one warp per chunk of max(b, 256)
-// elements (the register path below); for blocks of 1024 to 4096 a segment is
+// butterflies run in registers, one warp per (token, chunk of max(b, 256) elements), in
+// CTAs of two warps (the register path below); for blocks of 1024 to 4096 a segment is
 // 16 rows x 256 columns with one pass through shared memory (the segment path);
 // otherwise:
 //   k_glue_out: one CTA per (t, segment) rotates its segment of z_a (and z_b) in a
@@ -36,11 +36,11 @@ constexpr int kThreads = 512;
 constexpr int kPer = kSeg / kThreads;
 constexpr int kWarps = kThreads / 32;
 
-// Register path (GlueArgs::path 1: b <= 512, M % 8 == 0, 16-byte aligned vectors, 8-byte
-// aligned signs).  The CTA's 4096-element segment is cut into chunks of W = max(b, 256)
-// elements, one per warp; a warp keeps its chunk in registers (chunk_fwht: lane l holds
-// elements 256 h + 8 l + i) and needs no shared memory or barrier for the butterflies.
-// The signs are layer constants and are loaded before waiting for the previous kernel.
+// Register path (GlueArgs::path 3: b <= 512, M % 8 == 0, 16-byte aligned vectors, 8-byte
+// aligned signs): a warp keeps a chunk of W = max(b, 256) elements in registers (chunk_fwht:
+// lane l holds elements 256 h + 8 l + i) and needs no shared memory or barrier for the
+// butterflies.  The signs are layer constants and are loaded before waiting for the
+// previous kernel.
 
 // Load the 8 H fp32 values of a warp's chunk that starts at element c0 of row `row`.
 template <int H>
@@ -56,101 +56,6 @@ __device__ __forceinline__ void load_chunk(const float* base, const bool (&have)
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[8 * h + i] = 0.0f;
         }
-    }
-}
-
-template <bool PROD, int H>
-__device__ __forceinline__ void glue_out_reg(const GlueArgs& a, int t, int seg0, float* red) {
-    constexpr int W = 256 * H, NR = 8 * H;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int c0 = seg0 + warp * W;                    // this warp's chunk
-    const bool active = warp * W < kSeg && c0 < a.M;
-    bool have[H];
-    uint2 sa[H], sb[H];
-#pragma unroll
-    for (int h = 0; h < H; ++h) {
-        const int col = c0 + 256 * h + 8 * lane;
-        have[h] = active && col < a.M;
-        sa[h] = have[h] ? *reinterpret_cast<const uint2*>(a.sa + col) : make_uint2(0u, 0u);
-        sb[h] = (PROD && have[h]) ? *reinterpret_cast<const uint2*>(a.sb + col) : make_uint2(0u, 0u);
-    }
-    grid_dep_wait();                 // z_a, z_b come from the GEMM before this launch
-    const size_t row = (size_t)t * a.M + c0;
-    float ss = 0.0f;
-    if (active) {
-        float v[NR], w[NR];
-        load_chunk<H>(a.za + row, have, lane, v);
-        if constexpr (PROD) load_chunk<H>(a.zb + row, have, lane, w);
-        chunk_fwht<H>(v, a.L, lane);
-        if constexpr (PROD) chunk_fwht<H>(w, a.L, lane);
-#pragma unroll
-        for (int j = 0; j < NR; ++j) {
-            v[j] *= a.scale * chunk_sign<H>(sa, j);
-            if constexpr (PROD) v[j] *= w[j] * a.scale * chunk_sign<H>(sb, j);
-            ss += v[j] * v[j];
-        }
-        // h may overwrite z_a: this warp read its whole chunk above
-#pragma unroll
-        for (int h = 0; h < H; ++h) {
-            if (!have[h]) continue;
-            float4* hp = reinterpret_cast<float4*>(a.h + row + 256 * h + 8 * lane);
-            hp[0] = make_float4(v[8 * h + 0], v[8 * h + 1], v[8 * h + 2], v[8 * h + 3]);
-            hp[1] = make_float4(v[8 * h + 4], v[8 * h + 5], v[8 * h + 6], v[8 * h + 7]);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    if (threadIdx.x == 0) {                            // the warps' sums in a fixed order
-        float tot = 0.0f;
-        for (int i = 0; i < kWarps; ++i) tot += red[i];
-        a.work[blockIdx.x] = tot;
-    }
-}
-
-template <int H>
-__device__ __forceinline__ void glue_in_reg(const GlueArgs& a, const GlueNext& nx, int t, int seg0, int rem,
-                                            int per_next) {
-    constexpr int W = 256 * H, NR = 8 * H;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int c0 = seg0 + warp * W;
-    const bool active = warp * W < kSeg && c0 < a.M;
-    bool have[H];
-    uint2 sg[H];
-#pragma unroll
-    for (int h = 0; h < H; ++h) {
-        const int col = c0 + 256 * h + 8 * lane;
-        have[h] = active && col < a.M;
-        sg[h] = have[h] ? *reinterpret_cast<const uint2*>(nx.sign_in + col) : make_uint2(0u, 0u);
-    }
-    grid_dep_wait();                 // h and the segment sums come from k_glue_out
-    float v[NR];
-    if (active) load_chunk<H>(a.h + (size_t)t * a.M + c0, have, lane, v);
-    // this CTA's share of the next GEMM's accumulator, after the loads
-    if (nx.zero_out != nullptr) clear_share<kThreads>(nx.zero_out, nx.zero_count, rem, per_next);
-    if (!active) return;
-    // the token's sum of squares: every warp adds the segment sums in the same tree order
-    float ss = 0.0f;
-    for (int i = lane; i < a.nseg; i += 32) ss += __ldcg(a.work + t * a.nseg + i);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float rms = sqrtf(ss / (float)a.M);
-    const float inv = rms > 0.0f ? 1.0f / rms : 0.0f;
-#pragma unroll
-    for (int j = 0; j < NR; ++j)
-        v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * inv)) * chunk_sign<H>(sg, j);
-    chunk_fwht<H>(v, a.L, lane);
-#pragma unroll
-    for (int h = 0; h < H; ++h) {
-        if (!have[h]) continue;
-        const int col = c0 + 256 * h + 8 * lane;
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            w[e] = h2_as_u32(__floats2half2_rn(v[8 * h + 2 * e] * a.scale, v[8 * h + 2 * e + 1] * a.scale));
-        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(nx.xop) + xop_offset(col, t, a.NB)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -261,6 +166,118 @@ __device__ __forceinline__ void glue_in_seg(const GlueArgs& a, const GlueNext& n
         make_uint4(q[0], q[1], q[2], q[3]);
 }
 
+// Small launch shape for the register path (GlueArgs::path 3): CTAs of two warps with no
+// shared memory, each warp one (token, chunk of W = max(b, 256) elements), small enough to
+// become resident beside a running GEMM.  With no CTA-wide reduction, k_glue_out_small
+// writes one sum of squares per (token, chunk) (work [T][nchunk]) and k_glue_in_small adds a
+// token's nchunk partial sums with a fixed shuffle tree in every warp.
+constexpr int kSmallWarps = 2;
+
+template <bool PROD, int H>
+__device__ __forceinline__ void glue_out_small(const GlueArgs& a) {
+    constexpr int W = 256 * H, NR = 8 * H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int item = blockIdx.x * kSmallWarps + warp;
+    if (item >= a.T * a.nchunk) return;              // the same for the whole warp
+    const int t = item / a.nchunk, c = item - t * a.nchunk;
+    const int c0 = c * W, M = a.M;
+    bool have[H];
+    uint2 sa[H], sb[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const int col = c0 + 256 * h + 8 * lane;
+        have[h] = col < M;
+        sa[h] = have[h] ? *reinterpret_cast<const uint2*>(a.sa + col) : make_uint2(0u, 0u);
+        sb[h] = (PROD && have[h]) ? *reinterpret_cast<const uint2*>(a.sb + col) : make_uint2(0u, 0u);
+    }
+    grid_dep_wait();                 // z_a, z_b come from the GEMM before this launch
+    const size_t row = (size_t)t * M + c0;
+    float v[NR], w[NR];
+    load_chunk<H>(a.za + row, have, lane, v);
+    if constexpr (PROD) load_chunk<H>(a.zb + row, have, lane, w);
+    chunk_fwht<H>(v, a.L, lane);
+    if constexpr (PROD) chunk_fwht<H>(w, a.L, lane);
+    float ss = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+        v[j] *= a.scale * chunk_sign<H>(sa, j);
+        if constexpr (PROD) v[j] *= w[j] * a.scale * chunk_sign<H>(sb, j);
+        ss += v[j] * v[j];
+    }
+    // h may overwrite z_a: this warp read its whole chunk above
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        if (!have[h]) continue;
+        float4* hp = reinterpret_cast<float4*>(a.h + row + 256 * h + 8 * lane);
+        hp[0] = make_float4(v[8 * h + 0], v[8 * h + 1], v[8 * h + 2], v[8 * h + 3]);
+        hp[1] = make_float4(v[8 * h + 4], v[8 * h + 5], v[8 * h + 6], v[8 * h + 7]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) a.work[item] = ss;
+}
+
+template <int H>
+__device__ __forceinline__ void glue_in_small(const GlueArgs& a) {
+    constexpr int W = 256 * H, NR = 8 * H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per_next = (a.T * a.nchunk + kSmallWarps - 1) / kSmallWarps;   // CTAs of one next linear
+    const int jn = blockIdx.x / per_next, lc = blockIdx.x - jn * per_next;
+    const GlueNext& nx = a.next[jn];
+    const int item = lc * kSmallWarps + warp;
+    const bool active = item < a.T * a.nchunk;         // the same for the whole warp
+    const int t = active ? item / a.nchunk : 0, c = active ? item - t * a.nchunk : 0;
+    const int c0 = c * W, M = a.M;
+    bool have[H];
+    uint2 sg[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const int col = c0 + 256 * h + 8 * lane;
+        have[h] = active && col < M;
+        sg[h] = have[h] ? *reinterpret_cast<const uint2*>(nx.sign_in + col) : make_uint2(0u, 0u);
+    }
+    grid_dep_wait();                 // h and the chunk sums come from k_glue_out_small
+    float v[NR];
+    if (active) load_chunk<H>(a.h + (size_t)t * M + c0, have, lane, v);
+    // this CTA's share of the next GEMM's accumulator, after the loads
+    if (nx.zero_out != nullptr) clear_share<32 * kSmallWarps>(nx.zero_out, nx.zero_count, lc, per_next);
+    if (!active) return;
+    float ss = 0.0f;
+    for (int i = lane; i < a.nchunk; i += 32) ss += __ldcg(a.work + t * a.nchunk + i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rms = sqrtf(ss / (float)M);
+    const float inv = rms > 0.0f ? 1.0f / rms : 0.0f;
+#pragma unroll
+    for (int j = 0; j < NR; ++j)
+        v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * inv)) * chunk_sign<H>(sg, j);
+    chunk_fwht<H>(v, a.L, lane);
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        if (!have[h]) continue;
+        const int col = c0 + 256 * h + 8 * lane;
+        uint32_t q[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            q[e] = h2_as_u32(__floats2half2_rn(v[8 * h + 2 * e] * a.scale, v[8 * h + 2 * e + 1] * a.scale));
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(nx.xop) + xop_offset(col, t, a.NB)) =
+            make_uint4(q[0], q[1], q[2], q[3]);
+    }
+}
+
+template <bool PROD>
+__global__ void __launch_bounds__(32 * kSmallWarps) k_glue_out_small(const __grid_constant__ GlueArgs a) {
+    grid_dep_launch_dependents();
+    if (a.L <= 8) glue_out_small<PROD, 1>(a);
+    else glue_out_small<PROD, 2>(a);
+}
+
+__global__ void __launch_bounds__(32 * kSmallWarps) k_glue_in_small(const __grid_constant__ GlueArgs a) {
+    grid_dep_launch_dependents();
+    if (a.L <= 8) glue_in_small<1>(a);
+    else glue_in_small<2>(a);
+}
+
 template <bool PROD>
 __global__ void __launch_bounds__(kThreads) k_glue_out(const __grid_constant__ GlueArgs a) {
     __shared__ __align__(16) float buf[64][65];
@@ -271,11 +288,6 @@ __global__ void __launch_bounds__(kThreads) k_glue_out(const __grid_constant__ G
     const int seg0 = s * kSeg;
     if (a.path == 2) {
         glue_out_seg<PROD>(a, t, seg0, &buf[0][0], &buf2[0][0], red);
-        return;
-    }
-    if (a.path == 1) {
-        if (a.L <= 8) glue_out_reg<PROD, 1>(a, t, seg0, red);
-        else glue_out_reg<PROD, 2>(a, t, seg0, red);
         return;
     }
     const int count = a.M - seg0 < kSeg ? a.M - seg0 : kSeg;
@@ -329,11 +341,6 @@ __global__ void __launch_bounds__(kThreads) k_glue_in(const __grid_constant__ Gl
         glue_in_seg(a, nx, t, seg0, rem, per_next, &buf[0][0]);
         return;
     }
-    if (a.path == 1) {
-        if (a.L <= 8) glue_in_reg<1>(a, nx, t, seg0, rem, per_next);
-        else glue_in_reg<2>(a, nx, t, seg0, rem, per_next);
-        return;
-    }
     const int count = a.M - seg0 < kSeg ? a.M - seg0 : kSeg;
     const size_t row = (size_t)t * a.M + seg0;
     grid_dep_wait();                 // h and the segment sums come from k_glue_out
@@ -384,6 +391,16 @@ __global__ void __launch_bounds__(kThreads) k_glue_in(const __grid_constant__ Gl
 }  // namespace
 
 int glue_segments(int M) { return (M + kSeg - 1) / kSeg; }
+int glue_work_floats(int M, int T) {
+    // one partial sum per (token, chunk) on the register path (b <= 512), else per (token,
+    // 4096-element segment); a call may fall back from the register path to the tile path
+    const int segs = glue_segments(M), b = hadamard_block(M);
+    if (b > 512) return T * segs;
+    int L = 0;
+    while ((1 << L) < b) ++L;
+    const int chunks = (M + reg_chunk(L) - 1) / reg_chunk(L);
+    return T * (chunks > segs ? chunks : segs);
+}
 
 cudaError_t launch_glue(GlueArgs& a, cudaStream_t stream) {
     const int b = hadamard_block(a.M);
@@ -397,7 +414,16 @@ cudaError_t launch_glue(GlueArgs& a, cudaStream_t stream) {
     bool reg = b <= 512 && a.M % 8 == 0 && al(a.za, 16) && al(a.zb, 16) && al(a.h, 16) && al(a.sa, 8) && al(a.sb, 8);
     for (int j = 0; j < a.nnext; ++j) reg = reg && al(a.next[j].sign_in, 8);
     const bool seg = b >= 1024 && al(a.h, 16) && al(a.sa, 8) && al(a.sb, 8);
-    a.path = reg ? 1 : (seg ? 2 : 0);
+    a.path = reg ? 3 : (seg ? 2 : 0);
+    a.nchunk = (a.M + reg_chunk(L) - 1) / reg_chunk(L);
+    if (a.path == 3) {                 // two-warp CTAs, one (token, chunk) per warp
+        const int ctas = (a.T * a.nchunk + kSmallWarps - 1) / kSmallWarps;
+        const dim3 sblk(32 * kSmallWarps);
+        cudaError_t e = a.zb != nullptr ? launch_pdl(k_glue_out_small<true>, dim3(ctas), sblk, 0, stream, a)
+                                        : launch_pdl(k_glue_out_small<false>, dim3(ctas), sblk, 0, stream, a);
+        if (e != cudaSuccess || a.nnext == 0) return e;
+        return launch_pdl(k_glue_in_small, dim3(a.nnext * ctas), sblk, 0, stream, a);
+    }
     const dim3 blk(kThreads);
     cudaError_t e = a.zb != nullptr ? launch_pdl(k_glue_out<true>, dim3(a.T * a.nseg), blk, 0, stream, a)
                                     : launch_pdl(k_glue_out<false>, dim3(a.T * a.nseg), blk, 0, stream, a);

@@ -102,11 +102,12 @@ struct GlueArgs {
     float* h;                 // glue output before the RMS rescale, [T][M] (may be za)
     float* work;              // [T][nseg] segment sums of squares
     GlueNext next[kMaxChainNext];
-    int nnext, M, T, L, NB, nseg;
+    int nnext, M, T, L, NB, nseg, nchunk;
     float scale;
-    int path;                 // 0 shared-memory tile, 1 register (b <= 512), 2 segment (b >= 1024)
+    int path;                 // 0 shared-memory tile, 2 segment (b >= 1024), 3 register with two-warp CTAs (b <= 512)
 };
 int glue_segments(int M);     // 4096-element segments per token
+int glue_work_floats(int M, int T);   // floats of the work buffer of a glue call
 cudaError_t launch_glue(GlueArgs& a, cudaStream_t stream);
 
 cudaError_t launch_pack(const uint8_t* bc, const uint16_t* bs, const int8_t* rc, const uint16_t* rs,

@@ -115,7 +115,10 @@ def test_rotate_pack_quantize_validation(lib):
 
 def test_chain_and_rotate_group_validation(lib):
     ok = ctypes.c_void_p(0x50000)
-    assert lib.nest_chain_work_bytes(5376, 64) == 256 * ((64 * 2 * 4 + 255) // 256)
+    # one fp32 partial per (token, 256-element chunk) or per (token, 4096-element segment),
+    # whichever is more, rounded up to 256 bytes
+    assert lib.nest_chain_work_bytes(5376, 64) == 256 * ((64 * 21 * 4 + 255) // 256)
+    assert lib.nest_chain_work_bytes(300, 3) == 256 * ((3 * 2 * 4 + 255) // 256)
     assert lib.nest_chain_work_bytes(21504, 64) == 64 * 6 * 4
     assert lib.nest_chain_work_bytes(100, 257) == 0
     L = nest._Layer(256, 512, 0, 0x50000, None, 0x50000, 0x50000)
