@@ -10,12 +10,12 @@
 // in for the normalisation between them) is not on the pages; it is the plain
 // reading used by the chained-layer workload.
 //
-// Two launches, both spread over every (token, 4096-element segment) pair so that
-// a single token still occupies many SMs.  For blocks of up to 512 elements the
-// butterflies run in registers, one warp per (token, chunk of max(b, 256) elements), in
-// CTAs of two warps (the register path below); for blocks of 1024 to 4096 a segment is
-// 16 rows x 256 columns with one pass through shared memory (the segment path);
-// otherwise:
+// Two launches (out, then in), both spread over the token's elements so that a single
+// token still occupies many SMs.  For blocks of up to 512 elements the butterflies run in
+// registers, one warp per (token, chunk of max(b, 256) elements), in CTAs of two warps
+// without shared memory (the register path below; one partial sum of squares per chunk);
+// for blocks of 1024 to 4096 one CTA takes a (token, 4096-element segment) as 16 rows x 256
+// columns with one pass through shared memory (the segment path); otherwise:
 //   k_glue_out: one CTA per (t, segment) rotates its segment of z_a (and z_b) in a
 //               64 x 64 shared-memory tile, writes h and the segment's sum of
 //               squares.  A segment is a whole number of Hadamard blocks (the block

@@ -8,7 +8,8 @@
 // Three ways, chosen per vector set of a launch:
 // - blocks of at most 512 (and n % 8 == 0, 16-byte aligned vectors, 8-byte aligned
 //   signs): each warp takes one (token, chunk of max(b, 256) elements) and runs the
-//   butterflies in registers and warp shuffles, with no shared memory and no barrier;
+//   butterflies in registers and warp shuffles, with no shared memory and no barrier
+//   (in CTAs of two warps, k_rotate_small, when every set of the launch takes this path);
 // - blocks of 1024 to 4096 (aligned output and signs): one CTA per (token, 4096-element
 //   segment), butterflies over the high index bits per column, one pass through shared
 //   memory, then the low 8 bits along rows (rotate_seg);
