@@ -243,7 +243,8 @@ nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t v
  *   and for each of n_next (0..3) next linears j: x'_j = H_i S_i h' written as its GEMM operand.
  * The rotations are those of POC recipe steps 1 and 4 (feedman.me/posts/wZBTJ); the chaining
  * and the RMS rescale are the chained-layer workload's reading, not the pages'.
- * Two launches (rotation out with per-segment sums of squares; rescale, cast and rotation in).
+ * Two launches (rotation out with partial sums of squares per token and chunk or segment;
+ * rescale, cast and rotation in).
  * z_a           fp32 [T][M] GEMM accumulator of linear a (rotated basis).  When y is NULL, h
  *               overwrites z_a.
  * z_b           NULL, or the accumulator of the product partner (fp32 [T][M], read only);
@@ -254,8 +255,10 @@ nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t v
  * x_ops         host array of n_next operand buffers (out, nest_xop_bytes(M, T) bytes each).
  * z_next        NULL, or host array of n_next accumulators (fp32 [T][next[j].M], or NULL entries)
  *               that are cleared here for the GEMMs that follow.
- * work          nest_chain_work_bytes(M, T) bytes of device memory, no initial contents; calls
- *               whose work may overlap on the GPU need separate work buffers.
+ * work          nest_chain_work_bytes(M, T) bytes of device memory (one fp32 partial sum of
+ *               squares per token and 256/512-element chunk when the block size is at most 512,
+ *               else per token and 4096-element segment), no initial contents; calls whose work
+ *               may overlap on the GPU need separate work buffers.
  * Limits: T <= 256, M * T < 2^31, M % 128 == 0 when n_next > 0. */
 size_t nest_chain_work_bytes(int32_t M, int32_t T);
 nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,
