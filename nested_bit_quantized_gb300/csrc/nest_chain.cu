@@ -12,7 +12,7 @@
 //
 // Two launches (out, then in), both spread over the token's elements so that a single
 // token still occupies many SMs.  For blocks of up to 512 elements the butterflies run in
-// registers, one warp per (token, chunk of max(b, 256) elements), in CTAs of two warps
+// registers, one warp per (token, chunk of max(b, 256) elements), in CTAs of one warp
 // without shared memory (the register path below; one partial sum of squares per chunk);
 // for blocks of 1024 to 4096 one CTA takes a (token, 4096-element segment) as 16 rows x 256
 // columns with one pass through shared memory (the segment path); otherwise:
@@ -166,12 +166,12 @@ __device__ __forceinline__ void glue_in_seg(const GlueArgs& a, const GlueNext& n
         make_uint4(q[0], q[1], q[2], q[3]);
 }
 
-// Small launch shape for the register path (GlueArgs::path 3): CTAs of two warps with no
+// Small launch shape for the register path (GlueArgs::path 3): CTAs of one warp with no
 // shared memory, each warp one (token, chunk of W = max(b, 256) elements), small enough to
 // become resident beside a running GEMM.  With no CTA-wide reduction, k_glue_out_small
 // writes one sum of squares per (token, chunk) (work [T][nchunk]) and k_glue_in_small adds a
 // token's nchunk partial sums with a fixed shuffle tree in every warp.
-constexpr int kSmallWarps = 2;
+constexpr int kSmallWarps = 1;
 
 template <bool PROD, int H>
 __device__ __forceinline__ void glue_out_small(const GlueArgs& a) {

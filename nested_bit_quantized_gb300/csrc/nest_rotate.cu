@@ -9,7 +9,7 @@
 // - blocks of at most 512 (and n % 8 == 0, 16-byte aligned vectors, 8-byte aligned
 //   signs): each warp takes one (token, chunk of max(b, 256) elements) and runs the
 //   butterflies in registers and warp shuffles, with no shared memory and no barrier
-//   (in CTAs of two warps, k_rotate_small, when every set of the launch takes this path);
+//   (in CTAs of one warp, k_rotate_small, when every set of the launch takes this path);
 // - blocks of 1024 to 4096 (aligned output and signs): one CTA per (token, 4096-element
 //   segment), butterflies over the high index bits per column, one pass through shared
 //   memory, then the low 8 bits along rows (rotate_seg);
@@ -175,12 +175,12 @@ __device__ __forceinline__ void rotate_seg(const RotTask& tk, unsigned cta, floa
     }
 }
 
-// Launches whose vector sets all take the register path: CTAs of two warps with no shared
-// memory, small enough to become resident on an SM beside the GEMM's two CTAs, so that
-// the launch's CTAs are in place, signs loaded, when the GEMM before them completes (and
-// leave the GEMM after them every SM).
-constexpr int kSmallWarps = 2;
-constexpr long long kSmallClear = 2048;      // floats a small CTA clears at most
+// Launches whose vector sets all take the register path: CTAs of one warp with no shared
+// memory (1280 registers), small enough that several become resident on an SM beside the
+// GEMM's two CTAs, so that the launch's CTAs are in place, signs loaded, when the GEMM
+// before them completes (and leave the GEMM after them every SM).
+constexpr int kSmallWarps = 1;
+constexpr long long kSmallClear = 1024;      // floats a small CTA clears at most
 
 template <int MODE, bool BF16>
 __global__ void __launch_bounds__(32 * kSmallWarps)
