@@ -176,9 +176,9 @@ __device__ __forceinline__ void rotate_seg(const RotTask& tk, unsigned cta, floa
 }
 
 // Launches whose vector sets all take the register path: CTAs of one warp with no shared
-// memory (1280 registers), small enough that several become resident on an SM beside the
-// GEMM's two CTAs, so that the launch's CTAs are in place, signs loaded, when the GEMM
-// before them completes (and leave the GEMM after them every SM).
+// memory, small enough that two become resident on an SM beside the GEMM's two CTAs, so
+// that the launch's CTAs are in place, signs loaded, when the GEMM before them completes
+// (and leave the GEMM after them every SM).
 constexpr int kSmallWarps = 1;
 constexpr long long kSmallClear = 1024;      // floats a small CTA clears at most
 
