@@ -416,7 +416,7 @@ cudaError_t launch_glue(GlueArgs& a, cudaStream_t stream) {
     const bool seg = b >= 1024 && al(a.h, 16) && al(a.sa, 8) && al(a.sb, 8);
     a.path = reg ? 3 : (seg ? 2 : 0);
     a.nchunk = (a.M + reg_chunk(L) - 1) / reg_chunk(L);
-    if (a.path == 3) {                 // two-warp CTAs, one (token, chunk) per warp
+    if (a.path == 3) {                 // one-warp CTAs, one (token, chunk) per warp
         const int ctas = (a.T * a.nchunk + kSmallWarps - 1) / kSmallWarps;
         const dim3 sblk(32 * kSmallWarps);
         cudaError_t e = a.zb != nullptr ? launch_pdl(k_glue_out_small<true>, dim3(ctas), sblk, 0, stream, a)
