@@ -347,6 +347,14 @@ nest_status nest_kv_attention(const void* q, int32_t q_dtype, int32_t T, int32_t
  * the flag was set, NEST_ERR_CUDA on a CUDA error, NEST_OK otherwise. */
 nest_status nest_error_check(void* stream);
 
+/* The give-up path of the kernels' bounded waits, exercised without a fault: launches
+ * one warp that waits, through the same bounded wait as the GEMM pipelines, on a
+ * barrier that nothing arrives on.  The wait gives up after its limit (2 s), raises
+ * the device error flag and the kernel returns, so the context stays usable and the
+ * next nest_error_check returns NEST_ERR_TIMEOUT (and clears the flag).
+ * Asynchronous on `stream`; NEST_ERR_CUDA if the launch fails. */
+nest_status nest_wait_selftest(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -493,4 +493,8 @@ nest_status nest_error_check(void* stream) {
     return flag ? NEST_ERR_TIMEOUT : NEST_OK;
 }
 
+nest_status nest_wait_selftest(void* stream) {
+    return from_cuda(launch_wait_selftest(as_stream(stream)));
+}
+
 }  // extern "C"

@@ -74,6 +74,21 @@ __device__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, bo
     }
 }
 
+// The give-up path of the bounded wait, on its own: one warp waits on a barrier that
+// nothing arrives on, so the wait runs out after kWaitLimitNs, raises the CTA's abort
+// flag and the device error flag, and the kernel returns normally.
+__global__ void __launch_bounds__(32) k_wait_selftest() {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    warp_wait(smem_u32(&bar), 0, &abort_flag);
+}
+
 // Weight codecs of the GEMM kernels (template parameter BITS):
 //   0        2-bit Lloyd-Max base only (draft)
 //   6, 7, 8  2-bit base + b-bit uniform residual (verify)
@@ -1043,6 +1058,11 @@ cudaError_t launch_gemm(const GemmArgs& a, int bits, int grid, cudaStream_t stre
 }
 
 int gemm_ctas_per_sm(int T) { return T > 64 ? 1 : kGemmCtasPerSm; }
+
+cudaError_t launch_wait_selftest(cudaStream_t stream) {
+    k_wait_selftest<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+}
 
 cudaError_t read_and_clear_error(int* flag, cudaStream_t stream) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_nest_error, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);

@@ -77,6 +77,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_gemm(const GemmArgs& a, int bits, int grid, cudaStream_t stream);
 constexpr int kMaxGemmTasks = kMaxTasks;
 cudaError_t read_and_clear_error(int* flag, cudaStream_t stream);
+cudaError_t launch_wait_selftest(cudaStream_t stream);
 
 // zero_out (optional): a buffer of zero_count floats the kernel also clears (the
 // accumulator of the GEMM that follows it).

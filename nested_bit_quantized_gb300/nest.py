@@ -95,6 +95,7 @@ def load() -> ctypes.CDLL:
         "nest_kv_attention": ([_P, _I32, _I32, _I32, ctypes.POINTER(_KvCache), ctypes.POINTER(_KvCache), _I32, _I32,
                                _I32, _P, _P, _P], _I32),
         "nest_error_check": ([_P], _I32),
+        "nest_wait_selftest": ([_P], _I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -367,6 +368,12 @@ def linear(layer: Layer, x: torch.Tensor, verify: bool, y: Optional[torch.Tensor
 
 def error_check(stream=None) -> None:
     _check(load().nest_error_check(_stream(stream)), "nest_error_check")
+
+
+def wait_selftest(stream=None) -> None:
+    """Launch the bounded-wait give-up check (nest_wait_selftest); the next error_check
+    raises NestError with status 5 (timeout)."""
+    _check(load().nest_wait_selftest(_stream(stream)), "nest_wait_selftest")
 
 
 # ---------------------------------------------------------------------------
