@@ -42,8 +42,8 @@ PREFILL_T = (128, 256)
 # dram__bytes_write.sum of a grouped gate+up verify launch at T=16, divided by its two
 # linears).  Valid only for the kernel source it was taken on: reported as null otherwise.
 NCU_TRAFFIC = {"src": "nested_bit_quantized_gb300/csrc/nest_gemm.cu",
-               "sha256": "cf8d19861606cd7e5671a2ef0e1ebc5e4d713c30cbea8c0d5982aef012079c3d",
-               "bytes_per_linear": (59.046912e6 + 0.007680e6) / 2}
+               "sha256": "c5dbe9c81dfdf5262491e54484328e5ac759a9f27a0f16d45e236c909c77002f",
+               "bytes_per_linear": (59.046400e6 + 0.015872e6) / 2}
 
 
 def ncu_traffic():

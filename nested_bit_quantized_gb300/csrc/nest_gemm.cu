@@ -184,65 +184,61 @@ __device__ __forceinline__ void dequant_half_w4(const uint8_t* sb, const uint8_t
     }
 }
 
-// Decode 64 columns (half h of the 128-column group) of row r of one unit into
-// 32 fp16x2 registers: w = s_b * L[code] (+ s_r * q).
+// Decode 32 columns (quarter qq of half h of the 128-column group) of row r of one unit
+// into 16 fp16x2 registers: w = s_b * L[code] (+ s_r * q).  Quarter-size pieces keep 16
+// results live instead of 32, which takes the kernel from 96 to 79 registers at b = 7 and
+// leaves room on the SM for the small rotation CTAs that run beside it.  Local index l
+// stands for qd = 8 qq + l of the half; every shift below depends on qd & 7 = l only.
 template <int BITS>
-__device__ __forceinline__ void dequant_half(const uint8_t* sb, const uint8_t* sr, int r, int h,
-                                             uint32_t lut_lo, uint32_t lut_hi, __half2 sr2, __half2 off2,
-                                             uint32_t (&out)[32]) {
-    const uint4 bw4 = *reinterpret_cast<const uint4*>(sb + (h * kRows + r) * 16);
-    const uint32_t bw[4] = {bw4.x, bw4.y, bw4.z, bw4.w};
-    uint32_t rw[16];
-    uint32_t mid[4], hi[2];
+__device__ __forceinline__ void dequant_quarter(const uint8_t* sb, const uint8_t* sr, int r, int h, int qq,
+                                                uint32_t lut_lo, uint32_t lut_hi, __half2 sr2, __half2 off2,
+                                                uint32_t (&out)[16]) {
+    const uint2 bw2 = *reinterpret_cast<const uint2*>(sb + (h * kRows + r) * 16 + 8 * qq);
+    const uint32_t bw[2] = {bw2.x, bw2.y};
+    uint32_t rw[8];
+    uint32_t mid[2], hi = 0;
     if constexpr (BITS == 8) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(sr + ((4 * h + c) * kRows + r) * 16);
+        for (int c = 0; c < 2; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sr + ((4 * h + 2 * qq + c) * kRows + r) * 16);
             rw[4 * c] = v.x; rw[4 * c + 1] = v.y; rw[4 * c + 2] = v.z; rw[4 * c + 3] = v.w;
         }
     } else if constexpr (BITS == 6 || BITS == 7) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(sr + ((2 * h + c) * kRows + r) * 16);
-            rw[4 * c] = v.x; rw[4 * c + 1] = v.y; rw[4 * c + 2] = v.z; rw[4 * c + 3] = v.w;
-        }
-        const uint4 m = *reinterpret_cast<const uint4*>(sr + ((4 + h) * kRows + r) * 16);
-        mid[0] = m.x; mid[1] = m.y; mid[2] = m.z; mid[3] = m.w;
-        if constexpr (BITS == 7) {
-            const uint2 o = *reinterpret_cast<const uint2*>(sr + (6 * kRows + r) * 16 + 8 * h);
-            hi[0] = o.x; hi[1] = o.y;
-        }
+        const uint4 v = *reinterpret_cast<const uint4*>(sr + ((2 * h + qq) * kRows + r) * 16);
+        rw[0] = v.x; rw[1] = v.y; rw[2] = v.z; rw[3] = v.w;
+        const uint2 m = *reinterpret_cast<const uint2*>(sr + ((4 + h) * kRows + r) * 16 + 8 * qq);
+        mid[0] = m.x; mid[1] = m.y;
+        if constexpr (BITS == 7) hi = *reinterpret_cast<const uint32_t*>(sr + (6 * kRows + r) * 16 + 8 * h + 4 * qq);
     }
 #pragma unroll
-    for (int qd = 0; qd < 16; ++qd) {
-        // base: bytes of v hold the codes of columns 4Q .. 4Q+3 (Q = 16h + qd)
-        const uint32_t v = (bw[qd >> 2] >> (2 * (qd & 3))) & 0x03030303u;
+    for (int l = 0; l < 8; ++l) {
+        // base: bytes of v hold the codes of columns 4Q .. 4Q+3 (Q = 16h + 8qq + l)
+        const uint32_t v = (bw[l >> 2] >> (2 * (l & 3))) & 0x03030303u;
         const uint32_t sel = v * 0x11u + 0x40404040u;
         const uint32_t b01 = prmt(lut_lo, lut_hi, sel);
         const uint32_t b23 = prmt(lut_lo, lut_hi, sel >> 16);
         if constexpr (BITS == 0) {
-            out[2 * qd] = b01;
-            out[2 * qd + 1] = b23;
+            out[2 * l] = b01;
+            out[2 * l + 1] = b23;
         } else {
             uint32_t u;
             if constexpr (BITS == 8) {
-                u = rw[qd];
+                u = rw[l];
             } else {
-                const uint32_t lo = (rw[qd >> 1] >> (4 * (qd & 1))) & 0x0F0F0F0Fu;
-                const int pm = qd & 3;
-                const uint32_t ms = pm < 2 ? (mid[qd >> 2] << (4 - 2 * pm)) : (mid[qd >> 2] >> (2 * pm - 4));
+                const uint32_t lo = (rw[l >> 1] >> (4 * (l & 1))) & 0x0F0F0F0Fu;
+                const int pm = l & 3;
+                const uint32_t ms = pm < 2 ? (mid[l >> 2] << (4 - 2 * pm)) : (mid[l >> 2] >> (2 * pm - 4));
                 u = lo | (ms & 0x30303030u);
                 if constexpr (BITS == 7) {
-                    const int ph = qd & 7;
-                    const uint32_t hs = ph < 7 ? (hi[qd >> 3] << (6 - ph)) : (hi[qd >> 3] >> 1);
+                    const uint32_t hs = l < 7 ? (hi << (6 - l)) : (hi >> 1);
                     u |= hs & 0x40404040u;
                 }
             }
             // 1024 + u as fp16 (exact), minus 1024 + 2^(b-1), gives q exactly
             const __half2 q01 = __hsub2(u32_as_h2(prmt(u, 0x64646464u, 0x5140u)), off2);
             const __half2 q23 = __hsub2(u32_as_h2(prmt(u, 0x64646464u, 0x7362u)), off2);
-            out[2 * qd] = h2_as_u32(__hfma2(q01, sr2, u32_as_h2(b01)));
-            out[2 * qd + 1] = h2_as_u32(__hfma2(q23, sr2, u32_as_h2(b23)));
+            out[2 * l] = h2_as_u32(__hfma2(q01, sr2, u32_as_h2(b01)));
+            out[2 * l + 1] = h2_as_u32(__hfma2(q23, sr2, u32_as_h2(b23)));
         }
     }
 }
@@ -514,9 +510,13 @@ k_nest_gemm(const __grid_constant__ GemmArgs p) {
 #pragma unroll
                     for (int j = 0; j < kHalves; ++j) {
                         const int hh = h_first + j;
-                        uint32_t w[32];
-                        dequant_half<BITS>(sb, sr, r, hh, lut_lo, lut_hi, sr2, off2, w);
-                        tmem_st32_wait(tmem + lane_base + C::kColA + 64 * a + 32 * hh, w);
+#pragma unroll
+                        for (int qq = 0; qq < 2; ++qq) {
+                            uint32_t w[16];
+                            dequant_quarter<BITS>(sb, sr, r, hh, qq, lut_lo, lut_hi, sr2, off2, w);
+                            tmem_st16(tmem + lane_base + C::kColA + 64 * a + 32 * hh + 16 * qq, w);
+                        }
+                        tc_wait_st();
                     }
                 }
                 mbar_arrive(empty_w(s));             // this thread is done with the weight stage
