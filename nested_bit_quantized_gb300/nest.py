@@ -128,6 +128,39 @@ def _dev(t: torch.Tensor, dtype, name: str):
     return t
 
 
+def _buf(t, name: str, nbytes: int = 0, dtype=None):
+    """Check a tensor whose pointer goes to the library: contiguous, of `dtype` when given,
+    at least `nbytes` bytes, on the device.  The library sees only the pointer, so a short
+    or host buffer would be read or written out of bounds by a kernel.  The size is checked
+    before the device, so the checks can be exercised without a GPU."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes, needs {nbytes}")
+    _require_cuda(t, name)
+    return t
+
+
+def _require_cuda(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _act(x, name: str, T: int, K: int):
+    """An activation block [T][K] of bf16 or fp32; returns the library's dtype code."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 2 or x.shape[0] != T or x.shape[1] != K:
+        raise ValueError(f"{name} must be a [{T}][{K}] tensor, got {tuple(getattr(x, 'shape', ()))}")
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError(f"{name} must be float32 or bfloat16")
+    _buf(x, name)
+    return 1 if x.dtype == torch.bfloat16 else 0
+
+
 # ---------------------------------------------------------------------------
 # sizes
 # ---------------------------------------------------------------------------
@@ -165,12 +198,13 @@ def quantize(W: torch.Tensor, sign_out: torch.Tensor, sign_in: torch.Tensor, bit
              work: Optional[torch.Tensor] = None, stream=None) -> dict:
     """RTN quantizer on the device (nest_quantize).  Returns codes and fp16 scale bits."""
     _dev(W, torch.float32, "W")
-    _dev(sign_out, torch.int8, "sign_out")
-    _dev(sign_in, torch.int8, "sign_in")
     M, K = W.shape
+    _buf(sign_out, "sign_out", M, torch.int8)
+    _buf(sign_in, "sign_in", K, torch.int8)
     dev = W.device
     if work is None:
         work = torch.empty((M, K), dtype=torch.float64, device=dev)
+    _buf(work, "work", 8 * M * K, torch.float64)
     out = {
         "base_codes": torch.empty((M, K), dtype=torch.uint8, device=dev),
         "base_scales": torch.empty((M, K // 128), dtype=torch.int16, device=dev),
@@ -212,6 +246,12 @@ def pack(base_codes: torch.Tensor, base_scales: torch.Tensor, resid_codes: Optio
     """Pack device codes/scales into the unit format (nest_pack)."""
     _dev(base_codes, torch.uint8, "base_codes")
     M, K = base_codes.shape
+    _buf(base_scales, "base_scales", 2 * M * (K // 128))
+    if bits:
+        _buf(resid_codes, "resid_codes", M * K)
+        _buf(resid_scales, "resid_scales", 2 * M * (K // 128))
+    _buf(sign_out, "sign_out", M, torch.int8)
+    _buf(sign_in, "sign_in", K, torch.int8)
     dev = base_codes.device
     base = _u8(base_bytes(M, K), dev)
     resid = _u8(resid_bytes(M, K, bits), dev) if bits else None
@@ -225,12 +265,13 @@ def quantize_w4w8(W: torch.Tensor, sign_out: torch.Tensor, sign_in: torch.Tensor
                   work: Optional[torch.Tensor] = None, stream=None) -> dict:
     """BitNest W4/W8 quantizer on the device (nest_quantize_w4w8): q4, s4 (fp16 bits), q_r."""
     _dev(W, torch.float32, "W")
-    _dev(sign_out, torch.int8, "sign_out")
-    _dev(sign_in, torch.int8, "sign_in")
     M, K = W.shape
+    _buf(sign_out, "sign_out", M, torch.int8)
+    _buf(sign_in, "sign_in", K, torch.int8)
     dev = W.device
     if work is None:
         work = torch.empty((M, K), dtype=torch.float64, device=dev)
+    _buf(work, "work", 8 * M * K, torch.float64)
     out = {"q4": torch.empty((M, K), dtype=torch.int8, device=dev),
            "s4": torch.empty((M, K // 128), dtype=torch.int16, device=dev),
            "qr": torch.empty((M, K), dtype=torch.int8, device=dev) if refine else None}
@@ -245,6 +286,11 @@ def pack_w4w8(q4: torch.Tensor, s4: torch.Tensor, qr: Optional[torch.Tensor], si
     """Dual-plane packing (nest_pack_w4w8); a layer of codec W4W8 (resid_bits 4, or 0 without q_r)."""
     _dev(q4, torch.int8, "q4")
     M, K = q4.shape
+    _buf(s4, "s4", 2 * M * (K // 128))
+    if qr is not None:
+        _buf(qr, "qr", M * K)
+    _buf(sign_out, "sign_out", M, torch.int8)
+    _buf(sign_in, "sign_in", K, torch.int8)
     dev = q4.device
     lib = load()
     base = _u8(int(lib.nest_w4_base_bytes(M, K)), dev)
@@ -296,18 +342,22 @@ def quantize_and_pack(W: torch.Tensor, sign_out: torch.Tensor, sign_in: torch.Te
 def rotate(x: torch.Tensor, signs: torch.Tensor, mode: int, y: Optional[torch.Tensor] = None,
            x_op: Optional[torch.Tensor] = None, stream=None):
     """nest_rotate: mode 0 -> H S x (optionally into the GEMM operand), mode 1 -> S H x."""
-    if x.dtype == torch.bfloat16:
-        dt = 1
-    elif x.dtype == torch.float32:
-        dt = 0
-    else:
-        raise ValueError("x must be float32 or bfloat16")
-    _dev(x, x.dtype, "x")
-    _dev(signs, torch.int8, "signs")
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError("x must be a [T][n] tensor")
     T, n = x.shape
+    dt = _act(x, "x", T, n)
+    _rot_bufs(signs, y, x_op, T, n)
     st = load().nest_rotate(_ptr(x), dt, _ptr(signs), n, T, mode, _ptr(y), _ptr(x_op), _stream(stream))
     _check(st, "nest_rotate")
     return y, x_op
+
+
+def _rot_bufs(signs, y, x_op, T: int, n: int):
+    _buf(signs, "signs", n, torch.int8)
+    if y is not None:
+        _buf(y, "y", 4 * T * n, torch.float32)
+    if x_op is not None:
+        _buf(x_op, "x_op", xop_bytes(n, T))
 
 
 def rotate_group(xs, signs, mode: int, ys=None, x_ops=None, zero=None, stream=None):
@@ -321,11 +371,15 @@ def rotate_group(xs, signs, mode: int, ys=None, x_ops=None, zero=None, stream=No
     dt = 1 if xs[0].dtype == torch.bfloat16 else 0
     T = xs[0].shape[0]
     arr = (RotateTask * n_t)()
+    if not (len(signs) == len(ys) == len(x_ops) == len(zero) == n_t):
+        raise ValueError("one sign vector (and output / operand / clear entry) per input")
     for i, (x, s, y, xo, z) in enumerate(zip(xs, signs, ys, x_ops, zero)):
-        if x.dtype != xs[0].dtype or x.shape[0] != T:
-            raise ValueError("all inputs of a grouped rotation share dtype and T")
-        _dev(x, x.dtype, "x")
-        _dev(s, torch.int8, "signs")
+        if x.dtype != xs[0].dtype or x.dim() != 2 or x.shape[0] != T:
+            raise ValueError("all inputs of a grouped rotation are [T][n] and share dtype and T")
+        _act(x, "x", T, x.shape[1])
+        _rot_bufs(s, y, xo, T, x.shape[1])
+        if z is not None:
+            _buf(z, "zero", 0, torch.float32)
         arr[i] = RotateTask(_ptr(x), _ptr(s), x.shape[1], _ptr(y), _ptr(xo), _ptr(z), 0 if z is None else z.numel())
     st = load().nest_rotate_group(arr, n_t, dt, T, mode, _stream(stream))
     _check(st, "nest_rotate_group")
@@ -341,8 +395,10 @@ def gemm(layer: Layer, x_op: torch.Tensor, T: int, verify: bool, z: Optional[tor
 
     The library ACCUMULATES into z; a new z is zero-filled, a given z is added to."""
     dev = layer.base.device
+    _buf(x_op, "x_op", xop_bytes(layer.K, T))
     if z is None:
         z = torch.zeros((T, layer.M), dtype=torch.float32, device=dev)
+    _buf(z, "z", 4 * T * layer.M, torch.float32)
     L = layer.c_struct()
     fn = load().nest_verify_gemm if verify else load().nest_draft_gemv
     st = fn(ctypes.byref(L), _ptr(x_op), _ptr(z), T, _stream(stream))
@@ -354,12 +410,15 @@ def linear(layer: Layer, x: torch.Tensor, verify: bool, y: Optional[torch.Tensor
            scratch: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """nest_linear: y = S_o H_o (Q (H_i S_i x)) for x [T][K] (bf16 or fp32)."""
     T = x.shape[0]
+    dt = _act(x, "x", T, layer.K)
     dev = layer.base.device
     if y is None:
         y = torch.empty((T, layer.M), dtype=torch.float32, device=dev)
+    _buf(y, "y", 4 * T * layer.M, torch.float32)
+    need = linear_scratch_bytes(layer.M, layer.K, T)
     if scratch is None:
-        scratch = torch.empty(linear_scratch_bytes(layer.M, layer.K, T), dtype=torch.uint8, device=dev)
-    dt = 1 if x.dtype == torch.bfloat16 else 0
+        scratch = torch.empty(need, dtype=torch.uint8, device=dev)
+    _buf(scratch, "scratch", need)
     L = layer.c_struct()
     st = load().nest_linear(ctypes.byref(L), int(verify), _ptr(x), dt, T, _ptr(y), _ptr(scratch), _stream(stream))
     _check(st, "nest_linear")
@@ -397,6 +456,11 @@ def gemm_group(layers, x_ops, T: int, verify: bool, zs=None, stream=None):
     dev = layers[0].base.device
     if zs is None:
         zs = [torch.zeros((T, L.M), dtype=torch.float32, device=dev) for L in layers]
+    if not (len(x_ops) == len(zs) == len(layers)):
+        raise ValueError("one operand and one accumulator per layer")
+    for L, xo, z in zip(layers, x_ops, zs):
+        _buf(xo, "x_op", xop_bytes(L.K, T))
+        _buf(z, "z", 4 * T * L.M, torch.float32)
     arr = _layers(layers)
     fn = load().nest_verify_gemm_group if verify else load().nest_draft_gemv_group
     st = fn(arr, len(layers), _ptrs(x_ops), _ptrs(zs), T, _stream(stream))
@@ -414,9 +478,17 @@ def linear_group(layers, xs, verify: bool, ys=None, scratch: Optional[torch.Tens
     dev = layers[0].base.device
     if ys is None:
         ys = [torch.empty((T, L.M), dtype=torch.float32, device=dev) for L in layers]
+    if not (len(xs) == len(ys) == len(layers)):
+        raise ValueError("one input and one output per layer")
+    dt = _act(xs[0], "x", T, layers[0].K)
+    for L, x, y in zip(layers, xs, ys):
+        if _act(x, "x", T, L.K) != dt:
+            raise ValueError("all inputs of a grouped linear share one dtype")
+        _buf(y, "y", 4 * T * L.M, torch.float32)
+    need = linear_group_scratch_bytes(layers, T)
     if scratch is None:
-        scratch = torch.empty(linear_group_scratch_bytes(layers, T), dtype=torch.uint8, device=dev)
-    dt = 1 if xs[0].dtype == torch.bfloat16 else 0
+        scratch = torch.empty(need, dtype=torch.uint8, device=dev)
+    _buf(scratch, "scratch", need)
     st = load().nest_linear_group(_layers(layers), len(layers), int(verify), _ptrs(xs), dt, T, _ptrs(ys),
                                   _ptr(scratch), _stream(stream))
     _check(st, "nest_linear_group")
@@ -446,8 +518,12 @@ class KVCache:
 
 def kv_write(cache: KVCache, x: torch.Tensor, pos0: int, stream=None):
     """nest_kv_write: store x [T][H][128] (fp32 or bf16) at positions pos0 .. pos0+T-1."""
+    if x.dim() != 3 or x.shape[1] != cache.H or x.shape[2] != 128:
+        raise ValueError(f"x must be [T][{cache.H}][128], got {tuple(x.shape)}")
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("x must be float32 or bfloat16")
     dt = 1 if x.dtype == torch.bfloat16 else 0
-    _dev(x, x.dtype, "x")
+    _buf(x, "x")
     C = cache.c_struct()
     st = load().nest_kv_write(_ptr(x), dt, x.shape[0], ctypes.byref(C), pos0, _stream(stream))
     _check(st, "nest_kv_write")
@@ -456,15 +532,21 @@ def kv_write(cache: KVCache, x: torch.Tensor, pos0: int, stream=None):
 def kv_attention(q: torch.Tensor, k: KVCache, v: KVCache, L: int, view: int, recent_n: int = 0,
                  out: Optional[torch.Tensor] = None, work: Optional[torch.Tensor] = None, stream=None):
     """nest_kv_attention: q [T][Hq][128] -> out [T][Hq][128] fp32."""
+    if q.dim() != 3 or q.shape[2] != 128:
+        raise ValueError(f"q must be [T][Hq][128], got {tuple(q.shape)}")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q must be float32 or bfloat16")
     T, Hq, d = q.shape
     dt = 1 if q.dtype == torch.bfloat16 else 0
-    _dev(q, q.dtype, "q")
+    _buf(q, "q")
     lib = load()
     if out is None:
         out = torch.empty((T, Hq, d), dtype=torch.float32, device=q.device)
+    _buf(out, "out", 4 * T * Hq * d, torch.float32)
+    need = int(lib.nest_kv_attention_work_bytes(T, Hq, k.H, L))
     if work is None:
-        work = torch.empty(int(lib.nest_kv_attention_work_bytes(T, Hq, k.H, L)) // 4 + 1, dtype=torch.float32,
-                           device=q.device)
+        work = torch.empty(need // 4 + 1, dtype=torch.float32, device=q.device)
+    _buf(work, "work", need)
     K, V = k.c_struct(), v.c_struct()
     st = lib.nest_kv_attention(_ptr(q), dt, T, Hq, ctypes.byref(K), ctypes.byref(V), L, view, recent_n, _ptr(out),
                                _ptr(work), _stream(stream))
