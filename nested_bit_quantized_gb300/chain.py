@@ -41,9 +41,28 @@ def chain(z_a, s_a, z_b, s_b, T: int, work: torch.Tensor, y=None, nexts: Optiona
     """nest_chain (see include/nest.h).  Without y, the glue output overwrites z_a."""
     lib = nest.load()
     nexts = nexts or []
+    x_ops = x_ops or []
+    z_next = z_next or []
     M = z_a.shape[1]
-    if work.numel() * 4 < chain_work_bytes(M, T):
-        raise ValueError("work buffer too small")
+    nest._buf(z_a, "z_a", 4 * T * M, torch.float32)
+    nest._buf(s_a, "s_a", M, torch.int8)
+    if (z_b is None) != (s_b is None):
+        raise ValueError("z_b and s_b go together")
+    if z_b is not None:
+        nest._buf(z_b, "z_b", 4 * T * M, torch.float32)
+        nest._buf(s_b, "s_b", M, torch.int8)
+    if y is not None:
+        nest._buf(y, "y", 4 * T * M, torch.float32)
+    nest._buf(work, "work", chain_work_bytes(M, T))
+    if len(x_ops) != len(nexts) or (z_next and len(z_next) != len(nexts)):
+        raise ValueError("one operand (and one accumulator, if any) per next linear")
+    for L, xo in zip(nexts, x_ops):
+        if L.K != M:
+            raise ValueError(f"a next linear reads {L.K} features, the glue writes {M}")
+        nest._buf(L.sign_in, "sign_in", M, torch.int8)
+        nest._buf(xo, "x_op", nest.xop_bytes(M, T))
+    for L, zn in zip(nexts, z_next):
+        nest._buf(zn, "z_next", 4 * T * L.M, torch.float32)
     arr = nest._layers(nexts) if nexts else None
     xo = nest._ptrs(x_ops) if nexts else None
     zn = nest._ptrs(z_next) if z_next else None

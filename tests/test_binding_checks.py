@@ -125,3 +125,24 @@ def test_kv_buffers(no_device_check):
         nest.kv_attention(torch.zeros((1, 8, 64)), cache, cache, 16, 8)
     with pytest.raises(ValueError, match="out holds"):
         nest.kv_attention(torch.zeros((1, 8, 128)), cache, cache, 16, 8, out=torch.zeros((1, 8, 127)))
+
+
+def test_chain_buffers(no_device_check):
+    from nested_bit_quantized_gb300 import chain
+    M, T = 512, 4
+    za, sa = torch.zeros((T, M)), torch.ones(M, dtype=torch.int8)
+    work = torch.zeros(chain.chain_work_bytes(M, T) // 4)
+    nxt = [nest.Layer(256, M, 0, torch.zeros(16, dtype=torch.uint8), None, sa, sa)]
+    with pytest.raises(ValueError, match="work holds"):
+        chain.chain(za, sa, None, None, T, work[:-1], None, nxt, [_xop(M, T)], None)
+    with pytest.raises(ValueError, match="z_b and s_b"):
+        chain.chain(za, sa, za.clone(), None, T, work, None, nxt, [_xop(M, T)], None)
+    with pytest.raises(ValueError, match="x_op holds"):
+        chain.chain(za, sa, None, None, T, work, None, nxt, [_xop(M, T, short=True)], None)
+    with pytest.raises(ValueError, match="one operand"):
+        chain.chain(za, sa, None, None, T, work, None, nxt, [], None)
+    with pytest.raises(ValueError, match="reads 1024 features"):
+        bad = [nest.Layer(256, 2 * M, 0, torch.zeros(16, dtype=torch.uint8), None, sa, sa)]
+        chain.chain(za, sa, None, None, T, work, None, bad, [_xop(M, T)], None)
+    with pytest.raises(ValueError, match="z_next holds"):
+        chain.chain(za, sa, None, None, T, work, None, nxt, [_xop(M, T)], [torch.zeros((T, 255))])
