@@ -205,10 +205,12 @@ nest_status nest_draft_gemv(const nest_layer* layer, const uint16_t* x_op, float
  * Needs layer->resid_bits in {6, 7, 8}.  Arguments as nest_draft_gemv. */
 nest_status nest_verify_gemm(const nest_layer* layer, const uint16_t* x_op, float* z, int32_t T, void* stream);
 
-/* Grouped GEMMs: `count` (1..4) independent linears in ONE launch, e.g. the q/k/v
- * projections or the gate/up projections of a decoder layer, which read the same input.
- * Their (row tile, group) units are concatenated and split evenly over the CTAs, so the
- * launch's start-up and tail are paid once.  layers: host array of `count` descriptors
+/* Grouped GEMMs: `count` (1..64) independent linears in ONE launch, e.g. the q/k/v
+ * projections or the gate/up projections of a decoder layer, which read the same input,
+ * or the independent linears of a batch of layers whose inputs are all ready.  Their
+ * (row tile, group) units are concatenated and split evenly over the CTAs, which stay
+ * resident and stream their contiguous ranges, so the launch's start-up and tail are
+ * paid once for all of them.  layers: host array of `count` descriptors
  * (for verify, all with the same resid_bits); x_ops, z: host arrays of `count` device
  * pointers; each z[k] is fp32 [T][layers[k].M] and is accumulated into, as in
  * nest_draft_gemv / nest_verify_gemm.  T is shared. */

@@ -282,7 +282,7 @@ size_t nest_linear_scratch_bytes(int32_t M, int32_t K, int32_t T) {
 }
 
 size_t nest_linear_group_scratch_bytes(const nest_layer* layers, int32_t count, int32_t T) {
-    if (layers == nullptr || count < 1 || count > kMaxGemmTasks) return 0;
+    if (layers == nullptr || count < 1 || count > kMaxTasks) return 0;
     size_t total = 0;
     for (int k = 0; k < count; ++k) {
         const size_t b = nest_linear_scratch_bytes(layers[k].M, layers[k].K, T);
@@ -296,14 +296,14 @@ nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t v
                               int32_t x_dtype, int32_t T, float* const* ys, void* scratch, void* stream) {
     if (layers == nullptr || xs == nullptr || ys == nullptr || scratch == nullptr) return NEST_ERR_INVALID_ARG;
     if (count < 1) return NEST_ERR_INVALID_ARG;
-    if (count > kMaxGemmTasks) return NEST_ERR_UNSUPPORTED;
+    if (count > kMaxTasks) return NEST_ERR_UNSUPPORTED;
     if (x_dtype != 0 && x_dtype != 1) return NEST_ERR_INVALID_ARG;
     if (T < 1) return NEST_ERR_INVALID_ARG;
     if (T > kMaxT) return NEST_ERR_UNSUPPORTED;
     if (!aligned16(scratch)) return NEST_ERR_MISALIGNED;
     RotArgs rin = {}, rout = {};
-    const uint16_t* xops[kMaxGemmTasks];
-    float* zs[kMaxGemmTasks];
+    const uint16_t* xops[kMaxTasks];
+    float* zs[kMaxTasks];
     uint8_t* s = reinterpret_cast<uint8_t*>(scratch);
     for (int k = 0; k < count; ++k) {
         const nest_layer* L = &layers[k];

@@ -8,7 +8,8 @@
 
 namespace nest {
 
-constexpr int kMaxTasks = 4;           // linears in one grouped launch
+constexpr int kMaxTasks = 4;           // vector sets in one grouped rotation; linears of nest_linear_group
+constexpr int kMaxGemmTasks = 64;      // linears in one grouped draft/verify GEMM launch
 
 // One linear of a grouped draft/verify GEMM launch.
 struct GemmTask {
@@ -22,7 +23,7 @@ struct GemmTask {
 
 // Arguments of one grouped launch: the tasks' (tile, group) units are concatenated.
 struct GemmArgs {
-    GemmTask task[kMaxTasks];
+    GemmTask task[kMaxGemmTasks];
     int ntasks, T;
     long long units;          // total units of all tasks
 };
@@ -75,7 +76,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int bits, int grid, cudaStream_t stream);
-constexpr int kMaxGemmTasks = kMaxTasks;
 cudaError_t read_and_clear_error(int* flag, cudaStream_t stream);
 cudaError_t launch_wait_selftest(cudaStream_t stream);
 

@@ -85,7 +85,7 @@ def test_gemm_argument_validation(lib):
     ptrs = (ctypes.c_void_p * 2)(0x50000, 0x60000)
     g = lib.nest_verify_gemm_group
     assert g(arr, 0, ptrs, ptrs, 4, None) == 1                        # empty group
-    assert g(arr, 5, ptrs, ptrs, 4, None) == 2                        # more than 4 linears
+    assert g(arr, 65, ptrs, ptrs, 4, None) == 2                       # more than 64 linears
     assert g(arr, 2, ptrs, ptrs, 4, None) == 1                        # mixed residual widths
     assert g(None, 2, ptrs, ptrs, 4, None) == 1
     assert d(ctypes.byref(_layer(bits=0, resid=0)), ok, None, 4, None) == 1

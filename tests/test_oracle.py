@@ -625,3 +625,121 @@ def test_kv_attention_bruteforce_and_policies():
     assert np.allclose(one[0, 0], V4[0, 0], rtol=1e-12)
     mixed = O.kv_attention(q, k, v, L, 4, 3)
     assert not np.allclose(mixed, o4) and not np.allclose(mixed, out)
+
+
+# ----------------------------------------------------------------------------
+# sampled-row forwards and the chained decoder layer
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("verify", [False, True])
+def test_forward_rows_equals_triple_loop_and_rows_of_forward(verify):
+    """forward_rows (used for sampled checks at full size) on a subset of rows equals a
+    triple loop over the hand-dequantised rows, and the same rows of forward's z."""
+    M, K, T = 40, 256, 3
+    _, s_o, s_i, q = _layer(M, K, 7, seed=21)
+    _, x = synth.activations(T, K, 22)
+    full = O.forward(q, s_o, s_i, x, verify)
+    rows = np.array([0, 3, 17, 39, 20])
+    sub = {k: q[k][rows] for k in ("base_codes", "base_scales", "resid_codes", "resid_scales")}
+    z = O.forward_rows(sub, full["x_rot"], verify)
+    lv = [-1.5104, -0.4528, 0.4528, 1.5104]
+    ref = np.zeros((T, rows.size))
+    for t in range(T):
+        for j, m in enumerate(rows):
+            acc = 0.0
+            for k in range(K):
+                w = lv[q["base_codes"][m, k]] * float(q["base_scales"][m, k // 128])
+                if verify:
+                    w += float(q["resid_codes"][m, k]) * float(q["resid_scales"][m, k // 128])
+                acc += w * full["x_rot"][t, k]
+            ref[t, j] = acc
+    assert np.allclose(z, ref, rtol=1e-12, atol=1e-13)
+    assert np.allclose(z, full["z"][:, rows], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("verify", [False, True])
+def test_forward_rows_w4w8_equals_triple_loop_and_rows_of_forward(verify):
+    """forward_rows_w4w8 on a subset of rows equals a triple loop over q4 s4 (draft,
+    Eq. (6)) or (16 q4 + q_r) s4 / 16 (target, Eq. (10)), and forward_w4w8's rows."""
+    M, K, T = 24, 256, 2
+    W = synth.weights(M, K, 930, "entries")
+    s_o, s_i = synth.sign_pair(M, K, 931)
+    lay = O.quantize_layer_w4w8(W, s_o, s_i)
+    _, x = synth.activations(T, K, 932)
+    full = O.forward_w4w8(lay, s_o, s_i, x, verify)
+    rows = np.array([1, 0, 23, 11])
+    sub = {k: lay[k][rows] for k in ("q4", "s4", "qr")}
+    z = O.forward_rows_w4w8(sub, full["x_rot"], verify)
+    ref = np.zeros((T, rows.size))
+    for t in range(T):
+        for j, m in enumerate(rows):
+            for k in range(K):
+                s = float(lay["s4"][m, k // 128])
+                c = 16 * int(lay["q4"][m, k]) + int(lay["qr"][m, k]) if verify else int(lay["q4"][m, k])
+                ref[t, j] += c * (s / 16 if verify else s) * full["x_rot"][t, k]
+    assert np.allclose(z, ref, rtol=1e-12, atol=1e-13)
+    assert np.allclose(z, full["z"][:, rows], rtol=1e-12, atol=1e-13)
+
+
+def _bf16_bits(a):
+    """Round float64 to bfloat16 (8 significant bits, ties to even) on the IEEE bit pattern:
+    keep the top 7 of the 52 stored mantissa bits, round on the 45 dropped ones.  Normal
+    numbers only (the glue's values are O(1))."""
+    a = np.asarray(a, np.float64)
+    u = a.view(np.uint64)
+    lsb = (u >> np.uint64(45)) & np.uint64(1)
+    u = (u + np.uint64((1 << 44) - 1) + lsb) & ~np.uint64((1 << 45) - 1)
+    return u.view(np.float64)
+
+
+def test_decoder_layer_routing_against_dense_composition():
+    """decoder_layer_forward against an independently written composition of the chained
+    layer: each linear is the explicit dense matrix S_o H_o W_v H_i S_i (scipy's Hadamard
+    blocks, W_v dequantised by hand), each glue the unit-RMS rescale per token followed by
+    a bit-level bf16 rounding.  q, k, v read x; o reads glue(q); gate and up read glue(o);
+    down reads glue(gate * up); the next layer reads glue(down).  Distinct widths (hidden
+    256, q 128, intermediate 384) and the mis-routed variants checked at the end make a
+    wrong routing fail."""
+    hidden, qd, kvd, inter, bits = 256, 128, 128, 384, 8
+    shapes = {"q": (qd, hidden), "k": (kvd, hidden), "v": (kvd, hidden), "o": (hidden, qd),
+              "gate": (inter, hidden), "up": (inter, hidden), "down": (hidden, inter)}
+    lin = {}
+    for i, (n, (M, K)) in enumerate(shapes.items()):
+        W = synth.weights(M, K, 940 + i, "entries")
+        s_o, s_i = synth.sign_pair(M, K, 960 + 2 * i)
+        lin[n] = (O.quantize_layer(W, s_o, s_i, bits), s_o, s_i)
+    _, x = synth.activations(3, hidden, 980)
+    lv = np.array([-1.5104, -0.4528, 0.4528, 1.5104])
+
+    def dense(n, verify):
+        q, s_o, s_i = lin[n]
+        M, K = shapes[n]
+        sb = np.repeat(q["base_scales"].astype(np.float64), 128, axis=1)
+        Wv = lv[q["base_codes"]] * sb
+        if verify:
+            Wv = Wv + q["resid_codes"].astype(np.float64) * np.repeat(q["resid_scales"].astype(np.float64), 128, axis=1)
+        return np.diag(s_o.astype(np.float64)) @ _dense_blockdiag(M) @ Wv @ _dense_blockdiag(K) @ np.diag(
+            s_i.astype(np.float64))
+
+    def glue(h):
+        rms = np.sqrt(np.sum(h * h, axis=1, keepdims=True) / h.shape[1])
+        return _bf16_bits(h / rms)
+
+    for verify in (False, True):
+        Wd = {n: dense(n, verify) for n in shapes}
+        f = lambda n, xin: xin @ Wd[n].T
+        ref = {n: f(n, x) for n in ("q", "k", "v")}
+        ref["o"] = f("o", glue(ref["q"]))
+        xg = glue(ref["o"])
+        ref["gate"], ref["up"] = f("gate", xg), f("up", xg)
+        ref["down"] = f("down", glue(ref["gate"] * ref["up"]))
+        ref["next"] = glue(ref["down"])
+        got = O.decoder_layer_forward(lin, x, verify)
+        for n in ref:
+            assert got[n].shape == ref[n].shape, n
+            assert np.allclose(got[n], ref[n], rtol=1e-9, atol=1e-12), n
+        # the composition has the power to see a mis-routed layer
+        wrong_down = f("down", glue(ref["gate"]))                    # down reading gate alone
+        assert not np.allclose(got["down"], wrong_down, rtol=1e-3, atol=1e-6)
+        wrong_up = f("up", glue(f("o", glue(ref["k"]))))             # o reading k instead of q
+        assert not np.allclose(got["up"], wrong_up, rtol=1e-3, atol=1e-6)
