@@ -295,8 +295,10 @@ nest_status nest_rotate_group(const nest_rotate_task* tasks, int32_t count, int3
  * NEST_ERR_UNSUPPORTED without launching.  The first call on a device looks up the
  * array's address for that device (make that call before any stream capture).  Calls
  * share the array: calls whose work overlaps on the GPU (other streams or threads) race
- * and must be serialised by the caller; nothing needs clearing between calls.  Allocates
- * nothing (no cudaMalloc, cudaFree or allocating library routine). */
+ * and must be serialised by the caller; nothing needs clearing between calls.  The looked-up
+ * address is cached per device: cudaDeviceReset on a device ends the context holding the
+ * array, so do not call this entry point on that device again in the same process.
+ * Allocates nothing (no cudaMalloc, cudaFree or allocating library routine). */
 nest_status nest_linear_static(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype,
                                int32_t T, float* y, void* stream);
 

@@ -18,7 +18,10 @@
 // cached.  All calls share the one array and it keeps the last call's contents;
 // the path clears the accumulator itself, so nothing has to start at zero on
 // entry, but calls whose kernels overlap on the GPU (other streams, other host
-// threads) race on the array and must be serialised by the caller.
+// threads) race on the array and must be serialised by the caller.  The cached
+// address belongs to the device's primary context: after cudaDeviceReset the
+// array lives elsewhere (or nowhere), so the entry point must not be called on a
+// device that this process has reset.
 #include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>

@@ -6,8 +6,9 @@ without an allocator, loops that cannot afford cudaMalloc's implicit
 synchronisation.  nest_linear_static keeps those buffers in a fixed array in
 the library's own device memory.  This test calls it through the C ABI and
 checks that two calls in a row give the result of nest_linear with caller
-scratch, within the parity tolerance the other GPU tests use, and that shapes
-whose buffers exceed the array are refused before any launch.
+scratch, within the parity tolerance the other GPU tests use, that a call after
+the first changes the device's free memory by nothing, and that shapes whose
+buffers exceed the array are refused before any launch.
 
 The file is named so that pytest collects it after every other test.
 """
@@ -54,18 +55,24 @@ def test_static_scratch_linear_matches_caller_scratch_linear():
     L = layer.c_struct()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
+    ys = [torch.empty((T, M), dtype=torch.float32, device=dev) for _ in range(2)]
     for verify in (False, True):
         ref = nest.linear(layer, x, verify).cpu().numpy()
-        for _ in range(2):                                     # the second call reuses the array
-            y = torch.full((T, M), float("nan"), dtype=torch.float32, device=dev)
+        for i, y in enumerate(ys):                             # the second call reuses the array
+            y.fill_(float("nan"))
+            torch.cuda.synchronize()
+            free_before = torch.cuda.mem_get_info(dev)[0]
             st = fn(ctypes.byref(L), int(verify), ctypes.c_void_p(x.data_ptr()), 1, T,
                     ctypes.c_void_p(y.data_ptr()), stream)
             assert st == 0, f"nest_linear_static returned {st}"
             torch.cuda.synchronize()
+            if i == 1 or verify:                               # after the first call loaded the module
+                assert torch.cuda.mem_get_info(dev)[0] == free_before, "the call changed free device memory"
             parity(y.cpu().numpy(), ref)
 
     # shapes whose operand + accumulator exceed the fixed array are refused without a launch
     big = nest._Layer(100_000, 4096, 8, layer.base.data_ptr(), layer.resid.data_ptr(),
                       layer.sign_out.data_ptr(), layer.sign_in.data_ptr())
-    assert fn(ctypes.byref(big), 1, ctypes.c_void_p(x.data_ptr()), 1, 64, ctypes.c_void_p(y.data_ptr()), stream) == 2
+    assert fn(ctypes.byref(big), 1, ctypes.c_void_p(x.data_ptr()), 1, 64, ctypes.c_void_p(ys[0].data_ptr()),
+              stream) == 2
     nest.error_check()
