@@ -115,7 +115,7 @@ nest_status run_gemm_group(const nest_layer* layers, int count, bool verify, con
     const long long slots = (long long)gemm_ctas_per_sm(T) * sms;   // every CTA resident at once
     long long grid = units < slots ? units : slots;
     if (grid > kMaxGrid) grid = kMaxGrid;
-    return from_cuda(launch_gemm(a, kcodec, (int)grid, as_stream(stream)));
+    return from_cuda(launch_gemm(a, kcodec, (int)grid, sms, as_stream(stream)));
 }
 
 }  // namespace

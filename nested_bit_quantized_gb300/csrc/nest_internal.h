@@ -75,7 +75,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-cudaError_t launch_gemm(const GemmArgs& a, int bits, int grid, cudaStream_t stream);
+cudaError_t launch_gemm(const GemmArgs& a, int bits, int grid, int sms, cudaStream_t stream);
 cudaError_t read_and_clear_error(int* flag, cudaStream_t stream);
 cudaError_t launch_wait_selftest(cudaStream_t stream);
 

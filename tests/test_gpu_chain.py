@@ -10,7 +10,9 @@ its two factors, once per layer, so the difference grows about linearly with
 depth.  The gate for an output reached through c bf16 casts is relative
 L2 <= 1.5e-3 * c, every element within 6e-2 * rms.  Outputs with no cast on
 their path (k, v of the first layer) and the nest_chain kernel itself keep the
-GEMM gate (1e-3, 1e-2).
+GEMM gate (1e-3, 1e-2).  That end-to-end gate is an extra check only: the
+stage-wise test holds every stage of the chain (each GEMM, each glue) to the GEMM
+gate, each fed the GPU's own intermediate.
 """
 import numpy as np
 import pytest
@@ -146,4 +148,60 @@ def test_two_chained_decoder_layers(dev, T):
         chained(bufs[0].y["down"].cpu().numpy(), o0["down"], 3)       # q->o, o->gate/up, gate*up->down
         chained(bufs[1].y["k"].cpu().numpy(), o1["k"], 4)              # + down -> next layer
         chained(bufs[1].y["down"].cpu().numpy(), o1["down"], 7)
+    nest.error_check()
+
+
+@pytest.mark.parametrize("T", [1, 16, 64])
+def test_chained_layers_stagewise(dev, T):
+    """Every stage of two chained layers at the GEMM gate (relative L2 <= 1e-3, every element
+    within 1e-2 * rms), each stage fed the GPU's own intermediate.  After layer_forward the
+    in-place glue calls leave y_q, y_o and y_gate * y_up (fp32, rotated back) in z_q, z_o and
+    z_gate; z_up and z_down keep the rotated-basis accumulators; y_down is written apart.
+    The oracle's glue (unit RMS in fp64, bf16 cast) applied to a GPU intermediate gives the
+    next stage's input, so no stage inherits an earlier stage's rounding differences; the
+    operands the glue kernel wrote are checked against the same glue, rotated."""
+    bits = 8
+    ref = [_small_layer(l, bits) for l in range(2)]
+    lin = [{n: _dev_layer(q, bits, so, si, dev) for n, (q, so, si) in r.items()} for r in ref]
+    xb, xv = synth.activations(T, SMALL["hidden"], 78)
+    x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    host = lambda t: t.cpu().numpy().astype(np.float64)
+    for verify in (False, True):
+        bufs = [chain.LayerBuffers(l, T, dev) for l in lin]
+        chain.layer_input(lin[0], x, bufs[0])
+        chain.layer_forward(lin[0], bufs[0], verify, lin[1], bufs[1])
+        chain.layer_forward(lin[1], bufs[1], verify)
+        torch.cuda.synchronize()
+        fwd = lambda r, n, xin: O.forward(r[n][0], r[n][1], r[n][2], xin, verify)
+        xin = xv
+        for l in range(2):
+            r, b = ref[l], bufs[l]
+            y_q = host(b.z["q"])
+            parity(y_q, fwd(r, "q", xin)["y"])
+            parity(host(b.y["k"]), fwd(r, "k", xin)["y"])
+            parity(host(b.y["v"]), fwd(r, "v", xin)["y"])
+            h_q = O.chain_glue(y_q)
+            parity(decode_xop(b.xop["o"].cpu().numpy(), SMALL["q"], T).astype(np.float64),
+                   O.rotate_activations(h_q, r["o"][2]))
+            y_o = host(b.z["o"])
+            parity(y_o, fwd(r, "o", h_q)["y"])
+            h_o = O.chain_glue(y_o)
+            for n in ("gate", "up"):
+                parity(decode_xop(b.xop[n].cpu().numpy(), SMALL["hidden"], T).astype(np.float64),
+                       O.rotate_activations(h_o, r[n][2]))
+            parity(host(b.z["up"]), fwd(r, "up", h_o)["z"])
+            y_up_gpu = O.unrotate_outputs(host(b.z["up"]), r["up"][1])
+            prod = host(b.z["gate"])
+            parity(prod, fwd(r, "gate", h_o)["y"] * y_up_gpu)
+            h_gu = O.chain_glue(prod)
+            parity(decode_xop(b.xop["down"].cpu().numpy(), SMALL["inter"], T).astype(np.float64),
+                   O.rotate_activations(h_gu, r["down"][2]))
+            y_down = host(b.y["down"])
+            parity(host(b.z["down"]), fwd(r, "down", h_gu)["z"])
+            parity(y_down, fwd(r, "down", h_gu)["y"])
+            xin = O.chain_glue(y_down)
+            if l == 0:
+                for n in ("q", "k", "v"):
+                    parity(decode_xop(bufs[1].xop[n].cpu().numpy(), SMALL["hidden"], T).astype(np.float64),
+                           O.rotate_activations(xin, ref[1][n][2]))
     nest.error_check()

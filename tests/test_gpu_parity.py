@@ -237,6 +237,39 @@ def test_draft_grouped_many_units(dev):
     nest.error_check()
 
 
+def test_draft_lookup_kernel_grouped(dev, monkeypatch):
+    """The one-token draft's table look-up kernel on a grouped launch large enough that
+    each CTA's range wraps the 10-stage ring and crosses task boundaries: seven 4096x4096
+    linears and a ragged 4296x4096 one (its last 512-row block has two tiles, the last
+    tile 72 rows), random 2-bit codes and scales; against the oracle, and against the
+    register-fragment kernel forced on the same inputs."""
+    rng = np.random.default_rng(91)
+    shapes = [(4096, 4096)] * 7 + [(4296, 4096)]
+    layers, refs, xops = [], [], []
+    x, xv = bf16_x(1, 4096, 92, dev)
+    for i, (M, K) in enumerate(shapes):
+        G = K // 128
+        q = {"base_codes": rng.integers(0, 4, size=(M, K)).astype(np.uint8),
+             "base_scales": np.exp(rng.uniform(np.log(1e-3), np.log(3e-2), size=(M, G))).astype(np.float16),
+             "resid_codes": np.zeros((M, K), np.int8), "resid_scales": np.zeros((M, G), np.float16)}
+        s_o, s_i = synth.sign_pair(M, K, 93 + i)
+        L = dev_layer(q, 0, s_o, s_i, dev)
+        xop = nest.new_xop(K, 1, dev)
+        nest.rotate(x, L.sign_in, 0, x_op=xop)
+        layers.append(L)
+        refs.append((q, s_o, s_i))
+        xops.append(xop)
+    zs = nest.gemm_group(layers, xops, 1, False)
+    monkeypatch.setenv("NEST_GEMM_PATH", "rf")
+    zr = nest.gemm_group(layers, xops, 1, False)
+    monkeypatch.delenv("NEST_GEMM_PATH")
+    for (q, s_o, s_i), z, r in zip(refs, zs, zr):
+        ref = O.forward(q, s_o, s_i, xv, False)["z"]
+        parity(z.cpu().numpy(), ref)
+        parity(r.cpu().numpy(), ref)
+    nest.error_check()
+
+
 def _close(a, b, rel=1e-6):
     """Equal up to the order of the fp32 additions of the split K range."""
     scale = np.sqrt(np.mean(np.asarray(b, np.float64) ** 2))
