@@ -302,6 +302,24 @@ nest_status nest_rotate_group(const nest_rotate_task* tasks, int32_t count, int3
 nest_status nest_linear_static(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype,
                                int32_t T, float* y, void* stream);
 
+/* ---- row-sharded linears (several GPUs) ---------------------------------- */
+
+/* Reorder of a row-sharded linear's all-gathered output.  No page has a counterpart
+ * (the pages run on one device); this is the library's split of one linear over `world`
+ * GPUs by output rows.  Rank r holds whole 128-row tiles of the packed layer: rows
+ * [r * Mp, min((r + 1) * Mp, M)) with Mp = 128 * ceil(ceil(M / 128) / world), a view of
+ * its tiles' units (the packed buffers are tile-major).  Every rank rotates the
+ * replicated input itself (nest_rotate) and runs the draft or verify GEMM on its M_r =
+ * min(Mp, M - r * Mp) rows into the first T * M_r floats ([T][M_r]) of a block of T * Mp
+ * floats; one all-gather of those blocks (e.g. NCCL) gives every rank gathered =
+ * [world][T * Mp].  This call writes
+ *   z[t][r * Mp + j] = gathered[r * T * Mp + t * M_r + j]   for j < M_r,
+ * the token-major [T][M] rotated-basis output that nest_rotate (mode 1) turns into y.
+ * gathered: device fp32, world * T * Mp floats; z: device fp32 [T][M], not overlapping it.
+ * Limits: world, T, Mp, M >= 1, M <= world * Mp, world * T * Mp < 2^31; 4-byte aligned. */
+nest_status nest_shard_gather(const float* gathered, float* z, int32_t world, int32_t T, int32_t Mp, int32_t M,
+                              void* stream);
+
 /* ---- nested KV4/KV8 cache (BitNest paper, Section 3.4, Appendix A.2) ------ */
 
 /* One cache (keys or values) of H heads x Lmax positions, head dimension 128.

@@ -94,6 +94,7 @@ def load() -> ctypes.CDLL:
         "nest_kv_attention_work_bytes": ([_I32, _I32, _I32, _I32], _SZ),
         "nest_kv_attention": ([_P, _I32, _I32, _I32, ctypes.POINTER(_KvCache), ctypes.POINTER(_KvCache), _I32, _I32,
                                _I32, _P, _P, _P], _I32),
+        "nest_shard_gather": ([_P, _P, _I32, _I32, _I32, _I32, _P], _I32),
         "nest_error_check": ([_P], _I32),
         "nest_wait_selftest": ([_P], _I32),
     }
@@ -423,6 +424,17 @@ def linear(layer: Layer, x: torch.Tensor, verify: bool, y: Optional[torch.Tensor
     st = load().nest_linear(ctypes.byref(L), int(verify), _ptr(x), dt, T, _ptr(y), _ptr(scratch), _stream(stream))
     _check(st, "nest_linear")
     return y
+
+
+def shard_gather(gathered: torch.Tensor, world: int, T: int, Mp: int, M: int, z: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """nest_shard_gather: the all-gathered [world][T][Mp] row-shard blocks -> z [T][M]."""
+    _buf(gathered, "gathered", 4 * world * T * Mp, torch.float32)
+    if z is None:
+        z = torch.empty((T, M), dtype=torch.float32, device=gathered.device)
+    _buf(z, "z", 4 * T * M, torch.float32)
+    _check(load().nest_shard_gather(_ptr(gathered), _ptr(z), world, T, Mp, M, _stream(stream)), "nest_shard_gather")
+    return z
 
 
 def error_check(stream=None) -> None:

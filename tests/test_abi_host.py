@@ -206,3 +206,15 @@ def test_kv_cache_validation(lib):
     assert a(ok, 0, 2, 8, ctypes.byref(C), ctypes.byref(V), 1, 8, 0, ok, ok, None) == 1    # L < T
     assert a(ok, 0, 2, 8, ctypes.byref(C), ctypes.byref(V), 65, 8, 0, ok, ok, None) == 1   # L > Lmax
     assert a(ok, 0, 2, 8, ctypes.byref(C), ctypes.byref(V), 32, 4, -1, ok, ok, None) == 1  # recent_n
+
+
+def test_shard_gather_rejects_bad_arguments(lib):
+    """Validation before any device work: null pointers, sizes, a layout that cannot hold M rows."""
+    p = ctypes.c_void_p(16)
+    assert lib.nest_shard_gather(None, p, 2, 1, 128, 200, None) == 1
+    assert lib.nest_shard_gather(p, None, 2, 1, 128, 200, None) == 1
+    assert lib.nest_shard_gather(p, p, 0, 1, 128, 200, None) == 1
+    assert lib.nest_shard_gather(p, p, 2, 0, 128, 200, None) == 1
+    assert lib.nest_shard_gather(p, p, 1, 1, 128, 200, None) == 1          # 1 x 128 < 200 rows
+    assert lib.nest_shard_gather(p, p, 1 << 12, 1 << 10, 1 << 10, 200, None) == 2
+    assert lib.nest_shard_gather(ctypes.c_void_p(18), p, 2, 1, 128, 200, None) == 3
