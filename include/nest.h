@@ -187,12 +187,20 @@ nest_status nest_unpack(const nest_layer* layer, uint8_t* base_codes, uint16_t* 
 nest_status nest_rotate(const void* x, int32_t x_dtype, const int8_t* signs, int32_t n, int32_t T,
                         int32_t mode, float* y, uint16_t* x_op, void* stream);
 
+/* The GEMM operand from an already-rotated activation block (POC recipe step 4, with x'
+ * computed by the caller): x_op = fp16(x') in the operand layout above, round to nearest;
+ * the padding tokens T <= t < Np are written as zeros.  nest_rotate produces the same
+ * operand while it rotates; this call serves callers that hold x' = H_i S_i x in fp32.
+ * x_rot  device fp32 [T][K] (4-byte aligned); x_op  nest_xop_bytes(K, T) bytes (16-byte aligned).
+ * Limits: K % 128 == 0, 1 <= T <= 256, K * T < 2^31.  |x'| must stay within the fp16 range. */
+nest_status nest_operand(const float* x_rot, int32_t K, int32_t T, uint16_t* x_op, void* stream);
+
 /* Draft GEMV/GEMM: z[t][m] += sum_k Q_base[m][k] x'[t][k] for t < T, in the rotated
  * output basis (POC recipe step 4: the draft forward is the verifier's without y_r).
  * Reads the base buffer only.  For NEST_CODEC_W4W8 layers Q_base = q4 s4 (BitNest
  * Eq. (6)) and the verify below uses Q = (16 q4 + q_r) s4/16 (Eq. (10)).  A grouped
  * launch takes layers of one codec.
- * x_op  activation operand from nest_rotate (T tokens).
+ * x_op  activation operand from nest_rotate or nest_operand (T tokens).
  * z     fp32 [T][M], ACCUMULATED into: clear it first for a plain product.  The
  *       128-column groups of a row are split across CTAs and each part is added with
  *       fp32 atomics, so the order of those additions (and the last bits of z) may

@@ -95,6 +95,7 @@ def load() -> ctypes.CDLL:
         "nest_kv_attention": ([_P, _I32, _I32, _I32, ctypes.POINTER(_KvCache), ctypes.POINTER(_KvCache), _I32, _I32,
                                _I32, _P, _P, _P], _I32),
         "nest_shard_gather": ([_P, _P, _I32, _I32, _I32, _I32, _P], _I32),
+        "nest_operand": ([_P, _I32, _I32, _P, _P], _I32),
         "nest_error_check": ([_P], _I32),
         "nest_wait_selftest": ([_P], _I32),
     }
@@ -384,6 +385,19 @@ def rotate_group(xs, signs, mode: int, ys=None, x_ops=None, zero=None, stream=No
         arr[i] = RotateTask(_ptr(x), _ptr(s), x.shape[1], _ptr(y), _ptr(xo), _ptr(z), 0 if z is None else z.numel())
     st = load().nest_rotate_group(arr, n_t, dt, T, mode, _stream(stream))
     _check(st, "nest_rotate_group")
+
+
+def operand(x_rot: torch.Tensor, x_op: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """nest_operand: the GEMM operand from an already-rotated fp32 x' [T][K]."""
+    if not isinstance(x_rot, torch.Tensor) or x_rot.dim() != 2:
+        raise ValueError("x_rot must be a [T][K] tensor")
+    T, K = x_rot.shape
+    _buf(x_rot, "x_rot", 4 * T * K, torch.float32)
+    if x_op is None:
+        x_op = new_xop(K, T, x_rot.device)
+    _buf(x_op, "x_op", xop_bytes(K, T))
+    _check(load().nest_operand(_ptr(x_rot), K, T, _ptr(x_op), _stream(stream)), "nest_operand")
+    return x_op
 
 
 def new_xop(K: int, T: int, device="cuda") -> torch.Tensor:

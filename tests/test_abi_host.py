@@ -218,3 +218,12 @@ def test_shard_gather_rejects_bad_arguments(lib):
     assert lib.nest_shard_gather(p, p, 1, 1, 128, 200, None) == 1          # 1 x 128 < 200 rows
     assert lib.nest_shard_gather(p, p, 1 << 12, 1 << 10, 1 << 10, 200, None) == 2
     assert lib.nest_shard_gather(ctypes.c_void_p(18), p, 2, 1, 128, 200, None) == 3
+
+
+def test_operand_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.nest_operand(None, 128, 1, p, None) == 1
+    assert lib.nest_operand(p, 128, 0, p, None) == 1
+    assert lib.nest_operand(p, 100, 1, p, None) == 2          # K % 128
+    assert lib.nest_operand(p, 128, 257, p, None) == 2        # T > 256
+    assert lib.nest_operand(p, 128, 1, ctypes.c_void_p(24), None) == 3

@@ -403,3 +403,24 @@ def test_linear_and_group_prefill(dev):
             for (W, so, si, q), (x, xv), y in zip(refs, xs, ys):
                 parity(y.cpu().numpy(), O.forward(q, so, si, xv, verify)["y"])
     nest.error_check()
+
+
+@pytest.mark.parametrize("M,K,T,bits", [(384, 512, 1, 8), (200, 1024, 16, 7), (1280, 384, 40, 6)])
+def test_gemm_from_fp32_rotated_operand(dev, M, K, T, bits):
+    """A caller holding x' = H_i S_i x in fp32 (the oracle's own x') lays it out with
+    nest_operand and calls the GEMMs: draft and verify against the oracle's z, and the
+    operand equals fp16(x') element for element (padding tokens zero)."""
+    W, s_o, s_i, q = ref_layer(M, K, bits, seed=71)
+    layer = dev_layer(q, bits, s_o, s_i, dev)
+    _, xv = bf16_x(T, K, 72, dev)
+    xr = O.rotate_activations(xv, s_i)
+    x_op = nest.new_xop(K, T, dev).fill_(0x7E00)                       # NaN bits: every byte is written
+    nest.operand(torch.from_numpy(xr.astype(np.float32)).to(dev), x_op=x_op)
+    got = decode_xop(x_op.cpu().numpy(), K, T)
+    assert np.array_equal(got.view(np.uint16), xr.astype(np.float32).astype(np.float16).view(np.uint16))
+    Np = nest.xop_bytes(K, T) // (2 * K)
+    if Np > T:
+        assert not np.isnan(x_op.cpu().numpy().view(np.float16)).any()
+    for verify in (False, True):
+        parity(nest.gemm(layer, x_op, T, verify).cpu().numpy(), O.forward(q, s_o, s_i, xv, verify)["z"])
+    nest.error_check()
