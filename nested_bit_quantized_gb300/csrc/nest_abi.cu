@@ -487,10 +487,11 @@ nest_status nest_kv_attention(const void* q, int32_t q_dtype, int32_t T, int32_t
 }
 
 nest_status nest_error_check(void* stream) {
-    int flag = 0;
+    int flag = 0, lut_flag = 0;
     cudaError_t e = read_and_clear_error(&flag, as_stream(stream));
+    if (e == cudaSuccess) e = read_and_clear_lut_error(&lut_flag, as_stream(stream));
     if (e != cudaSuccess) return NEST_ERR_CUDA;
-    return flag ? NEST_ERR_TIMEOUT : NEST_OK;
+    return (flag || lut_flag) ? NEST_ERR_TIMEOUT : NEST_OK;
 }
 
 nest_status nest_wait_selftest(void* stream) {

@@ -76,6 +76,43 @@ __device__ __forceinline__ void grid_dep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------------------------------
+// bounded waits
+// ---------------------------------------------------------------------------
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for a whole warp (all 32 lanes converged); the result is the
+// same on every lane.  Gives up after kWaitLimitNs, or at once when another
+// role of the CTA has given up (*abort != 0) unless `honour_abort` is false
+// (used while draining in-flight copies and MMAs); on a timeout it raises the
+// CTA's abort flag and the device error flag *err.
+__device__ inline bool warp_wait_flag(uint32_t bar, uint32_t parity, volatile int* abort, int* err,
+                                      bool honour_abort = true) {
+    bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        if (!ok) ok = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        const bool timed_out = (it & 31u) == 31u && globaltimer() - t0 > kWaitLimitNs;
+        const bool stop = timed_out || (honour_abort && *abort != 0);
+        if (__any_sync(0xffffffffu, stop)) {
+            if (__any_sync(0xffffffffu, timed_out) && (threadIdx.x & 31) == 0) {
+                *abort = 1;
+                atomicExch(err, 1);
+            }
+            return false;
+        }
+    }
+}
+
 // named barrier over `count` threads
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");

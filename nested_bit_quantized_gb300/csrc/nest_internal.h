@@ -76,6 +76,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int bits, int grid, int sms, cudaStream_t stream);
+// The one-token 2-bit draft by table look-up (nest_lut.cu), and its error flag.
+cudaError_t launch_lut(const GemmArgs& a, int sms, cudaStream_t stream);
+cudaError_t read_and_clear_lut_error(int* flag, cudaStream_t stream);
 cudaError_t read_and_clear_error(int* flag, cudaStream_t stream);
 cudaError_t launch_wait_selftest(cudaStream_t stream);
 
