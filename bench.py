@@ -870,6 +870,63 @@ def kv_section(args, dev, timer):
 
 
 # ----------------------------------------------------------------------------
+# the 4096 x 4096 linear split over the ranks by output rows (one all-gather of z per linear)
+# ----------------------------------------------------------------------------
+
+def shard_rows_section(args, dev, timer, world, rank):
+    """Every rank holds its whole-tile row shard of each copy (views of the packed buffers),
+    rotates the replicated input, runs the verify GEMM on its rows, and the ranks all-gather
+    the rotated-basis blocks (NCCL) before the reorder and the output rotation, which every
+    rank runs.  Total work is fixed as ranks are added (strong scaling); the value counts
+    the whole job's algorithmic bytes."""
+    import numpy as np
+    import torch
+    from nested_bit_quantized_gb300 import nest, shard, synth
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    lin = wl.linears[0]
+    C = args.copies
+    copies = build_layers(wl.linears, BITS, C, dev)
+    lins = [shard.RowShardedLinear(row[0], world, rank, group=None) for row in copies]
+    b, _ = synth.activations(T_VERIFY, lin.K, wl.x_seed + 900)
+    x = torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+    ys = [torch.empty((T_VERIFY, lin.M), dtype=torch.float32, device=dev) for _ in range(C)]
+
+    def step():
+        for L, y in zip(lins, ys):
+            L.forward(x, True, y=y)
+
+    if world == 1:                            # no collective: the step is captured in a CUDA graph
+        g = timer.graph(step)
+        ms = timer.time("shard_rows", g, args.steps, args.warmup)
+        how = "CUDA graph"
+    else:                                     # the all-gathers run eagerly on the current stream
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        timer.dist.barrier()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream()
+        with ClockSampler(timer.gpu) as clk, nvtx_range("shard_rows"):
+            s.record(cur)
+            for _ in range(args.steps):
+                step()
+            e.record(cur)
+            torch.cuda.synchronize()
+        timer.clocks["shard_rows"] = clk.summary()
+        ms = max_over_ranks(s.elapsed_time(e) / args.steps, timer.dist, dev)
+        how = "eager launches"
+    nest.error_check()
+    by = C * lin_bytes(lin.M, lin.K, T_VERIFY, BITS)
+    plan = shard.RowPlan(lin.M, world)
+    return {"workload": f"{WORKLOAD_DESC}; each of {world} ranks holds its {plan.count(rank)}-row shard "
+                        f"(tiles of 128 rows) of {C} copies; per linear: rotation in, verify GEMM on the "
+                        f"rank's rows, one all-gather of z, reorder, rotation out ({how})",
+            "ms_per_step": ms, "GBps": by / (ms * 1e-3) / 1e9, "us_per_linear": 1e3 * ms / C,
+            "rows_per_rank": plan.Mp, "bytes_per_step": by}
+
+
+# ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
 
@@ -899,6 +956,10 @@ def run_gpu(args, rank, world):
         elif args.workload == "decoder_12b":
             sec = decoder12_section(args, dev, timer)
             value, unit, metric = sec["by_bits"]["8"]["four_launches"]["GBps"], "GB/s", METRIC
+        elif args.workload == "single_4096_rows":
+            sec = shard_rows_section(args, dev, timer, world, rank)
+            value, unit, metric = sec["GBps"], "GB/s", ("whole linear (rotation, verify GEMM on row shards, all-gather, "
+                                                        "output rotation) at T=16, effective HBM GB/s of the job")
         elif args.workload == "mlp_triplet_4b":
             sec = triplet_section(args, dev, timer, copies=args.copies_triplet, codec=args.codec)
             value, unit, metric = sec["step"]["GBps"], "GB/s", "draft T=1 + verify T=16 step, effective HBM GB/s"
@@ -907,8 +968,11 @@ def run_gpu(args, rank, world):
             sec = stack_section(args, dev, timer, cycle=cyc, n_layers=args.layers if args.layers else (60 if cyc else 1))
             value, unit, metric = sec["cycle_GBps"], "GB/s", "speculative cycle (draft passes + verify pass), effective HBM GB/s"
         if rank == 0:
+            scaling = "strong" if args.workload == "single_4096_rows" else "weak"
+            par = f"rows x{world}" if args.workload == "single_4096_rows" else f"replicas x{world}"
             line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "higher_is_better": True,
-                    "dtype": "f16", "data": "synthetic", "config": {"workload": args.workload}, "section": sec,
+                    "scaling": scaling, "dtype": "f16", "data": "synthetic",
+                    "config": {"workload": args.workload, "parallelism": par}, "section": sec,
                     "clocks_by_region": timer.clocks, "wall_s": time.time() - wall0}
             print(json.dumps(line), flush=True)
         if dist is not None:
@@ -1006,7 +1070,8 @@ def main():
                     help="--workload kv_31b: one case only (0 KV4 draft, 1 KV4 + Recent-1024, 2 KV8 verify "
                          "T=16, 3 KV8 draft)")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[WORKLOAD, "decoder_12b", "mlp_triplet_4b", "decoder_31b", "stack_31b", "kv_31b"],
+                    choices=[WORKLOAD, "single_4096_rows", "decoder_12b", "mlp_triplet_4b", "decoder_31b", "stack_31b",
+                             "kv_31b"],
                     help="single_4096 (default, the metric's workload) or one extra workload alone")
     ap.add_argument("--layers", type=int, default=0, help="layers of the 31B-class stack (default 1 or 60)")
     args = ap.parse_args()

@@ -116,21 +116,31 @@ class RowShardedLinear:
         self.M, self.K = full.M, full.K
         self.sign_out, self.sign_in = full.sign_out, full.sign_in
         self.local = shard_layer(full, self.plan, rank)
+        self._bufs = {}
+
+    def _buffers(self, T: int):
+        """This rank's block, the operand, the gathered blocks and z for T tokens, kept
+        between calls (so a call allocates nothing after the first at each T)."""
+        if T not in self._bufs:
+            dev, Mp, W = self.sign_in.device, self.plan.Mp, self.plan.world
+            self._bufs[T] = (torch.empty(T * Mp, dtype=torch.float32, device=dev), nest.new_xop(self.K, T, dev),
+                             torch.empty(W * T * Mp, dtype=torch.float32, device=dev) if W > 1 else None,
+                             torch.empty((T, self.M), dtype=torch.float32, device=dev))
+        return self._bufs[T]
 
     def forward(self, x: torch.Tensor, verify: bool, y: Optional[torch.Tensor] = None) -> torch.Tensor:
         """y = S_o H_o (W_v (H_i S_i x)) for x [T][K] (bf16 or fp32), on torch's current
-        stream (the collective runs there too)."""
+        stream (the collective runs there too).  Buffers are reused between calls, so calls
+        of one instance must not overlap on the GPU."""
         T = x.shape[0]
-        dev = self.sign_in.device
-        flat = torch.empty(T * self.plan.Mp, dtype=torch.float32, device=dev)
-        x_op = nest.new_xop(self.K, T, dev)
+        flat, x_op, gathered, z = self._buffers(T)
         # x' = H_i S_i x on every rank; the same launch clears this rank's block
         nest.rotate_group([x], [self.sign_in], 0, x_ops=[x_op], zero=[flat])
         if self.local is not None:
             nest.gemm(self.local, x_op, T, verify, z=block(flat, self.plan, self.rank, T))
-        gathered = all_gather_blocks(flat, self.plan, T, self.group)
-        z = nest.shard_gather(gathered, self.plan.world, T, self.plan.Mp, self.M)
+        gathered = all_gather_blocks(flat, self.plan, T, self.group, out=gathered)
+        nest.shard_gather(gathered, self.plan.world, T, self.plan.Mp, self.M, z=z)
         if y is None:
-            y = torch.empty((T, self.M), dtype=torch.float32, device=dev)
+            y = torch.empty((T, self.M), dtype=torch.float32, device=x.device)
         nest.rotate(z, self.sign_out, 1, y=y)
         return y
