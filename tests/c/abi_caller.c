@@ -58,6 +58,15 @@ int main(void) {
     CHECK(16, nest_rotate(NULL, 1, L.sign_in, 128, 4, 0, z, NULL, NULL) == NEST_ERR_INVALID_ARG);
     CHECK(17, nest_linear(&L, 1, NULL, 1, 4, z, (float*)(uintptr_t)0x70000, NULL) == NEST_ERR_INVALID_ARG);
 
+    /* the operand from an already-rotated x', and the row-shard reorder */
+    const float* xr = (const float*)(uintptr_t)0x80000;
+    uint16_t* xo = (uint16_t*)(uintptr_t)0x90000;
+    CHECK(18, nest_operand(NULL, 512, 4, xo, NULL) == NEST_ERR_INVALID_ARG);
+    CHECK(19, nest_operand(xr, 500, 4, xo, NULL) == NEST_ERR_UNSUPPORTED);
+    CHECK(20, nest_operand(xr, 512, 4, (uint16_t*)(uintptr_t)0x90008, NULL) == NEST_ERR_MISALIGNED);
+    CHECK(21, nest_shard_gather(xr, z, 2, 4, 128, 300, NULL) == NEST_ERR_INVALID_ARG);   /* 2 x 128 < 300 rows */
+    CHECK(22, nest_shard_gather(xr, z, 0, 4, 128, 100, NULL) == NEST_ERR_INVALID_ARG);
+
     printf("ok\n");
     return 0;
 }
