@@ -322,6 +322,13 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# The pages' own figures for this path, with their hardware (context, not a target): the CPU
+# residual kernel of the 2-bit-base post (feedman.me/posts/wZBTJ, Results, "CPU residual kernel").
+PAGES_CONTEXT = {"cpu_residual_kernel_ms_per_pass": {"T=1": 108, "T=4": 127, "T=8": 116, "T=16": 125, "T=32": 204},
+                 "working_set_GB": 4.29, "ram_GBps": "33-38",
+                 "hardware": "AMD Ryzen 9 9950X, 16 threads, DDR5 (int8 residual tiles, AVX-512)",
+                 "note": "no page reports a GPU timing of the split; context only"}
+
 WORKLOAD_DESC = ("single_4096: one linear 4096x4096, 2-bit base + 8-bit residual, g128 fp16 scales, "
                  "N(0,0.02^2) weights with 1% columns x8, bf16 N(0,1) activations")
 
@@ -509,6 +516,8 @@ def single_section(args, dev, timer, world):
                 key = "verify" if verify else "draft"
                 r[key + "_us"] = ms * 1e3 / C
                 r[key + "_GBps"] = by(T, verify) / (ms * 1e-3 / C) / 1e9
+                r[key + "_frac_of_measured_hbm"] = r[key + "_GBps"] / hbm
+                r[key + "_frac_of_8TBps"] = r[key + "_GBps"] / NOMINAL_HBM_GBS
             sweep.append(r)
         tpk, tsrc = tensor_peak()
         pre = []
@@ -986,6 +995,7 @@ def run_gpu(args, rank, world):
     extras = {}
     if world == 1 and not args.quick:
         for name, fn in (("decoder_12b", lambda: decoder12_section(args, dev, timer)),
+                         ("decoder_31b", lambda: stack_section(args, dev, timer, cycle=False, n_layers=1)),
                          ("mlp_triplet_4b", lambda: triplet_section(args, dev, timer, copies=args.copies_triplet)),
                          ("stack_31b", lambda: stack_section(args, dev, timer, cycle=True, n_layers=60))):
             if name == "stack_31b" and args.no_stack:
@@ -1034,6 +1044,7 @@ def run_gpu(args, rank, world):
                          "algorithmic_bytes_per_launch": C * main["bytes_per_linear_verify_T16"],
                          "algorithmic_bytes_per_linear": main["bytes_per_linear_verify_T16"]},
             "sweep": main["sweep"], "prefill": main.get("prefill", []),
+            "pages_context": PAGES_CONTEXT,
             "layer_step": main["layer_step"],
             "extras": extras,
             "cpu_baseline": cpu,
