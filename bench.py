@@ -253,7 +253,7 @@ def run_oracle_subprocess(cases, threads, cap_s):
 
 
 def cpu_baseline_section():
-    """The oracle timed per linear on the host cores (SURVEY-style per-config sample): the
+    """The oracle timed per linear on the host cores (a per-workload sample): the
     single linear (T = 1 draft, T = 1 and 16 verify), the MLP triplet, the Gemma-12B-like
     layer and one 31B-class layer (T = 1 draft, T = 16 verify), all threads; the single
     linear again on one thread; the 60-layer cycle extrapolated from the 31B-class layer."""
