@@ -742,6 +742,28 @@ def triplet_section(args, dev, timer, copies=12, codec="l2"):
             del gg
         sweep.append(r)
     res["sweep_gemm_only"] = sweep
+    # the same GEMMs with the copies' independent linears of one shape in one launch: all gate
+    # and up linears (24), then all down linears (12)
+    by_shape = [[L for trip in layers for L in trip[:2]], [trip[2] for trip in layers]]
+    grouped_rates = {}
+    for T, verify in ((1, False), (16, True)):
+        xo = {K: nest.new_xop(K, T, dev) for K in {l.K for l in wl.linears}}
+        for k, l in enumerate(layers[0]):
+            b, _ = synth.activations(T, l.K, wl.x_seed + 11 * T + k)
+            nest.rotate(torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16), l.sign_in, 0, x_op=xo[l.K])
+        zz = [[torch.zeros((T, L.M), dtype=torch.float32, device=dev) for L in grp] for grp in by_shape]
+
+        def fn_grouped():
+            for grp, zg in zip(by_shape, zz):
+                grouped(grp, [xo[L.K] for L in grp], zg, T, verify)
+        gg = timer.graph(fn_grouped)
+        per = timer.time(f"triplet_{codec}_grouped_{'v' if verify else 'd'}{T}", gg, 20, min_s=0.2) * 1e3 / n_lin
+        b_ = sum(lin_bytes(L.M, L.K, T, VC if verify else DC) for L in layers[0]) / 3
+        grouped_rates[f"{'verify' if verify else 'draft'}_T{T}"] = {
+            "us_per_linear": per, "GBps": b_ / (per * 1e-6) / 1e9, "frac_of_measured_hbm": b_ / (per * 1e-6) / 1e9 / hbm}
+        del gg
+    res["grouped_gemm_only"] = dict(grouped_rates, what="the 24 gate/up linears of the 12 copies in one launch, "
+                                                         "then the 12 down linears in one")
     nest.error_check()
     del layers, flat
     torch.cuda.empty_cache()
