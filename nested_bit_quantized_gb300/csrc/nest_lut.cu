@@ -28,7 +28,8 @@ __device__ bool lut_wait(uint32_t bar, uint32_t parity, volatile int* abort, boo
 // only 16 possible weight pairs.  The CTA builds, per pair, the 16 partial
 // sums L[c0] x'[k0] + L[c1] x'[k1] in fp32 once, and every row then reads its
 // pair's sum with the 4-bit index its packed codes already form: one
-// shared-memory load and one add per two weights, no per-weight decode.
+// shared-memory load per two weights and one packed two-lane fp32 FMA (with the
+// row's scale) per four, no per-weight decode.
 // Pairing, from the packed layout: byte b of code word w (w = 0..7) holds at
 // bit offsets 2s the codes of columns 16w + 4s + b, so its nibble n (bits
 // 4n..4n+3) is the pair (8C + b, 8C + b + 4) with C = 2w + n, index
@@ -38,16 +39,16 @@ __device__ bool lut_wait(uint32_t bar, uint32_t parity, volatile int* abort, boo
 // warp (32 rows) read one pair's 64-byte table at a time: 16 words in 16
 // banks, no bank conflicts.
 //
-// Work: super-units of (block of kLutTiles row tiles = 512 rows, group), in
-// task / row-block / group order, split into equal contiguous ranges, one CTA
-// per SM.  Warp roles:
+// Work: super-units of (block of kTiles row tiles, group) -- 8 tiles = 1024 rows
+// in the default shape -- in task / row-block / group order, split into equal
+// contiguous ranges, one CTA per SM.  Warp roles:
 //   producer : bulk copies of the block's base units and of the group's 16
 //              activation chunks of token 0 into a ring of stages;
 //   table    : builds super-unit j's 1024 sums into table buffer j % 4, ahead
 //              of the row warps;
-//   row warps: one row per lane; sums the row's 64 look-ups, times its (row,
-//              group) scale, into a register accumulator that is added into z
-//              when the CTA's range leaves the row block.
+//   row warps: R rows per lane (2 by default); each row's 64 look-ups, times its
+//              (row, group) scale, go into eight register partial sums that are
+//              added into z when the CTA's range leaves the row block.
 // Each row warp waits only for its stage and its table, so the row warps run
 // independently of each other.  All waits are bounded.
 // ---------------------------------------------------------------------------
