@@ -79,6 +79,8 @@ typedef struct {
     const int8_t* sign_out;     /* S_o, M entries of +-1 */
     const int8_t* sign_in;      /* S_i, K entries of +-1 */
     int32_t codec;              /* NEST_CODEC_L2 (0, the default of a zeroed descriptor) or NEST_CODEC_W4W8 */
+    int32_t group;              /* columns per scale group: 128, the storage format's group (0, the default of a
+                                   zeroed descriptor, means 128); any other value returns NEST_ERR_UNSUPPORTED */
 } nest_layer;
 
 /* Human-readable name of a status. */

@@ -51,6 +51,7 @@ bool bits_ok(int bits) { return bits == 6 || bits == 7 || bits == 8; }
 nest_status check_layer(const nest_layer* L, bool need_resid) {
     if (L == nullptr) return NEST_ERR_INVALID_ARG;
     if (L->M < 1 || L->K < 1) return NEST_ERR_INVALID_ARG;
+    if (L->group != 0 && L->group != 128) return NEST_ERR_UNSUPPORTED;   // the format's group is 128 columns
     if (L->K % 128 != 0) return NEST_ERR_UNSUPPORTED;
     if (L->base == nullptr) return NEST_ERR_INVALID_ARG;
     if (!aligned16(L->base)) return NEST_ERR_MISALIGNED;
@@ -351,6 +352,8 @@ nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, c
     if ((long long)M * T >= (1LL << 31)) return NEST_ERR_UNSUPPORTED;
     if (n_next > 0 && (next == nullptr || x_ops == nullptr)) return NEST_ERR_INVALID_ARG;
     if (n_next > 0 && M % 128) return NEST_ERR_UNSUPPORTED;
+    for (int j = 0; j < n_next; ++j)
+        if (next[j].group != 0 && next[j].group != 128) return NEST_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(z_a) & 3u) || (z_b && (reinterpret_cast<uintptr_t>(z_b) & 3u)) ||
         (y && (reinterpret_cast<uintptr_t>(y) & 3u)) || (reinterpret_cast<uintptr_t>(work) & 3u))
         return NEST_ERR_MISALIGNED;

@@ -37,7 +37,7 @@ class _KvCache(ctypes.Structure):
 
 class _Layer(ctypes.Structure):
     _fields_ = [("M", _I32), ("K", _I32), ("resid_bits", _I32),
-                ("base", _P), ("resid", _P), ("sign_out", _P), ("sign_in", _P), ("codec", _I32)]
+                ("base", _P), ("resid", _P), ("sign_out", _P), ("sign_in", _P), ("codec", _I32), ("group", _I32)]
 
 
 class RotateTask(ctypes.Structure):
@@ -235,7 +235,7 @@ class Layer:
     def c_struct(self) -> _Layer:
         return _Layer(self.M, self.K, self.bits, self.base.data_ptr(),
                       self.resid.data_ptr() if self.resid is not None else None,
-                      self.sign_out.data_ptr(), self.sign_in.data_ptr(), self.codec)
+                      self.sign_out.data_ptr(), self.sign_in.data_ptr(), self.codec, 128)
 
     @property
     def weight_bytes(self) -> int:

@@ -67,6 +67,13 @@ int main(void) {
     CHECK(21, nest_shard_gather(xr, z, 2, 4, 128, 300, NULL) == NEST_ERR_INVALID_ARG);   /* 2 x 128 < 300 rows */
     CHECK(22, nest_shard_gather(xr, z, 0, 4, 128, 100, NULL) == NEST_ERR_INVALID_ARG);
 
+    /* the scale group: 0 (zeroed) and 128 are the format's; others are refused */
+    L.resid_bits = 8;
+    L.group = 8;
+    CHECK(23, nest_verify_gemm(&L, xop, z, 4, NULL) == NEST_ERR_UNSUPPORTED);
+    L.group = 128;
+    CHECK(24, nest_verify_gemm(&L, (const uint16_t*)(uintptr_t)0x50008, z, 4, NULL) == NEST_ERR_MISALIGNED);
+
     printf("ok\n");
     return 0;
 }

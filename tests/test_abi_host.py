@@ -227,3 +227,17 @@ def test_operand_rejects_bad_arguments(lib):
     assert lib.nest_operand(p, 100, 1, p, None) == 2          # K % 128
     assert lib.nest_operand(p, 128, 257, p, None) == 2        # T > 256
     assert lib.nest_operand(p, 128, 1, ctypes.c_void_p(24), None) == 3
+
+
+def test_group_other_than_128_is_refused(lib):
+    """The descriptor's group: 0 or 128 pass validation, any other size is refused before a launch
+    (the storage format has one group size, 128 columns)."""
+    z = ctypes.c_void_p(0x60000)
+    xop = ctypes.c_void_p(0x50000)
+    for g in (8, 64, 256, -1):
+        L = nest._Layer(256, 512, 8, 0x10000, 0x20000, 0x30000, 0x40000, 0, g)
+        assert lib.nest_verify_gemm(ctypes.byref(L), xop, z, 4, None) == 2
+        assert lib.nest_draft_gemv(ctypes.byref(L), xop, z, 4, None) == 2
+    bad = (nest._Layer * 1)(nest._Layer(256, 512, 8, 0x10000, 0x20000, 0x30000, 0x40000, 0, 32))
+    assert lib.nest_chain(z, ctypes.c_void_p(0x30000), None, None, 512, 1, None, bad, 1,
+                          (nest._P * 1)(0x70000), None, z, None) == 2
