@@ -140,22 +140,23 @@ def base_threshold(levels: np.ndarray = LEVELS) -> float:
     return float((levels[2] + levels[3]) / 2.0)
 
 
-def quantize_base(Wr: np.ndarray, levels: np.ndarray = LEVELS) -> Tuple[np.ndarray, np.ndarray]:
-    """Per (row, 128-group): s = fp16(RMS of the block); code = nearest level of W~/s.
+def quantize_base(Wr: np.ndarray, levels: np.ndarray = LEVELS, group: int = GROUP) -> Tuple[np.ndarray, np.ndarray]:
+    """Per (row, group of `group` columns, 128 in the format): s = fp16(RMS of the block);
+    code = nearest level of W~/s.
 
     Returns (codes uint8 [M][K] in 0..3 indexing ``levels`` ascending,
-             scales float16 [M][K/128])."""
+             scales float16 [M][K/group])."""
     Wr = np.asarray(Wr, dtype=np.float64)
     M, K = Wr.shape
-    if K % GROUP:
-        raise ValueError("K must be a multiple of 128")
-    G = K // GROUP
-    blocks = Wr.reshape(M, G, GROUP)
+    if K % group:
+        raise ValueError(f"K must be a multiple of the group ({group})")
+    G = K // group
+    blocks = Wr.reshape(M, G, group)
     rms = np.sqrt(np.mean(blocks * blocks, axis=2))
     s16 = to_fp16(rms)
     s = s16.astype(np.float64)
     t = base_threshold(levels)
-    codes = np.full((M, G, GROUP), 2, dtype=np.uint8)
+    codes = np.full((M, G, group), 2, dtype=np.uint8)
     nz = s > 0
     with np.errstate(divide="ignore", invalid="ignore"):
         u = blocks / s[:, :, None]
@@ -167,10 +168,10 @@ def quantize_base(Wr: np.ndarray, levels: np.ndarray = LEVELS) -> Tuple[np.ndarr
 
 
 def dequant_base(codes: np.ndarray, scales16: np.ndarray, levels: np.ndarray = LEVELS) -> np.ndarray:
-    """Q_base = L[code] * s  (float64 [M][K])."""
+    """Q_base = L[code] * s  (float64 [M][K]); the group is K / (scales per row)."""
     M, K = codes.shape
-    G = K // GROUP
-    L = levels[codes.reshape(M, G, GROUP)]
+    G = scales16.shape[1]
+    L = levels[codes.reshape(M, G, K // G)]
     return (L * scales16.astype(np.float64)[:, :, None]).reshape(M, K)
 
 
@@ -183,19 +184,19 @@ def qmax(bits: int) -> int:
     return (1 << (bits - 1)) - 1
 
 
-def quantize_residual(R: np.ndarray, bits: int) -> Tuple[np.ndarray, np.ndarray]:
-    """Per (row, 128-group): s = fp16(max|R| / qm); q = clip(rint(R/s), -qm, qm).
+def quantize_residual(R: np.ndarray, bits: int, group: int = GROUP) -> Tuple[np.ndarray, np.ndarray]:
+    """Per (row, group of `group` columns): s = fp16(max|R| / qm); q = clip(rint(R/s), -qm, qm).
 
-    Returns (codes int8 [M][K], scales float16 [M][K/128])."""
+    Returns (codes int8 [M][K], scales float16 [M][K/group])."""
     R = np.asarray(R, dtype=np.float64)
     M, K = R.shape
-    G = K // GROUP
+    G = K // group
     qm = qmax(bits)
-    blocks = R.reshape(M, G, GROUP)
+    blocks = R.reshape(M, G, group)
     amax = np.max(np.abs(blocks), axis=2)
     s16 = to_fp16(amax / qm)
     s = s16.astype(np.float64)
-    q = np.zeros((M, G, GROUP), dtype=np.int64)
+    q = np.zeros((M, G, group), dtype=np.int64)
     nz = s > 0
     with np.errstate(divide="ignore", invalid="ignore"):
         r = np.rint(blocks / s[:, :, None])
@@ -205,10 +206,10 @@ def quantize_residual(R: np.ndarray, bits: int) -> Tuple[np.ndarray, np.ndarray]
 
 
 def dequant_residual(codes: np.ndarray, scales16: np.ndarray) -> np.ndarray:
-    """Q_resid = q * s (float64 [M][K])."""
+    """Q_resid = q * s (float64 [M][K]); the group is K / (scales per row)."""
     M, K = codes.shape
-    G = K // GROUP
-    q = codes.reshape(M, G, GROUP).astype(np.float64)
+    G = scales16.shape[1]
+    q = codes.reshape(M, G, K // G).astype(np.float64)
     return (q * scales16.astype(np.float64)[:, :, None]).reshape(M, K)
 
 
@@ -216,12 +217,14 @@ def dequant_residual(codes: np.ndarray, scales16: np.ndarray) -> np.ndarray:
 # offline pipeline and forward passes
 # ----------------------------------------------------------------------------
 
-def quantize_layer(W: np.ndarray, s_o: np.ndarray, s_i: np.ndarray, bits: int) -> Dict[str, np.ndarray]:
-    """Rotate, fit the base, quantize the residual.  Returns codes, scales and W~."""
+def quantize_layer(W: np.ndarray, s_o: np.ndarray, s_i: np.ndarray, bits: int,
+                   group: int = GROUP) -> Dict[str, np.ndarray]:
+    """Rotate, fit the base, quantize the residual.  Returns codes, scales and W~.  The
+    storage format's group is 128 columns; other groups serve the oracle's own checks."""
     Wr = rotate_weights(W, s_o, s_i)
-    bc, bs = quantize_base(Wr)
+    bc, bs = quantize_base(Wr, group=group)
     R = Wr - dequant_base(bc, bs)
-    rc, rs = quantize_residual(R, bits)
+    rc, rs = quantize_residual(R, bits, group=group)
     return {"Wr": Wr, "base_codes": bc, "base_scales": bs,
             "resid_codes": rc, "resid_scales": rs}
 

@@ -256,6 +256,54 @@ def test_residual_scale_is_fp16_of_absmax_over_qm():
                 assert s[m, g] == np.float16(amax / qm)
 
 
+def test_small_group_quantizers_and_forward_by_scalar_loops():
+    # A group of 8 columns on an 8 x 16 layer, every step redone by scalar loops from
+    # the post's POC recipe (steps 2-4): RMS scale, nearest level, absmax residual scale,
+    # rounding, and z = sum_k (Q_base + Q_resid)[m][k] x'[k].  Pins the group index
+    # arithmetic (a slip that mixes up groups shows only when a row has many of them).
+    M, K, G, bits, T = 8, 16, 8, 7, 3
+    rng = np.random.default_rng(21)
+    W = rng.normal(size=(M, K))
+    s_o = rng.choice([-1, 1], size=M).astype(np.int8)
+    s_i = rng.choice([-1, 1], size=K).astype(np.int8)
+    x = rng.normal(size=(T, K))
+    q = O.quantize_layer(W, s_o, s_i, bits, group=G)
+    Wr = q["Wr"]
+    levels = [-1.5104, -0.4528, 0.4528, 1.5104]
+    t = (0.4528 + 1.5104) / 2
+    qm = (1 << (bits - 1)) - 1
+    Wv = [[0.0] * K for _ in range(M)]
+    for m in range(M):
+        for g in range(K // G):
+            cols = range(g * G, (g + 1) * G)
+            sb = float(np.float16(math.sqrt(sum(Wr[m, k] ** 2 for k in cols) / G)))
+            assert float(q["base_scales"][m, g]) == sb
+            base = {}
+            for k in cols:
+                if sb == 0:
+                    c = 2
+                else:
+                    u = Wr[m, k] / sb
+                    c = (3 if abs(u) > t else 2) if u >= 0 else (0 if abs(u) > t else 1)
+                assert q["base_codes"][m, k] == c
+                base[k] = levels[c] * sb
+            sr = float(np.float16(max(abs(Wr[m, k] - base[k]) for k in cols) / qm))
+            assert float(q["resid_scales"][m, g]) == sr
+            for k in cols:
+                r = 0 if sr == 0 else int(np.clip(np.rint((Wr[m, k] - base[k]) / sr), -qm, qm))
+                assert q["resid_codes"][m, k] == r
+                Wv[m][k] = base[k] + r * sr
+    xr = O.rotate_activations(x, s_i)
+    z = O.forward(q, s_o, s_i, x, verify=True)["z"]
+    for tt in range(T):
+        for m in range(M):
+            ref = sum(Wv[m][k] * xr[tt, k] for k in range(K))
+            assert math.isclose(z[tt, m], ref, rel_tol=1e-12, abs_tol=1e-12)
+    # the group changes the fit: one group per row gives other scales and codes
+    q16 = O.quantize_layer(W, s_o, s_i, bits, group=K)
+    assert q16["base_scales"].shape == (M, 1) and not np.array_equal(q16["base_codes"], q["base_codes"])
+
+
 # ----------------------------------------------------------------------------
 # forward passes
 # ----------------------------------------------------------------------------
