@@ -42,10 +42,13 @@ __device__ bool lut_wait(uint32_t bar, uint32_t parity, volatile int* abort, boo
 // Work: super-units of (block of kTiles row tiles, group) -- 8 tiles = 1024 rows
 // in the default shape -- in task / row-block / group order, split into equal
 // contiguous ranges, one CTA per SM.  Warp roles:
-//   producer : bulk copies of the block's base units and of the group's 16
-//              activation chunks of token 0 into a ring of stages;
-//   table    : builds super-unit j's 1024 sums into table buffer j % 4, ahead
-//              of the row warps;
+//   producer : bulk copies of the block's base units into a ring of stages (the
+//              weights do not depend on the previous kernel, so the first
+//              stages are requested before it has finished);
+//   table    : reads the group's 128 activations of token 0 itself (plain
+//              loads, one super-unit ahead) and builds super-unit j's 1024
+//              sums into table buffer j % 4, up to four super-units ahead of
+//              the row warps and independent of the stage ring;
 //   row warps: R rows per lane (2 by default); each row's 64 look-ups, times its
 //              (row, group) scale, go into eight register partial sums that are
 //              added into z when the CTA's range leaves the row block.
@@ -59,14 +62,12 @@ template <int WARPS, int R, int CPS = 1>
 struct LutCfg {
     static constexpr int kCtasPerSm = CPS;
     static constexpr int kTiles = WARPS * 32 * R / kRows;
-    static constexpr int kXBytes = 256;                   // token 0 of one group: 16 chunks x 16 bytes
-    static constexpr int kStage = kTiles * kBaseUnit + kXBytes;
+    static constexpr int kStage = kTiles * kBaseUnit;     // the block's base units of one group
     static constexpr int kTable = 64 * 16 * 4;            // 64 pairs x 16 sums x fp32
     static constexpr int kTables = 4;                     // table buffers
-    static constexpr int kSmemBudget = CPS == 1 ? 220 * 1024 : 110 * 1024;
+    static constexpr int kSmemBudget = CPS == 1 ? 227 * 1024 : 110 * 1024;
     static constexpr int kStagesRaw = (kSmemBudget - kTables * kTable - 512) / kStage;
-    // a power of two, so the ring index and phase need no division
-    static constexpr int kStages = kStagesRaw >= 8 ? 8 : (kStagesRaw >= 4 ? 4 : 2);
+    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kProducer = WARPS;
     static constexpr int kTableWarp = WARPS + 1;
     static constexpr int kThreads = 32 * (WARPS + 2);
@@ -157,7 +158,7 @@ k_nest_lut(const __grid_constant__ GemmArgs p) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), WARPS + 1); }
+        for (int s = 0; s < S; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), WARPS); }
         for (int b = 0; b < NT; ++b) { mbar_init(tfull(b), 1); mbar_init(tempty(b), WARPS); }
         *abort_flag = 0;
         fence_barrier_init();
@@ -182,15 +183,10 @@ k_nest_lut(const __grid_constant__ GemmArgs p) {
             const int s = j % S;
             const GemmTask& t = p.task[c.k];
             const int nt = tiles_of(c);
-            mbar_arrive_expect_tx(full(s), nt * kBaseUnit + C::kXBytes);
+            mbar_arrive_expect_tx(full(s), nt * kBaseUnit);
             for (int i = 0; i < nt; ++i)
                 bulk_g2s(smem_u32(stage(s) + i * kBaseUnit),
                          t.base + ((long long)(c.rb * TILES + i) * t.G + c.g) * kBaseUnit, kBaseUnit, full(s));
-        };
-        auto issue_x = [&](int j, const Cursor& c) {        // lanes 0..15: chunk `lane` of token 0
-            if (lane < 16)
-                bulk_g2s(smem_u32(stage(j % S) + TILES * kBaseUnit + 16 * lane),
-                         p.task[c.k].xop + (size_t)c.g * 2048 + 128 * lane, 16, full(j % S));
         };
         Cursor cw = start;
         int j = 0;
@@ -199,14 +195,6 @@ k_nest_lut(const __grid_constant__ GemmArgs p) {
             __syncwarp();
             cw.next(p);
             ++j;
-        }
-        grid_dep_wait();                     // the activation operand comes from the previous kernel
-        {
-            Cursor cx = start;
-            for (int jj = 0; jj < j; ++jj) {
-                issue_x(jj, cx);
-                cx.next(p);
-            }
         }
         uint64_t t_last = globaltimer();
         while (j < n) {
@@ -217,7 +205,6 @@ k_nest_lut(const __grid_constant__ GemmArgs p) {
             if (__shfl_sync(0xffffffffu, ready, 0)) {
                 if (lane == 0) issue_w(j, cw);
                 __syncwarp();
-                issue_x(j, cw);
                 cw.next(p);
                 ++j;
                 t_last = globaltimer();
@@ -236,22 +223,37 @@ k_nest_lut(const __grid_constant__ GemmArgs p) {
     }
 
     if (warp == C::kTableWarp) {
-        // lane l builds the sums of pairs l and l + 32: pair P = 4 C + b reads x'[8C + b], x'[8C + b + 4].
+        // lane l builds the sums of pairs l and l + 32: pair P = 4 C + b reads x'[8C + b], x'[8C + b + 4],
+        // token 0's values at halves 128 C + b and 128 C + b + 4 of the group's operand block.
         // Sums 4q .. 4q + 3 (c1 = q) go out as one 16-byte store, q rotated by lane / 2 so that the
         // eight lanes of a quarter-warp write eight different 16-byte bank groups.
         float lv[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) lv[c] = level_f(c);
+        const int off = 128 * (lane >> 2) + (lane & 3);      // pair `lane`; pair lane + 32 is 8 chunks on
+        auto fetch = [&](const Cursor& c, unsigned short (&h)[4]) {
+            const unsigned short* x = p.task[c.k].xop + (size_t)c.g * 2048;
+            h[0] = __ldcg(x + off);
+            h[1] = __ldcg(x + off + 4);
+            h[2] = __ldcg(x + off + 1024);
+            h[3] = __ldcg(x + off + 1028);
+        };
+        grid_dep_wait();                     // the activation operand comes from the previous kernel
+        Cursor ct = start;
+        unsigned short xv[4] = {0, 0, 0, 0}, xn[4] = {0, 0, 0, 0};
+        if (n > 0) fetch(ct, xv);
         for (int j = 0; j < n; ++j) {
-            const int s = j % S, tb = j % NT;
-            if (!lut_wait(full(s), (j / S) & 1, abort_flag)) break;
+            const int tb = j % NT;
+            Cursor cn = ct;
+            cn.next(p);
+            if (j + 1 < n) fetch(cn, xn);        // the next super-unit's values, in flight meanwhile
             if (j >= NT && !lut_wait(tempty(tb), ((j / NT) - 1) & 1, abort_flag)) break;
-            const __half* xs = reinterpret_cast<const __half*>(stage(s) + TILES * kBaseUnit);
             float* t = reinterpret_cast<float*>(tables + tb * C::kTable);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int P = lane + 32 * h, Cc = P >> 2, b = P & 3;
-                const float x0 = __half2float(xs[8 * Cc + b]), x1 = __half2float(xs[8 * Cc + b + 4]);
+                const int P = lane + 32 * h;
+                const float x0 = __half2float(__ushort_as_half(xv[2 * h])),
+                            x1 = __half2float(__ushort_as_half(xv[2 * h + 1]));
                 float a[4], c1[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) { a[c] = lv[c] * x0; c1[c] = lv[c] * x1; }
@@ -264,7 +266,10 @@ k_nest_lut(const __grid_constant__ GemmArgs p) {
                 }
             }
             __syncwarp();
-            if (lane == 0) { mbar_arrive(tfull(tb)); mbar_arrive(empty(s)); }
+            if (lane == 0) mbar_arrive(tfull(tb));
+            ct = cn;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xv[i] = xn[i];
         }
         return;
     }
