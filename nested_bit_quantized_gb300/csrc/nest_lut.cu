@@ -39,9 +39,9 @@ __device__ bool lut_wait(uint32_t bar, uint32_t parity, volatile int* abort, boo
 // warp (32 rows) read one pair's 64-byte table at a time: 16 words in 16
 // banks, no bank conflicts.
 //
-// Work: super-units of (block of kTiles row tiles, group) -- 8 tiles = 1024 rows
+// Work: super-units of (block of kTiles row tiles, group) -- 2 tiles = 256 rows
 // in the default shape -- in task / row-block / group order, split into equal
-// contiguous ranges, one CTA per SM.  Warp roles:
+// contiguous ranges over the resident CTAs (four per SM by default).  Warp roles:
 //   producer : bulk copies of the block's base units into a ring of stages (the
 //              weights do not depend on the previous kernel, so the first
 //              stages are requested before it has finished);
@@ -65,7 +65,7 @@ struct LutCfg {
     static constexpr int kStage = kTiles * kBaseUnit;     // the block's base units of one group
     static constexpr int kTable = 64 * 16 * 4;            // 64 pairs x 16 sums x fp32
     static constexpr int kTables = 4;                     // table buffers
-    static constexpr int kSmemBudget = CPS == 1 ? 227 * 1024 : 110 * 1024;
+    static constexpr int kSmemBudget = CPS == 1 ? 227 * 1024 : (CPS == 2 ? 110 * 1024 : 54 * 1024);
     static constexpr int kStagesRaw = (kSmemBudget - kTables * kTable - 512) / kStage;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kProducer = WARPS;
@@ -370,16 +370,17 @@ cudaError_t launch_lut_shape(const GemmArgs& a, int sms, cudaStream_t stream) {
     return launch_pdl(k_nest_lut<WARPS, R, CPS>, dim3((unsigned)grid), dim3(C::kThreads), C::kSmem, stream, a);
 }
 
-// NEST_LUT_SHAPE=8x2x2 picks the other compiled shape, for measurement.
+// NEST_LUT_SHAPE=16x2x1 or 8x2x2 picks another compiled shape, for measurement.
 }  // namespace
 
 cudaError_t launch_lut(const GemmArgs& a, int sms, cudaStream_t stream) {
-    // 8 row warps x 2 rows in two CTAs per SM: measured equal in steady state, faster for a
-    // lone small launch, slower in a chain with rotations (its two CTAs leave no registers
-    // for the small rotation CTAs beside it); kept for measurement
+    // 4 row warps x 2 rows in four CTAs per SM (256-row blocks): equal to the larger shapes
+    // on a long grouped launch, faster on small launches and in the chained layer, where
+    // the finer super-units shorten each launch's tail
     const char* e = getenv("NEST_LUT_SHAPE");
+    if (e && strcmp(e, "16x2x1") == 0) return launch_lut_shape<16, 2, 1>(a, sms, stream);
     if (e && strcmp(e, "8x2x2") == 0) return launch_lut_shape<8, 2, 2>(a, sms, stream);
-    return launch_lut_shape<16, 2, 1>(a, sms, stream);
+    return launch_lut_shape<4, 2, 4>(a, sms, stream);
 }
 
 cudaError_t read_and_clear_lut_error(int* flag, cudaStream_t stream) {

@@ -237,12 +237,16 @@ def test_draft_grouped_many_units(dev):
     nest.error_check()
 
 
-def test_draft_lookup_kernel_grouped(dev, monkeypatch):
+@pytest.mark.parametrize("shape", [None, "8x2x2", "4x2x4"])
+def test_draft_lookup_kernel_grouped(dev, monkeypatch, shape):
     """The one-token draft's table look-up kernel on a grouped launch large enough that
-    each CTA's range wraps the 10-stage ring and crosses task boundaries: seven 4096x4096
-    linears and a ragged 4296x4096 one (its last 512-row block has two tiles, the last
-    tile 72 rows), random 2-bit codes and scales; against the oracle, and against the
-    register-fragment kernel forced on the same inputs."""
+    each CTA's range wraps its stage and table rings and crosses task boundaries: seven
+    4096x4096 linears and a ragged 4296x4096 one (its last row block has two tiles, the
+    last tile 72 rows), random 2-bit codes and scales; against the oracle, and against the
+    register-fragment kernel forced on the same inputs.  Every compiled shape of the
+    kernel (row warps x rows per lane x CTAs per SM) is run."""
+    if shape is not None:
+        monkeypatch.setenv("NEST_LUT_SHAPE", shape)
     rng = np.random.default_rng(91)
     shapes = [(4096, 4096)] * 7 + [(4296, 4096)]
     layers, refs, xops = [], [], []
