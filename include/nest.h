@@ -374,18 +374,22 @@ nest_status nest_kv_attention(const void* q, int32_t q_dtype, int32_t T, int32_t
                               const nest_kv_cache* v, int32_t L, int32_t view, int32_t recent_n, float* out,
                               float* work, void* stream);
 
-/* Reads and clears the device-side error flag that kernels set when a pipeline
- * wait runs past its limit.  Synchronises `stream`.  Returns NEST_ERR_TIMEOUT if
- * the flag was set, NEST_ERR_CUDA on a CUDA error, NEST_OK otherwise. */
+/* Reads and clears the device-side error flags that kernels set when a pipeline
+ * wait runs past its limit (one for the tensor-core and register-fragment GEMM
+ * kernels, one for the one-token look-up kernel).  Synchronises `stream`.  Returns
+ * NEST_ERR_TIMEOUT if either flag was set, NEST_ERR_CUDA on a CUDA error, NEST_OK
+ * otherwise. */
 nest_status nest_error_check(void* stream);
 
 /* The give-up path of the kernels' bounded waits, exercised without a fault: launches
- * one warp that waits, through the same bounded wait as the GEMM pipelines, on a
- * barrier that nothing arrives on.  The wait gives up after its limit (2 s), raises
- * the device error flag and the kernel returns, so the context stays usable and the
- * next nest_error_check returns NEST_ERR_TIMEOUT (and clears the flag).
- * Asynchronous on `stream`; NEST_ERR_CUDA if the launch fails. */
-nest_status nest_wait_selftest(void* stream);
+ * one warp that waits, through the same bounded wait as the pipelines of the GEMM
+ * kernels (which = 0) or of the one-token look-up kernel (which = 1), on a barrier that
+ * nothing arrives on.  The wait gives up after its limit (2 s), raises that kernel
+ * family's device error flag and the kernel returns, so the context stays usable and
+ * the next nest_error_check returns NEST_ERR_TIMEOUT (and clears the flag).
+ * Asynchronous on `stream`; NEST_ERR_INVALID_ARG for another `which`, NEST_ERR_CUDA if
+ * the launch fails. */
+nest_status nest_wait_selftest(int32_t which, void* stream);
 
 #ifdef __cplusplus
 }

@@ -497,8 +497,10 @@ nest_status nest_error_check(void* stream) {
     return (flag || lut_flag) ? NEST_ERR_TIMEOUT : NEST_OK;
 }
 
-nest_status nest_wait_selftest(void* stream) {
-    return from_cuda(launch_wait_selftest(as_stream(stream)));
+nest_status nest_wait_selftest(int32_t which, void* stream) {
+    if (which == 0) return from_cuda(launch_wait_selftest(as_stream(stream)));
+    if (which == 1) return from_cuda(launch_lut_wait_selftest(as_stream(stream)));
+    return NEST_ERR_INVALID_ARG;
 }
 
 }  // extern "C"

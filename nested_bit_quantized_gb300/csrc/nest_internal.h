@@ -81,6 +81,7 @@ cudaError_t launch_lut(const GemmArgs& a, int sms, cudaStream_t stream);
 cudaError_t read_and_clear_lut_error(int* flag, cudaStream_t stream);
 cudaError_t read_and_clear_error(int* flag, cudaStream_t stream);
 cudaError_t launch_wait_selftest(cudaStream_t stream);
+cudaError_t launch_lut_wait_selftest(cudaStream_t stream);
 
 // zero_out (optional): a buffer of zero_count floats the kernel also clears (the
 // accumulator of the GEMM that follows it).

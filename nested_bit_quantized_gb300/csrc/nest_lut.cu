@@ -383,6 +383,27 @@ cudaError_t launch_lut(const GemmArgs& a, int sms, cudaStream_t stream) {
     return launch_lut_shape<4, 2, 4>(a, sms, stream);
 }
 
+namespace {
+// One warp waiting, through the look-up kernel's bounded wait, on a barrier nothing arrives
+// on: the give-up path (error flag raised, kernel returns) without a fault.
+__global__ void __launch_bounds__(32) k_lut_wait_selftest() {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    lut_wait(smem_u32(&bar), 0, &abort_flag);
+}
+}  // namespace
+
+cudaError_t launch_lut_wait_selftest(cudaStream_t stream) {
+    k_lut_wait_selftest<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_lut_error(int* flag, cudaStream_t stream) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_lut_error, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);
     if (e != cudaSuccess) return e;

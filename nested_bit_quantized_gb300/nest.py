@@ -97,7 +97,7 @@ def load() -> ctypes.CDLL:
         "nest_shard_gather": ([_P, _P, _I32, _I32, _I32, _I32, _P], _I32),
         "nest_operand": ([_P, _I32, _I32, _P, _P], _I32),
         "nest_error_check": ([_P], _I32),
-        "nest_wait_selftest": ([_P], _I32),
+        "nest_wait_selftest": ([_I32, _P], _I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -455,10 +455,11 @@ def error_check(stream=None) -> None:
     _check(load().nest_error_check(_stream(stream)), "nest_error_check")
 
 
-def wait_selftest(stream=None) -> None:
-    """Launch the bounded-wait give-up check (nest_wait_selftest); the next error_check
-    raises NestError with status 5 (timeout)."""
-    _check(load().nest_wait_selftest(_stream(stream)), "nest_wait_selftest")
+def wait_selftest(which: int = 0, stream=None) -> None:
+    """Launch the bounded-wait give-up check (nest_wait_selftest) of the GEMM kernels
+    (which=0) or of the one-token look-up kernel (which=1); the next error_check raises
+    NestError with status 5 (timeout)."""
+    _check(load().nest_wait_selftest(int(which), _stream(stream)), "nest_wait_selftest")
 
 
 # ---------------------------------------------------------------------------

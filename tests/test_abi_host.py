@@ -241,3 +241,9 @@ def test_group_other_than_128_is_refused(lib):
     bad = (nest._Layer * 1)(nest._Layer(256, 512, 8, 0x10000, 0x20000, 0x30000, 0x40000, 0, 32))
     assert lib.nest_chain(z, ctypes.c_void_p(0x30000), None, None, 512, 1, None, bad, 1,
                           (nest._P * 1)(0x70000), None, z, None) == 2
+
+
+def test_wait_selftest_rejects_unknown_kernel_family(lib):
+    # 0 (GEMM kernels) and 1 (look-up kernel) launch; anything else is refused before any launch
+    for which in (-1, 2, 7):
+        assert lib.nest_wait_selftest(which, None) == 1

@@ -1,7 +1,8 @@
 """The kernels' bounded waits give up cleanly.
 
-Every pipeline wait of the GEMM kernels is bounded by %globaltimer; when it runs
-out the kernel raises a device error flag, returns, and nest_error_check reports
+Every pipeline wait of the GEMM kernels (and of the one-token look-up kernel) is
+bounded by %globaltimer; when it runs out the kernel raises a device error flag,
+returns, and nest_error_check reports
 NEST_ERR_TIMEOUT.  nest_wait_selftest runs that wait on a barrier nothing ever
 arrives on (no fault, no trap: the wait itself ends), so the give-up path runs
 for real.  Afterwards the flag is clear and the same context still computes a
@@ -33,11 +34,14 @@ def dev():
     return d
 
 
-def test_wait_gives_up_and_context_stays_usable(dev):
+@pytest.mark.parametrize("which", [0, 1])
+def test_wait_gives_up_and_context_stays_usable(dev, which):
+    """which = 0: the wait of the tensor-core and register-fragment GEMM kernels; 1: the
+    wait of the one-token look-up kernel (its own error flag)."""
     nest.error_check()                                   # no flag left over
     torch.cuda.synchronize()
     t0 = time.monotonic()
-    nest.wait_selftest()
+    nest.wait_selftest(which)
     with pytest.raises(nest.NestError) as err:
         nest.error_check()                               # synchronises
     waited = time.monotonic() - t0
@@ -58,4 +62,10 @@ def test_wait_gives_up_and_context_stays_usable(dev):
     nest.rotate(x, layer.sign_in, 0, x_op=xop)
     z = nest.gemm(layer, xop, T, True)
     parity(z.cpu().numpy(), O.forward(q, s_o, s_i, xv, True)["z"])
+    # and the one-token draft (the look-up kernel)
+    x1 = x[:1].contiguous()
+    xop1 = nest.new_xop(K, 1, dev)
+    nest.rotate(x1, layer.sign_in, 0, x_op=xop1)
+    z1 = nest.gemm(layer, xop1, 1, False)
+    parity(z1.cpu().numpy(), O.forward(q, s_o, s_i, xv[:1], False)["z"])
     nest.error_check()
