@@ -478,7 +478,7 @@ def _ptrs(ts):
 
 
 def gemm_group(layers, x_ops, T: int, verify: bool, zs=None, stream=None):
-    """nest_verify_gemm_group / nest_draft_gemv_group: one launch over up to 4 linears.
+    """nest_verify_gemm_group / nest_draft_gemv_group: one launch over up to 64 linears.
     Accumulates into zs (new zs are zero-filled)."""
     dev = layers[0].base.device
     if zs is None:

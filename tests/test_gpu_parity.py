@@ -376,6 +376,42 @@ def test_full_size_sampled_rows(dev, name, idx, T):
         parity(z[:, rows], O.forward_rows(sub, xr, verify))
 
 
+@pytest.mark.slow
+def test_grouped_launch_as_benched(dev):
+    """The default bench line's launches at full size and in its launch configuration: 32
+    distinct packed copies of the 4096x4096 linear (b = 8) in one grouped gemm_group call
+    sharing one activation operand, as the bench graphs them: verify at T = 16 (the line's
+    value) and T = 1, and the draft at T = 1 (the look-up kernel).  Every token of every row
+    of three tiles of three copies against the oracle's rows; codes drawn uniformly over
+    their stored ranges, so the check does not go through any quantiser."""
+    lin = synth.WORKLOADS["single_4096"].linears[0]
+    M, K, C, bits = lin.M, lin.K, 32, 8
+    picked = (0, 13, 31)
+    tiles = (0, 16, 31)
+    rows = np.concatenate([np.arange(t * 128, t * 128 + 128) for t in tiles])
+    layers, subs = [], {}
+    for c in range(C):
+        bc, bs, rc, rs = synth.uniform_codes(M, K, bits, 500 + c)
+        s_o, s_i = synth.sign_pair(M, K, 600 + c)
+        layers.append(nest.pack(to_dev(bc, torch, dev), to_dev(bs, torch, dev), to_dev(rc, torch, dev),
+                                to_dev(rs, torch, dev), bits, to_dev(s_o, torch, dev), to_dev(s_i, torch, dev)))
+        if c in picked:
+            subs[c] = {"base_codes": bc[rows], "base_scales": bs[rows].view(np.float16),
+                       "resid_codes": rc[rows], "resid_scales": rs[rows].view(np.float16)}
+        if c == 0:
+            s_i0 = s_i
+    for T, verify in ((16, True), (1, True), (1, False)):
+        x, xv = bf16_x(T, K, 900 + T, dev)
+        xop = nest.new_xop(K, T, dev)
+        nest.rotate(x, layers[0].sign_in, 0, x_op=xop)
+        zs = nest.gemm_group(layers, [xop] * C, T, verify)
+        xr = O.rotate_activations(xv, s_i0)
+        for c in picked:
+            parity(zs[c].cpu().numpy()[:, rows], O.forward_rows(subs[c], xr, verify))
+        del zs
+    nest.error_check()
+
+
 def test_error_flag_clear(dev):
     nest.error_check()
 
