@@ -44,6 +44,7 @@ WORKLOAD = "single_4096"
 BITS = 8
 T_VERIFY, T_DRAFT = 16, 1
 SWEEP_T = (1, 4, 8, 16, 32, 64)
+LINEAR_GROUP = 32          # whole linears per nest_linear_group call (the library takes up to 64)
 PREFILL_T = (128, 256)
 NOMINAL_HBM_GBS = 8000.0
 # DRAM bytes per linear of the roofline kernel from one ncu capture of a grouped verify launch
@@ -532,27 +533,29 @@ def single_section(args, dev, timer, world):
     nest.error_check()
 
     # the whole linear (rotation in, GEMM, rotation out): draft T = 1 then verify T = 16, per copy,
-    # four copies per nest_linear_group call
+    # the copies' whole linears, LINEAR_GROUP per nest_linear_group call (one call for 32 copies)
     xs = {}
     for T in (T_DRAFT, T_VERIFY):
         b, _ = synth.activations(T, K, wl.x_seed + 100 + T)
         xs[T] = torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
     ys = {T: [torch.empty((T, M), dtype=torch.float32, device=dev) for _ in range(C)] for T in (T_DRAFT, T_VERIFY)}
-    scratch = torch.empty(max(nest.linear_group_scratch_bytes(layers[:4], T) for T in (T_DRAFT, T_VERIFY)),
+    LG = min(C, LINEAR_GROUP)
+    calls = (C + LG - 1) // LG
+    scratch = torch.empty(max(nest.linear_group_scratch_bytes(layers[:LG], T) for T in (T_DRAFT, T_VERIFY)),
                           dtype=torch.uint8, device=dev)
 
     def layer_pass(T, verify, xlist=None):
-        for i in range(0, C, 4):
-            n = min(4, C - i)
+        for i in range(0, C, LG):
+            n = min(LG, C - i)
             nest.linear_group(layers[i:i + n], xlist[i:i + n] if xlist else [xs[T]] * n, verify,
                               ys=ys[T][i:i + n], scratch=scratch)
 
     g = timer.graph(lambda: (layer_pass(T_DRAFT, False), layer_pass(T_VERIFY, True)))
     ms = timer.time("layer_step", g, 20, min_s=0.3)
     step_bytes = C * (by(T_DRAFT, False) + by(T_VERIFY, True))
-    out["layer_step"] = {"ms": ms, "GBps": step_bytes / (ms * 1e-3) / 1e9, "launches": 2 * 3 * ((C + 3) // 4),
+    out["layer_step"] = {"ms": ms, "GBps": step_bytes / (ms * 1e-3) / 1e9, "launches": 2 * 3 * calls,
                          "what": "per copy: rotation in, draft GEMV, rotation out at T=1, then rotation in, "
-                                 "verify GEMM, rotation out at T=16 (nest_linear_group over 4 copies)"}
+                                 f"verify GEMM, rotation out at T=16 (nest_linear_group over {LG} copies)"}
     del g
     nest.error_check()
 
@@ -572,8 +575,8 @@ def single_section(args, dev, timer, world):
     def e2e_once():
         with torch.cuda.stream(stream):
             xin.copy_(hx, non_blocking=True)
-            for i in range(0, C, 4):
-                n = min(4, C - i)
+            for i in range(0, C, LG):
+                n = min(LG, C - i)
                 nest.linear_group(layers[i:i + n], xl[i:i + n], True, ys=yl[i:i + n], scratch=scratch)
             hy.copy_(yout, non_blocking=True)
 
@@ -595,8 +598,8 @@ def single_section(args, dev, timer, world):
     out["e2e"] = {"value": world * C * by(T_VERIFY, True) / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                   "ms_per_step": e2e_ms, "h2d_bytes_per_step": C * T_VERIFY * K * 2,
                   "d2h_bytes_per_step": C * T_VERIFY * M * 4, "outputs_finite": ok,
-                  "what": f"per step: the {C} pinned bf16 input blocks copied in (one copy), {(C + 3) // 4} "
-                          f"nest_linear_group calls (rotation in, verify GEMM, rotation out; ctypes into the C "
+                  "what": f"per step: the {C} pinned bf16 input blocks copied in (one copy), {calls} "
+                          f"nest_linear_group call(s) (rotation in, verify GEMM, rotation out; ctypes into the C "
                           f"entry point), all {C} fp32 outputs copied back to pinned host memory (one copy); "
                           f"no CUDA graph"}
     nest.error_check()

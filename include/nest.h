@@ -240,7 +240,7 @@ size_t nest_linear_scratch_bytes(int32_t M, int32_t K, int32_t T);
 nest_status nest_linear(const nest_layer* layer, int32_t verify, const void* x, int32_t x_dtype,
                         int32_t T, float* y, void* scratch, void* stream);
 
-/* Whole linears for `count` (1..4) independent layers in three launches (one grouped
+/* Whole linears for `count` (1..64) independent layers in three launches (one grouped
  * rotation in, one grouped GEMM, one grouped rotation out).  layers: host array; xs, ys:
  * host arrays of device pointers ([T][K_k] inputs, [T][M_k] fp32 outputs); scratch:
  * nest_linear_group_scratch_bytes(layers, count, T) bytes of device memory. */
@@ -277,7 +277,7 @@ nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, c
                        int32_t M, int32_t T, float* y, const nest_layer* next, int32_t n_next,
                        uint16_t* const* x_ops, float* const* z_next, float* work, void* stream);
 
-/* Grouped rotation: `count` (1..4) independent nest_rotate calls sharing x_dtype, T and mode,
+/* Grouped rotation: `count` (1..64) independent nest_rotate calls sharing x_dtype, T and mode,
  * in ONE launch (e.g. one layer input rotated into the q, k and v operands, or the k and v
  * outputs rotated back).  Each task may also clear a buffer of zero_count floats (e.g. the
  * accumulator of the GEMM that reads its operand), which saves a separate fill launch.

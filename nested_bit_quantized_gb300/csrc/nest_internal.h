@@ -8,7 +8,7 @@
 
 namespace nest {
 
-constexpr int kMaxTasks = 4;           // vector sets in one grouped rotation; linears of nest_linear_group
+constexpr int kMaxTasks = 64;          // vector sets in one grouped rotation; linears of nest_linear_group
 constexpr int kMaxGemmTasks = 64;      // linears in one grouped draft/verify GEMM launch
 
 // One linear of a grouped draft/verify GEMM launch.

@@ -363,7 +363,7 @@ def _rot_bufs(signs, y, x_op, T: int, n: int):
 
 
 def rotate_group(xs, signs, mode: int, ys=None, x_ops=None, zero=None, stream=None):
-    """nest_rotate_group: up to 4 rotations (same dtype, T and mode) in one launch.
+    """nest_rotate_group: up to 64 rotations (same dtype, T and mode) in one launch.
     xs, signs: lists; ys / x_ops: lists (entries may be None) or None; zero: list of
     fp32 tensors (or None entries) cleared by the same launch."""
     n_t = len(xs)
@@ -500,7 +500,7 @@ def linear_group_scratch_bytes(layers, T: int) -> int:
 
 
 def linear_group(layers, xs, verify: bool, ys=None, scratch: Optional[torch.Tensor] = None, stream=None):
-    """nest_linear_group: y_k = S_o H_o (Q_k (H_i S_i x_k)) for up to 4 linears in 3 launches."""
+    """nest_linear_group: y_k = S_o H_o (Q_k (H_i S_i x_k)) for up to 64 linears in 3 launches."""
     T = xs[0].shape[0]
     dev = layers[0].base.device
     if ys is None:

@@ -137,7 +137,7 @@ def test_chain_and_rotate_group_validation(lib):
     one = (T * 1)(T(0x50000, 0x50000, 128, 0x50000, None, None, 0))
     g = lib.nest_rotate_group
     assert g(one, 0, 1, 4, 0, None) == 1
-    assert g(one, 5, 1, 4, 0, None) == 2
+    assert g(one, 65, 1, 4, 0, None) == 2
     assert g(one, 1, 2, 4, 0, None) == 1                                                # dtype
     bad = (T * 1)(T(0x50000, 0x50000, 128, 0x50000, None, None, 16))
     assert g(bad, 1, 1, 4, 0, None) == 1                                                # zero_count without buffer

@@ -432,6 +432,22 @@ def test_gemm_parity_prefill(dev, M, K, bits):
     nest.error_check()
 
 
+def test_linear_group_of_64(dev):
+    """nest_linear_group at its largest count: 64 independent linears of mixed shapes (ragged
+    row tiles; input widths with Hadamard blocks of 128 and 1024, so the grouped rotation in
+    mixes its register and segment paths) in three launches, draft at T = 1 and verify at
+    T = 16, against the oracle."""
+    shapes = [(128, 256), (200, 384), (384, 1024), (72, 128)]
+    refs = [ref_layer(*shapes[i % 4], 8, seed=300 + i % 8) for i in range(64)]
+    layers = [dev_layer(q, 8, so, si, dev) for (W, so, si, q) in refs]
+    for T, verify in ((1, False), (16, True)):
+        xs = [bf16_x(T, L.K, 400 + i, dev) for i, L in enumerate(layers)]
+        ys = nest.linear_group(layers, [x for x, _ in xs], verify)
+        for (W, so, si, q), (x, xv), y in zip(refs, xs, ys):
+            parity(y.cpu().numpy(), O.forward(q, so, si, xv, verify)["y"])
+    nest.error_check()
+
+
 def test_linear_and_group_prefill(dev):
     shapes = [(384, 512), (200, 1024)]
     refs = [ref_layer(M, K, 7, seed=21 + i) for i, (M, K) in enumerate(shapes)]
