@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 from typing import Optional
 
 import torch
@@ -231,11 +231,15 @@ class Layer:
     sign_out: torch.Tensor
     sign_in: torch.Tensor
     codec: int = CODEC_L2
+    _cs: Optional[_Layer] = field(default=None, init=False, repr=False, compare=False)
 
     def c_struct(self) -> _Layer:
-        return _Layer(self.M, self.K, self.bits, self.base.data_ptr(),
-                      self.resid.data_ptr() if self.resid is not None else None,
-                      self.sign_out.data_ptr(), self.sign_in.data_ptr(), self.codec, 128)
+        """The C descriptor (built once: the layer's buffers do not move)."""
+        if self._cs is None:
+            self._cs = _Layer(self.M, self.K, self.bits, self.base.data_ptr(),
+                              self.resid.data_ptr() if self.resid is not None else None,
+                              self.sign_out.data_ptr(), self.sign_in.data_ptr(), self.codec, 128)
+        return self._cs
 
     @property
     def weight_bytes(self) -> int:
@@ -495,8 +499,9 @@ def gemm_group(layers, x_ops, T: int, verify: bool, zs=None, stream=None):
     return zs
 
 
-def linear_group_scratch_bytes(layers, T: int) -> int:
-    return int(load().nest_linear_group_scratch_bytes(_layers(layers), len(layers), T))
+def linear_group_scratch_bytes(layers, T: int, arr=None) -> int:
+    arr = _layers(layers) if arr is None else arr
+    return int(load().nest_linear_group_scratch_bytes(arr, len(layers), T))
 
 
 def linear_group(layers, xs, verify: bool, ys=None, scratch: Optional[torch.Tensor] = None, stream=None):
@@ -512,11 +517,12 @@ def linear_group(layers, xs, verify: bool, ys=None, scratch: Optional[torch.Tens
         if _act(x, "x", T, L.K) != dt:
             raise ValueError("all inputs of a grouped linear share one dtype")
         _buf(y, "y", 4 * T * L.M, torch.float32)
-    need = linear_group_scratch_bytes(layers, T)
+    arr = _layers(layers)
+    need = linear_group_scratch_bytes(layers, T, arr)
     if scratch is None:
         scratch = torch.empty(need, dtype=torch.uint8, device=dev)
     _buf(scratch, "scratch", need)
-    st = load().nest_linear_group(_layers(layers), len(layers), int(verify), _ptrs(xs), dt, T, _ptrs(ys),
+    st = load().nest_linear_group(arr, len(layers), int(verify), _ptrs(xs), dt, T, _ptrs(ys),
                                   _ptr(scratch), _stream(stream))
     _check(st, "nest_linear_group")
     return ys
