@@ -559,58 +559,64 @@ def single_section(args, dev, timer, world):
     del g
     nest.error_check()
 
-    # end to end through the C entry point: the step's inputs copied in from pinned host memory,
-    # nest_linear_group calls (verify, T = 16), every output copied back, all inside the timed
-    # region; no graph.  The copies are cut into chunks of --e2e-chunk, alternating over two
-    # streams, so one chunk's copies overlap another chunk's GEMM (copy engines and SMs at once).
+    # end to end through the C entry point: every step copies its inputs in from pinned host
+    # memory, runs one nest_linear_group call over the copies (verify, T = 16) and copies every
+    # output back, all inside the timed region; no graph.  With --e2e-buffers 2 consecutive steps
+    # alternate over two streams, each with its own device and host buffers, so one step's copies
+    # overlap the neighbouring step's kernels (copy engines and SMs at once), as a serving loop
+    # that uploads the next batch while the current one runs would.
     hx = torch.empty((C, T_VERIFY, K), dtype=torch.bfloat16, pin_memory=True)
     for c in range(C):
         b, _ = synth.activations(T_VERIFY, K, wl.x_seed + 500 + c)
         hx[c].copy_(torch.from_numpy(b.view(np.int16)).view(torch.bfloat16))
-    xin = torch.empty((C, T_VERIFY, K), dtype=torch.bfloat16, device=dev)
-    yout = torch.empty((C, T_VERIFY, M), dtype=torch.float32, device=dev)
-    hy = torch.empty((C, T_VERIFY, M), dtype=torch.float32, pin_memory=True)
-    xl, yl = [xin[c] for c in range(C)], [yout[c] for c in range(C)]
     stream = timer.stream
-    ck = max(1, min(args.e2e_chunk, C, LINEAR_GROUP))
-    chunks = [(i, min(ck, C - i)) for i in range(0, C, ck)]
-    streams = [stream, torch.cuda.Stream(device=dev)]
-    scratches = [torch.empty(nest.linear_group_scratch_bytes(layers[:ck], T_VERIFY), dtype=torch.uint8, device=dev)
-                 for _ in streams]
+    nb = 2 if args.e2e_buffers == 2 else 1
+    streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(nb - 1)]
+    bufs = []
+    for _ in range(nb):
+        xin = torch.empty((C, T_VERIFY, K), dtype=torch.bfloat16, device=dev)
+        yout = torch.empty((C, T_VERIFY, M), dtype=torch.float32, device=dev)
+        hy = torch.empty((C, T_VERIFY, M), dtype=torch.float32, pin_memory=True)
+        sc = torch.empty(nest.linear_group_scratch_bytes(layers[:LG], T_VERIFY), dtype=torch.uint8, device=dev)
+        bufs.append((xin, yout, hy, [xin[c] for c in range(C)], [yout[c] for c in range(C)], sc))
 
-    def e2e_once():
-        for j, (i, n) in enumerate(chunks):
-            with torch.cuda.stream(streams[j % 2]):
-                xin[i:i + n].copy_(hx[i:i + n], non_blocking=True)
-                nest.linear_group(layers[i:i + n], xl[i:i + n], True, ys=yl[i:i + n], scratch=scratches[j % 2])
-                hy[i:i + n].copy_(yout[i:i + n], non_blocking=True)
+    def e2e_once(step):
+        xin, yout, hy, xl, yl, sc = bufs[step % nb]
+        with torch.cuda.stream(streams[step % nb]):
+            xin.copy_(hx, non_blocking=True)
+            for i in range(0, C, LG):
+                n = min(LG, C - i)
+                nest.linear_group(layers[i:i + n], xl[i:i + n], True, ys=yl[i:i + n], scratch=sc)
+            hy.copy_(yout, non_blocking=True)
 
-    for _ in range(max(3, args.warmup)):
-        e2e_once()
+    for i in range(max(3, args.warmup)):
+        e2e_once(i)
     torch.cuda.synchronize()
     if timer.dist is not None:
         timer.dist.barrier()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(timer.gpu) as clk, nvtx_range("e2e"):
         s.record(stream)
-        streams[1].wait_stream(stream)          # nothing of the timed steps starts before s
-        for _ in range(args.steps):
-            e2e_once()
-        stream.wait_stream(streams[1])          # ... or ends after e
+        for st in streams[1:]:
+            st.wait_stream(stream)              # nothing of the timed steps starts before s
+        for i in range(args.steps):
+            e2e_once(i)
+        for st in streams[1:]:
+            stream.wait_stream(st)              # ... or ends after e
         e.record(stream)
         torch.cuda.synchronize()
     timer.clocks["e2e"] = clk.summary()
     e2e_ms = max_over_ranks(s.elapsed_time(e) / args.steps, timer.dist, dev)
-    ok = bool(torch.isfinite(hy).all().item())
+    ok = all(bool(torch.isfinite(b[2]).all().item()) for b in bufs)
     out["e2e"] = {"value": world * C * by(T_VERIFY, True) / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                   "ms_per_step": e2e_ms, "h2d_bytes_per_step": C * T_VERIFY * K * 2,
-                  "d2h_bytes_per_step": C * T_VERIFY * M * 4, "outputs_finite": ok,
-                  "chunk": ck,
-                  "what": f"per step, in {len(chunks)} chunk(s) of {ck} copies alternating over two streams: the "
-                          f"chunk's pinned bf16 input blocks copied in, one nest_linear_group call (rotation in, "
-                          f"verify GEMM, rotation out; ctypes into the C entry point), its fp32 outputs copied "
-                          f"back to pinned host memory; all {C} inputs in and outputs out every step; no CUDA "
-                          f"graph"}
+                  "d2h_bytes_per_step": C * T_VERIFY * M * 4, "outputs_finite": ok, "buffers": nb,
+                  "what": f"per step: the {C} pinned bf16 input blocks copied in (one copy), {calls} "
+                          f"nest_linear_group call(s) (rotation in, verify GEMM, rotation out; ctypes into the C "
+                          f"entry point), all {C} fp32 outputs copied back to pinned host memory (one copy); "
+                          f"no CUDA graph" + ("; consecutive steps alternate over two streams with their own "
+                                              "buffers, so one step's copies overlap the next step's kernels"
+                                              if nb == 2 else "")}
     nest.error_check()
     out["copies"] = C
     out["bytes_per_linear_verify_T16"] = by(T_VERIFY, True)
@@ -1107,9 +1113,8 @@ def main():
     ap.add_argument("--copies", type=int, default=32, help="distinct copies of the 4096x4096 linear (>= 4x L2)")
     ap.add_argument("--copies-triplet", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-chunk", type=int, default=32,
-                    help="copies per chunk of the end-to-end leg (chunks alternate over two streams; "
-                         "measured 8: 1821, 16: 3005, 32 (one chunk): 3045 GB/s)")
+    ap.add_argument("--e2e-buffers", type=int, default=2, choices=[1, 2],
+                    help="end-to-end leg: 2 = consecutive steps alternate over two streams and buffer sets")
     ap.add_argument("--no-sweep", action="store_true", help="skip the GEMM-only sweep over T")
     ap.add_argument("--no-stack", action="store_true", help="skip the 60-layer 31B-class cycle in the default line")
     ap.add_argument("--quick", action="store_true", help="default workload only, no extra workloads")
