@@ -81,6 +81,35 @@ def test_chain_kernel(dev, M, T, product, in_place, n_next):
     nest.error_check()
 
 
+@pytest.mark.parametrize("M,product", [(5376, False), (8192, True), (21504, True)])
+def test_chain_zero_token(dev, M, product):
+    """A token whose glue input is all zero (RMS 0): the rescale gives zeros, so its rows of
+    every next operand are zero, while the other tokens are unaffected; on the register path
+    (blocks of 256) and the segment path (one 4096 block per segment, and 1024-blocks over
+    six segments)."""
+    T = 3
+    rng = np.random.default_rng(M)
+    za = rng.normal(size=(T, M)).astype(np.float32)
+    za[1] = 0.0
+    zb = rng.normal(size=(T, M)).astype(np.float32) if product else None
+    sa, sb = synth.signs(M, 1), synth.signs(M, 2)
+    nxt = [synth.signs(M, 3)]
+    dummy = torch.zeros(16, dtype=torch.uint8, device=dev)
+    layers = [nest.Layer(640, M, 0, dummy, None, to_dev(sa, torch, dev), to_dev(nxt[0], torch, dev))]
+    xops = [nest.new_xop(M, T, dev)]
+    y = torch.empty((T, M), dtype=torch.float32, device=dev)
+    work = torch.full((chain.chain_work_bytes(M, T) // 4,), float("nan"), device=dev)
+    chain.chain(to_dev(za, torch, dev), to_dev(sa, torch, dev), to_dev(zb, torch, dev) if product else None,
+                to_dev(sb, torch, dev) if product else None, T, work, y, layers, xops, None)
+    ya = O.unrotate_outputs(za, sa)
+    h = O.chain_glue(ya * O.unrotate_outputs(zb, sb) if product else ya)
+    assert np.all(h[1] == 0)
+    got = decode_xop(xops[0].cpu().numpy(), M, T).astype(np.float64)
+    assert np.all(got[1] == 0) and np.all(y.cpu().numpy()[1] == 0)
+    parity(got, O.rotate_activations(h, nxt[0]))
+    nest.error_check()
+
+
 def test_rotate_group_matches_single_calls(dev):
     """nest_rotate_group: three operands of one input plus cleared accumulators, and two
     output rotations, each equal to the single-call result."""

@@ -106,6 +106,44 @@ def test_quantize_matches_oracle(dev, M, K, bits, outl):
     _boundary_ok(q, mb, mr, bits)
 
 
+def test_degenerate_weights_and_tokens(dev):
+    """The method's degenerate cases on the GPU path.  One output Hadamard block of W all
+    zero (M = 384, blocks of 128 rows): its rotated rows are zero, so every group there
+    takes base scale 0 and code 2, residual scale 0 and code 0; the GPU quantiser must give
+    exactly those.  All-zero activation tokens (the first and, at T = 17, the last): their
+    z and y rows are zero.  The draft and verify GEMMs (T = 1 on the look-up kernel, T = 17
+    on the tensor cores) and the whole linear against the oracle, zeros exactly."""
+    M, K, bits = 384, 512, 7
+    W = synth.weights(M, K, 41, "entries")
+    W[128:256] = 0.0
+    s_o, s_i = synth.sign_pair(M, K, 42)
+    q = O.quantize_layer(W, s_o, s_i, bits)
+    assert np.all(q["base_scales"][128:256] == 0) and np.all(q["base_codes"][128:256] == 2)
+    assert np.all(q["resid_scales"][128:256] == 0) and np.all(q["resid_codes"][128:256] == 0)
+    g = nest.quantize(to_dev(W, torch, dev), to_dev(s_o, torch, dev), to_dev(s_i, torch, dev), bits)
+    for key in ("base_scales", "resid_scales"):
+        assert np.array_equal(g[key].cpu().numpy().view(np.uint16), q[key].view(np.uint16))
+    assert np.all(g["base_codes"].cpu().numpy()[128:256] == 2)
+    assert np.all(g["resid_codes"].cpu().numpy()[128:256] == 0)
+    layer = dev_layer(q, bits, s_o, s_i, dev)
+    for T in (1, 17):
+        xb, xv = synth.activations(T, K, 43 + T)
+        xb, xv = xb.copy(), xv.copy()
+        for t in {0, T - 1}:
+            xb[t] = 0
+            xv[t] = 0.0
+        x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+        for verify in (False, True):
+            ref = O.forward(q, s_o, s_i, xv, verify)
+            z = run_gemm(layer, x, verify, dev)
+            parity(z, ref["z"])
+            assert np.all(z[[0, T - 1]] == 0) and np.all(z[:, 128:256] == 0)
+            y = nest.linear(layer, x, verify).cpu().numpy()
+            parity(y, ref["y"])
+            assert np.all(y[[0, T - 1]] == 0) and np.all(y[:, 128:256] == 0)
+    nest.error_check()
+
+
 # ----------------------------------------------------------------------------
 # rotation
 # ----------------------------------------------------------------------------
