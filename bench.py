@@ -865,7 +865,9 @@ def stack_section(args, dev, timer, cycle=True, n_layers=60):
            "verify_pass": {"T": T_v, "ms": ms_v, "us_per_layer": 1e3 * ms_v / n_layers,
                            "GBps": lbytes(T_v, True) / (ms_v * 1e-3) / 1e9,
                            "frac_of_measured_hbm": lbytes(T_v, True) / (ms_v * 1e-3) / 1e9 / hbm},
-           "launches_per_cycle": (gamma + 1) * (1 + 13 * n_layers), "prep_seconds": prep_s}
+           # per layer: four grouped GEMMs and two launches per glue (the k and v output
+           # rotations ride in the q glue's first launch)
+           "launches_per_cycle": (gamma + 1) * (1 + 12 * n_layers), "prep_seconds": prep_s}
     res["cycle_over_ideal"] = ms / res["ideal_ms_at_measured_hbm"]
     del bufs, lin
     torch.cuda.empty_cache()

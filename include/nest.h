@@ -248,6 +248,24 @@ size_t nest_linear_group_scratch_bytes(const nest_layer* layers, int32_t count, 
 nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t verify, const void* const* xs,
                               int32_t x_dtype, int32_t T, float* const* ys, void* scratch, void* stream);
 
+/* Grouped rotation: `count` (1..64) independent nest_rotate calls sharing x_dtype, T and mode,
+ * in ONE launch (e.g. one layer input rotated into the q, k and v operands, or the k and v
+ * outputs rotated back).  Each task may also clear a buffer of zero_count floats (e.g. the
+ * accumulator of the GEMM that reads its operand), which saves a separate fill launch.
+ * Task fields have nest_rotate's meaning and limits; zero_out may be NULL when zero_count
+ * is 0 and must not overlap any other buffer of the call. */
+typedef struct {
+    const void* x;          /* [T][n] fp32 or bf16 bits */
+    const int8_t* signs;    /* int8 [n] */
+    int32_t n;
+    float* y;               /* fp32 [T][n] out, or NULL */
+    uint16_t* x_op;         /* operand out (mode 0), or NULL */
+    float* zero_out;        /* cleared here, or NULL */
+    int64_t zero_count;     /* floats to clear */
+} nest_rotate_task;
+nest_status nest_rotate_group(const nest_rotate_task* tasks, int32_t count, int32_t x_dtype, int32_t T,
+                              int32_t mode, void* stream);
+
 /* Glue between chained linears, fused with the rotations on both sides of it:
  *   h = S_o H_o z_a  (or the elementwise product h_a * h_b of two linears' outputs, e.g. gate * up),
  *   h' = bf16(h / rms(h)) per token (unit-RMS rescale standing in for the normalisation
@@ -271,29 +289,19 @@ nest_status nest_linear_group(const nest_layer* layers, int32_t count, int32_t v
  *               squares per token and 256/512-element chunk when the block size is at most 512,
  *               else per token and 4096-element segment), no initial contents; calls whose work
  *               may overlap on the GPU need separate work buffers.
+ * side          NULL, or host array of n_side (0..2) output rotations y = S_o H_o z of other
+ *               linears (e.g. the k and v outputs of the layer whose q output this glue reads),
+ *               run as extra CTAs of the glue's first launch, so they add no launch to the
+ *               chain.  Each task: x = z (fp32 [T][n], read only), signs = its S_o, y (fp32
+ *               [T][n] out), x_op and zero_out NULL; n >= 1, n * T < 2^31, 4-byte aligned.
+ *               A task whose block size falls on another path than the glue's runs in a
+ *               launch of its own.  Its z and y must not overlap z_a, z_b, y or each other.
  * Limits: T <= 256, M * T < 2^31, M % 128 == 0 when n_next > 0. */
 size_t nest_chain_work_bytes(int32_t M, int32_t T);
 nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,
                        int32_t M, int32_t T, float* y, const nest_layer* next, int32_t n_next,
-                       uint16_t* const* x_ops, float* const* z_next, float* work, void* stream);
-
-/* Grouped rotation: `count` (1..64) independent nest_rotate calls sharing x_dtype, T and mode,
- * in ONE launch (e.g. one layer input rotated into the q, k and v operands, or the k and v
- * outputs rotated back).  Each task may also clear a buffer of zero_count floats (e.g. the
- * accumulator of the GEMM that reads its operand), which saves a separate fill launch.
- * Task fields have nest_rotate's meaning and limits; zero_out may be NULL when zero_count
- * is 0 and must not overlap any other buffer of the call. */
-typedef struct {
-    const void* x;          /* [T][n] fp32 or bf16 bits */
-    const int8_t* signs;    /* int8 [n] */
-    int32_t n;
-    float* y;               /* fp32 [T][n] out, or NULL */
-    uint16_t* x_op;         /* operand out (mode 0), or NULL */
-    float* zero_out;        /* cleared here, or NULL */
-    int64_t zero_count;     /* floats to clear */
-} nest_rotate_task;
-nest_status nest_rotate_group(const nest_rotate_task* tasks, int32_t count, int32_t x_dtype, int32_t T,
-                              int32_t mode, void* stream);
+                       uint16_t* const* x_ops, float* const* z_next, float* work,
+                       const nest_rotate_task* side, int32_t n_side, void* stream);
 
 /* nest_linear without caller scratch, for callers that cannot allocate device memory
  * (a process whose memory pool is fixed at start-up, a plain C caller without an

@@ -37,12 +37,14 @@ def chain_work_bytes(M: int, T: int) -> int:
 
 
 def chain(z_a, s_a, z_b, s_b, T: int, work: torch.Tensor, y=None, nexts: Optional[List[nest.Layer]] = None,
-          x_ops=None, z_next=None, stream=None):
-    """nest_chain (see include/nest.h).  Without y, the glue output overwrites z_a."""
+          x_ops=None, z_next=None, stream=None, side=None):
+    """nest_chain (see include/nest.h).  Without y, the glue output overwrites z_a.  side: up to
+    two (z, sign_out, y) output rotations of other linears run in the glue's first launch."""
     lib = nest.load()
     nexts = nexts or []
     x_ops = x_ops or []
     z_next = z_next or []
+    side = side or []
     M = z_a.shape[1]
     nest._buf(z_a, "z_a", 4 * T * M, torch.float32)
     nest._buf(s_a, "s_a", M, torch.int8)
@@ -63,11 +65,18 @@ def chain(z_a, s_a, z_b, s_b, T: int, work: torch.Tensor, y=None, nexts: Optiona
         nest._buf(xo, "x_op", nest.xop_bytes(M, T))
     for L, zn in zip(nexts, z_next):
         nest._buf(zn, "z_next", 4 * T * L.M, torch.float32)
+    sd = (nest.RotateTask * len(side))() if side else None
+    for i, (zs, ss, ys) in enumerate(side):
+        n = zs.shape[1]
+        nest._buf(zs, "side z", 4 * T * n, torch.float32)
+        nest._buf(ss, "side sign_out", n, torch.int8)
+        nest._buf(ys, "side y", 4 * T * n, torch.float32)
+        sd[i] = nest.RotateTask(zs.data_ptr(), ss.data_ptr(), n, ys.data_ptr(), None, None, 0)
     arr = nest._layers(nexts) if nexts else None
     xo = nest._ptrs(x_ops) if nexts else None
     zn = nest._ptrs(z_next) if z_next else None
     st = lib.nest_chain(nest._ptr(z_a), nest._ptr(s_a), nest._ptr(z_b), nest._ptr(s_b), M, T, nest._ptr(y),
-                        arr, len(nexts), xo, zn, nest._ptr(work), nest._stream(stream))
+                        arr, len(nexts), xo, zn, nest._ptr(work), sd, len(side), nest._stream(stream))
     nest._check(st, "nest_chain")
 
 
@@ -87,10 +96,9 @@ def layer_forward(lin: Dict[str, nest.Layer], buf: LayerBuffers, verify: bool,
     g = lambda names: nest.gemm_group([lin[n] for n in names], [buf.xop[n] for n in names], T, verify,
                                       zs=[buf.z[n] for n in names], stream=stream)
     g(("q", "k", "v"))
+    # the k and v outputs are rotated back by extra CTAs of the q glue's first launch
     chain(buf.z["q"], lin["q"].sign_out, None, None, T, buf.work, None, [lin["o"]], [buf.xop["o"]], [buf.z["o"]],
-          stream)
-    nest.rotate_group([buf.z["k"], buf.z["v"]], [lin["k"].sign_out, lin["v"].sign_out], 1,
-                      ys=[buf.y["k"], buf.y["v"]], stream=stream)
+          stream, side=[(buf.z["k"], lin["k"].sign_out, buf.y["k"]), (buf.z["v"], lin["v"].sign_out, buf.y["v"])])
     g(("o",))
     chain(buf.z["o"], lin["o"].sign_out, None, None, T, buf.work, None, [lin["gate"], lin["up"]],
           [buf.xop["gate"], buf.xop["up"]], [buf.z["gate"], buf.z["up"]], stream)

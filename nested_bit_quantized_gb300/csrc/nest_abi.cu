@@ -343,8 +343,11 @@ size_t nest_chain_work_bytes(int32_t M, int32_t T) {
 
 nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, const int8_t* sign_out_b,
                        int32_t M, int32_t T, float* y, const nest_layer* next, int32_t n_next,
-                       uint16_t* const* x_ops, float* const* z_next, float* work, void* stream) {
+                       uint16_t* const* x_ops, float* const* z_next, float* work,
+                       const nest_rotate_task* side, int32_t n_side, void* stream) {
     if (z_a == nullptr || sign_out_a == nullptr || work == nullptr) return NEST_ERR_INVALID_ARG;
+    if (n_side < 0 || (n_side > 0 && side == nullptr)) return NEST_ERR_INVALID_ARG;
+    if (n_side > kMaxChainSide) return NEST_ERR_UNSUPPORTED;
     if ((z_b == nullptr) != (sign_out_b == nullptr)) return NEST_ERR_INVALID_ARG;
     if (z_b == z_a || (y != nullptr && y == z_b)) return NEST_ERR_INVALID_ARG;
     if (M < 1 || T < 1 || n_next < 0) return NEST_ERR_INVALID_ARG;
@@ -375,6 +378,23 @@ nest_status nest_chain(float* z_a, const int8_t* sign_out_a, const float* z_b, c
         if (zn && (reinterpret_cast<uintptr_t>(zn) & 3u)) return NEST_ERR_MISALIGNED;
         c.next[j] = GlueNext{L.sign_in, x_ops[j], zn, zn ? (long long)T * L.M : 0};
     }
+    // side output rotations: plain z -> y tasks on buffers of their own
+    for (int k = 0; k < n_side; ++k) {
+        const nest_rotate_task& r = side[k];
+        if (!r.x || !r.signs || !r.y || r.x_op || r.zero_out || r.zero_count || r.n < 1) return NEST_ERR_INVALID_ARG;
+        if ((long long)r.n * T >= (1LL << 31)) return NEST_ERR_UNSUPPORTED;
+        if ((reinterpret_cast<uintptr_t>(r.x) & 3u) || (reinterpret_cast<uintptr_t>(r.y) & 3u))
+            return NEST_ERR_MISALIGNED;
+        const void* mine[2] = {r.x, r.y};
+        for (const void* p : mine) {
+            if (p == z_a || (z_b && p == z_b) || (y && p == y)) return NEST_ERR_INVALID_ARG;
+            for (int o = 0; o < k; ++o)
+                if (p == side[o].x || p == side[o].y) return NEST_ERR_INVALID_ARG;
+        }
+        if (r.x == r.y) return NEST_ERR_INVALID_ARG;
+        c.side[k] = GlueSide{static_cast<const float*>(r.x), r.signs, r.y, r.n, 0, 0, 0, 0.0f, 0};
+    }
+    c.nside = n_side;
     return from_cuda(launch_glue(c, as_stream(stream)));
 }
 

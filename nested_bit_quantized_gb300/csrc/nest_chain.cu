@@ -63,8 +63,35 @@ __device__ __forceinline__ void load_chunk(const float* base, const bool (&have)
 // signs): the CTA's (token, 4096-element segment) as 16 rows x 256 columns (seg_col in
 // nest_device.cuh): coalesced column loads and the butterflies over the high index bits,
 // one pass through shared memory, then the low 8 bits along the rows, one row per warp.
+// What an out-rotation CTA (register path: warp) works on: the glue's linear a (and its
+// product partner), or an extra output rotation run in the same launch (no partner, and its
+// sums of squares are not kept).
+struct OutJob {
+    const float* za;
+    const int8_t* sa;
+    const float* zb;
+    const int8_t* sb;
+    float* h;
+    float* work;              // partial sums of squares, or nullptr
+    int M, L;
+    float scale;
+};
+__device__ __forceinline__ OutJob glue_job(const GlueArgs& a) {
+    return OutJob{a.za, a.sa, a.zb, a.sb, a.h, a.work, a.M, a.L, a.scale};
+}
+__device__ __forceinline__ OutJob side_job(const GlueSide& d) {
+    return OutJob{d.z, d.s, nullptr, nullptr, d.y, nullptr, d.M, d.L, d.scale};
+}
+// The side task of a launch that holds CTA (warp item) i, i past the glue's own.
+__device__ __forceinline__ const GlueSide& side_of(const GlueArgs& a, int i) {
+    int k = 0;
+    while (k + 1 < a.nside && a.side[k + 1].cta_begin <= i) ++k;
+    return a.side[k];
+}
+
 template <bool PROD>
-__device__ __forceinline__ void glue_out_seg(const GlueArgs& a, int t, int seg0, float* sm, float* sm2, float* red) {
+__device__ __forceinline__ void glue_out_seg(const OutJob& a, int t, int seg0, int slot, float* sm, float* sm2,
+                                             float* red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int L = a.L, M = a.M;
     const SegCol sc = seg_col(L);
@@ -114,10 +141,10 @@ __device__ __forceinline__ void glue_out_seg(const GlueArgs& a, int t, int seg0,
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) red[warp] = ss;
     __syncthreads();
-    if (threadIdx.x == 0) {                            // the warps' sums in a fixed order
+    if (threadIdx.x == 0 && a.work != nullptr) {      // the warps' sums in a fixed order
         float tot = 0.0f;
         for (int i = 0; i < kWarps; ++i) tot += red[i];
-        a.work[blockIdx.x] = tot;
+        a.work[slot] = tot;
     }
 }
 
@@ -174,12 +201,10 @@ __device__ __forceinline__ void glue_in_seg(const GlueArgs& a, const GlueNext& n
 constexpr int kSmallWarps = 1;
 
 template <bool PROD, int H>
-__device__ __forceinline__ void glue_out_small(const GlueArgs& a) {
+__device__ __forceinline__ void glue_out_small(const OutJob& a, int item, int nchunk) {
     constexpr int W = 256 * H, NR = 8 * H;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int item = blockIdx.x * kSmallWarps + warp;
-    if (item >= a.T * a.nchunk) return;              // the same for the whole warp
-    const int t = item / a.nchunk, c = item - t * a.nchunk;
+    const int lane = threadIdx.x & 31;
+    const int t = item / nchunk, c = item - t * nchunk;
     const int c0 = c * W, M = a.M;
     bool have[H];
     uint2 sa[H], sb[H];
@@ -214,7 +239,7 @@ __device__ __forceinline__ void glue_out_small(const GlueArgs& a) {
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) a.work[item] = ss;
+    if (lane == 0 && a.work != nullptr) a.work[item] = ss;
 }
 
 template <int H>
@@ -268,8 +293,18 @@ __device__ __forceinline__ void glue_in_small(const GlueArgs& a) {
 template <bool PROD>
 __global__ void __launch_bounds__(32 * kSmallWarps) k_glue_out_small(const __grid_constant__ GlueArgs a) {
     grid_dep_launch_dependents();
-    if (a.L <= 8) glue_out_small<PROD, 1>(a);
-    else glue_out_small<PROD, 2>(a);
+    const int item = blockIdx.x * kSmallWarps + (threadIdx.x >> 5);   // the same for the whole warp
+    if (item < a.glue_ctas) {
+        if (a.L <= 8) glue_out_small<PROD, 1>(glue_job(a), item, a.nchunk);
+        else glue_out_small<PROD, 2>(glue_job(a), item, a.nchunk);
+        return;
+    }
+    if (a.nside == 0) return;
+    const GlueSide& d = side_of(a, item);
+    const int it = item - d.cta_begin;
+    if (it >= a.T * d.nchunk) return;
+    if (d.L <= 8) glue_out_small<false, 1>(side_job(d), it, d.nchunk);
+    else glue_out_small<false, 2>(side_job(d), it, d.nchunk);
 }
 
 __global__ void __launch_bounds__(32 * kSmallWarps) k_glue_in_small(const __grid_constant__ GlueArgs a) {
@@ -284,10 +319,16 @@ __global__ void __launch_bounds__(kThreads) k_glue_out(const __grid_constant__ G
     __shared__ __align__(16) float buf2[PROD ? 64 : 1][65];
     __shared__ float red[32];
     grid_dep_launch_dependents();
+    if ((int)blockIdx.x >= a.glue_ctas) {             // an extra output rotation (segment path)
+        const GlueSide& d = side_of(a, blockIdx.x);
+        const int l = blockIdx.x - d.cta_begin, td = l / d.nseg;
+        glue_out_seg<false>(side_job(d), td, (l - td * d.nseg) * kSeg, 0, &buf[0][0], &buf2[0][0], red);
+        return;
+    }
     const int t = blockIdx.x / a.nseg, s = blockIdx.x - t * a.nseg;
     const int seg0 = s * kSeg;
     if (a.path == 2) {
-        glue_out_seg<PROD>(a, t, seg0, &buf[0][0], &buf2[0][0], red);
+        glue_out_seg<PROD>(glue_job(a), t, seg0, blockIdx.x, &buf[0][0], &buf2[0][0], red);
         return;
     }
     const int count = a.M - seg0 < kSeg ? a.M - seg0 : kSeg;
@@ -416,19 +457,54 @@ cudaError_t launch_glue(GlueArgs& a, cudaStream_t stream) {
     const bool seg = b >= 1024 && al(a.h, 16) && al(a.sa, 8) && al(a.sb, 8);
     a.path = reg ? 3 : (seg ? 2 : 0);
     a.nchunk = (a.M + reg_chunk(L) - 1) / reg_chunk(L);
-    if (a.path == 3) {                 // one-warp CTAs, one (token, chunk) per warp
-        const int ctas = (a.T * a.nchunk + kSmallWarps - 1) / kSmallWarps;
-        const dim3 sblk(32 * kSmallWarps);
-        cudaError_t e = a.zb != nullptr ? launch_pdl(k_glue_out_small<true>, dim3(ctas), sblk, 0, stream, a)
-                                        : launch_pdl(k_glue_out_small<false>, dim3(ctas), sblk, 0, stream, a);
-        if (e != cudaSuccess || a.nnext == 0) return e;
-        return launch_pdl(k_glue_in_small, dim3(a.nnext * ctas), sblk, 0, stream, a);
+    // Side rotations whose block size puts them on the glue's path (register or segment) ride
+    // in its first launch as extra CTAs; any other runs in a grouped rotation launch of its own.
+    a.glue_ctas = a.path == 3 ? a.T * a.nchunk : a.T * a.nseg;
+    long long items = a.glue_ctas;
+    RotArgs rest = {};
+    int keep = 0;
+    for (int k = 0; k < a.nside; ++k) {
+        GlueSide d = a.side[k];
+        const int bs = hadamard_block(d.M);
+        int Ls = 0;
+        while ((1 << Ls) < bs) ++Ls;
+        d.L = Ls;
+        d.scale = (float)(1.0 / sqrt((double)bs));
+        d.nseg = glue_segments(d.M);
+        d.nchunk = (d.M + reg_chunk(Ls) - 1) / reg_chunk(Ls);
+        const bool ok = a.path == 3 ? (bs <= 512 && d.M % 8 == 0 && al(d.z, 16) && al(d.y, 16) && al(d.s, 8))
+                                    : (a.path == 2 && bs >= 1024 && al(d.y, 16) && al(d.s, 8));
+        if (ok) {
+            d.cta_begin = (int)items;
+            items += (long long)a.T * (a.path == 3 ? d.nchunk : d.nseg);
+            a.side[keep++] = d;
+        } else {
+            RotTask& r = rest.task[rest.ntasks++];
+            r = RotTask{};
+            r.x = d.z;
+            r.signs = d.s;
+            r.y = d.y;
+            r.n = (unsigned)d.M;
+        }
     }
-    const dim3 blk(kThreads);
-    cudaError_t e = a.zb != nullptr ? launch_pdl(k_glue_out<true>, dim3(a.T * a.nseg), blk, 0, stream, a)
-                                    : launch_pdl(k_glue_out<false>, dim3(a.T * a.nseg), blk, 0, stream, a);
-    if (e != cudaSuccess || a.nnext == 0) return e;
-    return launch_pdl(k_glue_in, dim3(a.nnext * a.T * a.nseg), blk, 0, stream, a);
+    a.nside = keep;
+    if (items >= (1LL << 31)) return cudaErrorInvalidValue;
+    cudaError_t e;
+    if (a.path == 3) {                 // one-warp CTAs, one (token, chunk) per warp
+        const int ctas = (int)((items + kSmallWarps - 1) / kSmallWarps);
+        const int glue = (a.glue_ctas + kSmallWarps - 1) / kSmallWarps;
+        const dim3 sblk(32 * kSmallWarps);
+        e = a.zb != nullptr ? launch_pdl(k_glue_out_small<true>, dim3(ctas), sblk, 0, stream, a)
+                            : launch_pdl(k_glue_out_small<false>, dim3(ctas), sblk, 0, stream, a);
+        if (e == cudaSuccess && a.nnext > 0) e = launch_pdl(k_glue_in_small, dim3(a.nnext * glue), sblk, 0, stream, a);
+    } else {
+        const dim3 blk(kThreads);
+        e = a.zb != nullptr ? launch_pdl(k_glue_out<true>, dim3((unsigned)items), blk, 0, stream, a)
+                            : launch_pdl(k_glue_out<false>, dim3((unsigned)items), blk, 0, stream, a);
+        if (e == cudaSuccess && a.nnext > 0) e = launch_pdl(k_glue_in, dim3(a.nnext * a.T * a.nseg), blk, 0, stream, a);
+    }
+    if (e == cudaSuccess && rest.ntasks > 0) e = launch_rotate_group(rest, 0, 1, a.T, stream);
+    return e;
 }
 
 }  // namespace nest

@@ -99,6 +99,17 @@ struct GlueNext {
     long long zero_count;
 };
 constexpr int kMaxChainNext = 3;
+// An output rotation y = S_o H_o z of another linear run by extra CTAs (one-warp CTAs on the
+// register path: warps) of the glue's first launch.
+struct GlueSide {
+    const float* z;
+    const int8_t* s;
+    float* y;
+    int M, L, nseg, nchunk;   // length, log2 block size, 4096-segments and register chunks per token
+    float scale;
+    int cta_begin;            // first CTA (register path: first warp item) of the task in the launch
+};
+constexpr int kMaxChainSide = 2;
 struct GlueArgs {
     const float* za;          // accumulator of linear a, [T][M], rotated basis
     const int8_t* sa;         // S_o of linear a
@@ -107,9 +118,11 @@ struct GlueArgs {
     float* h;                 // glue output before the RMS rescale, [T][M] (may be za)
     float* work;              // [T][nseg] segment sums of squares
     GlueNext next[kMaxChainNext];
-    int nnext, M, T, L, NB, nseg, nchunk;
+    GlueSide side[kMaxChainSide];
+    int nnext, nside, M, T, L, NB, nseg, nchunk;
+    int glue_ctas;            // CTAs (register path: warp items) of the glue itself in the first launch
     float scale;
-    int path;                 // 0 shared-memory tile, 2 segment (b >= 1024), 3 register with two-warp CTAs (b <= 512)
+    int path;                 // 0 shared-memory tile, 2 segment (b >= 1024), 3 register with one-warp CTAs (b <= 512)
 };
 int glue_segments(int M);     // 4096-element segments per token
 int glue_work_floats(int M, int T);   // floats of the work buffer of a glue call

@@ -87,7 +87,7 @@ def load() -> ctypes.CDLL:
         "nest_pack_w4w8": ([_P, _P, _P, _I32, _I32, _P, _P, _P], _I32),
         "nest_unpack_w4w8": ([ctypes.POINTER(_Layer), _P, _P, _P, _P], _I32),
         "nest_chain": ([_P, _P, _P, _P, _I32, _I32, _P, ctypes.POINTER(_Layer), _I32, ctypes.POINTER(_P),
-                        ctypes.POINTER(_P), _P, _P], _I32),
+                        ctypes.POINTER(_P), _P, ctypes.POINTER(RotateTask), _I32, _P], _I32),
         "nest_rotate_group": ([ctypes.POINTER(RotateTask), _I32, _I32, _I32, _I32, _P], _I32),
         "nest_kv_plane_bytes": ([_I32, _I32], _SZ),
         "nest_kv_write": ([_P, _I32, _I32, ctypes.POINTER(_KvCache), _I32, _P], _I32),

@@ -125,14 +125,29 @@ def test_chain_and_rotate_group_validation(lib):
     nx = (nest._Layer * 1)(L)
     xo = (ctypes.c_void_p * 1)(0x50000)
     c = lib.nest_chain
-    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, None, None) == 1       # work missing
-    assert c(ok, ok, ok, None, 512, 4, None, nx, 1, xo, None, ok, None) == 1         # partner sign missing
-    assert c(ok, ok, ok, ok, 512, 4, None, nx, 1, xo, None, ok, None) == 1           # z_b aliases z_a
-    assert c(ok, ok, None, None, 512, 257, None, nx, 1, xo, None, ok, None) == 2     # T > 256
-    assert c(ok, ok, None, None, 640, 4, None, nx, 1, xo, None, ok, None) == 1       # next K != M
-    assert c(ok, ok, None, None, 500, 4, None, nx, 1, xo, None, ok, None) == 2       # operand needs M % 128
-    assert c(ok, ok, None, None, 512, 4, None, nx, 4, xo, None, ok, None) == 2       # more than 3 next
-    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, ctypes.c_void_p(0x50002), None) == 3
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, None, None, 0, None) == 1       # work missing
+    assert c(ok, ok, ok, None, 512, 4, None, nx, 1, xo, None, ok, None, 0, None) == 1         # partner sign missing
+    assert c(ok, ok, ok, ok, 512, 4, None, nx, 1, xo, None, ok, None, 0, None) == 1           # z_b aliases z_a
+    assert c(ok, ok, None, None, 512, 257, None, nx, 1, xo, None, ok, None, 0, None) == 2     # T > 256
+    assert c(ok, ok, None, None, 640, 4, None, nx, 1, xo, None, ok, None, 0, None) == 1       # next K != M
+    assert c(ok, ok, None, None, 500, 4, None, nx, 1, xo, None, ok, None, 0, None) == 2       # operand needs M % 128
+    assert c(ok, ok, None, None, 512, 4, None, nx, 4, xo, None, ok, None, 0, None) == 2       # more than 3 next
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, ctypes.c_void_p(0x50002), None, 0, None) == 3
+    # side output rotations: at most two, plain z -> y tasks on buffers of their own
+    R = nest.RotateTask
+    sd = lambda *t: (R * len(t))(*t)
+    good = R(0x60000, 0x60000, 256, 0x68000, None, None, 0)
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, ok, None, 1, None) == 1          # side missing
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, ok, sd(good, good, good), 3, None) == 2
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, ok,
+             sd(R(0x60000, 0x60000, 256, None, None, None, 0)), 1, None) == 1                       # no y
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, ok,
+             sd(R(0x60000, 0x60000, 256, 0x68000, 0x69000, None, 0)), 1, None) == 1                 # operand
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, ok,
+             sd(R(0x60000, 0x60000, 256, 0x50000, None, None, 0)), 1, None) == 1                    # y is z_a
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, ok, sd(good, good), 2, None) == 1  # overlap
+    assert c(ok, ok, None, None, 512, 4, None, nx, 1, xo, None, ok,
+             sd(R(0x60000, 0x60000, 256, 0x68002, None, None, 0)), 1, None) == 3                    # misaligned
     T = nest.RotateTask
     one = (T * 1)(T(0x50000, 0x50000, 128, 0x50000, None, None, 0))
     g = lib.nest_rotate_group
@@ -240,7 +255,7 @@ def test_group_other_than_128_is_refused(lib):
         assert lib.nest_draft_gemv(ctypes.byref(L), xop, z, 4, None) == 2
     bad = (nest._Layer * 1)(nest._Layer(256, 512, 8, 0x10000, 0x20000, 0x30000, 0x40000, 0, 32))
     assert lib.nest_chain(z, ctypes.c_void_p(0x30000), None, None, 512, 1, None, bad, 1,
-                          (nest._P * 1)(0x70000), None, z, None) == 2
+                          (nest._P * 1)(0x70000), None, z, None, 0, None) == 2
 
 
 def test_wait_selftest_rejects_unknown_kernel_family(lib):

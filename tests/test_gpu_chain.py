@@ -81,6 +81,44 @@ def test_chain_kernel(dev, M, T, product, in_place, n_next):
     nest.error_check()
 
 
+@pytest.mark.parametrize("M,T,product,side_ms", [
+    (8192, 1, False, (4096, 4096)), (8192, 16, False, (4096, 5376)), (5376, 1, True, (512, 2560)),
+    (5376, 17, False, (4096, 768)), (300, 4, False, (256,)), (21504, 3, True, (1024, 8192))])
+def test_chain_side_rotations(dev, M, T, product, side_ms):
+    """Output rotations of other linears handed to nest_chain (the k and v outputs beside
+    the q glue): those whose block size puts them on the glue's path run as extra CTAs of
+    its first launch, the others in a launch of their own; either way y = S_o H_o z against
+    the oracle, and the glue's own results are those without side tasks."""
+    rng = np.random.default_rng(M + 7 * T)
+    za = rng.normal(size=(T, M)).astype(np.float32)
+    zb = rng.normal(size=(T, M)).astype(np.float32) if product else None
+    sa, sb, sn = synth.signs(M, 11), synth.signs(M, 12), synth.signs(M, 13)
+    dummy = torch.zeros(16, dtype=torch.uint8, device=dev)
+    layers = [nest.Layer(640, M, 0, dummy, None, to_dev(sa, torch, dev), to_dev(sn, torch, dev))] if M % 128 == 0 \
+        else []
+    zs = [rng.normal(size=(T, m)).astype(np.float32) for m in side_ms]
+    ss = [synth.signs(m, 20 + i) for i, m in enumerate(side_ms)]
+    ys = [torch.full((T, m), float("nan"), device=dev) for m in side_ms]
+    side = [(to_dev(z, torch, dev), to_dev(sg, torch, dev), y) for z, sg, y in zip(zs, ss, ys)]
+    runs = []
+    for with_side in (True, False):
+        xops = [nest.new_xop(M, T, dev) for _ in layers]
+        y = torch.empty((T, M), dtype=torch.float32, device=dev)
+        work = torch.full((chain.chain_work_bytes(M, T) // 4,), float("nan"), device=dev)
+        chain.chain(to_dev(za, torch, dev), to_dev(sa, torch, dev), to_dev(zb, torch, dev) if product else None,
+                    to_dev(sb, torch, dev) if product else None, T, work, y, layers, xops, None,
+                    side=side if with_side else None)
+        runs.append((y.cpu().numpy(), [decode_xop(x.cpu().numpy(), M, T) for x in xops]))
+    for z, sg, yd in zip(zs, ss, ys):
+        parity(yd.cpu().numpy(), O.unrotate_outputs(z, sg))
+    assert np.array_equal(runs[0][0], runs[1][0])
+    for a, b in zip(runs[0][1], runs[1][1]):
+        assert np.array_equal(a, b)
+    ya = O.unrotate_outputs(za, sa)
+    parity(runs[0][0], ya * O.unrotate_outputs(zb, sb) if product else ya)
+    nest.error_check()
+
+
 @pytest.mark.parametrize("M,product", [(5376, False), (8192, True), (21504, True)])
 def test_chain_zero_token(dev, M, product):
     """A token whose glue input is all zero (RMS 0): the rescale gives zeros, so its rows of
