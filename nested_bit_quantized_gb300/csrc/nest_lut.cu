@@ -1,4 +1,6 @@
-// The draft GEMV at one token by table look-up (k_nest_lut): see the description below.
+// The draft GEMV at one token by table look-up (k_nest_lut): z = Q_base x', the draft
+// forward of the "2-bit base in VRAM, residual in RAM" post (feedman.me/posts/wZBTJ), POC
+// recipe step 4, "the same but without y_r".  See the description below.
 #include <cstdlib>
 #include <cstring>
 #include <utility>
