@@ -51,10 +51,10 @@ NOMINAL_HBM_GBS = 8000.0
 # (dram__bytes_read.sum + dram__bytes_write.sum divided by the linears of the launch).  Valid
 # only for the kernel source it was taken on: reported as null once that source changes.
 NCU_TRAFFIC = {"src": "nested_bit_quantized_gb300/csrc/nest_gemm.cu",
-               "sha256": "cfbbb0b63a84ff7b12eee38e03e758094c12c422cfd205f7f67197f840746fb1",
-               "bytes_per_linear": (698809600 + 7069440) / 32,
-               "what": "ncu --set full of one grouped k_nest_gemm<8,16> launch over 32 copies of the 4096x4096 "
-                       "linear at T=16: 698.81 MB read + 7.07 MB written"}
+               "sha256": "0197d71816886f6c163bbd26f1a9c65afef789bd75b70222a2282b4f43f94896",
+               "bytes_per_linear": (698800128 + 7088896) / 32,
+               "what": "ncu DRAM read/write counters of one grouped k_nest_gemm<8,16> launch over 32 copies of "
+                       "the 4096x4096 linear at T=16 (the third of four): 698.80 MB read + 7.09 MB written"}
 
 
 def ncu_traffic():

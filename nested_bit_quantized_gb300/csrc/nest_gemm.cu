@@ -6,12 +6,12 @@
 //  the draft is the same without y_r.)  All T tokens share one pass over the
 // packed weights, so the weight bytes are streamed from HBM once per call.
 //
-// Design (one CTA per SM, warp-specialised pipeline):
+// Design (warp-specialised pipeline; two CTAs per SM up to 64 tokens, one at 128 and 256):
 //   producer warp  : 1-D bulk copies (TMA engine) of one unit per stage -- the
 //                    base unit, the residual unit and the fp16 activation block
 //                    of the unit's 128-column group -- into shared memory.
-//   dequant warps  : two warpgroups; thread r of a warpgroup owns row r of the
-//                    tile.  It decodes its row's 128 weights of the unit into
+//   dequant warps  : two warpgroups (four at 128 and 256 tokens); thread r of a
+//                    warpgroup owns row r of the tile.  It decodes its row's 128 weights of the unit into
 //                    fp16 w = s_b*L[code] + s_r*q in registers (PRMT look-up of
 //                    the four scaled levels, fp16 magic-number decode of the
 //                    residual) and stores them to tensor memory with tcgen05.st.
