@@ -25,6 +25,9 @@
 //               rescales and rounds its segment of h, applies S_j, rotates and
 //               writes the fp16 operand; it also clears a share of the next GEMM's
 //               accumulator.
+// Side tasks: up to two plain output rotations y = S_o H_o z of other linears (the k and v
+// outputs beside the q glue) run as extra CTAs of the first launch, on the glue's own path,
+// so they add no launch to the chain (OutJob below; no sum of squares is kept for them).
 #include "nest_device.cuh"
 #include "nest_internal.h"
 
