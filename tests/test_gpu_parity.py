@@ -450,6 +450,37 @@ def test_grouped_launch_as_benched(dev):
     nest.error_check()
 
 
+def test_concurrent_streams(dev):
+    """The one-token look-up draft and the 16-token tensor-core verify launched on two
+    streams at once, ten times each, so their CTAs share the SMs: every result against the
+    oracle (the kernels share no state but the error flags)."""
+    M, K, bits = 1280, 1024, 8
+    W, s_o, s_i, q = ref_layer(M, K, bits, seed=61)
+    layer = dev_layer(q, bits, s_o, s_i, dev)
+    x1, xv1 = bf16_x(1, K, 62, dev)
+    x16, xv16 = bf16_x(16, K, 63, dev)
+    op1, op16 = nest.new_xop(K, 1, dev), nest.new_xop(K, 16, dev)
+    nest.rotate(x1, layer.sign_in, 0, x_op=op1)
+    nest.rotate(x16, layer.sign_in, 0, x_op=op16)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    za = [torch.zeros((1, M), device=dev) for _ in range(10)]
+    zb = [torch.zeros((16, M), device=dev) for _ in range(10)]
+    torch.cuda.synchronize()                 # the cleared accumulators before either stream starts
+    for i in range(10):
+        with torch.cuda.stream(sa):
+            nest.gemm(layer, op1, 1, False, z=za[i])
+        with torch.cuda.stream(sb):
+            nest.gemm(layer, op16, 16, True, z=zb[i])
+    torch.cuda.synchronize()
+    ra = O.forward(q, s_o, s_i, xv1, False)["z"]
+    rb = O.forward(q, s_o, s_i, xv16, True)["z"]
+    for i in range(10):
+        parity(za[i].cpu().numpy(), ra)
+        parity(zb[i].cpu().numpy(), rb)
+    nest.error_check()
+
+
 def test_error_flag_clear(dev):
     nest.error_check()
 
